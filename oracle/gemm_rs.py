@@ -1,0 +1,81 @@
+"""GEMM -> ReduceScatter oracle (test infrastructure only).
+
+Follows the TileLink talk summary ("TileLink: Generating Efficient
+Compute-Communication Overlapping Kernels using Tile-Centric Primitives"):
+
+* Key Findings / Experimental Setup & Results: GEMM-ReduceScatter; every rank
+  r holds A_r and B_r (the contraction dimension is split across ranks) and
+  computes its partial product; the partials are summed and row shard d of the
+  sum ends on rank d.
+* Technical Deep Dive, persistent kernels: the GEMM part notifies each finished
+  partial tile; a reduce stage waits on its own tile and on its peers' tiles
+  before summing.
+
+The sum runs in fixed rank order, S = (((P_0 + P_1) + P_2) + ... ), P_r in
+float64 from exactly decoded bf16 inputs.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import bf16
+
+
+def partial(A_r, B_r):
+    """P_r = A_r . B_r in float64."""
+    return bf16.decode(A_r) @ bf16.decode(B_r)
+
+
+def reduced(A_list, B_list):
+    """S = sum of the partials in rank order 0..R-1 (float64), full [M, N]."""
+    S = None
+    for A_r, B_r in zip(A_list, B_list):
+        P = partial(A_r, B_r)
+        S = P if S is None else S + P
+    return S
+
+
+def gemm_rs(A_list, B_list):
+    """Row shards out[d] = S[d*M/R:(d+1)*M/R, :] for d = 0..R-1 (float64)."""
+    R = len(A_list)
+    M = A_list[0].shape[0]
+    if M % R:
+        raise ValueError("M must be a multiple of R")
+    Md = M // R
+    S = reduced(A_list, B_list)
+    return [S[d * Md:(d + 1) * Md, :] for d in range(R)]
+
+
+def gemm_rs_at(A_list, B_list, rows, cols):
+    """S[rows[i], cols[i]] one element at a time, rank-ordered sum of per-rank dots."""
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    out = np.empty(rows.shape[0], dtype=np.float64)
+    for i, (row, col) in enumerate(zip(rows, cols)):
+        s = 0.0
+        for A_r, B_r in zip(A_list, B_list):
+            s = s + float(np.dot(bf16.decode(A_r[row, :]), bf16.decode(B_r[:, col])))
+        out[i] = s
+    return out
+
+
+# ---------------------------------------------------------------- tile bookkeeping
+
+def output_tiles(R, M, N, BM, BN):
+    """Output tiles (d, m_tile_in_d, n_tile) in destination order; tiles never straddle a shard."""
+    Md = M // R
+    Mt, Nt = -(-Md // BM), -(-N // BN)
+    return [(d, m, n) for d in range(R) for m in range(Mt) for n in range(Nt)]
+
+
+def item_order(R, M, N, BM, BN):
+    """Production order of partial tiles: (tau, d, m, n, r).
+
+    Tile tau's R partials are consecutive; the j-th has rank
+    r = (d + 1 + tau + j) mod R, so the destination rank's own partial (the one
+    that also reduces, r == d) sits at a position that rotates with tau."""
+    items = []
+    for tau, (d, m, n) in enumerate(output_tiles(R, M, N, BM, BN)):
+        for j in range(R):
+            items.append((tau, d, m, n, (d + 1 + tau + j) % R))
+    return items

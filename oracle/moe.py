@@ -1,0 +1,110 @@
+"""AllGather + grouped MoE GEMM oracle (test infrastructure only).
+
+Follows the TileLink talk summary ("TileLink: Generating Efficient
+Compute-Communication Overlapping Kernels using Tile-Centric Primitives"):
+
+* Key Findings / Experimental Setup & Results: the MoE layer gathers the
+  token shards of all ranks and runs a grouped GEMM (one GEMM per expert over
+  the tokens routed to it); this module covers that AllGather + GroupGEMM
+  part, with no gate weighting and no combine.
+* Technical Deep Dive, dynamic workloads: routing makes the tile -> rank
+  dependencies data dependent, so they are handed to the kernel as lookup
+  tables built from the routing.
+
+Routing bookkeeping (integer, plain loops):
+  counts[e]   number of (token, slot) pairs routed to expert e
+  offsets     exclusive prefix sum of counts, offsets[E] = T*k
+  perm[i]     sorted position i -> token*k + slot, sorted by
+              (expert, global token id, slot); global token id = r*T_r + local
+  tile table  for each expert, ceil(count/BM) row tiles (expert, first row, rows)
+  per tile    the bitmask of source ranks of its tokens, and the lowest and
+              highest producer barrier (token chunk) its tokens come from.
+Products: bf16 inputs decoded exactly, float64 arithmetic.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import bf16
+
+
+def route(topk_ids, E):
+    """(counts[E], offsets[E+1], perm[T*k]) as int64 arrays, by plain loops and a sort."""
+    ids = np.asarray(topk_ids)
+    T, k = ids.shape
+    counts = [0] * E
+    for t in range(T):
+        for s in range(k):
+            counts[int(ids[t, s])] += 1
+    offsets = [0]
+    for e in range(E):
+        offsets.append(offsets[-1] + counts[e])
+    pairs = sorted((int(ids[t, s]), t, s) for t in range(T) for s in range(k))
+    perm = [t * k + s for (_, t, s) in pairs]
+    return (np.array(counts, dtype=np.int64), np.array(offsets, dtype=np.int64),
+            np.array(perm, dtype=np.int64))
+
+
+def tile_table(counts, offsets, BM):
+    """[(expert, first_sorted_row, rows)] in expert order."""
+    out = []
+    for e in range(len(counts)):
+        c = int(counts[e])
+        for j in range(-(-c // BM)):
+            out.append((e, int(offsets[e]) + j * BM, min(BM, c - j * BM)))
+    return out
+
+
+def tile_sources(perm, k, table, T_r, rows_per_barrier):
+    """Per tile: (rank bitmask, lowest barrier id, highest barrier id) of its tokens."""
+    bpr = -(-T_r // rows_per_barrier)
+    out = []
+    for (_, start, rows) in table:
+        mask, lo, hi = 0, None, None
+        for i in range(start, start + rows):
+            tok = int(perm[i]) // k
+            r = tok // T_r
+            b = r * bpr + (tok % T_r) // rows_per_barrier
+            mask |= 1 << r
+            lo = b if lo is None else min(lo, b)
+            hi = b if hi is None else max(hi, b)
+        out.append((mask, lo, hi))
+    return out
+
+
+def sorted_tokens(X_shards, perm, k):
+    """Row i = gathered token perm[i] // k (bf16 bits): the gathered tokens in expert order."""
+    G = np.concatenate([np.asarray(x, dtype=np.uint16) for x in X_shards], axis=0)
+    return G[np.asarray(perm, dtype=np.int64) // k]
+
+
+def moe_ag_gemm(X_shards, topk_ids, W):
+    """Y [T*k, N] float64: Y[i] = token(perm[i]) . W_{expert of row i}."""
+    E = len(W)
+    k = np.asarray(topk_ids).shape[1]
+    counts, offsets, perm = route(topk_ids, E)
+    Gs = bf16.decode(sorted_tokens(X_shards, perm, k))
+    N = W[0].shape[1]
+    Y = np.zeros((Gs.shape[0], N), dtype=np.float64)
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            Y[lo:hi] = Gs[lo:hi] @ bf16.decode(W[e])
+    return Y
+
+
+def moe_at(X_shards, topk_ids, W, rows, cols, route_result=None):
+    """Y[rows[i], cols[i]] one element at a time."""
+    E = len(W)
+    k = np.asarray(topk_ids).shape[1]
+    counts, offsets, perm = route_result if route_result is not None else route(topk_ids, E)
+    T_r = X_shards[0].shape[0]
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    out = np.empty(rows.shape[0], dtype=np.float64)
+    for i, (row, col) in enumerate(zip(rows, cols)):
+        e = int(np.searchsorted(offsets, row, side="right") - 1)
+        tok = int(perm[row]) // k
+        x = bf16.decode(X_shards[tok // T_r][tok % T_r, :])
+        out[i] = np.dot(x, bf16.decode(W[e][:, col]))
+    return out

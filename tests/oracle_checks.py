@@ -1,0 +1,251 @@
+"""Pin checks for the oracle, written as functions of the implementation under
+test so that the same checks run on the oracle itself (must pass) and on
+copies of it with a planted mistake (must fail).
+
+Each check compares against something other than the oracle: brute-force
+loops, closed forms, invariants that a plausible mistake breaks, or the
+hand-worked fixtures in tests/golden/.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden_json(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _bits(x):
+    """Exact small values -> bf16 bits, by the binary32 upper-half definition (no rounding needed)."""
+    x = np.asarray(x, dtype=np.float32)
+    u = x.view(np.uint32)
+    assert np.all((u & 0xFFFF) == 0), "value not exactly representable in bf16"
+    return (u >> 16).astype(np.uint16)
+
+
+def _rand_bits(rng, shape, lo=-4, hi=4):
+    """Random small integers / 8 -> exact bf16 values (brute force stays exact)."""
+    return _bits(rng.integers(lo * 8, hi * 8 + 1, size=shape).astype(np.float32) / 8.0)
+
+
+# ------------------------------------------------------------------ AG-GEMM
+
+def brute_ag(A_shards, B):
+    """Triple loop over plain Python floats; the gather is explicit row copying."""
+    rows = []
+    for a in A_shards:
+        for i in range(a.shape[0]):
+            rows.append([float(np.float32(np.uint32(int(v) << 16).view(np.float32))) for v in a[i]])
+    Bv = [[float(np.uint32(int(v) << 16).view(np.float32)) for v in row] for row in B]
+    M, K, N = len(rows), len(Bv), len(Bv[0])
+    C = [[0.0] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            s = 0.0
+            for k in range(K):
+                s += rows[i][k] * Bv[k][j]
+            C[i][j] = s
+    return np.array(C)
+
+
+def check_ag_gemm(ag_gemm, ag_gemm_at, gathered, decode):
+    rng = np.random.default_rng(7)
+    # brute force, uneven shapes so that a transposed operand cannot pass
+    A = [_rand_bits(rng, (3, 5)) for _ in range(3)]
+    B = _rand_bits(rng, (5, 4))
+    C = ag_gemm(A, B)
+    assert C.shape == (9, 4)
+    np.testing.assert_array_equal(C, brute_ag(A, B))
+    # shard order: shard r constant (r+1) -> its rows are (r+1) * column sums of B
+    A = [_bits(np.full((2, 6), r + 1.0)) for r in range(4)]
+    B = _rand_bits(rng, (6, 3))
+    C = ag_gemm(A, B)
+    colsum = decode(B).sum(axis=0)
+    for r in range(4):
+        np.testing.assert_array_equal(C[2 * r:2 * r + 2], np.tile((r + 1) * colsum, (2, 1)))
+    # closed forms: identity B returns the gathered rows exactly; all-ones gives K
+    A = [_rand_bits(rng, (4, 8)) for _ in range(2)]
+    np.testing.assert_array_equal(ag_gemm(A, _bits(np.eye(8))), decode(gathered(A)))
+    ones = [_bits(np.ones((3, 7))) for _ in range(2)]
+    np.testing.assert_array_equal(ag_gemm(ones, _bits(np.ones((7, 5)))), np.full((6, 5), 7.0))
+    # R = 1 is a plain GEMM (brute force)
+    A1 = [_rand_bits(rng, (4, 3))]
+    B1 = _rand_bits(rng, (3, 2))
+    np.testing.assert_array_equal(ag_gemm(A1, B1), brute_ag(A1, B1))
+    # element sampler agrees with the full product at every element
+    A = [_rand_bits(rng, (3, 6)) for _ in range(2)]
+    B = _rand_bits(rng, (6, 5))
+    C = ag_gemm(A, B)
+    ii, jj = np.meshgrid(np.arange(6), np.arange(5), indexing="ij")
+    np.testing.assert_array_equal(ag_gemm_at(A, B, ii.ravel(), jj.ravel()), C.ravel())
+    # gathered buffer: rank order, exact bits
+    A = [_rand_bits(rng, (2, 3)) for _ in range(3)]
+    G = gathered(A)
+    for r in range(3):
+        np.testing.assert_array_equal(G[2 * r:2 * r + 2], A[r])
+
+
+def check_ag_tile_maps(consumer_order, tile_barriers, copy_order, tile_is_local):
+    fx = golden_json("ag_tile_maps_small.json")
+    for c in fx["cases"]:
+        got = consumer_order(c["R"], c["self"], c["M_shard"], c["N"], c["BM"], c["BN"])
+        assert [list(t) for t in got] == c["consumer_order"]
+    b = fx["barriers"]
+    got = [tile_barriers(m, b["BM"], b["R"], b["M_shard"], b["rows_per_barrier"]) for m in range(3)]
+    assert got == b["tile_barriers"]
+    got = copy_order(b["R"], 0, b["M_shard"], b["rows_per_barrier"])
+    assert [list(t) for t in got] == b["copy_order_self0"]
+    # properties on a mid case: a permutation of all tiles; self tiles first; each
+    # shard's tiles are contiguous and shards come in arrival order
+    R, s, Ms, N, BM, BN = 4, 2, 256, 512, 128, 256
+    order = consumer_order(R, s, Ms, N, BM, BN)
+    assert sorted(order) == list(itertools.product(range(R * Ms // BM), range(N // BN)))
+    shard_seq = [(m * BM) // Ms for (m, _) in order]
+    assert shard_seq == sorted(shard_seq, key=lambda r: (r - s) % R)
+    assert shard_seq[0] == s
+    assert all(tile_is_local(m, BM, R, Ms, s) == ((m * BM) // Ms == s) for m in range(R * Ms // BM))
+    # every copied row appears exactly once, self shard last
+    items = copy_order(R, s, Ms, 96)
+    rows = sorted(row for (_, _, g, n) in items for row in range(g, g + n))
+    assert rows == list(range(R * Ms))
+    assert all(it[0] == s for it in items[-3:]) and items[0][0] == (s + 1) % R
+
+
+# ------------------------------------------------------------------ GEMM-RS
+
+def check_gemm_rs(gemm_rs, gemm_rs_at, reduced):
+    rng = np.random.default_rng(11)
+    # brute force against per-rank triple loops summed in rank order
+    R, M, Kr, N = 3, 6, 4, 5
+    A = [_rand_bits(rng, (M, Kr)) for _ in range(R)]
+    B = [_rand_bits(rng, (Kr, N)) for _ in range(R)]
+    S = None
+    for r in range(R):
+        P = brute_ag([A[r]], B[r])
+        S = P if S is None else S + P
+    out = gemm_rs(A, B)
+    assert len(out) == R
+    for d in range(R):
+        np.testing.assert_array_equal(out[d], S[2 * d:2 * d + 2])
+    # scatter mapping: A_r[:,0] = global row index, B_r[0,:] = 1 -> out[d][i,j] = R*(d*Md+i)
+    R, M, Kr, N = 4, 8, 3, 3
+    A = []
+    for r in range(R):
+        a = np.zeros((M, Kr), dtype=np.float32)
+        a[:, 0] = np.arange(M)
+        A.append(_bits(a))
+    Bm = np.zeros((Kr, N), dtype=np.float32)
+    Bm[0, :] = 1.0
+    B = [_bits(Bm)] * R
+    out = gemm_rs(A, B)
+    for d in range(R):
+        expect = R * (d * 2 + np.arange(2))[:, None] * np.ones((1, N))
+        np.testing.assert_array_equal(out[d], expect)
+    # rank weights: A_r = (r+1) ones, B_r = ones -> every element K_r * sum(r+1)
+    A = [_bits(np.full((4, 5), r + 1.0)) for r in range(4)]
+    B = [_bits(np.ones((5, 2)))] * 4
+    for d, o in enumerate(gemm_rs(A, B)):
+        np.testing.assert_array_equal(o, np.full((1, 2), 5.0 * 10))
+    # fixed rank order of the float64 sum: P_0 = 2^53, P_1 = 1, P_2 = -2^53.
+    # ((2^53 + 1) - 2^53) = 0 in float64 (2^53+1 rounds to 2^53); any order that
+    # adds P_2 before P_1 gives 1.
+    A = [_bits(np.array([[2.0 ** 53]])), _bits(np.array([[1.0]])), _bits(np.array([[-(2.0 ** 53)]]))]
+    B = [_bits(np.array([[1.0]]))] * 3
+    assert reduced(A, B)[0, 0] == 0.0
+    assert gemm_rs_at(A, B, [0], [0])[0] == 0.0
+    # element sampler agrees with the full reduction
+    R, M, Kr, N = 2, 4, 3, 3
+    A = [_rand_bits(rng, (M, Kr)) for _ in range(R)]
+    B = [_rand_bits(rng, (Kr, N)) for _ in range(R)]
+    S = reduced(A, B)
+    ii, jj = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    np.testing.assert_array_equal(gemm_rs_at(A, B, ii.ravel(), jj.ravel()), S.ravel())
+
+
+def check_rs_item_order(item_order):
+    fx = golden_json("rs_item_order_small.json")
+    got = item_order(fx["R"], fx["M"], fx["N"], fx["BM"], fx["BN"])
+    assert [list(t) for t in got] == fx["items"]
+    # properties: every (tile, rank) once; the reducer (r == d) position rotates
+    R, M, N, BM, BN = 8, 2048, 512, 128, 256
+    items = item_order(R, M, N, BM, BN)
+    assert sorted((t, r) for (t, _, _, _, r) in items) == [(t, r) for t in range(len(items) // R) for r in range(R)]
+    pos = [j for j, it in enumerate(items) if it[4] == it[1]]
+    assert len({p % R for p in pos}) == R
+
+
+# ------------------------------------------------------------------ MoE
+
+def check_moe_routing(route, tile_table, tile_sources):
+    fx = golden_json("moe_routing_small.json")
+    ids = np.array(fx["topk_ids"])
+    counts, offsets, perm = route(ids, fx["E"])
+    assert list(counts) == fx["counts"]
+    assert list(offsets) == fx["offsets"]
+    assert list(perm) == fx["perm"]
+    table = tile_table(counts, offsets, fx["BM"])
+    assert [list(t) for t in table] == fx["tile_table"]
+    src = tile_sources(perm, fx["k"], table, fx["T_r"], fx["rows_per_barrier"])
+    assert [list(t) for t in src] == fx["tile_sources"]
+    # invariants on a random routing
+    rng = np.random.default_rng(3)
+    T, k, E = 200, 2, 7
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    counts, offsets, perm = route(ids, E)
+    np.testing.assert_array_equal(counts, np.bincount(ids.ravel(), minlength=E))
+    assert offsets[0] == 0 and offsets[-1] == T * k
+    assert sorted(perm) == list(range(T * k))
+    for e in range(E):
+        seg = perm[offsets[e]:offsets[e + 1]]
+        assert all(ids[p // k, p % k] == e for p in seg)
+        toks = [p // k for p in seg]
+        assert toks == sorted(toks)                      # stable by global token id
+    table = tile_table(counts, offsets, 16)
+    assert sum(t[2] for t in table) == T * k
+    assert all(0 < t[2] <= 16 for t in table)
+
+
+def check_moe_gemm(moe_ag_gemm, moe_at, sorted_tokens, route, ag_gemm, decode):
+    rng = np.random.default_rng(5)
+    # E = 1, k = 1 routing is a plain AllGather-GEMM
+    X = [_rand_bits(rng, (3, 4)) for _ in range(2)]
+    W = [_rand_bits(rng, (4, 5))]
+    ids = np.zeros((6, 1), dtype=np.int32)
+    np.testing.assert_array_equal(moe_ag_gemm(X, ids, W), ag_gemm(X, W[0]))
+    # identity routing token t -> expert t mod E, k = 1: sorted rows are the
+    # tokens of each residue class, each times its own expert's weight
+    E = 3
+    X = [_rand_bits(rng, (4, 3)) for _ in range(2)]
+    W = [_rand_bits(rng, (3, 2)) for _ in range(E)]
+    ids = (np.arange(8) % E).astype(np.int32)[:, None]
+    Y = moe_ag_gemm(X, ids, W)
+    G = np.concatenate(X)
+    row = 0
+    for e in range(E):
+        for t in range(e, 8, E):
+            np.testing.assert_array_equal(Y[row], brute_ag([G[t:t + 1]], W[e])[0])
+            row += 1
+    # top-2 brute force: every sorted row is token . W_expert, and rows are
+    # grouped by expert with tokens ascending
+    X = [_rand_bits(rng, (3, 4)) for _ in range(2)]
+    W = [_rand_bits(rng, (4, 3)) for _ in range(3)]
+    ids = np.array([[0, 2], [1, 0], [2, 1], [0, 1], [2, 0], [1, 2]], dtype=np.int32)
+    Y = moe_ag_gemm(X, ids, W)
+    G = np.concatenate(X)
+    expect = []
+    for e in range(3):
+        for t in range(6):
+            if e in ids[t]:
+                expect.append(brute_ag([G[t:t + 1]], W[e])[0])
+    np.testing.assert_array_equal(Y, np.array(expect))
+    counts, offsets, perm = route(ids, 3)
+    Gs = sorted_tokens(X, perm, 2)
+    for i in range(12):
+        np.testing.assert_array_equal(Gs[i], G[perm[i] // 2])
+    ii, jj = np.meshgrid(np.arange(12), np.arange(3), indexing="ij")
+    np.testing.assert_array_equal(moe_at(X, ids, W, ii.ravel(), jj.ravel()), Y.ravel())

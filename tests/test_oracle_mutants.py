@@ -1,0 +1,131 @@
+"""The oracle pins must catch plausible mistakes.  Each test plants one mistake
+in a copy of an oracle function (on the CPU, never in the oracle itself) and
+checks that the corresponding pin check fails."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle import bf16
+from tests import oracle_checks as C
+
+A = oracle.ag_gemm
+G = oracle.gemm_rs
+M = oracle.moe
+
+
+def _fails(fn, *args):
+    with pytest.raises(AssertionError):
+        fn(*args)
+
+
+def test_pins_catch_dropped_k_term():
+    def bad(A_shards, B):
+        Gm = bf16.decode(A.gathered(A_shards))[:, :-1]
+        return Gm @ bf16.decode(B)[:-1]
+    _fails(C.check_ag_gemm, bad, A.ag_gemm_at, A.gathered, bf16.decode)
+
+
+def test_pins_catch_reversed_shard_order():
+    def bad_gathered(A_shards):
+        return np.concatenate([np.asarray(a) for a in A_shards[::-1]])
+    def bad(A_shards, B):
+        return bf16.decode(bad_gathered(A_shards)) @ bf16.decode(B)
+    _fails(C.check_ag_gemm, bad, A.ag_gemm_at, bad_gathered, bf16.decode)
+
+
+def test_pins_catch_wrong_sign():
+    def bad(A_shards, B):
+        return -A.ag_gemm(A_shards, B)
+    _fails(C.check_ag_gemm, bad, A.ag_gemm_at, A.gathered, bf16.decode)
+
+
+def test_pins_catch_sampler_index_swap():
+    def bad_at(A_shards, B, rows, cols):
+        return A.ag_gemm_at(A_shards, B, cols, rows) if max(rows) < B.shape[1] else A.ag_gemm_at(A_shards, B, rows, cols[::-1])
+    _fails(C.check_ag_gemm, A.ag_gemm, bad_at, A.gathered, bf16.decode)
+
+
+def test_pins_catch_n_outer_consumer_order():
+    def bad(R, s, Ms, N, BM, BN):
+        order = A.consumer_order(R, s, Ms, N, BM, BN)
+        return sorted(order, key=lambda t: (t[1], order.index(t)))
+    _fails(C.check_ag_tile_maps, bad, A.tile_barriers, A.copy_order, A.tile_is_local)
+
+
+def test_pins_catch_off_by_one_barrier():
+    def bad(m, BM, R, Ms, rpb):
+        return A.tile_barriers(m, BM, R, Ms, rpb + 1)
+    _fails(C.check_ag_tile_maps, A.consumer_order, bad, A.copy_order, A.tile_is_local)
+
+
+def test_pins_catch_reverse_rank_order_sum():
+    def bad_reduced(A_list, B_list):
+        return G.reduced(A_list[::-1], B_list[::-1])
+    def bad_rs(A_list, B_list):
+        R = len(A_list)
+        S = bad_reduced(A_list, B_list)
+        Md = S.shape[0] // R
+        return [S[d * Md:(d + 1) * Md] for d in range(R)]
+    _fails(C.check_gemm_rs, bad_rs, G.gemm_rs_at, bad_reduced)
+
+
+def test_pins_catch_scatter_to_wrong_destination():
+    def bad_rs(A_list, B_list):
+        out = G.gemm_rs(A_list, B_list)
+        return out[1:] + out[:1]
+    _fails(C.check_gemm_rs, bad_rs, G.gemm_rs_at, G.reduced)
+
+
+def test_pins_catch_transposed_partial():
+    def bad_reduced(A_list, B_list):
+        S = None
+        for a, b in zip(A_list, B_list):
+            P = bf16.decode(a) @ bf16.decode(b)
+            P = P[::-1]
+            S = P if S is None else S + P
+        return S
+    def bad_rs(A_list, B_list):
+        R = len(A_list)
+        S = bad_reduced(A_list, B_list)
+        Md = S.shape[0] // R
+        return [S[d * Md:(d + 1) * Md] for d in range(R)]
+    _fails(C.check_gemm_rs, bad_rs, G.gemm_rs_at, bad_reduced)
+
+
+def test_pins_catch_unrotated_rs_order():
+    def bad(R, Mm, N, BM, BN):
+        return [(t, d, m, n, j) for (t, d, m, n, _), j in
+                zip(G.item_order(R, Mm, N, BM, BN), [j for _ in range(10 ** 6) for j in range(R)])]
+    _fails(C.check_rs_item_order, bad)
+
+
+def test_pins_catch_unstable_sort():
+    def bad_route(ids, E):
+        counts, offsets, perm = M.route(ids, E)
+        k = ids.shape[1]
+        out = perm.copy()
+        for e in range(E):
+            seg = out[offsets[e]:offsets[e + 1]]
+            out[offsets[e]:offsets[e + 1]] = seg[::-1]
+        return counts, offsets, out
+    _fails(C.check_moe_routing, bad_route, M.tile_table, M.tile_sources)
+
+
+def test_pins_catch_inclusive_scan():
+    def bad_route(ids, E):
+        counts, offsets, perm = M.route(ids, E)
+        return counts, np.concatenate([offsets[1:], offsets[-1:]]), perm
+    _fails(C.check_moe_routing, bad_route, M.tile_table, M.tile_sources)
+
+
+def test_pins_catch_wrong_expert_weight():
+    def bad(X, ids, W):
+        return M.moe_ag_gemm(X, ids, W[1:] + W[:1])
+    _fails(C.check_moe_gemm, bad, M.moe_at, M.sorted_tokens, M.route, A.ag_gemm, bf16.decode)
+
+
+def test_pins_catch_slot_for_token_confusion():
+    def bad_sorted(X, perm, k):
+        Gm = np.concatenate([np.asarray(x) for x in X])
+        return Gm[np.asarray(perm) % Gm.shape[0]]
+    _fails(C.check_moe_gemm, M.moe_ag_gemm, M.moe_at, bad_sorted, M.route, A.ag_gemm, bf16.decode)
