@@ -1,0 +1,187 @@
+/*
+ * tilelink.h -- C ABI of libtilelink: tile-centric compute/communication
+ * overlap on one NVIDIA GB300 (sm_103a).
+ *
+ * The method follows the TileLink talk summary ("TileLink: Generating Efficient
+ * Compute-Communication Overlapping Kernels using Tile-Centric Primitives",
+ * MLSys 2025): producers and consumers of tiles synchronise through per-tile
+ * signals (Technical Deep Dive: signal primitives consume_tile_wait,
+ * produce_tile_notify, peer_tile_wait; data primitives push and pull; tile-id
+ * to rank/barrier maps; swizzled tile orders), applied to AllGather-GEMM,
+ * GEMM-ReduceScatter and the AllGather + GroupGEMM part of an MoE layer (Key
+ * Findings; Experimental Setup & Results).
+ *
+ * The R communicating ranks are emulated on one GPU: every rank's data is a
+ * separate allocation that the caller passes as an array of pointers, and
+ * "communication" is a copy between those allocations performed by the
+ * library's own copy warps.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Matrices are row-major.  bf16 = IEEE bfloat16 (uint16 storage).
+ *  - Pointers named "device" must be device (or device-mapped) memory, 16-byte
+ *    aligned.  Arrays of pointers (A_shards, A, B, out, X, W) are HOST arrays
+ *    read during the call; the pointers in them are device pointers.
+ *  - Ownership: the caller owns every buffer passed in.  The library allocates
+ *    only the flag/status memory of a tl_signals object.
+ *  - Ordering: every call that takes a stream is asynchronous and ordered on
+ *    that stream (a cudaStream_t passed as void*, NULL = legacy default
+ *    stream).  Argument errors are returned synchronously and launch nothing.
+ *    Device-side errors (a bounded wait that ran out) are recorded in the
+ *    signals object's status word and read with tl_query_status.
+ *  - Epochs: a flag is "set for epoch E" when its value v satisfies
+ *    (int32_t)(v - E) >= 0.  Each call that uses a signals object releases its
+ *    flags with the caller's epoch, so flags are never reset between calls; a
+ *    later call on the same object must use a larger epoch (mod 2^32).
+ *  - Every wait inside a kernel is bounded by timeout_ns (0 = 1 s).  When a
+ *    bound runs out the kernel records TL_ERR_TIMEOUT, stops waiting for the
+ *    rest of the launch, and finishes; its outputs are then undefined.
+ *  - Failure: no call aborts the process; no exception crosses the ABI.
+ *    tl_last_error() returns a message for the calling thread's last error.
+ *  - Not capturable into CUDA graphs for replay: epochs are launch parameters.
+ */
+#ifndef TILELINK_H
+#define TILELINK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TL_VERSION 1
+#define TL_MAX_RANKS 64
+#define TL_MAX_EXPERTS 256
+
+typedef enum {
+  TL_OK = 0,
+  TL_ERR_INVALID = 1,      /* bad argument (null, negative, misaligned, too small) */
+  TL_ERR_CUDA = 2,         /* a CUDA runtime/driver call failed */
+  TL_ERR_TIMEOUT = 3,      /* a bounded device wait ran out (see tl_query_status) */
+  TL_ERR_UNSUPPORTED = 4,  /* valid but outside what the kernels handle */
+  TL_ERR_INTERNAL = 5      /* a device-side consistency check failed */
+} tl_status;
+
+typedef enum { TL_MODE_PULL = 0, TL_MODE_PUSH = 1 } tl_mode;
+
+/* Opaque per-tile signal buffer: device uint32 flags plus a device status word. */
+typedef struct tl_signals tl_signals;
+
+/* Library version (TL_VERSION) and the last error message of this thread. */
+int tl_version(void);
+const char* tl_last_error(void);
+
+/* ---------------------------------------------------------------- signals
+ * Signal primitives (talk summary, Technical Deep Dive: produce_tile_notify,
+ * consume_tile_wait).  A signals object owns num_flags device uint32 flags,
+ * zero at creation, and a status word.  The object belongs to the device that
+ * is current at creation.
+ */
+tl_status tl_signals_create(int num_flags, tl_signals** out);
+tl_status tl_signals_destroy(tl_signals* s);
+/* Device pointer to the flags (for tests and for the caller's own kernels). */
+tl_status tl_signals_flags(const tl_signals* s, uint32_t** dev_flags, int* num_flags);
+/* Zero every flag and the status word (stream-ordered). */
+tl_status tl_signals_reset(tl_signals* s, void* stream);
+
+/* produce_tile_notify: release-store `value` into flags [first, first+count)
+ * after all earlier work on `stream` (one thread per flag, st.release.gpu). */
+tl_status tl_tile_notify(tl_signals* s, int first, int count, uint32_t value, void* stream);
+
+/* consume_tile_wait: block `stream` until every flag in [first, first+count)
+ * is set for epoch `value` (acquire loads), or until timeout_ns elapses; on
+ * timeout the status word records TL_ERR_TIMEOUT with the flag index.  The
+ * wait must be satisfiable by work already ordered before it: a flag that only
+ * a later or concurrent launch would set is a timeout, never a hang. */
+tl_status tl_tile_wait(tl_signals* s, int first, int count, uint32_t value,
+                       uint64_t timeout_ns, void* stream);
+
+/* Synchronise `stream`, return the first device error recorded since the last
+ * query (TL_OK if none) and clear it.  *where receives the flag index or tile
+ * that failed (-1 if none).  Either out pointer may be NULL. */
+tl_status tl_query_status(tl_signals* s, void* stream, int* code, int* where);
+
+/* ---------------------------------------------------------------- AllGather-GEMM
+ * C = G . B with G = [A_0; A_1; ...; A_{R-1}] (talk summary, Key Findings and
+ * Experimental Setup & Results: AllGather-GEMM).  One launch holds both sides:
+ *  - producer: copy warps move each shard, rows_per_barrier rows at a time, into
+ *    `gathered` with bulk TMA copies and release one flag per row chunk
+ *    (produce_tile_notify).  Pull mode first waits on the source's readiness
+ *    flag of the same id (two barriers per tile); push mode has one barrier.
+ *  - consumer: tcgen05 GEMM tiles of 128 x 256 acquire every flag guarding
+ *    their rows (consume_tile_wait; flag id = rank * barriers_per_rank +
+ *    row_in_shard / rows_per_barrier, an affine map of the row) before loading
+ *    A, and run in arrival order: shards self, self+1, ..., self+R-1
+ *    (consume_tile_swizzle).  Tiles wholly inside the self shard read A_self in
+ *    place and never wait.  Copies run in the order self+1, ..., self+R-1, self.
+ * Output is independent of self_rank, mode and rows_per_barrier.
+ */
+typedef struct tl_ag_gemm_args {
+  int32_t R;                   /* ranks, 1..TL_MAX_RANKS */
+  int32_t self_rank;           /* 0..R-1 */
+  int32_t M_shard;             /* rows per shard, >= 1 */
+  int32_t K;                   /* contraction, >= 8, multiple of 8 */
+  int32_t N;                   /* output columns, >= 8, multiple of 8 */
+  int32_t mode;                /* tl_mode */
+  int32_t rows_per_barrier;    /* rows per producer tile / flag; 0 = about 32 KB of A */
+  int32_t reserved0;
+  const void* const* A_shards; /* host array of R device pointers, bf16 [M_shard, K] */
+  const void* B;               /* device bf16 [K, N] */
+  void* gathered;              /* device bf16 [R*M_shard, K], written (the gathered A) */
+  void* C;                     /* device bf16 [R*M_shard, N], written */
+  float* C_f32;                /* optional device float [R*M_shard, N], written; NULL = none */
+  tl_signals* signals;         /* arrival flags, >= tl_ag_gemm_num_flags(...) */
+  const tl_signals* src_ready; /* pull mode: source readiness flags (same ids); else NULL */
+  uint32_t epoch;              /* nonzero */
+  uint32_t reserved1;
+  uint64_t timeout_ns;         /* 0 = 1 s */
+  int32_t* trace;              /* optional device int32 [num m tiles * num n tiles]:
+                                  trace[slot] = m_tile * n_tiles + n_tile of the tile
+                                  the consumer ran at schedule slot `slot` */
+} tl_ag_gemm_args;
+
+/* Flags an AG-GEMM call needs: R * ceil(M_shard / rows_per_barrier) (after
+ * replacing 0 by the default); also returns the effective rows_per_barrier. */
+int tl_ag_gemm_num_flags(int R, int M_shard, int K, int rows_per_barrier, int* effective_rpb);
+/* Host copy of the consumer's row-tile order (the swizzle): writes the
+ * ceil(R*M_shard/128) m-tile indices in the order the consumer runs them. */
+tl_status tl_ag_gemm_tile_order(int R, int self_rank, int M_shard, int32_t* m_order, int capacity);
+tl_status tl_ag_gemm(const tl_ag_gemm_args* args, void* stream);
+
+/* ---------------------------------------------------------------- GEMM-ReduceScatter
+ * out[d] = rows [d*M/R, (d+1)*M/R) of S = (((P_0 + P_1) + P_2) + ...), P_r =
+ * A_r . B_r (talk summary, Key Findings and Technical Deep Dive: a persistent
+ * GEMM that notifies each finished partial tile, and a reduce stage that waits
+ * on its own and its peers' tiles).  One launch: every 128 x 256 partial tile
+ * (fp32) is pushed into its receive slot in `workspace` and its flag released;
+ * the R partial tiles of one output tile are produced back to back, rank
+ * (d + 1 + tau + j) mod R at position j of output tile tau, and the CTAs that
+ * computed them each reduce one row slice of the tile after waiting on all R
+ * flags, adding the partials in rank order 0..R-1 in fp32, and write bf16 rows
+ * into out[d].
+ */
+typedef struct tl_gemm_rs_args {
+  int32_t R;                   /* ranks, 1..TL_MAX_RANKS */
+  int32_t M;                   /* rows of every A_r; multiple of R */
+  int32_t K_r;                 /* per-rank contraction, >= 8, multiple of 8 */
+  int32_t N;                   /* >= 8, multiple of 8 */
+  const void* const* A;        /* host array of R device pointers, bf16 [M, K_r] */
+  const void* const* B;        /* host array of R device pointers, bf16 [K_r, N] */
+  void* const* out;            /* host array of R device pointers, bf16 [M/R, N] */
+  void* workspace;             /* device, >= tl_gemm_rs_workspace_size(R, M, N) bytes */
+  size_t workspace_bytes;
+  tl_signals* signals;         /* >= tl_gemm_rs_num_flags(R, M, N) flags */
+  uint32_t epoch;              /* nonzero */
+  uint32_t reserved0;
+  uint64_t timeout_ns;         /* 0 = 1 s */
+} tl_gemm_rs_args;
+
+size_t tl_gemm_rs_workspace_size(int R, int M, int N);
+int tl_gemm_rs_num_flags(int R, int M, int N);
+tl_status tl_gemm_rs(const tl_gemm_rs_args* args, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TILELINK_H */

@@ -1,0 +1,164 @@
+"""AllGather-GEMM through the C ABI against the oracle.
+
+Every call poisons `gathered` and C with NaN first, so a consumer tile that
+reads rows before their arrival flag is set shows up as a mismatch."""
+import numpy as np
+import pytest
+
+import oracle
+from tests.helpers import check_bf16, check_f32, dev_bf16, to_bits, to_f64
+from tile_centric_gemm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    import __graft_entry__
+    __graft_entry__.build()
+    from tile_centric_gemm_gb300 import binding
+    return binding
+
+
+class Epoch:
+    v = 0
+
+    @classmethod
+    def next(cls):
+        cls.v += 1
+        return cls.v
+
+
+def run_ag(B, A, Bm, *, self_rank=0, mode=None, rpb=0, f32=False, notify_ready=True, timeout_ns=0,
+           withhold=None, trace=False):
+    import torch
+    R, (Ms, K), N = len(A), A[0].shape, Bm.shape[1]
+    mode = B.TL_MODE_PUSH if mode is None else mode
+    dA = [dev_bf16(a) for a in A]
+    dB = dev_bf16(Bm)
+    G = torch.full((R * Ms, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C = torch.full((R * Ms, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C32 = torch.full((R * Ms, N), float("nan"), dtype=torch.float32, device="cuda") if f32 else None
+    nflags, eff_rpb = B.tl_ag_gemm_num_flags(R, Ms, K, rpb)
+    sig = B.Signals(nflags)
+    ready = None
+    epoch = Epoch.next()
+    if mode == B.TL_MODE_PULL:
+        ready = B.Signals(nflags)
+        if notify_ready:
+            B.tl_tile_notify(ready, 0, nflags, epoch)
+            if withhold is not None:
+                B.tl_tile_notify(ready, withhold, 1, epoch - 1)
+    Mt, Nt = -(-R * Ms // 128), -(-N // 256)
+    tr = torch.full((Mt * Nt,), -1, dtype=torch.int32, device="cuda") if trace else None
+    B.tl_ag_gemm(dA, dB, G, C, sig, epoch, self_rank=self_rank, C_f32=C32, mode=mode, src_ready=ready,
+                 rows_per_barrier=rpb, timeout_ns=timeout_ns, trace=tr)
+    status = B.tl_query_status(sig)
+    out = dict(G=G, C=C, C32=C32, sig=sig, ready=ready, epoch=epoch, status=status, nflags=nflags,
+               rpb=eff_rpb, trace=tr, Mt=Mt, Nt=Nt)
+    return out
+
+
+def check_all(B, A, Bm, r, self_rank=0):
+    assert r["status"] == (0, -1), r["status"]
+    want = oracle.ag_gemm.ag_gemm(A, Bm)
+    check_bf16(to_f64(r["C"]), want, "C")
+    if r["C32"] is not None:
+        check_f32(to_f64(r["C32"]), want, "C_f32")
+    np.testing.assert_array_equal(to_bits(r["G"]), oracle.ag_gemm.gathered(A))
+    flags = r["sig"].read_flags()
+    assert np.all(flags[:r["nflags"]] == r["epoch"])
+    if r["trace"] is not None:
+        R, Ms, N = len(A), A[0].shape[0], Bm.shape[1]
+        order = oracle.ag_gemm.consumer_order(R, self_rank, Ms, N, 128, 256)
+        want_trace = [m * r["Nt"] + n for (m, n) in order]
+        assert r["trace"].cpu().tolist() == want_trace
+
+
+def test_ag_tiny_bf16_and_fp32(B):
+    c = inputs.CONFIGS["ag_tiny"]
+    A, Bm = inputs.ag_gemm_inputs(c["R"], c["M_shard"], c["K"], c["N"], c["dist"], seed=0)
+    r = run_ag(B, A, Bm, f32=True, trace=True)
+    check_all(B, A, Bm, r)
+
+
+def test_ag_identity_b_returns_gathered_rows_exactly(B):
+    rng = np.random.default_rng(0)
+    A = [inputs.uniform_bf16((128, 256), 10 + r) for r in range(2)]
+    eye = inputs.bf16_bits_from_f32(np.eye(256, dtype=np.float32))
+    r = run_ag(B, A, eye, self_rank=1)
+    assert r["status"] == (0, -1)
+    np.testing.assert_array_equal(to_bits(r["C"]), oracle.ag_gemm.gathered(A))
+
+
+@pytest.mark.parametrize("R,Ms,K,N,self_rank,rpb", [
+    (3, 100, 136, 264, 1, 16),     # tiles straddle shards; K and N tails
+    (5, 77, 64, 8, 4, 0),          # tiny N, ragged everything
+    (1, 300, 520, 512, 0, 0),      # one rank: plain GEMM
+    (4, 256, 1024, 768, 2, 32),    # several tiles per shard, rotation from rank 2
+])
+def test_ag_ragged_shapes(B, R, Ms, K, N, self_rank, rpb):
+    A, Bm = inputs.ag_gemm_inputs(R, Ms, K, N, "normal", seed=R * 100 + Ms)
+    r = run_ag(B, A, Bm, self_rank=self_rank, rpb=rpb, f32=True, trace=True)
+    check_all(B, A, Bm, r, self_rank)
+
+
+def test_ag_pull_mode_matches_push(B):
+    A, Bm = inputs.ag_gemm_inputs(4, 256, 512, 512, "normal", seed=5)
+    r1 = run_ag(B, A, Bm, self_rank=3, mode=B.TL_MODE_PULL, trace=True)
+    check_all(B, A, Bm, r1, 3)
+    r2 = run_ag(B, A, Bm, self_rank=3, mode=B.TL_MODE_PUSH)
+    check_all(B, A, Bm, r2, 3)
+    np.testing.assert_array_equal(to_bits(r1["C"]), to_bits(r2["C"]))
+
+
+def test_ag_pull_missing_source_flag_times_out(B):
+    import torch
+    A, Bm = inputs.ag_gemm_inputs(2, 128, 256, 256, "normal", seed=6)
+    nflags, _ = B.tl_ag_gemm_num_flags(2, 128, 256)
+    r = run_ag(B, A, Bm, mode=B.TL_MODE_PULL, withhold=nflags - 1, timeout_ns=20_000_000)
+    assert r["status"][0] == B.TL_ERR_TIMEOUT
+    # the withheld flag, or a consumer flag that depends on it, is reported
+    assert 0 <= r["status"][1] < nflags
+    # the context stays usable: the same call with every flag set now succeeds
+    r = run_ag(B, A, Bm, mode=B.TL_MODE_PULL)
+    check_all(B, A, Bm, r)
+    assert float(torch.ones(8, device="cuda").sum()) == 8.0
+
+
+def test_ag_repeated_calls_same_signals_advance_epoch(B):
+    import torch
+    A, Bm = inputs.ag_gemm_inputs(2, 256, 256, 256, "normal", seed=8)
+    dA = [dev_bf16(a) for a in A]
+    dB = dev_bf16(Bm)
+    nflags, _ = B.tl_ag_gemm_num_flags(2, 256, 256)
+    sig = B.Signals(nflags)
+    want = oracle.ag_gemm.ag_gemm(A, Bm)
+    for e in range(1, 4):
+        G = torch.full((512, 256), float("nan"), dtype=torch.bfloat16, device="cuda")
+        C = torch.full((512, 256), float("nan"), dtype=torch.bfloat16, device="cuda")
+        B.tl_ag_gemm(dA, dB, G, C, sig, e, self_rank=e % 2)
+        assert B.tl_query_status(sig) == (0, -1)
+        check_bf16(to_f64(C), want, f"C epoch {e}")
+        assert np.all(sig.read_flags() == e)
+
+
+@pytest.mark.slow
+def test_ag_llm_full_size_sampled(B):
+    c = inputs.CONFIGS["ag_llm"]
+    A, Bm = inputs.ag_gemm_inputs(c["R"], c["M_shard"], c["K"], c["N"], c["dist"], seed=0)
+    r = run_ag(B, A, Bm, trace=True)
+    assert r["status"] == (0, -1)
+    np.testing.assert_array_equal(to_bits(r["G"]), oracle.ag_gemm.gathered(A))
+    assert np.all(r["sig"].read_flags() == r["epoch"])
+    rng = np.random.default_rng(1)
+    M, N = c["R"] * c["M_shard"], c["N"]
+    rows = np.concatenate([rng.integers(0, M, 3000), [0, M - 1, M - 1]])
+    cols = np.concatenate([rng.integers(0, N, 3000), [0, 0, N - 1]])
+    want = oracle.ag_gemm.ag_gemm_at(A, Bm, rows, cols)
+    got = to_f64(r["C"])[rows, cols]
+    check_bf16(got, want, "C sampled")
+    # every element: finite (no NaN left from the poison) and the trace is the swizzle
+    assert np.isfinite(to_f64(r["C"])).all()
+    order = oracle.ag_gemm.consumer_order(c["R"], 0, c["M_shard"], N, 128, 256)
+    assert r["trace"].cpu().tolist() == [m * r["Nt"] + n for (m, n) in order]

@@ -1,0 +1,135 @@
+"""GEMM-ReduceScatter through the C ABI against the oracle.
+
+Outputs and the receive workspace are poisoned with NaN before every call, so a
+reduce that read a partial before its flag was released shows up."""
+import numpy as np
+import pytest
+
+import oracle
+from tests.helpers import check_bf16, dev_bf16, to_bits, to_f64
+from tile_centric_gemm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    import __graft_entry__
+    __graft_entry__.build()
+    from tile_centric_gemm_gb300 import binding
+    return binding
+
+
+_epoch = [0]
+
+
+def run_rs(B, A, Bl, *, timeout_ns=0):
+    import torch
+    R = len(A)
+    M, K_r = A[0].shape
+    N = Bl[0].shape[1]
+    dA = [dev_bf16(a) for a in A]
+    dB = [dev_bf16(b) for b in Bl]
+    out = [torch.full((M // R, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    ws_bytes = B.tl_gemm_rs_workspace_size(R, M, N)
+    ws = torch.full((ws_bytes // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    nflags = B.tl_gemm_rs_num_flags(R, M, N)
+    sig = B.Signals(nflags)
+    _epoch[0] += 1
+    B.tl_gemm_rs(dA, dB, out, ws, sig, _epoch[0], timeout_ns=timeout_ns)
+    status = B.tl_query_status(sig)
+    return dict(out=out, sig=sig, status=status, epoch=_epoch[0], nflags=nflags)
+
+
+def check(B, A, Bl, r):
+    assert r["status"] == (0, -1), r["status"]
+    want = oracle.gemm_rs.gemm_rs(A, Bl)
+    for d, (o, w) in enumerate(zip(r["out"], want)):
+        check_bf16(to_f64(o), w, f"out[{d}]")
+    assert np.all(r["sig"].read_flags()[:r["nflags"]] == r["epoch"])
+
+
+@pytest.mark.parametrize("R,M,K_r,N", [
+    (2, 256, 128, 256),
+    (3, 300, 72, 264),      # ragged rows per destination, K and N tails
+    (8, 2048, 256, 512),
+    (1, 200, 64, 136),      # one rank: plain GEMM, bf16 out
+    (5, 5 * 130, 520, 72),  # R that does not divide the tile height
+])
+def test_rs_parity(B, R, M, K_r, N):
+    A, Bl = inputs.gemm_rs_inputs(R, M, K_r, N, seed=R * 7 + M)
+    r = run_rs(B, A, Bl)
+    check(B, A, Bl, r)
+
+
+def test_rs_sums_partials_in_rank_order(B):
+    # P_0 = 2^24, P_1 = 1, P_2 = -2^24 in every element (exact tensor-core products).
+    # In fp32, ((2^24 + 1) + -2^24) = 0 because 2^24 + 1 rounds to 2^24; every
+    # other order gives 1.  The output must be exactly 0.
+    R, M, K_r, N = 3, 384, 8, 256
+    vals = [(2.0 ** 12, 2.0 ** 12), (1.0, 1.0), (-(2.0 ** 12), 2.0 ** 12)]
+    A, Bl = [], []
+    for a, b in vals:
+        Am = np.zeros((M, K_r), np.float32)
+        Am[:, 0] = a
+        Bm = np.zeros((K_r, N), np.float32)
+        Bm[0, :] = b
+        A.append(inputs.bf16_bits_from_f32(Am))
+        Bl.append(inputs.bf16_bits_from_f32(Bm))
+    r = run_rs(B, A, Bl)
+    assert r["status"] == (0, -1)
+    p = [np.float32(a * b) for a, b in vals]
+    want = np.float32(np.float32(p[0] + p[1]) + p[2])
+    assert want == 0.0
+    for o in r["out"]:
+        assert np.all(to_f64(o) == float(want))
+
+
+def test_rs_repeated_calls_reuse_signals(B):
+    import torch
+    R, M, K_r, N = 4, 512, 128, 256
+    A, Bl = inputs.gemm_rs_inputs(R, M, K_r, N, seed=3)
+    dA = [dev_bf16(a) for a in A]
+    dB = [dev_bf16(b) for b in Bl]
+    ws = torch.empty(B.tl_gemm_rs_workspace_size(R, M, N) // 4, dtype=torch.float32, device="cuda")
+    sig = B.Signals(B.tl_gemm_rs_num_flags(R, M, N))
+    want = oracle.gemm_rs.gemm_rs(A, Bl)
+    for e in (1, 2, 3):
+        ws.fill_(float("nan"))
+        out = [torch.full((M // R, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+        B.tl_gemm_rs(dA, dB, out, ws, sig, e)
+        assert B.tl_query_status(sig) == (0, -1)
+        for d in range(R):
+            check_bf16(to_f64(out[d]), want[d], f"epoch {e} out[{d}]")
+
+
+def test_rs_rejects_bad_arguments(B):
+    import torch
+    A, Bl = inputs.gemm_rs_inputs(2, 256, 64, 256, seed=1)
+    dA = [dev_bf16(a) for a in A]
+    dB = [dev_bf16(b) for b in Bl]
+    out = [torch.empty(128, 256, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    ws = torch.empty(16, dtype=torch.float32, device="cuda")   # far too small
+    sig = B.Signals(B.tl_gemm_rs_num_flags(2, 256, 256))
+    with pytest.raises(B.TLError) as e:
+        B.tl_gemm_rs(dA, dB, out, ws, sig, 1)
+    assert e.value.code == B.TL_ERR_INVALID and "workspace" in str(e.value)
+
+
+@pytest.mark.slow
+def test_rs_llm_full_size_sampled(B):
+    c = inputs.CONFIGS["rs_llm"]
+    R, M, K_r, N = c["R"], c["M"], c["K_r"], c["N"]
+    A, Bl = inputs.gemm_rs_inputs(R, M, K_r, N, seed=0)
+    r = run_rs(B, A, Bl)
+    assert r["status"] == (0, -1)
+    assert np.all(r["sig"].read_flags() == r["epoch"])
+    rng = np.random.default_rng(2)
+    rows = np.concatenate([rng.integers(0, M, 2500), [0, M - 1]])
+    cols = np.concatenate([rng.integers(0, N, 2500), [N - 1, 0]])
+    want = oracle.gemm_rs.gemm_rs_at(A, Bl, rows, cols)
+    Md = M // R
+    full = [to_f64(o) for o in r["out"]]
+    got = np.array([full[row // Md][row % Md, col] for row, col in zip(rows, cols)])
+    check_bf16(got, want, "sampled")
+    assert all(np.isfinite(f).all() for f in full)

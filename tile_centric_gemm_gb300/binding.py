@@ -1,0 +1,239 @@
+"""Thin ctypes binding over libtilelink.so with the C ABI's names.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Importing this module loads the library and fails loudly when it is
+missing (build it with ``python -m tile_centric_gemm_gb300.build``); there is
+no fallback.  Tensors are torch tensors on the device the call runs on; the
+stream is torch's current stream unless one is given.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libtilelink.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libtilelink.so not built: {_LIB_PATH} (run python -m tile_centric_gemm_gb300.build)")
+
+lib = ctypes.CDLL(_LIB_PATH)
+
+TL_OK, TL_ERR_INVALID, TL_ERR_CUDA, TL_ERR_TIMEOUT, TL_ERR_UNSUPPORTED, TL_ERR_INTERNAL = range(6)
+TL_MODE_PULL, TL_MODE_PUSH = 0, 1
+STATUS_NAMES = {0: "TL_OK", 1: "TL_ERR_INVALID", 2: "TL_ERR_CUDA", 3: "TL_ERR_TIMEOUT",
+                4: "TL_ERR_UNSUPPORTED", 5: "TL_ERR_INTERNAL"}
+
+# Every symbol the header declares; tests check that the library exports all of them.
+EXPORTED = [
+    "tl_version", "tl_last_error", "tl_signals_create", "tl_signals_destroy", "tl_signals_flags",
+    "tl_signals_reset", "tl_tile_notify", "tl_tile_wait", "tl_query_status",
+    "tl_ag_gemm_num_flags", "tl_ag_gemm_tile_order", "tl_ag_gemm",
+    "tl_gemm_rs_workspace_size", "tl_gemm_rs_num_flags", "tl_gemm_rs",
+]
+
+
+class TLError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_vp = ctypes.c_void_p
+
+
+class tl_ag_gemm_args(ctypes.Structure):
+    _fields_ = [
+        ("R", ctypes.c_int32), ("self_rank", ctypes.c_int32), ("M_shard", ctypes.c_int32),
+        ("K", ctypes.c_int32), ("N", ctypes.c_int32), ("mode", ctypes.c_int32),
+        ("rows_per_barrier", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("A_shards", ctypes.POINTER(_vp)), ("B", _vp), ("gathered", _vp), ("C", _vp), ("C_f32", _vp),
+        ("signals", _vp), ("src_ready", _vp),
+        ("epoch", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
+        ("timeout_ns", ctypes.c_uint64), ("trace", _vp),
+    ]
+
+
+class tl_gemm_rs_args(ctypes.Structure):
+    _fields_ = [
+        ("R", ctypes.c_int32), ("M", ctypes.c_int32), ("K_r", ctypes.c_int32), ("N", ctypes.c_int32),
+        ("A", ctypes.POINTER(_vp)), ("B", ctypes.POINTER(_vp)), ("out", ctypes.POINTER(_vp)),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("signals", _vp),
+        ("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32), ("timeout_ns", ctypes.c_uint64),
+    ]
+
+
+def _decl(name, restype, *argtypes):
+    f = getattr(lib, name)
+    f.restype = restype
+    f.argtypes = list(argtypes)
+    return f
+
+
+_i, _u32, _u64, _sz = ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_size_t
+_decl("tl_version", _i)
+_decl("tl_last_error", ctypes.c_char_p)
+_decl("tl_signals_create", _i, _i, ctypes.POINTER(_vp))
+_decl("tl_signals_destroy", _i, _vp)
+_decl("tl_signals_flags", _i, _vp, ctypes.POINTER(_vp), ctypes.POINTER(_i))
+_decl("tl_signals_reset", _i, _vp, _vp)
+_decl("tl_tile_notify", _i, _vp, _i, _i, _u32, _vp)
+_decl("tl_tile_wait", _i, _vp, _i, _i, _u32, _u64, _vp)
+_decl("tl_query_status", _i, _vp, _vp, ctypes.POINTER(_i), ctypes.POINTER(_i))
+_decl("tl_ag_gemm_num_flags", _i, _i, _i, _i, _i, ctypes.POINTER(_i))
+_decl("tl_ag_gemm_tile_order", _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int32), _i)
+_decl("tl_ag_gemm", _i, ctypes.POINTER(tl_ag_gemm_args), _vp)
+_decl("tl_gemm_rs_workspace_size", _sz, _i, _i, _i)
+_decl("tl_gemm_rs_num_flags", _i, _i, _i, _i)
+_decl("tl_gemm_rs", _i, ctypes.POINTER(tl_gemm_rs_args), _vp)
+
+
+def _check(code):
+    if code != TL_OK:
+        raise TLError(code, lib.tl_last_error().decode(errors="replace"))
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _ptr_array(ts):
+    arr = (_vp * len(ts))(*[t.data_ptr() for t in ts])
+    return arr
+
+
+def tl_version():
+    return lib.tl_version()
+
+
+def tl_last_error():
+    return lib.tl_last_error().decode(errors="replace")
+
+
+class Signals:
+    """Owner of a tl_signals object (device flags + status word)."""
+
+    def __init__(self, num_flags: int):
+        h = _vp()
+        _check(lib.tl_signals_create(int(num_flags), ctypes.byref(h)))
+        self.handle = h
+        self.num_flags = int(num_flags)
+
+    def flags_ptr(self):
+        p, n = _vp(), _i()
+        _check(lib.tl_signals_flags(self.handle, ctypes.byref(p), ctypes.byref(n)))
+        return p.value, n.value
+
+    def flags_tensor(self):
+        """A zero-copy torch uint32-as-int32 CUDA view of the flags (memory owned by the library)."""
+        ptr, n = self.flags_ptr()
+        return _device_view(ptr, n, "<i4")
+
+    def read_flags(self):
+        """The flags as a CPU numpy uint32 array (synchronises the device)."""
+        import numpy as np
+        import torch
+        torch.cuda.synchronize()
+        return self.flags_tensor().cpu().numpy().view(np.uint32)
+
+    def close(self):
+        if self.handle:
+            lib.tl_signals_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _device_view(dev_ptr, n, typestr):
+    """A torch CUDA tensor viewing n elements at dev_ptr (no copy)."""
+    import torch
+
+    class _CAI:
+        def __init__(self):
+            self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (dev_ptr, False),
+                                             "version": 3, "strides": None}
+    return torch.as_tensor(_CAI(), device="cuda")
+
+
+def tl_signals_reset(sig: Signals, stream=None):
+    _check(lib.tl_signals_reset(sig.handle, _stream(stream)))
+
+
+def tl_tile_notify(sig: Signals, first: int, count: int, value: int, stream=None):
+    _check(lib.tl_tile_notify(sig.handle, int(first), int(count), int(value) & 0xFFFFFFFF, _stream(stream)))
+
+
+def tl_tile_wait(sig: Signals, first: int, count: int, value: int, timeout_ns: int = 0, stream=None):
+    _check(lib.tl_tile_wait(sig.handle, int(first), int(count), int(value) & 0xFFFFFFFF, int(timeout_ns),
+                            _stream(stream)))
+
+
+def tl_query_status(sig: Signals, stream=None):
+    """Returns (code, where); code 0 = no device error.  Clears the status word."""
+    code, where = _i(), _i()
+    rc = lib.tl_query_status(sig.handle, _stream(stream), ctypes.byref(code), ctypes.byref(where))
+    if rc not in (TL_OK,) and code.value == 0:
+        _check(rc)
+    return code.value, where.value
+
+
+def tl_ag_gemm_num_flags(R, M_shard, K, rows_per_barrier=0):
+    eff = _i()
+    n = lib.tl_ag_gemm_num_flags(R, M_shard, K, rows_per_barrier, ctypes.byref(eff))
+    return n, eff.value
+
+
+def tl_ag_gemm_tile_order(R, self_rank, M_shard):
+    Mt = -(-R * M_shard // 128)
+    out = (ctypes.c_int32 * Mt)()
+    _check(lib.tl_ag_gemm_tile_order(R, self_rank, M_shard, out, Mt))
+    return list(out)
+
+
+def tl_ag_gemm(A_shards, B, gathered, C, signals: Signals, epoch: int, *, self_rank=0, C_f32=None,
+               mode=TL_MODE_PUSH, src_ready: Signals | None = None, rows_per_barrier=0, timeout_ns=0,
+               trace=None, stream=None):
+    """C = [A_0; ...; A_{R-1}] . B, gathered rows written to `gathered` (see tilelink.h)."""
+    R = len(A_shards)
+    M_shard, K = A_shards[0].shape
+    N = B.shape[1]
+    ptrs = _ptr_array(A_shards)
+    a = tl_ag_gemm_args(R=R, self_rank=self_rank, M_shard=M_shard, K=K, N=N, mode=mode,
+                        rows_per_barrier=rows_per_barrier, reserved0=0,
+                        A_shards=ctypes.cast(ptrs, ctypes.POINTER(_vp)), B=_ptr(B), gathered=_ptr(gathered),
+                        C=_ptr(C), C_f32=_ptr(C_f32), signals=signals.handle,
+                        src_ready=src_ready.handle if src_ready is not None else None,
+                        epoch=int(epoch) & 0xFFFFFFFF, reserved1=0, timeout_ns=int(timeout_ns), trace=_ptr(trace))
+    _check(lib.tl_ag_gemm(ctypes.byref(a), _stream(stream)))
+
+
+def tl_gemm_rs_workspace_size(R, M, N):
+    return int(lib.tl_gemm_rs_workspace_size(R, M, N))
+
+
+def tl_gemm_rs_num_flags(R, M, N):
+    return int(lib.tl_gemm_rs_num_flags(R, M, N))
+
+
+def tl_gemm_rs(A, B, out, workspace, signals: Signals, epoch: int, *, timeout_ns=0, stream=None):
+    """out[d] = rows d of sum_r A_r . B_r in rank order (see tilelink.h)."""
+    R = len(A)
+    M, K_r = A[0].shape
+    N = B[0].shape[1]
+    pa, pb, po = _ptr_array(A), _ptr_array(B), _ptr_array(out)
+    a = tl_gemm_rs_args(R=R, M=M, K_r=K_r, N=N, A=ctypes.cast(pa, ctypes.POINTER(_vp)),
+                        B=ctypes.cast(pb, ctypes.POINTER(_vp)), out=ctypes.cast(po, ctypes.POINTER(_vp)),
+                        workspace=_ptr(workspace), workspace_bytes=workspace.numel() * workspace.element_size(),
+                        signals=signals.handle, epoch=int(epoch) & 0xFFFFFFFF, reserved0=0,
+                        timeout_ns=int(timeout_ns))
+    _check(lib.tl_gemm_rs(ctypes.byref(a), _stream(stream)))

@@ -1,0 +1,399 @@
+// tl_ag_gemm.cu -- AllGather -> GEMM fused at tile granularity in one launch.
+//
+// TileLink talk summary ("TileLink: Generating Efficient Compute-Communication
+// Overlapping Kernels using Tile-Centric Primitives"):
+//  * Key Findings / Experimental Setup & Results -- AllGather-GEMM.
+//  * Technical Deep Dive -- produce_tile_notify / consume_tile_wait signals;
+//    pull mode (readiness barrier + completion barrier) and push mode (one
+//    barrier); a wait's tile id maps affinely to (rank, barrier); consumer
+//    tiles are swizzled into data-arrival order.
+//
+// Every CTA of a persistent, cooperative grid (one CTA per SM) has:
+//   warp 0      TMA producer: acquires the arrival flags of a row tile, then
+//               streams A (gathered rows, or the self shard in place) and B
+//               k-blocks into a 4-stage shared-memory ring.
+//   warp 1      tcgen05 MMA issuer: 128x256x16 bf16 MMAs into one of two TMEM
+//               accumulators.
+//   warps 2-5   epilogue: TMEM -> registers -> bf16 (and fp32) rows of C.
+//   warp 6      copy (AllGather producer): bulk-TMA copies of shard row chunks
+//               into `gathered`, then a release store of the chunk's flag.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "tl_common.cuh"
+#include "tl_internal.h"
+
+namespace tl {
+namespace {
+
+constexpr int AG_MAX_MTILES = 1024;
+constexpr int kWarpCopy = 6;
+constexpr int AG_THREADS = 7 * 32;
+constexpr uint32_t AG_SMEM_COPY = SMEM_GEMM_END;
+constexpr uint32_t AG_SMEM_BARS = AG_SMEM_COPY + COPY_NBUF * COPY_CHUNK;
+constexpr uint32_t AG_SMEM_BYTES = AG_SMEM_BARS + sizeof(Barriers) + 1024;
+
+struct AgParams {
+  CUtensorMap map_g;     // gathered [M, K]
+  CUtensorMap map_self;  // A_self [M_shard, K]
+  CUtensorMap map_b;     // B [K, N]
+  const uint8_t* shard[TL_MAX_RANKS];
+  uint8_t* gathered;
+  uint16_t* C;
+  float* C_f32;
+  uint32_t* flags;
+  const uint32_t* ready;  // pull mode readiness flags, or nullptr
+  uint32_t* status;
+  int32_t* trace;
+  uint64_t timeout_ns;       // bound of each flag wait
+  uint64_t pipe_timeout_ns;  // bound of each pipeline (mbarrier) wait: 2 x flag bound + 1 s
+  int32_t R, self, M_shard, K, N, M;
+  int32_t rpb, bpr, Mt, Nt, KB, num_items, num_work;
+  uint32_t epoch;
+  uint16_t m_order[AG_MAX_MTILES];
+};
+
+// Flag id guarding global row `row` of the gathered matrix (affine tile map).
+__device__ __forceinline__ int row_flag(const AgParams& p, int row) {
+  return (row / p.M_shard) * p.bpr + (row % p.M_shard) / p.rpb;
+}
+
+__global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_constant__ AgParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + AG_SMEM_BARS);
+  const int warp = int(warp_id());
+  const int lane = int(lane_id());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars->tmem_full[a], 1);
+      mbar_init(&bars->tmem_empty[a], kNumEpiWarps);
+    }
+    for (int b = 0; b < COPY_NBUF; ++b) mbar_init(&bars->copy[b], 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpTma && lane == 0) {
+    tma_prefetch_desc(&p.map_g);
+    tma_prefetch_desc(&p.map_self);
+    tma_prefetch_desc(&p.map_b);
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+  volatile uint32_t* abort = &bars->abort;
+
+  if (warp == kWarpTma) {
+    // ---------------------------------------------------------------- TMA producer
+    int s = 0;
+    uint32_t ph = 0;
+    int last_m = -1;
+    for (int w = blockIdx.x; w < p.num_work; w += gridDim.x) {
+      const int n = w % p.Nt;
+      const int m = p.m_order[w / p.Nt];
+      const int row0 = m * BM;
+      const int row1 = min(p.M, row0 + BM) - 1;
+      const bool local = (row0 / p.M_shard == p.self) && (row1 / p.M_shard == p.self);
+      if (!local && m != last_m) {
+        // consume_tile_wait: every flag guarding rows [row0, row1]; lanes poll in parallel
+        const int id0 = row_flag(p, row0), id1 = row_flag(p, row1);
+        for (int id = id0 + lane; id <= id1; id += 32)
+          wait_flag(p.flags + id, p.epoch, p.status, p.timeout_ns, uint32_t(id), TL_ERR_TIMEOUT);
+      }
+      last_m = m;
+      __syncwarp();
+      if (lane == 0) {
+        if (p.trace) p.trace[w] = m * p.Nt + n;
+        if (!local) fence_proxy_async_global();
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort, p.status, p.pipe_timeout_ns, 1)) break;
+          mbar_arrive_expect_tx(&bars->full[s], STAGE_TX);
+          uint8_t* a_dst = smem + SMEM_A + s * A_STAGE_BYTES;
+          uint8_t* b_dst = smem + SMEM_B + s * B_STAGE_BYTES;
+          if (local)
+            tma_load_2d(a_dst, &p.map_self, &bars->full[s], kb * BK, row0 - p.self * p.M_shard);
+          else
+            tma_load_2d(a_dst, &p.map_g, &bars->full[s], kb * BK, row0);
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i)
+            tma_load_2d(b_dst + i * B_BOX_BYTES, &p.map_b, &bars->full[s], n * BN + i * 64, kb * BK);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // warp-uniform exit decision
+      if (__shfl_sync(0xffffffffu, *abort, 0)) break;
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int j = 0;
+      for (int w = blockIdx.x; w < p.num_work && !*abort; w += gridDim.x, ++j) {
+        const int acc = j & 1;
+        const uint32_t acc_ph = uint32_t(j >> 1) & 1u;
+        if (!mbar_wait(&bars->tmem_empty[acc], acc_ph ^ 1u, abort, p.status, p.pipe_timeout_ns, 2)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(&bars->full[s], ph, abort, p.status, p.pipe_timeout_ns, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_kblock(smem, s, d_tmem, kb == 0);
+          tc_commit(&bars->empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&bars->tmem_full[acc]);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
+    // ---------------------------------------------------------------- epilogue
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    int j = 0;
+    for (int w = blockIdx.x; w < p.num_work; w += gridDim.x, ++j) {
+      const int acc = j & 1;
+      const uint32_t acc_ph = uint32_t(j >> 1) & 1u;
+      const int n = w % p.Nt;
+      const int m = p.m_order[w / p.Nt];
+      const bool ok = mbar_wait(&bars->tmem_full[acc], acc_ph, abort, p.status, p.pipe_timeout_ns, 4);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int row = m * BM + wq * 32 + lane;
+      const bool row_ok = row < p.M;
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = n * BN + c * 32;
+        if (col0 >= p.N) break;
+        uint32_t v[32];
+        tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * BN + c * 32), v);
+        tmem_ld_wait();
+        if (row_ok) {
+          uint16_t* crow = p.C + size_t(row) * p.N + col0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (col0 + g * 8 < p.N) {
+              const float* f = reinterpret_cast<const float*>(v + g * 8);
+              st_global_v4(crow + g * 8, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                           pack_bf16x2(f[6], f[7]));
+            }
+          }
+          if (p.C_f32) {
+            float* frow = p.C_f32 + size_t(row) * p.N + col0;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              if (col0 + g * 4 < p.N) {
+                const float* f = reinterpret_cast<const float*>(v + g * 4);
+                st_global_cg_v4f(frow + g * 4, f[0], f[1], f[2], f[3]);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tmem_empty[acc]);
+    }
+  } else if (warp == kWarpCopy) {
+    // ---------------------------------------------------------------- AllGather producer
+    if (lane == 0) {
+      uint8_t* stage = smem + AG_SMEM_COPY;
+      uint32_t seq = 0;  // chunks this CTA has loaded: buffer seq % NBUF, parity (seq / NBUF) & 1
+      bool dead = false;
+      for (int it = blockIdx.x; it < p.num_items && !dead; it += gridDim.x) {
+        // copy order: shards self+1, ..., self+R-1, then self; chunks ascending
+        const int jj = it / p.bpr, b = it % p.bpr;
+        const int r = (p.self + 1 + jj) % p.R;
+        const int lo = b * p.rpb;
+        const int rows = min(p.rpb, p.M_shard - lo);
+        const uint8_t* src = p.shard[r] + size_t(lo) * p.K * 2;
+        uint8_t* dst = p.gathered + (size_t(r) * p.M_shard + lo) * size_t(p.K) * 2;
+        const uint32_t bytes = uint32_t(rows) * uint32_t(p.K) * 2u;
+        const int flag_id = r * p.bpr + b;
+        // pull mode: the source publishes readiness first (second barrier of the pull protocol)
+        if (p.ready) wait_flag(p.ready + flag_id, p.epoch, p.status, p.timeout_ns, uint32_t(flag_id), TL_ERR_TIMEOUT);
+        const int nch = int((bytes + COPY_CHUNK - 1) / COPY_CHUNK);
+        int issued = 0, stored = 0;
+        while (stored < nch) {
+          while (issued < nch && issued - stored < COPY_NBUF) {
+            const uint32_t q = seq + uint32_t(issued);
+            const int buf = int(q % COPY_NBUF);
+            // the store that last read `buf` (chunk q - NBUF) must have finished reading it
+            bulk_wait_read_dyn(stored - issued + COPY_NBUF - 1);
+            const uint32_t off = uint32_t(issued) * COPY_CHUNK;
+            const uint32_t sz = min(COPY_CHUNK, bytes - off);
+            mbar_arrive_expect_tx(&bars->copy[buf], sz);
+            bulk_g2s(stage + buf * COPY_CHUNK, src + off, sz, &bars->copy[buf]);
+            ++issued;
+          }
+          const uint32_t q = seq + uint32_t(stored);
+          const int buf = int(q % COPY_NBUF);
+          if (!mbar_wait(&bars->copy[buf], (q / COPY_NBUF) & 1u, abort, p.status, p.pipe_timeout_ns, 5)) {
+            dead = true;
+            break;
+          }
+          const uint32_t off = uint32_t(stored) * COPY_CHUNK;
+          bulk_s2g(dst + off, stage + buf * COPY_CHUNK, min(COPY_CHUNK, bytes - off));
+          bulk_commit();
+          ++stored;
+        }
+        seq += uint32_t(nch);
+        // produce_tile_notify: writes complete -> order with the generic proxy -> release
+        bulk_wait<0>();
+        if (dead) break;
+        fence_proxy_async_global();
+        st_release(p.flags + flag_id, p.epoch);
+      }
+      bulk_wait<0>();
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort) {
+    // a pipeline wait gave up: let any TMA load still in flight land before the CTA exits
+    const uint64_t t0 = now_ns();
+    while (now_ns() - t0 < 50000) {
+    }
+  }
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+int default_rpb(int K, int M_shard) {
+  int rpb = std::max(1, int(32768 / (size_t(K) * 2)));
+  return std::min(rpb, M_shard);
+}
+
+}  // namespace
+}  // namespace tl
+
+extern "C" int tl_ag_gemm_num_flags(int R, int M_shard, int K, int rows_per_barrier, int* effective_rpb) {
+  if (R < 1 || M_shard < 1 || K < 1) return -1;
+  int rpb = rows_per_barrier > 0 ? std::min(rows_per_barrier, M_shard) : tl::default_rpb(K, M_shard);
+  if (effective_rpb) *effective_rpb = rpb;
+  return R * tl::cdiv(M_shard, rpb);
+}
+
+extern "C" tl_status tl_ag_gemm_tile_order(int R, int self_rank, int M_shard, int32_t* m_order, int capacity) {
+  if (R < 1 || R > TL_MAX_RANKS || self_rank < 0 || self_rank >= R || M_shard < 1 || !m_order)
+    return tl::fail(TL_ERR_INVALID, "tl_ag_gemm_tile_order: bad arguments");
+  const long long M = (long long)R * M_shard;
+  const int Mt = int((M + tl::BM - 1) / tl::BM);
+  if (capacity < Mt) return tl::fail(TL_ERR_INVALID, "tl_ag_gemm_tile_order: capacity %d < %d tiles", capacity, Mt);
+  // arrival position of shard r is (r - self) mod R; a row tile takes the latest
+  // position among the shards its rows come from; stable by tile index
+  std::vector<std::pair<int, int>> key(Mt);
+  for (int m = 0; m < Mt; ++m) {
+    const long long r0 = (long long)m * tl::BM, r1 = std::min(M, r0 + tl::BM) - 1;
+    int best = 0;
+    for (long long r = r0 / M_shard; r <= r1 / M_shard; ++r) best = std::max(best, int((r - self_rank + R) % R));
+    key[m] = {best, m};
+  }
+  std::sort(key.begin(), key.end());
+  for (int i = 0; i < Mt; ++i) m_order[i] = key[i].second;
+  return TL_OK;
+}
+
+extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
+  using namespace tl;
+  if (!a) return fail(TL_ERR_INVALID, "tl_ag_gemm: NULL args");
+  if (a->R < 1 || a->R > TL_MAX_RANKS) return fail(TL_ERR_INVALID, "tl_ag_gemm: R=%d outside 1..%d", a->R, TL_MAX_RANKS);
+  if (a->self_rank < 0 || a->self_rank >= a->R) return fail(TL_ERR_INVALID, "tl_ag_gemm: self_rank %d", a->self_rank);
+  if (a->M_shard < 1 || a->K < 1 || a->N < 1) return fail(TL_ERR_INVALID, "tl_ag_gemm: empty shape");
+  if (a->K % 8 || a->N % 8)
+    return fail(TL_ERR_UNSUPPORTED, "tl_ag_gemm: K (%d) and N (%d) must be multiples of 8", a->K, a->N);
+  if (a->mode != TL_MODE_PULL && a->mode != TL_MODE_PUSH) return fail(TL_ERR_INVALID, "tl_ag_gemm: mode %d", a->mode);
+  if (a->mode == TL_MODE_PULL && !a->src_ready)
+    return fail(TL_ERR_INVALID, "tl_ag_gemm: pull mode needs src_ready flags");
+  if (!a->A_shards || !a->B || !a->gathered || !a->C || !a->signals)
+    return fail(TL_ERR_INVALID, "tl_ag_gemm: NULL pointer argument");
+  if (a->epoch == 0) return fail(TL_ERR_INVALID, "tl_ag_gemm: epoch must be nonzero");
+  for (int r = 0; r < a->R; ++r)
+    if (!a->A_shards[r] || !aligned16(a->A_shards[r])) return fail(TL_ERR_INVALID, "tl_ag_gemm: shard %d pointer", r);
+  if (!aligned16(a->B) || !aligned16(a->gathered) || !aligned16(a->C) || (a->C_f32 && !aligned16(a->C_f32)))
+    return fail(TL_ERR_INVALID, "tl_ag_gemm: pointers must be 16-byte aligned");
+  const long long M = (long long)a->R * a->M_shard;
+  const int Mt = int((M + BM - 1) / BM);
+  if (M > (1ll << 30) || Mt > AG_MAX_MTILES)
+    return fail(TL_ERR_UNSUPPORTED, "tl_ag_gemm: %lld rows exceeds %d row tiles", M, AG_MAX_MTILES);
+  int rpb = 0;
+  const int nflags = tl_ag_gemm_num_flags(a->R, a->M_shard, a->K, a->rows_per_barrier, &rpb);
+  if (rpb < 1 || size_t(rpb) * a->K * 2 > (size_t(1) << 31))
+    return fail(TL_ERR_INVALID, "tl_ag_gemm: rows_per_barrier %d", rpb);
+  if (a->signals->num_flags < nflags)
+    return fail(TL_ERR_INVALID, "tl_ag_gemm: signals hold %d flags, need %d", a->signals->num_flags, nflags);
+  if (a->mode == TL_MODE_PULL && a->src_ready->num_flags < nflags)
+    return fail(TL_ERR_INVALID, "tl_ag_gemm: src_ready holds %d flags, need %d", a->src_ready->num_flags, nflags);
+  DeviceInfo di{};
+  if (tl_status s = device_info(&di)) return s;
+  if (a->signals->device != di.device) return fail(TL_ERR_INVALID, "tl_ag_gemm: signals belong to another device");
+
+  AgParams* p = new (std::nothrow) AgParams;
+  if (!p) return fail(TL_ERR_INTERNAL, "out of host memory");
+  std::memset(p, 0, sizeof(AgParams));
+  tl_status st = TL_OK;
+  do {
+    if ((st = make_map_bf16(&p->map_g, a->gathered, M, a->K, size_t(a->K) * 2, BM, BK))) break;
+    if ((st = make_map_bf16(&p->map_self, a->A_shards[a->self_rank], a->M_shard, a->K, size_t(a->K) * 2, BM, BK)))
+      break;
+    if ((st = make_map_bf16(&p->map_b, a->B, a->K, a->N, size_t(a->N) * 2, BK, 64))) break;
+    for (int r = 0; r < a->R; ++r) p->shard[r] = static_cast<const uint8_t*>(a->A_shards[r]);
+    p->gathered = static_cast<uint8_t*>(a->gathered);
+    p->C = static_cast<uint16_t*>(a->C);
+    p->C_f32 = a->C_f32;
+    p->flags = a->signals->flags;
+    p->ready = a->mode == TL_MODE_PULL ? a->src_ready->flags : nullptr;
+    p->status = a->signals->status;
+    p->trace = a->trace;
+    p->timeout_ns = a->timeout_ns ? a->timeout_ns : kDefaultTimeoutNs;
+    p->pipe_timeout_ns = 2 * p->timeout_ns + 1000000000ull;
+    p->R = a->R;
+    p->self = a->self_rank;
+    p->M_shard = a->M_shard;
+    p->K = a->K;
+    p->N = a->N;
+    p->M = int(M);
+    p->rpb = rpb;
+    p->bpr = cdiv(a->M_shard, rpb);
+    p->Mt = Mt;
+    p->Nt = cdiv(a->N, BN);
+    p->KB = cdiv(a->K, BK);
+    p->num_items = a->R * p->bpr;
+    p->num_work = Mt * p->Nt;
+    p->epoch = a->epoch;
+    int32_t order[AG_MAX_MTILES];
+    if ((st = tl_ag_gemm_tile_order(a->R, a->self_rank, a->M_shard, order, AG_MAX_MTILES))) break;
+    for (int i = 0; i < Mt; ++i) p->m_order[i] = uint16_t(order[i]);
+    const int grid = std::max(1, std::min(di.sm_count, std::max(p->num_work, p->num_items)));
+    void* args[] = {p};
+    st = launch_coop(reinterpret_cast<const void*>(&ag_gemm_kernel), grid, AG_THREADS, AG_SMEM_BYTES,
+                     (cudaStream_t)stream, args);
+  } while (false);
+  delete p;
+  return st;
+}

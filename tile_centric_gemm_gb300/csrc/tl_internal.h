@@ -1,0 +1,50 @@
+// tl_internal.h -- host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tilelink.h"
+
+struct tl_signals {
+  int device;
+  int num_flags;
+  uint32_t* flags;   // device, num_flags words
+  uint32_t* status;  // device, 4 words: code, where, seen, expected
+};
+
+namespace tl {
+
+constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // 1 s
+
+// Record a message for tl_last_error() and return `code`.
+tl_status fail(tl_status code, const char* fmt, ...);
+// Map a CUDA runtime error to TL_ERR_CUDA with a message; TL_OK on success.
+tl_status cuda_ok(cudaError_t e, const char* what);
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int max_smem_optin;
+  int cc_major;
+  int cc_minor;
+  int coop_launch;
+};
+tl_status device_info(DeviceInfo* out);
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with the given row
+// pitch; box = box_rows x box_cols elements; 128-byte swizzle; out-of-range
+// elements read as zero.
+tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint64_t row_pitch_bytes, uint32_t box_rows, uint32_t box_cols);
+
+// Launch with every CTA co-resident (cooperative launch); fails instead of
+// launching when the grid cannot be resident at once.
+tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cudaStream_t st, void** args);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace tl
