@@ -1,0 +1,369 @@
+#!/usr/bin/env python3
+"""Benchmark of the tile-centric overlap path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic inputs:
+  * AllGather-GEMM, R=8 emulated ranks, A_r [1024, 4096] ~ N(0,1),
+    B [4096, 1792] ~ N(0, 0.02) -> C [8192, 1792]     (tl_ag_gemm)
+  * GEMM-ReduceScatter, R=8, A_r [8192, 1792], B_r [1792, 4096]
+    -> 8 row shards [1024, 4096]                      (tl_gemm_rs)
+Metric: whole-job TFLOP/s = algorithmic FLOPs of the step / device time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With N > 1 (launched by torchrun) every rank runs the same step on its own GPU
+(independent replicas, weak scaling); rank 0 prints the JSON line with the
+max-over-ranks time.  ``--impl reference`` times the CPU oracle on a bounded
+sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+AG = dict(R=8, M_shard=1024, K=4096, N=1792)
+RS = dict(R=8, M=8192, K_r=1792, N=4096)
+AG_FLOPS = 2 * AG["R"] * AG["M_shard"] * AG["N"] * AG["K"]
+RS_FLOPS = 2 * RS["R"] * RS["M"] * RS["N"] * RS["K_r"]
+METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s on 1 GB300"
+WORKLOAD = ("AG-GEMM R=8 [8192x4096]x[4096x1792] + GEMM-RS R=8 8x[8192x1792]x[1792x4096] "
+            "(TP MLP up/down projection, emulated ranks)")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 100 ms, timestamped."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                pass
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "timed"
+        if len(inside) < 3:
+            inside = [s for s in self.samples if t0 - 1.0 <= s[0] <= t1 + 0.2]
+            window = "timed+1s before"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i, v in enumerate(s[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+class OracleSample:
+    """The oracle, as it stands, on a row sample of the same workload: the AG-GEMM
+    shards cut to `rows` rows each and the GEMM-RS operands cut to R*rows rows."""
+
+    def __init__(self):
+        from tile_centric_gemm_gb300 import inputs
+        self.A, self.B = inputs.ag_gemm_inputs(AG["R"], AG["M_shard"], AG["K"], AG["N"], "normal", seed=0)
+        self.Ar, self.Br = inputs.gemm_rs_inputs(RS["R"], RS["M"], RS["K_r"], RS["N"], seed=0)
+        self.rows = 16
+
+    def flops(self):
+        return 2 * AG["R"] * self.rows * AG["N"] * AG["K"] + 2 * RS["R"] * (RS["R"] * self.rows) * RS["N"] * RS["K_r"]
+
+    def describe(self):
+        return (f"AG-GEMM with {self.rows} of {AG['M_shard']} rows per shard + GEMM-RS with "
+                f"{RS['R'] * self.rows} of {RS['M']} rows ({self.flops() / 1e9:.1f} GFLOP; float64 numpy oracle)")
+
+    def step(self):
+        import oracle
+        t0 = time.perf_counter()
+        oracle.ag_gemm.ag_gemm([a[:self.rows] for a in self.A], self.B)
+        oracle.gemm_rs.gemm_rs([a[:RS["R"] * self.rows] for a in self.Ar], self.Br)
+        return time.perf_counter() - t0
+
+    def size_to(self, seconds):
+        """Grow the sample until one step takes about `seconds` (at most the full shard)."""
+        while True:
+            dt = self.step()
+            if dt >= 0.5 * seconds or self.rows >= AG["M_shard"]:
+                return dt
+            self.rows = min(AG["M_shard"], self.rows * max(2, int(seconds / max(dt, 1e-3))))
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def time_oracle(budget_s=12.0):
+    """(TFLOP/s, seconds, sample description) of the oracle on a ~budget_s sample."""
+    o = OracleSample()
+    o.size_to(budget_s)
+    dt = o.step()
+    return o.flops() / dt / 1e12, dt, o.describe()
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle timed step by step on a bounded sample."""
+    if rank != 0:
+        return
+    o = OracleSample()
+    o.size_to(1.0)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = o.step()
+        if i >= args.warmup:
+            times.append(dt)
+    t = statistics.mean(times)
+    value = o.flops() / t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": o.describe()},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": o.describe()},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+class Workload:
+    def __init__(self, B, torch):
+        from tile_centric_gemm_gb300 import inputs
+        self.B, self.torch = B, torch
+        dev = "cuda"
+        A, Bm = inputs.ag_gemm_inputs(AG["R"], AG["M_shard"], AG["K"], AG["N"], "normal", seed=0)
+        Ar, Br = inputs.gemm_rs_inputs(RS["R"], RS["M"], RS["K_r"], RS["N"], seed=0)
+        tb = inputs.to_torch_bf16
+        # host (pinned) copies for the end-to-end measurement
+        self.h_ag = [tb(a).pin_memory() for a in A] + [tb(Bm).pin_memory()]
+        self.h_rs = [tb(a).pin_memory() for a in Ar] + [tb(b).pin_memory() for b in Br]
+        self.d_ag = [t.to(dev) for t in self.h_ag]
+        self.d_rs = [t.to(dev) for t in self.h_rs]
+        R = AG["R"]
+        M = R * AG["M_shard"]
+        self.G = torch.empty(M, AG["K"], dtype=torch.bfloat16, device=dev)
+        self.C = torch.empty(M, AG["N"], dtype=torch.bfloat16, device=dev)
+        nf, _ = B.tl_ag_gemm_num_flags(R, AG["M_shard"], AG["K"])
+        self.sig_ag = B.Signals(nf)
+        Rr = RS["R"]
+        self.out = [torch.empty(RS["M"] // Rr, RS["N"], dtype=torch.bfloat16, device=dev) for _ in range(Rr)]
+        self.ws = torch.empty(B.tl_gemm_rs_workspace_size(Rr, RS["M"], RS["N"]) // 4, dtype=torch.float32,
+                              device=dev)
+        self.sig_rs = B.Signals(B.tl_gemm_rs_num_flags(Rr, RS["M"], RS["N"]))
+        self.h_C = torch.empty_like(self.C, device="cpu").pin_memory()
+        self.h_out = [torch.empty_like(o, device="cpu").pin_memory() for o in self.out]
+        self.epoch = 0
+        self.launches_per_step = 2
+
+    def ag(self):
+        self.epoch += 1
+        R = AG["R"]
+        self.B.tl_ag_gemm(self.d_ag[:R], self.d_ag[R], self.G, self.C, self.sig_ag, self.epoch)
+
+    def rs(self):
+        self.epoch += 1
+        R = RS["R"]
+        self.B.tl_gemm_rs(self.d_rs[:R], self.d_rs[R:], self.out, self.ws, self.sig_rs, self.epoch)
+
+    def h2d(self):
+        for h, d in zip(self.h_ag + self.h_rs, self.d_ag + self.d_rs):
+            d.copy_(h, non_blocking=True)
+
+    def d2h(self):
+        self.h_C.copy_(self.C, non_blocking=True)
+        for h, d in zip(self.h_out, self.out):
+            h.copy_(d, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.h_ag + self.h_rs)
+
+    def d2h_bytes(self):
+        return self.h_C.numel() * 2 + sum(t.numel() * 2 for t in self.h_out)
+
+    def check_status(self):
+        for s in (self.sig_ag, self.sig_rs):
+            code, where = self.B.tl_query_status(s)
+            if code:
+                raise RuntimeError(f"device error {code} at {where}")
+
+
+def main():
+    args = parse()
+    world, rank, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from tile_centric_gemm_gb300 import binding as B
+
+    torch.cuda.set_device(local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+
+    def barrier():
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+
+    peaks, peak_src = load_peaks()
+    wl = Workload(B, torch)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        wl.ag()
+        wl.rs()
+    wl.check_status()
+
+    sampler = ClockSampler(local_rank)
+    time.sleep(0.3)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier()
+    t_host0 = time.time()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        wl.ag()
+        ev[i][1].record(stream)
+        wl.rs()
+        ev[i][2].record(stream)
+    end.record(stream)
+    barrier()
+    t_host1 = time.time()
+    sampler.stop()
+    wl.check_status()
+    total_ms = start.elapsed_time(end)
+    ag_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    rs_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    ms_per_step = total_ms / K
+    if pg:
+        t = torch.tensor([ms_per_step])
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_per_step = float(t[0])
+    step_flops = AG_FLOPS + RS_FLOPS
+    value = world * step_flops / (ms_per_step * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: H2D inputs, both calls, D2H outputs
+    E = max(3, args.e2e_steps)
+    for _ in range(2):
+        wl.h2d(); wl.ag(); wl.rs(); wl.d2h()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        wl.h2d()
+        wl.ag()
+        wl.rs()
+        wl.d2h()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / E
+    if pg:
+        t = torch.tensor([e2e_ms])
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    wl.check_status()
+
+    rs_avg = statistics.mean(rs_ms)
+    ag_avg = statistics.mean(ag_ms)
+    achieved = RS_FLOPS / (rs_avg * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    clocks = sampler.summary(t_host0, t_host1)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "ag": AG, "rs": RS, "step_gflop": step_flops / 1e9,
+                   "l2": "inputs larger than L2: a step touches ~1.7 GB (129 MB L2); no flush",
+                   "parallelism": f"{world} independent replica(s), 8 emulated ranks each"},
+        "breakdown": {"ag_gemm_us": ag_avg * 1e3, "ag_gemm_tflops": AG_FLOPS / (ag_avg * 1e-3) / 1e12,
+                      "gemm_rs_us": rs_avg * 1e3, "gemm_rs_tflops": achieved},
+        "roofline": {"bound": "tensor", "kernel": "gemm_rs_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
+                     "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),
+                     "traffic": None},
+        "clocks": clocks,
+        "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes()},
+        "gpu_launches": K * wl.launches_per_step,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, dt, sample = time_oracle()
+        line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                                "sample": sample, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -162,3 +162,18 @@ def test_ag_llm_full_size_sampled(B):
     assert np.isfinite(to_f64(r["C"])).all()
     order = oracle.ag_gemm.consumer_order(c["R"], 0, c["M_shard"], N, 128, 256)
     assert r["trace"].cpu().tolist() == [m * r["Nt"] + n for (m, n) in order]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("R,M", [(4, 4096), (2, 1024), (8, 16384)])
+def test_ag_sweep_points(B, R, M):
+    # AG sweep workload: K=8192, N=1024, activations N(0,1), weights N(0,0.02)
+    A, Bm = inputs.ag_gemm_inputs(R, M // R, 8192, 1024, "normal", seed=M + R)
+    r = run_ag(B, A, Bm, self_rank=R - 1, trace=True)
+    assert r["status"] == (0, -1)
+    np.testing.assert_array_equal(to_bits(r["G"]), oracle.ag_gemm.gathered(A))
+    rng = np.random.default_rng(R)
+    rows, cols = rng.integers(0, M, 2000), rng.integers(0, 1024, 2000)
+    check_bf16(to_f64(r["C"])[rows, cols], oracle.ag_gemm.ag_gemm_at(A, Bm, rows, cols), "C sampled")
+    order = oracle.ag_gemm.consumer_order(R, R - 1, M // R, 1024, 128, 256)
+    assert r["trace"].cpu().tolist() == [m * r["Nt"] + n for (m, n) in order]

@@ -133,3 +133,18 @@ def test_rs_llm_full_size_sampled(B):
     got = np.array([full[row // Md][row % Md, col] for row, col in zip(rows, cols)])
     check_bf16(got, want, "sampled")
     assert all(np.isfinite(f).all() for f in full)
+
+
+@pytest.mark.slow
+def test_rs_mid_size_sampled(B):
+    # R=8, M=4096, K_r=1792, N=4096: 0.8 GB on the device, inputs larger than L2
+    R, M, K_r, N = 8, 4096, 1792, 4096
+    A, Bl = inputs.gemm_rs_inputs(R, M, K_r, N, seed=11)
+    r = run_rs(B, A, Bl)
+    assert r["status"] == (0, -1)
+    rng = np.random.default_rng(3)
+    rows, cols = rng.integers(0, M, 1500), rng.integers(0, N, 1500)
+    want = oracle.gemm_rs.gemm_rs_at(A, Bl, rows, cols)
+    Md = M // R
+    full = [to_f64(o) for o in r["out"]]
+    check_bf16(np.array([full[row // Md][row % Md, col] for row, col in zip(rows, cols)]), want, "sampled")
