@@ -181,6 +181,34 @@ size_t tl_gemm_rs_workspace_size(int R, int M, int N);
 int tl_gemm_rs_num_flags(int R, int M, int N);
 tl_status tl_gemm_rs(const tl_gemm_rs_args* args, void* stream);
 
+/* ---------------------------------------------------------------- GEMM-RS without allocation
+ * The talk summary has no counterpart of this entry point.  It exists for
+ * callers that cannot allocate device memory -- a runtime whose allocator owns
+ * the device and forbids cudaMalloc on its hot path, code that runs before any
+ * allocator exists, or an embedding that may only pass the buffers it already
+ * holds.  Same operation, arguments and kernel as tl_gemm_rs, except:
+ *  - args->workspace, args->workspace_bytes and args->signals must be NULL/0.
+ *    The flags, a status word and the fp32 receive slots live in one static
+ *    device array of TL_GEMM_RS_NOALLOC_MAX_BYTES (64 MiB), which every GPU
+ *    that loads the library holds until the process exits.
+ *  - A problem that needs more scratch than that fails with
+ *    TL_ERR_UNSUPPORTED and launches nothing.  It needs
+ *    roundup256(256 + 4*F) + F * 128 KiB bytes, F = tl_gemm_rs_num_flags(R, M, N).
+ *  - dev_status: optional caller-owned device pointer to 4 uint32 words
+ *    (16-byte aligned) where the kernel records its first device-side error
+ *    (code, where, value seen, value expected); the caller zeroes it.  With
+ *    NULL, device-side timeouts go unreported.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call shares the array and it keeps the last call's contents: each
+ *    call clears the flags (a stream-ordered memset) before its launch.  Calls
+ *    that overlap on the GPU (different streams without ordering) race.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define TL_GEMM_RS_NOALLOC_MAX_BYTES (64ull << 20)
+tl_status tl_gemm_rs_noalloc(const tl_gemm_rs_args* args, uint32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,7 @@ EXPORTED = [
     "tl_version", "tl_last_error", "tl_signals_create", "tl_signals_destroy", "tl_signals_flags",
     "tl_signals_reset", "tl_tile_notify", "tl_tile_wait", "tl_query_status",
     "tl_ag_gemm_num_flags", "tl_ag_gemm_tile_order", "tl_ag_gemm",
-    "tl_gemm_rs_workspace_size", "tl_gemm_rs_num_flags", "tl_gemm_rs",
+    "tl_gemm_rs_workspace_size", "tl_gemm_rs_num_flags", "tl_gemm_rs", "tl_gemm_rs_noalloc",
 ]
 
 
@@ -85,6 +85,7 @@ _decl("tl_ag_gemm", _i, ctypes.POINTER(tl_ag_gemm_args), _vp)
 _decl("tl_gemm_rs_workspace_size", _sz, _i, _i, _i)
 _decl("tl_gemm_rs_num_flags", _i, _i, _i, _i)
 _decl("tl_gemm_rs", _i, ctypes.POINTER(tl_gemm_rs_args), _vp)
+_decl("tl_gemm_rs_noalloc", _i, ctypes.POINTER(tl_gemm_rs_args), _vp, _vp)
 
 
 def _check(code):
@@ -237,3 +238,18 @@ def tl_gemm_rs(A, B, out, workspace, signals: Signals, epoch: int, *, timeout_ns
                         signals=signals.handle, epoch=int(epoch) & 0xFFFFFFFF, reserved0=0,
                         timeout_ns=int(timeout_ns))
     _check(lib.tl_gemm_rs(ctypes.byref(a), _stream(stream)))
+
+
+def tl_gemm_rs_noalloc(A, B, out, epoch: int, *, dev_status=None, timeout_ns=0, stream=None):
+    """GEMM-RS for callers that cannot allocate device memory: the library's
+    static device scratch replaces the workspace and the signals object.
+    dev_status: optional int32 CUDA tensor of 4 words that receives device errors."""
+    R = len(A)
+    M, K_r = A[0].shape
+    N = B[0].shape[1]
+    pa, pb, po = _ptr_array(A), _ptr_array(B), _ptr_array(out)
+    a = tl_gemm_rs_args(R=R, M=M, K_r=K_r, N=N, A=ctypes.cast(pa, ctypes.POINTER(_vp)),
+                        B=ctypes.cast(pb, ctypes.POINTER(_vp)), out=ctypes.cast(po, ctypes.POINTER(_vp)),
+                        workspace=None, workspace_bytes=0, signals=None, epoch=int(epoch) & 0xFFFFFFFF,
+                        reserved0=0, timeout_ns=int(timeout_ns))
+    _check(lib.tl_gemm_rs_noalloc(ctypes.byref(a), _ptr(dev_status), _stream(stream)))

@@ -23,6 +23,7 @@
 //      out[d].
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "tl_common.cuh"
@@ -359,3 +360,126 @@ extern "C" tl_status tl_gemm_rs(const tl_gemm_rs_args* a, void* stream) {
   delete p;
   return st;
 }
+
+// ---------------------------------------------------------------- GEMM-RS without allocation
+// Some callers cannot allocate device memory: code that runs while a custom
+// allocator owns the device, inside a runtime that forbids cudaMalloc on its
+// hot path, or before any allocator exists.  tl_gemm_rs_noalloc serves them
+// with the GEMM-RS kernel above, taking its scratch (flags, status word and
+// fp32 receive slots) from a fixed file-scope device array instead of a
+// caller-provided workspace and a tl_signals object.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;  // TL_GEMM_RS_NOALLOC_MAX_BYTES
+constexpr size_t kNoAllocHeader = 256;                       // status words, then flags
+
+static_assert(kNoAllocScratchBytes == size_t(TL_GEMM_RS_NOALLOC_MAX_BYTES), "header and library disagree");
+
+// Held by every GPU that loads this library, until the process exits.
+static __device__ __align__(256) uint8_t g_rs_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch array, looked up once per device with that
+// device current.  In host code the array's name is only a host-side stand-in.
+tl_status noalloc_scratch(int dev, uint8_t** out) {
+  static std::mutex mu;
+  static uint8_t* addr[64] = {};
+  if (dev < 0 || dev >= 64) return tl::fail(TL_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_rs_noalloc_scratch);
+    if (e != cudaSuccess) return tl::cuda_ok(e, "cudaGetSymbolAddress(GEMM-RS scratch)");
+    addr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = addr[dev];
+  return TL_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+namespace {
+size_t noalloc_scratch_needed(int R, int M, int N);
+}  // namespace
+
+extern "C" tl_status tl_gemm_rs_noalloc(const tl_gemm_rs_args* a, uint32_t* dev_status, void* stream) {
+  using namespace tl;
+  if (!a) return fail(TL_ERR_INVALID, "tl_gemm_rs_noalloc: NULL args");
+  if (a->workspace || a->workspace_bytes || a->signals)
+    return fail(TL_ERR_INVALID, "tl_gemm_rs_noalloc: workspace and signals must be NULL (the scratch is static)");
+  if (a->R < 1 || a->R > RS_MAX_RANKS)
+    return fail(a->R > RS_MAX_RANKS ? TL_ERR_UNSUPPORTED : TL_ERR_INVALID, "tl_gemm_rs_noalloc: R=%d outside 1..%d",
+                a->R, RS_MAX_RANKS);
+  if (a->M < a->R || a->M % a->R)
+    return fail(TL_ERR_INVALID, "tl_gemm_rs_noalloc: M=%d must be a positive multiple of R", a->M);
+  if (a->K_r < 1 || a->N < 1) return fail(TL_ERR_INVALID, "tl_gemm_rs_noalloc: empty shape");
+  if (a->K_r % 8 || a->N % 8)
+    return fail(TL_ERR_UNSUPPORTED, "tl_gemm_rs_noalloc: K_r (%d) and N (%d) must be multiples of 8", a->K_r, a->N);
+  if (!a->A || !a->B || !a->out) return fail(TL_ERR_INVALID, "tl_gemm_rs_noalloc: NULL pointer argument");
+  if (a->epoch == 0) return fail(TL_ERR_INVALID, "tl_gemm_rs_noalloc: epoch must be nonzero");
+  if (dev_status && !aligned16(dev_status)) return fail(TL_ERR_INVALID, "tl_gemm_rs_noalloc: dev_status alignment");
+  for (int r = 0; r < a->R; ++r) {
+    if (!a->A[r] || !a->B[r] || !a->out[r] || !aligned16(a->A[r]) || !aligned16(a->B[r]) || !aligned16(a->out[r]))
+      return fail(TL_ERR_INVALID, "tl_gemm_rs_noalloc: rank %d pointer NULL or not 16-byte aligned", r);
+  }
+  const size_t need = noalloc_scratch_needed(a->R, a->M, a->N);
+  if (need == 0 || need > kNoAllocScratchBytes)
+    return fail(TL_ERR_UNSUPPORTED,
+                "tl_gemm_rs_noalloc: R=%d M=%d N=%d needs %zu bytes of scratch; the static scratch holds %zu "
+                "(use tl_gemm_rs with a caller-allocated workspace)",
+                a->R, a->M, a->N, need, kNoAllocScratchBytes);
+  DeviceInfo di{};
+  if (tl_status s = device_info(&di)) return s;
+  uint8_t* scratch = nullptr;
+  if (tl_status s = noalloc_scratch(di.device, &scratch)) return s;
+
+  const int num_tiles = rs_num_tiles(a->R, a->M, a->N);
+  const int nflags = num_tiles * a->R;
+  uint32_t* status = reinterpret_cast<uint32_t*>(scratch);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(scratch + kNoAllocHeader);
+  float* slots = reinterpret_cast<float*>(scratch + align_up(kNoAllocHeader + size_t(nflags) * 4, 256));
+  cudaStream_t st = (cudaStream_t)stream;
+  // the array keeps the previous call's flags: clear them (and the internal status word)
+  if (tl_status s = cuda_ok(cudaMemsetAsync(scratch, 0, kNoAllocHeader + size_t(nflags) * 4, st),
+                            "cudaMemsetAsync(GEMM-RS scratch flags)"))
+    return s;
+
+  RsParams p;  // on the stack: no heap allocation on this path
+  std::memset(&p, 0, sizeof(RsParams));
+  for (int r = 0; r < a->R; ++r) {
+    if (tl_status s = make_map_bf16(&p.map_a[r], a->A[r], a->M, a->K_r, size_t(a->K_r) * 2, BM, BK)) return s;
+    if (tl_status s = make_map_bf16(&p.map_b[r], a->B[r], a->K_r, a->N, size_t(a->N) * 2, BK, 64)) return s;
+    p.out[r] = static_cast<uint16_t*>(a->out[r]);
+  }
+  p.slots = slots;
+  p.flags = flags;
+  p.status = dev_status ? dev_status : status;
+  p.timeout_ns = a->timeout_ns ? a->timeout_ns : kDefaultTimeoutNs;
+  p.pipe_timeout_ns = 2 * p.timeout_ns + 1000000000ull;
+  p.R = a->R;
+  p.M = a->M;
+  p.Md = a->M / a->R;
+  p.K = a->K_r;
+  p.N = a->N;
+  p.Mt_d = cdiv(p.Md, BM);
+  p.Nt = cdiv(a->N, BN);
+  p.KB = cdiv(a->K_r, BK);
+  p.num_tiles = num_tiles;
+  p.num_items = nflags;
+  p.slice_rows = cdiv(BM, a->R);
+  p.epoch = a->epoch;
+  int grid = (di.sm_count / a->R) * a->R;
+  grid = std::min(grid, ((p.num_items + a->R - 1) / a->R) * a->R);
+  if (grid < a->R) return fail(TL_ERR_UNSUPPORTED, "tl_gemm_rs_noalloc: R=%d exceeds the %d SMs", a->R, di.sm_count);
+  void* args[] = {&p};
+  return launch_coop(reinterpret_cast<const void*>(&gemm_rs_kernel), grid, RS_THREADS, RS_SMEM_BYTES, st, args);
+}
+
+namespace {
+size_t noalloc_scratch_needed(int R, int M, int N) {
+  if (R < 1 || M < R || N < 1 || M % R) return 0;
+  const size_t nflags = size_t(tl::rs_num_tiles(R, M, N)) * R;
+  return align_up(kNoAllocHeader + nflags * 4, 256) + nflags * size_t(tl::SLOT_FLOATS) * sizeof(float);
+}
+}  // namespace
