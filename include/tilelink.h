@@ -154,12 +154,15 @@ tl_status tl_ag_gemm(const tl_ag_gemm_args* args, void* stream);
  * A_r . B_r (talk summary, Key Findings and Technical Deep Dive: a persistent
  * GEMM that notifies each finished partial tile, and a reduce stage that waits
  * on its own and its peers' tiles).  One launch: every 128 x 256 partial tile
- * (fp32) is pushed into its receive slot in `workspace` and its flag released;
- * the R partial tiles of one output tile are produced back to back, rank
- * (d + 1 + tau + j) mod R at position j of output tile tau, and the CTAs that
- * computed them each reduce one row slice of the tile after waiting on all R
- * flags, adding the partials in rank order 0..R-1 in fp32, and write bf16 rows
- * into out[d].
+ * (fp32) is pushed into a receive slot of `workspace` (a ring of two waves of
+ * slots, reused as the launch proceeds) and its flag released; output tiles
+ * run in destination order, m tiles innermost, and the R partial tiles of one
+ * output tile are produced back to back, rank (d + 1 + tau + j) mod R at
+ * position j of output tile tau.  The CTAs that computed them each reduce one
+ * row slice of the tile after waiting on all R flags, adding the partials in
+ * rank order 0..R-1 in fp32, and write bf16 rows into out[d].  Flags: one
+ * arrival flag per (tile, rank) and one "reduced" flag per (tile, slice); a
+ * pusher reuses a ring slot only after the reduced flags of its previous tile.
  */
 typedef struct tl_gemm_rs_args {
   int32_t R;                   /* ranks, 1..TL_MAX_RANKS */
@@ -175,9 +178,17 @@ typedef struct tl_gemm_rs_args {
   uint32_t epoch;              /* nonzero */
   uint32_t reserved0;
   uint64_t timeout_ns;         /* 0 = 1 s */
+  int32_t* trace;              /* optional device int32 [tl_gemm_rs_num_flags(R, M, N) / 2]:
+                                  trace[item] = ((d * m_tiles + m) * n_tiles + n) * R + r,
+                                  the output tile and rank of each produced partial,
+                                  m_tiles = ceil(M/R/128), n_tiles = ceil(N/256) */
 } tl_gemm_rs_args;
 
+/* Workspace bytes for the current device: min(items, 2 * CTAs) slots of
+ * 128 KiB, CTAs = the largest multiple of R not above the SM count. */
 size_t tl_gemm_rs_workspace_size(int R, int M, int N);
+/* Flags a GEMM-RS call needs: 2 * R * tiles (arrival and reduced flags),
+ * tiles = R * ceil(M/R/128) * ceil(N/256). */
 int tl_gemm_rs_num_flags(int R, int M, int N);
 tl_status tl_gemm_rs(const tl_gemm_rs_args* args, void* stream);
 
@@ -192,8 +203,9 @@ tl_status tl_gemm_rs(const tl_gemm_rs_args* args, void* stream);
  *    device array of TL_GEMM_RS_NOALLOC_MAX_BYTES (64 MiB), which every GPU
  *    that loads the library holds until the process exits.
  *  - A problem that needs more scratch than that fails with
- *    TL_ERR_UNSUPPORTED and launches nothing.  It needs
- *    roundup256(256 + 4*F) + F * 128 KiB bytes, F = tl_gemm_rs_num_flags(R, M, N).
+ *    TL_ERR_UNSUPPORTED and launches nothing.  It needs roundup256(256 + 4*F)
+ *    bytes of flags plus tl_gemm_rs_workspace_size(R, M, N) bytes of slots,
+ *    F = tl_gemm_rs_num_flags(R, M, N).
  *  - dev_status: optional caller-owned device pointer to 4 uint32 words
  *    (16-byte aligned) where the kernel records its first device-side error
  *    (code, where, value seen, value expected); the caller zeroes it.  With

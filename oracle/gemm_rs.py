@@ -62,10 +62,13 @@ def gemm_rs_at(A_list, B_list, rows, cols):
 # ---------------------------------------------------------------- tile bookkeeping
 
 def output_tiles(R, M, N, BM, BN):
-    """Output tiles (d, m_tile_in_d, n_tile) in destination order; tiles never straddle a shard."""
+    """Output tiles (d, m_tile_in_d, n_tile) in destination order, and within a
+    destination n-tile by n-tile with the m tiles innermost (the tiles that run
+    side by side share B columns and the destination's A rows); tiles never
+    straddle a destination's row shard."""
     Md = M // R
     Mt, Nt = -(-Md // BM), -(-N // BN)
-    return [(d, m, n) for d in range(R) for m in range(Mt) for n in range(Nt)]
+    return [(d, m, n) for d in range(R) for n in range(Nt) for m in range(Mt)]
 
 
 def item_order(R, M, N, BM, BN):

@@ -169,8 +169,9 @@ def check_gemm_rs(gemm_rs, gemm_rs_at, reduced):
 
 def check_rs_item_order(item_order):
     fx = golden_json("rs_item_order_small.json")
-    got = item_order(fx["R"], fx["M"], fx["N"], fx["BM"], fx["BN"])
-    assert [list(t) for t in got] == fx["items"]
+    for c in fx["cases"]:
+        got = item_order(c["R"], c["M"], c["N"], c["BM"], c["BN"])
+        assert [list(t) for t in got] == c["items"]
     # properties: every (tile, rank) once; the reducer (r == d) position rotates
     R, M, N, BM, BN = 8, 2048, 512, 128, 256
     items = item_order(R, M, N, BM, BN)

@@ -35,10 +35,16 @@ def run_rs(B, A, Bl, *, timeout_ns=0):
     ws = torch.full((ws_bytes // 4,), float("nan"), dtype=torch.float32, device="cuda")
     nflags = B.tl_gemm_rs_num_flags(R, M, N)
     sig = B.Signals(nflags)
+    trace = torch.full((nflags,), -1, dtype=torch.int32, device="cuda")
     _epoch[0] += 1
-    B.tl_gemm_rs(dA, dB, out, ws, sig, _epoch[0], timeout_ns=timeout_ns)
+    B.tl_gemm_rs(dA, dB, out, ws, sig, _epoch[0], timeout_ns=timeout_ns, trace=trace)
     status = B.tl_query_status(sig)
-    return dict(out=out, sig=sig, status=status, epoch=_epoch[0], nflags=nflags)
+    return dict(out=out, sig=sig, status=status, epoch=_epoch[0], nflags=nflags, trace=trace)
+
+
+def expected_trace(R, M, N):
+    Mt, Nt = -(-(M // R) // 128), -(-N // 256)
+    return [((d * Mt + m) * Nt + n) * R + r for (_, d, m, n, r) in oracle.gemm_rs.item_order(R, M, N, 128, 256)]
 
 
 def check(B, A, Bl, r):
@@ -47,6 +53,8 @@ def check(B, A, Bl, r):
     for d, (o, w) in enumerate(zip(r["out"], want)):
         check_bf16(to_f64(o), w, f"out[{d}]")
     assert np.all(r["sig"].read_flags()[:r["nflags"]] == r["epoch"])
+    R, M, N = len(A), A[0].shape[0], Bl[0].shape[1]
+    assert r["trace"].cpu().tolist()[:r["nflags"] // 2] == expected_trace(R, M, N)
 
 
 @pytest.mark.parametrize("R,M,K_r,N", [
@@ -124,6 +132,7 @@ def test_rs_llm_full_size_sampled(B):
     r = run_rs(B, A, Bl)
     assert r["status"] == (0, -1)
     assert np.all(r["sig"].read_flags() == r["epoch"])
+    assert r["trace"].cpu().tolist()[:r["nflags"] // 2] == expected_trace(R, M, N)
     rng = np.random.default_rng(2)
     rows = np.concatenate([rng.integers(0, M, 2500), [0, M - 1]])
     cols = np.concatenate([rng.integers(0, N, 2500), [N - 1, 0]])

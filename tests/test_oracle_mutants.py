@@ -129,3 +129,12 @@ def test_pins_catch_slot_for_token_confusion():
         Gm = np.concatenate([np.asarray(x) for x in X])
         return Gm[np.asarray(perm) % Gm.shape[0]]
     _fails(C.check_moe_gemm, M.moe_ag_gemm, M.moe_at, bad_sorted, M.route, A.ag_gemm, bf16.decode)
+
+
+def test_pins_catch_n_innermost_rs_tiles():
+    def bad(R, Mm, N, BM, BN):
+        Md = Mm // R
+        Mt, Nt = -(-Md // BM), -(-N // BN)
+        tiles = [(d, m, n) for d in range(R) for m in range(Mt) for n in range(Nt)]
+        return [(t, d, m, n, (d + 1 + t + j) % R) for t, (d, m, n) in enumerate(tiles) for j in range(R)]
+    _fails(C.check_rs_item_order, bad)

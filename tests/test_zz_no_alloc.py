@@ -51,11 +51,34 @@ def test_noalloc_matches_allocating_entry_point_twice(B, R, M, K_r, N):
 
 
 def test_noalloc_rejects_a_problem_beyond_the_static_scratch(B):
+    # R=32, 8192 rows per destination, N=32768: 8.4M flags do not fit in the
+    # static scratch.  The call must refuse before touching any buffer, so one
+    # small tensor stands in for every pointer.
+    import ctypes
     import torch
-    R, M, K_r, N = 8, 8192, 64, 4096           # needs ~1 GiB of receive slots
-    A = [torch.zeros(M, K_r, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
-    Bl = [torch.zeros(K_r, N, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
-    out = [torch.zeros(M // R, N, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
-    with pytest.raises(B.TLError) as e:
-        B.tl_gemm_rs_noalloc(A, Bl, out, epoch=1)
-    assert e.value.code == B.TL_ERR_UNSUPPORTED and "static scratch" in str(e.value)
+    R, M, K_r, N = 32, 32 * 8192, 64, 32768
+    t = torch.zeros(1024, dtype=torch.bfloat16, device="cuda")
+    ptrs = (ctypes.c_void_p * R)(*([t.data_ptr()] * R))
+    pp = ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p))
+    a = B.tl_gemm_rs_args(R=R, M=M, K_r=K_r, N=N, A=pp, B=pp, out=pp, workspace=None, workspace_bytes=0,
+                          signals=None, epoch=1, reserved0=0, timeout_ns=0, trace=None)
+    rc = B.lib.tl_gemm_rs_noalloc(ctypes.byref(a), None, torch.cuda.current_stream().cuda_stream)
+    assert rc == B.TL_ERR_UNSUPPORTED
+    assert "static scratch" in B.tl_last_error()
+
+
+def test_noalloc_rejects_workspace_or_signals(B):
+    import torch
+    A, Bl = inputs.gemm_rs_inputs(2, 256, 64, 256, seed=1)
+    dA = [dev_bf16(a) for a in A]
+    dB = [dev_bf16(b) for b in Bl]
+    out = [torch.empty(128, 256, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    import ctypes
+    pa, pb, po = B._ptr_array(dA), B._ptr_array(dB), B._ptr_array(out)
+    ws = torch.empty(1 << 20, dtype=torch.float32, device="cuda")
+    a = B.tl_gemm_rs_args(R=2, M=256, K_r=64, N=256, A=ctypes.cast(pa, ctypes.POINTER(ctypes.c_void_p)),
+                          B=ctypes.cast(pb, ctypes.POINTER(ctypes.c_void_p)),
+                          out=ctypes.cast(po, ctypes.POINTER(ctypes.c_void_p)), workspace=ws.data_ptr(),
+                          workspace_bytes=ws.numel() * 4, signals=None, epoch=1, reserved0=0, timeout_ns=0,
+                          trace=None)
+    assert B.lib.tl_gemm_rs_noalloc(ctypes.byref(a), None, None) == B.TL_ERR_INVALID

@@ -59,6 +59,7 @@ class tl_gemm_rs_args(ctypes.Structure):
         ("A", ctypes.POINTER(_vp)), ("B", ctypes.POINTER(_vp)), ("out", ctypes.POINTER(_vp)),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("signals", _vp),
         ("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32), ("timeout_ns", ctypes.c_uint64),
+        ("trace", _vp),
     ]
 
 
@@ -226,7 +227,7 @@ def tl_gemm_rs_num_flags(R, M, N):
     return int(lib.tl_gemm_rs_num_flags(R, M, N))
 
 
-def tl_gemm_rs(A, B, out, workspace, signals: Signals, epoch: int, *, timeout_ns=0, stream=None):
+def tl_gemm_rs(A, B, out, workspace, signals: Signals, epoch: int, *, timeout_ns=0, trace=None, stream=None):
     """out[d] = rows d of sum_r A_r . B_r in rank order (see tilelink.h)."""
     R = len(A)
     M, K_r = A[0].shape
@@ -236,7 +237,7 @@ def tl_gemm_rs(A, B, out, workspace, signals: Signals, epoch: int, *, timeout_ns
                         B=ctypes.cast(pb, ctypes.POINTER(_vp)), out=ctypes.cast(po, ctypes.POINTER(_vp)),
                         workspace=_ptr(workspace), workspace_bytes=workspace.numel() * workspace.element_size(),
                         signals=signals.handle, epoch=int(epoch) & 0xFFFFFFFF, reserved0=0,
-                        timeout_ns=int(timeout_ns))
+                        timeout_ns=int(timeout_ns), trace=_ptr(trace))
     _check(lib.tl_gemm_rs(ctypes.byref(a), _stream(stream)))
 
 
@@ -251,5 +252,5 @@ def tl_gemm_rs_noalloc(A, B, out, epoch: int, *, dev_status=None, timeout_ns=0, 
     a = tl_gemm_rs_args(R=R, M=M, K_r=K_r, N=N, A=ctypes.cast(pa, ctypes.POINTER(_vp)),
                         B=ctypes.cast(pb, ctypes.POINTER(_vp)), out=ctypes.cast(po, ctypes.POINTER(_vp)),
                         workspace=None, workspace_bytes=0, signals=None, epoch=int(epoch) & 0xFFFFFFFF,
-                        reserved0=0, timeout_ns=int(timeout_ns))
+                        reserved0=0, timeout_ns=int(timeout_ns), trace=None)
     _check(lib.tl_gemm_rs_noalloc(ctypes.byref(a), _ptr(dev_status), _stream(stream)))
