@@ -6,6 +6,8 @@ One step = one pass of the whole hot path over one batch of synthetic inputs:
     B [4096, 1792] ~ N(0, 0.02) -> C [8192, 1792]     (tl_ag_gemm)
   * GEMM-ReduceScatter, R=8, A_r [8192, 1792], B_r [1792, 4096]
     -> 8 row shards [1024, 4096]                      (tl_gemm_rs)
+  * AllGather + grouped MoE GEMM, R=8 x [1024, 4096] tokens, top-2 of 32
+    experts (Zipf 1.2), W_e [4096, 1408]               (tl_moe_ag_gemm)
 Metric: whole-job TFLOP/s = algorithmic FLOPs of the step / device time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -26,16 +28,21 @@ import sys
 import threading
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 AG = dict(R=8, M_shard=1024, K=4096, N=1792)
 RS = dict(R=8, M=8192, K_r=1792, N=4096)
+MOE = dict(R=8, T_r=1024, H=4096, N=1408, E=32, topk=2, zipf_s=1.2)
 AG_FLOPS = 2 * AG["R"] * AG["M_shard"] * AG["N"] * AG["K"]
 RS_FLOPS = 2 * RS["R"] * RS["M"] * RS["N"] * RS["K_r"]
+MOE_FLOPS = 2 * MOE["R"] * MOE["T_r"] * MOE["topk"] * MOE["N"] * MOE["H"]
 METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s on 1 GB300"
 WORKLOAD = ("AG-GEMM R=8 [8192x4096]x[4096x1792] + GEMM-RS R=8 8x[8192x1792]x[1792x4096] "
-            "(TP MLP up/down projection, emulated ranks)")
+            "+ MoE AG+grouped GEMM R=8 8192 tokens top-2/32 experts [16384x4096]x[4096x1408] "
+            "(TP MLP up/down projection and MoE expert up-projection, emulated ranks)")
 
 
 def parse():
@@ -122,20 +129,27 @@ class OracleSample:
         from tile_centric_gemm_gb300 import inputs
         self.A, self.B = inputs.ag_gemm_inputs(AG["R"], AG["M_shard"], AG["K"], AG["N"], "normal", seed=0)
         self.Ar, self.Br = inputs.gemm_rs_inputs(RS["R"], RS["M"], RS["K_r"], RS["N"], seed=0)
+        self.X, self.ids, self.W = inputs.moe_inputs(MOE["R"], MOE["T_r"], MOE["H"], MOE["N"], MOE["E"],
+                                                     MOE["topk"], MOE["zipf_s"], seed=0)
         self.rows = 16
 
     def flops(self):
-        return 2 * AG["R"] * self.rows * AG["N"] * AG["K"] + 2 * RS["R"] * (RS["R"] * self.rows) * RS["N"] * RS["K_r"]
+        return (2 * AG["R"] * self.rows * AG["N"] * AG["K"] + 2 * RS["R"] * (RS["R"] * self.rows) * RS["N"] * RS["K_r"]
+                + 2 * MOE["R"] * self.rows * MOE["topk"] * MOE["N"] * MOE["H"])
 
     def describe(self):
         return (f"AG-GEMM with {self.rows} of {AG['M_shard']} rows per shard + GEMM-RS with "
-                f"{RS['R'] * self.rows} of {RS['M']} rows ({self.flops() / 1e9:.1f} GFLOP; float64 numpy oracle)")
+                f"{RS['R'] * self.rows} of {RS['M']} rows + MoE with {self.rows} of {MOE['T_r']} tokens per shard "
+                f"({self.flops() / 1e9:.1f} GFLOP; float64 numpy oracle)")
 
     def step(self):
         import oracle
         t0 = time.perf_counter()
         oracle.ag_gemm.ag_gemm([a[:self.rows] for a in self.A], self.B)
         oracle.gemm_rs.gemm_rs([a[:RS["R"] * self.rows] for a in self.Ar], self.Br)
+        T_r = MOE["T_r"]
+        keep = np.concatenate([np.arange(r * T_r, r * T_r + self.rows) for r in range(MOE["R"])])
+        oracle.moe.moe_ag_gemm([x[:self.rows] for x in self.X], self.ids[keep], self.W)
         return time.perf_counter() - t0
 
     def size_to(self, seconds):
@@ -211,10 +225,24 @@ class Workload:
         self.ws = torch.empty(B.tl_gemm_rs_workspace_size(Rr, RS["M"], RS["N"]) // 4, dtype=torch.float32,
                               device=dev)
         self.sig_rs = B.Signals(B.tl_gemm_rs_num_flags(Rr, RS["M"], RS["N"]))
+        X, ids, W = inputs.moe_inputs(MOE["R"], MOE["T_r"], MOE["H"], MOE["N"], MOE["E"], MOE["topk"],
+                                      MOE["zipf_s"], seed=0)
+        self.h_moe = [tb(x).pin_memory() for x in X] + [tb(w).pin_memory() for w in W] + \
+            [torch.from_numpy(ids).pin_memory()]
+        self.d_moe = [t.to(dev) for t in self.h_moe]
+        P = MOE["R"] * MOE["T_r"] * MOE["topk"]
+        self.S = torch.empty(P, MOE["H"], dtype=torch.bfloat16, device=dev)
+        self.Y = torch.empty(P, MOE["N"], dtype=torch.bfloat16, device=dev)
+        self.perm = torch.empty(P, dtype=torch.int32, device=dev)
+        self.offs = torch.empty(MOE["E"] + 1, dtype=torch.int32, device=dev)
+        self.ws_moe = torch.empty(B.tl_moe_workspace_size(MOE["R"], MOE["T_r"], MOE["E"], MOE["topk"]) // 4,
+                                  dtype=torch.int32, device=dev)
+        self.sig_moe = B.Signals(B.tl_moe_num_flags(MOE["R"], MOE["T_r"], MOE["H"])[0])
         self.h_C = torch.empty_like(self.C, device="cpu").pin_memory()
         self.h_out = [torch.empty_like(o, device="cpu").pin_memory() for o in self.out]
+        self.h_Y = torch.empty_like(self.Y, device="cpu").pin_memory()
         self.epoch = 0
-        self.launches_per_step = 2
+        self.launches_per_step = 4  # ag_gemm, gemm_rs, moe route, moe gemm
 
     def ag(self):
         self.epoch += 1
@@ -226,23 +254,31 @@ class Workload:
         R = RS["R"]
         self.B.tl_gemm_rs(self.d_rs[:R], self.d_rs[R:], self.out, self.ws, self.sig_rs, self.epoch)
 
+    def moe(self):
+        self.epoch += 1
+        R, E = MOE["R"], MOE["E"]
+        d = self.d_moe
+        self.B.tl_moe_ag_gemm(d[:R], d[R + E], d[R:R + E], self.S, self.Y, self.perm, self.offs, self.ws_moe,
+                              self.sig_moe, self.epoch)
+
     def h2d(self):
-        for h, d in zip(self.h_ag + self.h_rs, self.d_ag + self.d_rs):
+        for h, d in zip(self.h_ag + self.h_rs + self.h_moe, self.d_ag + self.d_rs + self.d_moe):
             d.copy_(h, non_blocking=True)
 
     def d2h(self):
         self.h_C.copy_(self.C, non_blocking=True)
         for h, d in zip(self.h_out, self.out):
             h.copy_(d, non_blocking=True)
+        self.h_Y.copy_(self.Y, non_blocking=True)
 
     def h2d_bytes(self):
-        return sum(t.numel() * t.element_size() for t in self.h_ag + self.h_rs)
+        return sum(t.numel() * t.element_size() for t in self.h_ag + self.h_rs + self.h_moe)
 
     def d2h_bytes(self):
-        return self.h_C.numel() * 2 + sum(t.numel() * 2 for t in self.h_out)
+        return self.h_C.numel() * 2 + sum(t.numel() * 2 for t in self.h_out) + self.h_Y.numel() * 2
 
     def check_status(self):
-        for s in (self.sig_ag, self.sig_rs):
+        for s in (self.sig_ag, self.sig_rs, self.sig_moe):
             code, where = self.B.tl_query_status(s)
             if code:
                 raise RuntimeError(f"device error {code} at {where}")
@@ -277,12 +313,13 @@ def main():
     for _ in range(max(3, args.warmup)):
         wl.ag()
         wl.rs()
+        wl.moe()
     wl.check_status()
 
     sampler = ClockSampler(local_rank)
     time.sleep(0.3)
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     barrier()
     t_host0 = time.time()
     start = torch.cuda.Event(enable_timing=True)
@@ -294,6 +331,8 @@ def main():
         ev[i][1].record(stream)
         wl.rs()
         ev[i][2].record(stream)
+        wl.moe()
+        ev[i][3].record(stream)
     end.record(stream)
     barrier()
     t_host1 = time.time()
@@ -302,18 +341,19 @@ def main():
     total_ms = start.elapsed_time(end)
     ag_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     rs_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    moe_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
     ms_per_step = total_ms / K
     if pg:
         t = torch.tensor([ms_per_step])
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms_per_step = float(t[0])
-    step_flops = AG_FLOPS + RS_FLOPS
+    step_flops = AG_FLOPS + RS_FLOPS + MOE_FLOPS
     value = world * step_flops / (ms_per_step * 1e-3) / 1e12
 
     # end to end through the public API with host buffers: H2D inputs, both calls, D2H outputs
     E = max(3, args.e2e_steps)
     for _ in range(2):
-        wl.h2d(); wl.ag(); wl.rs(); wl.d2h()
+        wl.h2d(); wl.ag(); wl.rs(); wl.moe(); wl.d2h()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -322,6 +362,7 @@ def main():
         wl.h2d()
         wl.ag()
         wl.rs()
+        wl.moe()
         wl.d2h()
     e1.record(stream)
     barrier()
@@ -334,6 +375,7 @@ def main():
 
     rs_avg = statistics.mean(rs_ms)
     ag_avg = statistics.mean(ag_ms)
+    moe_avg = statistics.mean(moe_ms)
     achieved = RS_FLOPS / (rs_avg * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     clocks = sampler.summary(t_host0, t_host1)
@@ -341,11 +383,12 @@ def main():
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "ag": AG, "rs": RS, "step_gflop": step_flops / 1e9,
-                   "l2": "inputs larger than L2: a step touches ~1.7 GB (129 MB L2); no flush",
+        "config": {"workload": WORKLOAD, "ag": AG, "rs": RS, "moe": MOE, "step_gflop": step_flops / 1e9,
+                   "l2": "inputs larger than L2: a step touches ~2.3 GB (129 MB L2); no flush",
                    "parallelism": f"{world} independent replica(s), 8 emulated ranks each"},
         "breakdown": {"ag_gemm_us": ag_avg * 1e3, "ag_gemm_tflops": AG_FLOPS / (ag_avg * 1e-3) / 1e12,
-                      "gemm_rs_us": rs_avg * 1e3, "gemm_rs_tflops": achieved},
+                      "gemm_rs_us": rs_avg * 1e3, "gemm_rs_tflops": achieved,
+                      "moe_us": moe_avg * 1e3, "moe_tflops": MOE_FLOPS / (moe_avg * 1e-3) / 1e12},
         "roofline": {"bound": "tensor", "kernel": "gemm_rs_kernel", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
                      "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),

@@ -221,6 +221,67 @@ tl_status tl_gemm_rs(const tl_gemm_rs_args* args, void* stream);
 #define TL_GEMM_RS_NOALLOC_MAX_BYTES (64ull << 20)
 tl_status tl_gemm_rs_noalloc(const tl_gemm_rs_args* args, uint32_t* dev_status, void* stream);
 
+/* ---------------------------------------------------------------- AllGather + grouped MoE GEMM
+ * The AllGather + GroupGEMM part of an MoE layer (talk summary, Key Findings
+ * and Experimental Setup & Results: MoE layers; Technical Deep Dive: lookup
+ * tables built from the routing carry the tile -> rank/barrier map of a
+ * dynamic workload).  T = R*T_r tokens, P = T*topk routed rows.
+ *   perm[i]            sorted row i -> token*topk + slot, rows sorted by
+ *                      (expert, global token id, slot); global id = r*T_r + local
+ *   expert_offsets[e]  first sorted row of expert e; expert_offsets[E] = P
+ *   sorted_tokens[i]   = token perm[i]/topk  (the gathered tokens, expert order)
+ *   Y[i, :]            = sorted_tokens[i] . W_{expert of row i}   (fp32 accumulate, bf16)
+ * Two stream-ordered launches: a one-CTA routing kernel (histogram, scan,
+ * stable counting sort, tile table, tile order) and one cooperative kernel in
+ * which copy warps gather the shards' token rows and scatter each to its topk
+ * sorted positions (one flag per chunk of rows_per_barrier tokens of a shard,
+ * shards in the order self, self+1, ...) while tcgen05 GEMM tiles wait on the
+ * flags their lookup-table entry names and multiply their sorted rows by their
+ * expert's weight.  No gate weighting, no combine.
+ * Workspace layout (int32 words; read-only for the caller, documented for
+ * tests), max_tiles = ceil(P/128) + E:
+ *   [0]                         number of tiles
+ *   [16 + 6*t .. 16 + 6*t + 5]  tile t: expert, first sorted row, rows,
+ *                               lowest barrier, highest barrier, source-rank mask
+ *   [16 + 6*max_tiles + i]      i-th tile in consumer order (swizzle: tiles by
+ *                               the latest arrival position among their barriers,
+ *                               barrier (r, c) arriving at ((r-self) mod R)*chunks + c)
+ *   [16 + 7*max_tiles + q]      sorted row of pair q (the inverse of perm)
+ * Barrier id of token t: (t / T_r) * chunks + (t % T_r) / rows_per_barrier,
+ * chunks = ceil(T_r / rows_per_barrier).  Limits: R <= 32, E <= 64, H and N
+ * multiples of 8.  A topk id outside [0, E) records TL_ERR_INVALID in the
+ * status word (the pair is clamped into range).
+ */
+typedef struct tl_moe_args {
+  int32_t R;                    /* ranks, 1..32 */
+  int32_t self_rank;            /* 0..R-1 */
+  int32_t T_r;                  /* tokens per shard */
+  int32_t H;                    /* hidden size (contraction), multiple of 8 */
+  int32_t N;                    /* expert output columns, multiple of 8 */
+  int32_t E;                    /* experts, 1..64 */
+  int32_t topk;                 /* routed experts per token, 1..E */
+  int32_t rows_per_barrier;     /* tokens per producer chunk / flag; 0 = about 32 KB of rows */
+  const void* const* X;         /* host array of R device pointers, bf16 [T_r, H] */
+  const int32_t* topk_ids;      /* device int32 [R*T_r, topk] */
+  const void* const* W;         /* host array of E device pointers, bf16 [H, N] */
+  void* sorted_tokens;          /* device bf16 [P, H], written */
+  void* Y;                      /* device bf16 [P, N], written */
+  int32_t* perm;                /* device int32 [P], written */
+  int32_t* expert_offsets;      /* device int32 [E+1], written */
+  void* workspace;              /* device, >= tl_moe_workspace_size(...) bytes, 16-byte aligned */
+  size_t workspace_bytes;
+  tl_signals* signals;          /* >= tl_moe_num_flags(...) flags */
+  uint32_t epoch;               /* nonzero */
+  uint32_t reserved0;
+  uint64_t timeout_ns;          /* 0 = 1 s */
+  int32_t* trace;               /* optional device int32 [max_tiles * ceil(N/256)]:
+                                   tile * n_tiles + n of the work run at each schedule slot */
+} tl_moe_args;
+
+size_t tl_moe_workspace_size(int R, int T_r, int E, int topk);
+int tl_moe_num_flags(int R, int T_r, int H, int rows_per_barrier, int* effective_rpb);
+tl_status tl_moe_ag_gemm(const tl_moe_args* args, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -72,6 +72,21 @@ def tile_sources(perm, k, table, T_r, rows_per_barrier):
     return out
 
 
+def tile_order(sources, R, self_rank, T_r, rows_per_barrier):
+    """Consumer order of the tiles (the swizzle for a dynamic workload).
+
+    Producer barriers arrive shard by shard starting at the self shard: barrier
+    (rank r, chunk c) has arrival position ((r - self) mod R) * chunks + c.  A
+    tile is keyed by the latest position among the barriers it waits on (every
+    id from its lowest to its highest barrier) and tiles run by (key, index)."""
+    bpr = -(-T_r // rows_per_barrier)
+    keys = []
+    for t, (_, lo, hi) in enumerate(sources):
+        key = max(((b // bpr - self_rank) % R) * bpr + b % bpr for b in range(lo, hi + 1))
+        keys.append((key, t))
+    return [t for (_, t) in sorted(keys)]
+
+
 def sorted_tokens(X_shards, perm, k):
     """Row i = gathered token perm[i] // k (bf16 bits): the gathered tokens in expert order."""
     G = np.concatenate([np.asarray(x, dtype=np.uint16) for x in X_shards], axis=0)

@@ -182,6 +182,27 @@ def check_rs_item_order(item_order):
 
 # ------------------------------------------------------------------ MoE
 
+def check_moe_tile_order(tile_order, tile_sources):
+    fx = golden_json("moe_routing_small.json")
+    src = [tuple(t) for t in fx["tile_sources"]]
+    assert tile_order(src, fx["R"], 0, fx["T_r"], fx["rows_per_barrier"]) == fx["tile_order_self0"]
+    assert tile_order(src, fx["R"], 1, fx["T_r"], fx["rows_per_barrier"]) == fx["tile_order_self1"]
+    # a permutation whose keys never decrease, on a random case
+    rng = np.random.default_rng(9)
+    R, T_r, rpb = 4, 64, 8
+    src = []
+    for _ in range(40):
+        lo = int(rng.integers(0, R * T_r // rpb))
+        hi = int(rng.integers(lo, R * T_r // rpb))
+        src.append((0, lo, hi))
+    order = tile_order(src, R, 2, T_r, rpb)
+    assert sorted(order) == list(range(40))
+    bpr = T_r // rpb
+    key = lambda t: max(((b // bpr - 2) % R) * bpr + b % bpr for b in range(src[t][1], src[t][2] + 1))
+    ks = [key(t) for t in order]
+    assert ks == sorted(ks)
+
+
 def check_moe_routing(route, tile_table, tile_sources):
     fx = golden_json("moe_routing_small.json")
     ids = np.array(fx["topk_ids"])

@@ -138,3 +138,11 @@ def test_pins_catch_n_innermost_rs_tiles():
         tiles = [(d, m, n) for d in range(R) for m in range(Mt) for n in range(Nt)]
         return [(t, d, m, n, (d + 1 + t + j) % R) for t, (d, m, n) in enumerate(tiles) for j in range(R)]
     _fails(C.check_rs_item_order, bad)
+
+
+def test_pins_catch_moe_order_by_lowest_barrier():
+    def bad(sources, R, s, T_r, rpb):
+        bpr = -(-T_r // rpb)
+        keys = [(((lo // bpr - s) % R) * bpr + lo % bpr, t) for t, (_, lo, hi) in enumerate(sources)]
+        return [t for (_, t) in sorted(keys)]
+    _fails(C.check_moe_tile_order, bad, M.tile_sources)

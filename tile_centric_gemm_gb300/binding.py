@@ -29,6 +29,7 @@ EXPORTED = [
     "tl_signals_reset", "tl_tile_notify", "tl_tile_wait", "tl_query_status",
     "tl_ag_gemm_num_flags", "tl_ag_gemm_tile_order", "tl_ag_gemm",
     "tl_gemm_rs_workspace_size", "tl_gemm_rs_num_flags", "tl_gemm_rs", "tl_gemm_rs_noalloc",
+    "tl_moe_workspace_size", "tl_moe_num_flags", "tl_moe_ag_gemm",
 ]
 
 
@@ -63,6 +64,17 @@ class tl_gemm_rs_args(ctypes.Structure):
     ]
 
 
+class tl_moe_args(ctypes.Structure):
+    _fields_ = [
+        ("R", ctypes.c_int32), ("self_rank", ctypes.c_int32), ("T_r", ctypes.c_int32), ("H", ctypes.c_int32),
+        ("N", ctypes.c_int32), ("E", ctypes.c_int32), ("topk", ctypes.c_int32), ("rows_per_barrier", ctypes.c_int32),
+        ("X", ctypes.POINTER(_vp)), ("topk_ids", _vp), ("W", ctypes.POINTER(_vp)), ("sorted_tokens", _vp),
+        ("Y", _vp), ("perm", _vp), ("expert_offsets", _vp), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("signals", _vp), ("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32),
+        ("timeout_ns", ctypes.c_uint64), ("trace", _vp),
+    ]
+
+
 def _decl(name, restype, *argtypes):
     f = getattr(lib, name)
     f.restype = restype
@@ -87,6 +99,9 @@ _decl("tl_gemm_rs_workspace_size", _sz, _i, _i, _i)
 _decl("tl_gemm_rs_num_flags", _i, _i, _i, _i)
 _decl("tl_gemm_rs", _i, ctypes.POINTER(tl_gemm_rs_args), _vp)
 _decl("tl_gemm_rs_noalloc", _i, ctypes.POINTER(tl_gemm_rs_args), _vp, _vp)
+_decl("tl_moe_workspace_size", _sz, _i, _i, _i, _i)
+_decl("tl_moe_num_flags", _i, _i, _i, _i, _i, ctypes.POINTER(_i))
+_decl("tl_moe_ag_gemm", _i, ctypes.POINTER(tl_moe_args), _vp)
 
 
 def _check(code):
@@ -254,3 +269,31 @@ def tl_gemm_rs_noalloc(A, B, out, epoch: int, *, dev_status=None, timeout_ns=0, 
                         workspace=None, workspace_bytes=0, signals=None, epoch=int(epoch) & 0xFFFFFFFF,
                         reserved0=0, timeout_ns=int(timeout_ns), trace=None)
     _check(lib.tl_gemm_rs_noalloc(ctypes.byref(a), _ptr(dev_status), _stream(stream)))
+
+
+def tl_moe_workspace_size(R, T_r, E, topk):
+    return int(lib.tl_moe_workspace_size(R, T_r, E, topk))
+
+
+def tl_moe_num_flags(R, T_r, H, rows_per_barrier=0):
+    eff = _i()
+    n = lib.tl_moe_num_flags(R, T_r, H, rows_per_barrier, ctypes.byref(eff))
+    return n, eff.value
+
+
+def tl_moe_ag_gemm(X, topk_ids, W, sorted_tokens, Y, perm, expert_offsets, workspace, signals: Signals, epoch: int,
+                   *, self_rank=0, rows_per_barrier=0, timeout_ns=0, trace=None, stream=None):
+    """AllGather + grouped MoE GEMM (see tilelink.h): Y rows in expert-sorted order."""
+    R = len(X)
+    T_r, H = X[0].shape
+    E = len(W)
+    N = W[0].shape[1]
+    topk = topk_ids.shape[1]
+    px, pw = _ptr_array(X), _ptr_array(W)
+    a = tl_moe_args(R=R, self_rank=self_rank, T_r=T_r, H=H, N=N, E=E, topk=topk, rows_per_barrier=rows_per_barrier,
+                    X=ctypes.cast(px, ctypes.POINTER(_vp)), topk_ids=_ptr(topk_ids),
+                    W=ctypes.cast(pw, ctypes.POINTER(_vp)), sorted_tokens=_ptr(sorted_tokens), Y=_ptr(Y),
+                    perm=_ptr(perm), expert_offsets=_ptr(expert_offsets), workspace=_ptr(workspace),
+                    workspace_bytes=workspace.numel() * workspace.element_size(), signals=signals.handle,
+                    epoch=int(epoch) & 0xFFFFFFFF, reserved0=0, timeout_ns=int(timeout_ns), trace=_ptr(trace))
+    _check(lib.tl_moe_ag_gemm(ctypes.byref(a), _stream(stream)))

@@ -1,0 +1,548 @@
+// tl_moe.cu -- AllGather + grouped MoE GEMM at tile granularity.
+//
+// TileLink talk summary ("TileLink: Generating Efficient Compute-Communication
+// Overlapping Kernels using Tile-Centric Primitives"):
+//  * Key Findings / Experimental Setup & Results -- the MoE layer overlaps an
+//    AllGather of tokens with a GroupGEMM over experts (this file covers that
+//    part; ReduceScatter, TopK-reduce and scatter of the layer are not here).
+//  * Technical Deep Dive -- for dynamic workloads the tile -> rank/barrier
+//    dependencies come from lookup tables built from the routing and passed
+//    to the kernel.
+//
+// Two stream-ordered launches:
+//  1. moe_route_kernel (one CTA): histogram of topk_ids over experts,
+//     exclusive scan, stable counting sort of the (token, slot) pairs by expert
+//     (perm and its inverse), then the tile table -- per 128-row tile its
+//     expert, first sorted row, rows, lowest and highest producer barrier and
+//     source-rank mask -- and the consumer tile order.
+//  2. moe_gemm_kernel (cooperative, one CTA per SM): copy warps gather every
+//     token row of every shard and scatter it to its k sorted positions in
+//     `sorted_tokens` (bulk TMA, one flag per chunk of rows_per_barrier tokens,
+//     shards in the order self, self+1, ...); the TMA warp of each GEMM tile
+//     acquires the flags of its barrier range, then a tcgen05 grouped GEMM
+//     multiplies the tile's sorted rows by its expert's weight.
+#include <algorithm>
+#include <cstring>
+#include <new>
+
+#include "tl_common.cuh"
+#include "tl_internal.h"
+
+namespace tl {
+namespace {
+
+constexpr int MOE_MAX_E = 64;
+constexpr int MOE_MAX_R = 32;
+constexpr int MOE_MAX_TILES = 8192;
+constexpr int ROUTE_THREADS = 1024;
+constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
+constexpr int kWarpCopy = 6;
+constexpr int MOE_THREADS = 7 * 32;
+constexpr uint32_t MOE_SMEM_COPY = SMEM_GEMM_END;
+constexpr uint32_t MOE_SMEM_BARS = MOE_SMEM_COPY + COPY_NBUF * COPY_CHUNK;
+constexpr uint32_t MOE_SMEM_BYTES = MOE_SMEM_BARS + sizeof(Barriers) + 1024;
+
+// Workspace layout, in int32 words (documented in tilelink.h).
+constexpr int WS_HEADER = 16;  // [0] = number of tiles
+__host__ __device__ inline int ws_tiles(int) { return WS_HEADER; }
+__host__ __device__ inline int ws_order(int max_tiles) { return WS_HEADER + 6 * max_tiles; }
+__host__ __device__ inline int ws_inv(int max_tiles) { return WS_HEADER + 7 * max_tiles; }
+
+struct RouteParams {
+  const int32_t* topk;    // [T, k]
+  int32_t* perm;          // [P] sorted position -> token*k + slot
+  int32_t* offsets;       // [E+1]
+  int32_t* ws;            // workspace
+  uint32_t* status;
+  int32_t T, k, E, R, T_r, rpb, bpr, self, max_tiles;
+};
+
+// Stable counting sort of the P = T*k pairs by expert, then the tile table.
+__global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const RouteParams p) {
+  extern __shared__ int32_t sm[];
+  const int E = p.E;
+  int32_t* cnt = sm;                           // [ROUTE_WARPS][E] per-warp counts, then bases
+  int32_t* s_off = cnt + ROUTE_WARPS * E;      // [E+1]
+  int32_t* s_toff = s_off + (E + 1);           // [E+1] tile offsets
+  int32_t* s_key = s_toff + (E + 1);           // [max_tiles]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int P = p.T * p.k;
+  const int per_warp = ((P + ROUTE_WARPS - 1) / ROUTE_WARPS + 31) / 32 * 32;
+  const int q0 = warp * per_warp, q1 = min(P, q0 + per_warp);
+  int32_t* tiles = p.ws + ws_tiles(p.max_tiles);
+  int32_t* order = p.ws + ws_order(p.max_tiles);
+  int32_t* inv = p.ws + ws_inv(p.max_tiles);
+
+  for (int i = tid; i < ROUTE_WARPS * E; i += ROUTE_THREADS) cnt[i] = 0;
+  __syncthreads();
+  // 1. per-warp histograms over contiguous ranges of pairs
+  for (int base = q0; base < q1; base += 32) {
+    const int q = base + lane;
+    const bool act = q < q1;
+    int e = act ? p.topk[q] : -1;
+    if (act && (e < 0 || e >= E)) {
+      record_error(p.status, TL_ERR_INVALID, uint32_t(q), uint32_t(e), uint32_t(E));
+      e = min(max(e, 0), E - 1);
+    }
+    const unsigned am = __ballot_sync(0xffffffffu, act);
+    if (act) {
+      const unsigned peers = __match_any_sync(am, e);
+      if (lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  // 2. expert counts, exclusive scan, and each warp's first position per expert
+  if (tid == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      s_off[e] = acc;
+      int c = 0;
+      for (int w = 0; w < ROUTE_WARPS; ++w) c += cnt[w * E + e];
+      acc += c;
+    }
+    s_off[E] = acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += ROUTE_THREADS) {
+    int run = s_off[e];
+    for (int w = 0; w < ROUTE_WARPS; ++w) {
+      const int c = cnt[w * E + e];
+      cnt[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // 3. stable scatter: pairs keep their (token, slot) order inside an expert
+  for (int base = q0; base < q1; base += 32) {
+    const int q = base + lane;
+    const bool act = q < q1;
+    int e = act ? min(max(p.topk[q], 0), E - 1) : 0;
+    const unsigned am = __ballot_sync(0xffffffffu, act);
+    if (act) {
+      const unsigned peers = __match_any_sync(am, e);
+      const int pos = cnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
+      p.perm[pos] = q;
+      inv[q] = pos;
+      __syncwarp(am);
+      if (lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  // 4. tiles per expert and their offsets
+  if (tid == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      s_toff[e] = acc;
+      acc += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+    }
+    s_toff[E] = acc;
+    p.ws[0] = min(acc, p.max_tiles);
+    if (acc > p.max_tiles) record_error(p.status, TL_ERR_INTERNAL, 0xFFFE0000u, uint32_t(acc), uint32_t(p.max_tiles));
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += ROUTE_THREADS) p.offsets[e] = s_off[e];
+  const int ntiles = min(s_toff[E], p.max_tiles);
+  // 5. the tile table: rows of a tile are one expert's, tokens ascending
+  for (int t = tid; t < ntiles; t += ROUTE_THREADS) {
+    int lo_e = 0, hi_e = E - 1;  // last expert whose first tile <= t
+    while (lo_e < hi_e) {
+      const int mid = (lo_e + hi_e + 1) >> 1;
+      if (s_toff[mid] <= t) lo_e = mid; else hi_e = mid - 1;
+    }
+    const int e = lo_e;
+    const int j = t - s_toff[e];
+    const int row0 = s_off[e] + j * BM;
+    const int rows = min(BM, s_off[e + 1] - row0);
+    uint32_t mask = 0;
+    int blo = 0x7fffffff, bhi = -1;
+    for (int i = 0; i < rows; ++i) {
+      const int tok = p.perm[row0 + i] / p.k;
+      const int r = tok / p.T_r;
+      const int b = r * p.bpr + (tok % p.T_r) / p.rpb;
+      mask |= 1u << r;
+      blo = min(blo, b);
+      bhi = max(bhi, b);
+    }
+    int32_t* tr = tiles + 6 * t;
+    tr[0] = e;
+    tr[1] = row0;
+    tr[2] = rows;
+    tr[3] = blo;
+    tr[4] = bhi;
+    tr[5] = int32_t(mask);
+    // arrival key: latest position among the barriers in [blo, bhi]; barrier (r, c)
+    // arrives at ((r - self) mod R) * bpr + c
+    int key = 0;
+    for (int r = blo / p.bpr; r <= bhi / p.bpr; ++r) {
+      const int c_hi = (r == bhi / p.bpr) ? bhi % p.bpr : p.bpr - 1;
+      key = max(key, ((r - p.self + p.R) % p.R) * p.bpr + c_hi);
+    }
+    s_key[t] = key;
+  }
+  __syncthreads();
+  // 6. consumer order: tiles by (key, index)
+  for (int t = tid; t < ntiles; t += ROUTE_THREADS) {
+    const int kt = s_key[t];
+    int rank = 0;
+    for (int u = 0; u < ntiles; ++u) {
+      const int ku = s_key[u];
+      rank += (ku < kt) || (ku == kt && u < t);
+    }
+    order[rank] = t;
+  }
+}
+
+struct MoeParams {
+  CUtensorMap map_a;               // sorted tokens [P, H]
+  CUtensorMap map_w[MOE_MAX_E];    // W_e [H, N]
+  const uint8_t* x[MOE_MAX_R];     // shards [T_r, H]
+  uint8_t* sorted;
+  uint16_t* Y;
+  const int32_t* ws;
+  uint32_t* flags;
+  uint32_t* status;
+  int32_t* trace;
+  uint64_t timeout_ns;
+  uint64_t pipe_timeout_ns;
+  int32_t R, self, T_r, H, N, E, k, rpb, bpr, Nt, KB, num_items, max_tiles;
+  uint32_t epoch;
+};
+
+__global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_constant__ MoeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + MOE_SMEM_BARS);
+  const int warp = int(warp_id());
+  const int lane = int(lane_id());
+  const int32_t* tiles = p.ws + ws_tiles(p.max_tiles);
+  const int32_t* order = p.ws + ws_order(p.max_tiles);
+  const int32_t* inv = p.ws + ws_inv(p.max_tiles);
+  const int num_work = p.ws[0] * p.Nt;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars->tmem_full[a], 1);
+      mbar_init(&bars->tmem_empty[a], kNumEpiWarps);
+    }
+    for (int b = 0; b < COPY_NBUF; ++b) mbar_init(&bars->copy[b], 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = bars->tmem_base;
+  volatile uint32_t* abort = &bars->abort;
+
+  if (warp == kWarpTma) {
+    // ---------------------------------------------------------------- TMA producer
+    int s = 0;
+    uint32_t ph = 0;
+    int last_t = -1;
+    for (int w = blockIdx.x; w < num_work; w += gridDim.x) {
+      const int t = order[w / p.Nt];
+      const int n = w % p.Nt;
+      const int32_t* tr = tiles + 6 * t;
+      const int e = tr[0], row0 = tr[1];
+      if (t != last_t) {
+        // consume_tile_wait through the lookup table: every barrier in [lo, hi]
+        for (int id = tr[3] + lane; id <= tr[4]; id += 32)
+          wait_flag(p.flags + id, p.epoch, p.status, p.timeout_ns, uint32_t(id), TL_ERR_TIMEOUT);
+      }
+      last_t = t;
+      __syncwarp();
+      if (lane == 0) {
+        if (p.trace) p.trace[w] = t * p.Nt + n;
+        fence_proxy_async_global();
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort, p.status, p.pipe_timeout_ns, 1)) break;
+          mbar_arrive_expect_tx(&bars->full[s], STAGE_TX);
+          tma_load_2d(smem + SMEM_A + s * A_STAGE_BYTES, &p.map_a, &bars->full[s], kb * BK, row0);
+          uint8_t* b_dst = smem + SMEM_B + s * B_STAGE_BYTES;
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i)
+            tma_load_2d(b_dst + i * B_BOX_BYTES, &p.map_w[e], &bars->full[s], n * BN + i * 64, kb * BK);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      if (__shfl_sync(0xffffffffu, *abort, 0)) break;
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int j = 0;
+      for (int w = blockIdx.x; w < num_work && !*abort; w += gridDim.x, ++j) {
+        const int acc = j & 1;
+        const uint32_t acc_ph = uint32_t(j >> 1) & 1u;
+        if (!mbar_wait(&bars->tmem_empty[acc], acc_ph ^ 1u, abort, p.status, p.pipe_timeout_ns, 2)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!mbar_wait(&bars->full[s], ph, abort, p.status, p.pipe_timeout_ns, 3)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          mma_kblock(smem, s, d_tmem, kb == 0);
+          tc_commit(&bars->empty[s]);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(&bars->tmem_full[acc]);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
+    // ---------------------------------------------------------------- epilogue: rows of this expert only
+    const int wq = warp & 3;
+    int j = 0;
+    for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++j) {
+      const int acc = j & 1;
+      const uint32_t acc_ph = uint32_t(j >> 1) & 1u;
+      const int32_t* tr = tiles + 6 * order[w / p.Nt];
+      const int n = w % p.Nt;
+      const int row0 = tr[1], rows = tr[2];
+      const bool ok = mbar_wait(&bars->tmem_full[acc], acc_ph, abort, p.status, p.pipe_timeout_ns, 4);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int lr = wq * 32 + lane;
+      const bool row_ok = lr < rows;
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = n * BN + c * 32;
+        if (col0 >= p.N) break;
+        uint32_t v[32];
+        tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * BN + c * 32), v);
+        tmem_ld_wait();
+        if (row_ok) {
+          uint16_t* yrow = p.Y + size_t(row0 + lr) * p.N + col0;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (col0 + g * 8 < p.N) {
+              const float* f = reinterpret_cast<const float*>(v + g * 8);
+              st_global_v4(yrow + g * 8, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                           pack_bf16x2(f[6], f[7]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tmem_empty[acc]);
+    }
+  } else if (warp == kWarpCopy) {
+    // ---------------------------------------------------------------- AllGather + local scatter
+    if (lane == 0) {
+      uint8_t* stage = smem + MOE_SMEM_COPY;
+      const uint32_t row_bytes = uint32_t(p.H) * 2u;
+      const int pieces = int((row_bytes + COPY_CHUNK - 1) / COPY_CHUNK);
+      uint32_t seq = 0;  // pieces loaded by this CTA: buffer seq % NBUF, parity (seq / NBUF) & 1
+      bool dead = false;
+      for (int it = blockIdx.x; it < p.num_items && !dead; it += gridDim.x) {
+        const int jj = it / p.bpr, c = it % p.bpr;
+        const int r = (p.self + jj) % p.R;  // shards self, self+1, ...
+        const int t0 = c * p.rpb, t1 = min(p.T_r, t0 + p.rpb);
+        const int nunits = (t1 - t0) * pieces;
+        int issued = 0, stored = 0;
+        while (stored < nunits) {
+          while (issued < nunits && issued - stored < COPY_NBUF) {
+            const uint32_t q = seq + uint32_t(issued);
+            const int buf = int(q % COPY_NBUF);
+            bulk_wait_read_dyn(stored - issued + COPY_NBUF - 1);
+            const int tl = t0 + issued / pieces, pc = issued % pieces;
+            const uint32_t off = uint32_t(pc) * COPY_CHUNK;
+            const uint32_t sz = min(COPY_CHUNK, row_bytes - off);
+            mbar_arrive_expect_tx(&bars->copy[buf], sz);
+            bulk_g2s(stage + buf * COPY_CHUNK, p.x[r] + size_t(tl) * row_bytes + off, sz, &bars->copy[buf]);
+            ++issued;
+          }
+          const uint32_t q = seq + uint32_t(stored);
+          const int buf = int(q % COPY_NBUF);
+          if (!mbar_wait(&bars->copy[buf], (q / COPY_NBUF) & 1u, abort, p.status, p.pipe_timeout_ns, 5)) {
+            dead = true;
+            break;
+          }
+          const int tl = t0 + stored / pieces, pc = stored % pieces;
+          const uint32_t off = uint32_t(pc) * COPY_CHUNK;
+          const uint32_t sz = min(COPY_CHUNK, row_bytes - off);
+          const int tok = r * p.T_r + tl;
+          for (int sl = 0; sl < p.k; ++sl) {
+            const int pos = inv[tok * p.k + sl];
+            bulk_s2g(p.sorted + size_t(pos) * row_bytes + off, stage + buf * COPY_CHUNK, sz);
+          }
+          bulk_commit();
+          ++stored;
+        }
+        seq += uint32_t(nunits);
+        bulk_wait<0>();
+        if (dead) break;
+        fence_proxy_async_global();
+        st_release(p.flags + r * p.bpr + c, p.epoch);
+      }
+      bulk_wait<0>();
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort) {
+    const uint64_t t0 = now_ns();
+    while (now_ns() - t0 < 50000) {
+    }
+  }
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+int moe_max_tiles(int P, int E) { return (P + BM - 1) / BM + E; }
+
+int moe_default_rpb(int H, int T_r) { return std::min(T_r, std::max(1, int(32768 / (size_t(H) * 2)))); }
+
+}  // namespace
+}  // namespace tl
+
+extern "C" size_t tl_moe_workspace_size(int R, int T_r, int E, int topk) {
+  if (R < 1 || T_r < 1 || E < 1 || topk < 1) return 0;
+  const long long P = (long long)R * T_r * topk;
+  if (P > (1ll << 30)) return 0;
+  const int mt = tl::moe_max_tiles(int(P), E);
+  return size_t(tl::ws_inv(mt) + P) * sizeof(int32_t);
+}
+
+extern "C" int tl_moe_num_flags(int R, int T_r, int H, int rows_per_barrier, int* effective_rpb) {
+  if (R < 1 || T_r < 1 || H < 1) return -1;
+  const int rpb = rows_per_barrier > 0 ? std::min(rows_per_barrier, T_r) : tl::moe_default_rpb(H, T_r);
+  if (effective_rpb) *effective_rpb = rpb;
+  return R * tl::cdiv(T_r, rpb);
+}
+
+extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
+  using namespace tl;
+  if (!a) return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: NULL args");
+  if (a->R < 1 || a->R > MOE_MAX_R)
+    return fail(a->R > MOE_MAX_R ? TL_ERR_UNSUPPORTED : TL_ERR_INVALID, "tl_moe_ag_gemm: R=%d outside 1..%d", a->R,
+                MOE_MAX_R);
+  if (a->E < 1 || a->E > MOE_MAX_E)
+    return fail(a->E > MOE_MAX_E ? TL_ERR_UNSUPPORTED : TL_ERR_INVALID, "tl_moe_ag_gemm: E=%d outside 1..%d", a->E,
+                MOE_MAX_E);
+  if (a->self_rank < 0 || a->self_rank >= a->R) return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: self_rank");
+  if (a->T_r < 1 || a->H < 1 || a->N < 1 || a->topk < 1 || a->topk > a->E)
+    return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: bad shape (T_r=%d H=%d N=%d topk=%d E=%d)", a->T_r, a->H, a->N,
+                a->topk, a->E);
+  if (a->H % 8 || a->N % 8)
+    return fail(TL_ERR_UNSUPPORTED, "tl_moe_ag_gemm: H (%d) and N (%d) must be multiples of 8", a->H, a->N);
+  if (!a->X || !a->topk_ids || !a->W || !a->sorted_tokens || !a->Y || !a->perm || !a->expert_offsets ||
+      !a->workspace || !a->signals)
+    return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: NULL pointer argument");
+  if (a->epoch == 0) return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: epoch must be nonzero");
+  for (int r = 0; r < a->R; ++r)
+    if (!a->X[r] || !aligned16(a->X[r])) return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: shard %d pointer", r);
+  for (int e = 0; e < a->E; ++e)
+    if (!a->W[e] || !aligned16(a->W[e])) return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: weight %d pointer", e);
+  if (!aligned16(a->sorted_tokens) || !aligned16(a->Y) || !aligned16(a->workspace) ||
+      (reinterpret_cast<uintptr_t>(a->topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(a->perm) & 3u) ||
+      (reinterpret_cast<uintptr_t>(a->expert_offsets) & 3u))
+    return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: pointer alignment");
+  const long long T = (long long)a->R * a->T_r;
+  const long long P = T * a->topk;
+  if (P > (1ll << 30)) return fail(TL_ERR_UNSUPPORTED, "tl_moe_ag_gemm: too many routed rows");
+  const int max_tiles = moe_max_tiles(int(P), a->E);
+  if (max_tiles > MOE_MAX_TILES)
+    return fail(TL_ERR_UNSUPPORTED, "tl_moe_ag_gemm: %d row tiles exceed %d", max_tiles, MOE_MAX_TILES);
+  const size_t need = tl_moe_workspace_size(a->R, a->T_r, a->E, a->topk);
+  if (a->workspace_bytes < need)
+    return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: workspace %zu bytes, need %zu", a->workspace_bytes, need);
+  int rpb = 0;
+  const int nflags = tl_moe_num_flags(a->R, a->T_r, a->H, a->rows_per_barrier, &rpb);
+  if (a->signals->num_flags < nflags)
+    return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: signals hold %d flags, need %d", a->signals->num_flags, nflags);
+  DeviceInfo di{};
+  if (tl_status s = device_info(&di)) return s;
+  if (a->signals->device != di.device) return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: signals belong to another device");
+  cudaStream_t st = (cudaStream_t)stream;
+
+  // 1. routing and lookup tables
+  RouteParams rp{};
+  rp.topk = a->topk_ids;
+  rp.perm = a->perm;
+  rp.offsets = a->expert_offsets;
+  rp.ws = static_cast<int32_t*>(a->workspace);
+  rp.status = a->signals->status;
+  rp.T = int(T);
+  rp.k = a->topk;
+  rp.E = a->E;
+  rp.R = a->R;
+  rp.T_r = a->T_r;
+  rp.rpb = rpb;
+  rp.bpr = cdiv(a->T_r, rpb);
+  rp.self = a->self_rank;
+  rp.max_tiles = max_tiles;
+  const size_t route_smem = (size_t(ROUTE_WARPS) * a->E + 2 * (a->E + 1) + max_tiles) * sizeof(int32_t);
+  if (tl_status s = cuda_ok(cudaFuncSetAttribute(reinterpret_cast<const void*>(&moe_route_kernel),
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(route_smem)),
+                            "cudaFuncSetAttribute(route)"))
+    return s;
+  moe_route_kernel<<<1, ROUTE_THREADS, route_smem, st>>>(rp);
+  if (tl_status s = cuda_ok(cudaGetLastError(), "route launch")) return s;
+
+  // 2. AllGather + scatter and grouped GEMM
+  MoeParams* p = new (std::nothrow) MoeParams;
+  if (!p) return fail(TL_ERR_INTERNAL, "out of host memory");
+  std::memset(p, 0, sizeof(MoeParams));
+  tl_status res = TL_OK;
+  do {
+    if ((res = make_map_bf16(&p->map_a, a->sorted_tokens, P, a->H, size_t(a->H) * 2, BM, BK))) break;
+    for (int e = 0; e < a->E && !res; ++e)
+      res = make_map_bf16(&p->map_w[e], a->W[e], a->H, a->N, size_t(a->N) * 2, BK, 64);
+    if (res) break;
+    for (int r = 0; r < a->R; ++r) p->x[r] = static_cast<const uint8_t*>(a->X[r]);
+    p->sorted = static_cast<uint8_t*>(a->sorted_tokens);
+    p->Y = static_cast<uint16_t*>(a->Y);
+    p->ws = static_cast<const int32_t*>(a->workspace);
+    p->flags = a->signals->flags;
+    p->status = a->signals->status;
+    p->trace = a->trace;
+    p->timeout_ns = a->timeout_ns ? a->timeout_ns : kDefaultTimeoutNs;
+    p->pipe_timeout_ns = 2 * p->timeout_ns + 1000000000ull;
+    p->R = a->R;
+    p->self = a->self_rank;
+    p->T_r = a->T_r;
+    p->H = a->H;
+    p->N = a->N;
+    p->E = a->E;
+    p->k = a->topk;
+    p->rpb = rpb;
+    p->bpr = cdiv(a->T_r, rpb);
+    p->Nt = cdiv(a->N, BN);
+    p->KB = cdiv(a->H, BK);
+    p->num_items = a->R * p->bpr;
+    p->max_tiles = max_tiles;
+    p->epoch = a->epoch;
+    const int grid = std::max(1, std::min(di.sm_count, std::max(max_tiles * p->Nt, p->num_items)));
+    void* args[] = {p};
+    res = launch_coop(reinterpret_cast<const void*>(&moe_gemm_kernel), grid, MOE_THREADS, MOE_SMEM_BYTES, st, args);
+  } while (false);
+  delete p;
+  return res;
+}
