@@ -102,6 +102,29 @@ tl_status tl_tile_wait(tl_signals* s, int first, int count, uint32_t value,
  * that failed (-1 if none).  Either out pointer may be NULL. */
 tl_status tl_query_status(tl_signals* s, void* stream, int* code, int* where);
 
+/* ---------------------------------------------------------------- GEMM
+ * C = A . B, bf16 in, fp32 accumulate, bf16 (and optionally fp32) out, with no
+ * communication and no waits: the compute half of AllGather-GEMM alone, used to
+ * measure the fused kernels' overlap and as the compute step of a decomposed
+ * (per-shard, multi-stream) baseline (talk summary, Background: decomposition-
+ * based overlap splits operators into sub-operators on several streams).
+ * tcgen05 MMAs of pairs of CTAs (cta_group::2), 256 x 256 tiles.
+ */
+typedef struct tl_gemm_args {
+  int32_t M;                   /* rows of A and C, >= 1 */
+  int32_t N;                   /* columns of B and C, multiple of 8 */
+  int32_t K;                   /* contraction, multiple of 8 */
+  int32_t reserved0;
+  const void* A;               /* device bf16 [M, K] */
+  const void* B;               /* device bf16 [K, N] */
+  void* C;                     /* device bf16 [M, N], written */
+  float* C_f32;                /* optional device float [M, N], written; NULL = none */
+  tl_signals* signals;         /* receives device-side errors in its status word (any size >= 1) */
+  uint64_t timeout_ns;         /* bound of the pipeline waits is 2 * timeout + 1 s; 0 = 1 s */
+} tl_gemm_args;
+
+tl_status tl_gemm(const tl_gemm_args* args, void* stream);
+
 /* ---------------------------------------------------------------- AllGather-GEMM
  * C = G . B with G = [A_0; A_1; ...; A_{R-1}] (talk summary, Key Findings and
  * Experimental Setup & Results: AllGather-GEMM).  One launch holds both sides:

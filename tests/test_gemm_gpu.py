@@ -1,0 +1,56 @@
+"""Plain GEMM (CTA-pair tcgen05 kernel) through the C ABI against the oracle
+(an AllGather-GEMM over one shard is the plain product)."""
+import numpy as np
+import pytest
+
+import oracle
+from tests.helpers import check_bf16, check_f32, dev_bf16, to_bits, to_f64
+from tile_centric_gemm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    import __graft_entry__
+    __graft_entry__.build()
+    from tile_centric_gemm_gb300 import binding
+    return binding
+
+
+def run_gemm(B, A, Bm, f32=True):
+    import torch
+    M, K = A.shape
+    N = Bm.shape[1]
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    C32 = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") if f32 else None
+    sig = B.Signals(1)
+    B.tl_gemm(dev_bf16(A), dev_bf16(Bm), C, sig, C_f32=C32)
+    assert B.tl_query_status(sig) == (0, -1)
+    return C, C32
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (512, 512, 512), (300, 264, 136), (8, 8, 8), (1000, 1032, 520),
+                                   (2048, 1792, 4096)])
+def test_gemm_parity(B, M, N, K):
+    A, Bm = inputs.ag_gemm_inputs(1, M, K, N, "normal", seed=M + N + K)
+    C, C32 = run_gemm(B, A[0], Bm)
+    want = oracle.ag_gemm.ag_gemm(A, Bm)
+    check_bf16(to_f64(C), want, "C")
+    check_f32(to_f64(C32), want, "C_f32")
+
+
+def test_gemm_identity_exact(B):
+    A = inputs.uniform_bf16((512, 256), 3)
+    eye = inputs.bf16_bits_from_f32(np.eye(256, dtype=np.float32))
+    C, _ = run_gemm(B, A, eye, f32=False)
+    np.testing.assert_array_equal(to_bits(C), A)
+
+
+@pytest.mark.slow
+def test_gemm_llm_shape_sampled(B):
+    A, Bm = inputs.ag_gemm_inputs(1, 8192, 4096, 1792, "normal", seed=1)
+    C, _ = run_gemm(B, A[0], Bm, f32=False)
+    rng = np.random.default_rng(0)
+    rows, cols = rng.integers(0, 8192, 3000), rng.integers(0, 1792, 3000)
+    check_bf16(to_f64(C)[rows, cols], oracle.ag_gemm.ag_gemm_at(A, Bm, rows, cols), "C sampled")

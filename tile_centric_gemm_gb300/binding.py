@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "TL_OK", 1: "TL_ERR_INVALID", 2: "TL_ERR_CUDA", 3: "TL_ERR_TI
 EXPORTED = [
     "tl_version", "tl_last_error", "tl_signals_create", "tl_signals_destroy", "tl_signals_flags",
     "tl_signals_reset", "tl_tile_notify", "tl_tile_wait", "tl_query_status",
-    "tl_ag_gemm_num_flags", "tl_ag_gemm_tile_order", "tl_ag_gemm",
+    "tl_gemm", "tl_ag_gemm_num_flags", "tl_ag_gemm_tile_order", "tl_ag_gemm",
     "tl_gemm_rs_workspace_size", "tl_gemm_rs_num_flags", "tl_gemm_rs", "tl_gemm_rs_noalloc",
     "tl_moe_workspace_size", "tl_moe_num_flags", "tl_moe_ag_gemm",
 ]
@@ -51,6 +51,13 @@ class tl_ag_gemm_args(ctypes.Structure):
         ("signals", _vp), ("src_ready", _vp),
         ("epoch", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
         ("timeout_ns", ctypes.c_uint64), ("trace", _vp),
+    ]
+
+
+class tl_gemm_args(ctypes.Structure):
+    _fields_ = [
+        ("M", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("A", _vp), ("B", _vp), ("C", _vp), ("C_f32", _vp), ("signals", _vp), ("timeout_ns", ctypes.c_uint64),
     ]
 
 
@@ -92,6 +99,7 @@ _decl("tl_signals_reset", _i, _vp, _vp)
 _decl("tl_tile_notify", _i, _vp, _i, _i, _u32, _vp)
 _decl("tl_tile_wait", _i, _vp, _i, _i, _u32, _u64, _vp)
 _decl("tl_query_status", _i, _vp, _vp, ctypes.POINTER(_i), ctypes.POINTER(_i))
+_decl("tl_gemm", _i, ctypes.POINTER(tl_gemm_args), _vp)
 _decl("tl_ag_gemm_num_flags", _i, _i, _i, _i, _i, ctypes.POINTER(_i))
 _decl("tl_ag_gemm_tile_order", _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int32), _i)
 _decl("tl_ag_gemm", _i, ctypes.POINTER(tl_ag_gemm_args), _vp)
@@ -202,6 +210,15 @@ def tl_query_status(sig: Signals, stream=None):
     if rc not in (TL_OK,) and code.value == 0:
         _check(rc)
     return code.value, where.value
+
+
+def tl_gemm(A, B, C, signals: Signals, *, C_f32=None, timeout_ns=0, stream=None):
+    """C = A . B (bf16 in, fp32 accumulate) with no communication."""
+    M, K = A.shape
+    N = B.shape[1]
+    a = tl_gemm_args(M=M, N=N, K=K, reserved0=0, A=_ptr(A), B=_ptr(B), C=_ptr(C), C_f32=_ptr(C_f32),
+                     signals=signals.handle, timeout_ns=int(timeout_ns))
+    _check(lib.tl_gemm(ctypes.byref(a), _stream(stream)))
 
 
 def tl_ag_gemm_num_flags(R, M_shard, K, rows_per_barrier=0):

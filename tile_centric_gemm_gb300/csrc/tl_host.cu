@@ -98,28 +98,48 @@ tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint6
   return TL_OK;
 }
 
-tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cudaStream_t st, void** args) {
+tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cudaStream_t st, void** args,
+                      int cluster) {
   if (tl_status s = cuda_ok(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
                             "cudaFuncSetAttribute(max dynamic smem)"))
     return s;
-  int per_sm = 0;
-  if (tl_status s = cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, smem), "occupancy"))
-    return s;
   DeviceInfo di{};
   if (tl_status s = device_info(&di)) return s;
-  if (per_sm < 1 || grid > per_sm * di.sm_count)
-    return fail(TL_ERR_UNSUPPORTED, "grid of %d CTAs cannot be co-resident (%d per SM x %d SMs)", grid, per_sm,
-                di.sm_count);
+  if (cluster < 1 || grid % cluster) return fail(TL_ERR_INTERNAL, "grid %d is not a multiple of cluster %d", grid, cluster);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  int nattr = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = unsigned(cluster);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    nattr = 2;
+    int max_clusters = 0;
+    cfg.attrs = attr + 1;
+    cfg.numAttrs = 1;
+    if (tl_status s = cuda_ok(cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg), "cluster occupancy"))
+      return s;
+    if (grid / cluster > max_clusters)
+      return fail(TL_ERR_UNSUPPORTED, "%d clusters of %d CTAs cannot be co-resident (at most %d)", grid / cluster,
+                  cluster, max_clusters);
+  } else {
+    int per_sm = 0;
+    if (tl_status s = cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, smem),
+                              "occupancy"))
+      return s;
+    if (per_sm < 1 || grid > per_sm * di.sm_count)
+      return fail(TL_ERR_UNSUPPORTED, "grid of %d CTAs cannot be co-resident (%d per SM x %d SMs)", grid, per_sm,
+                  di.sm_count);
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = nattr;
   return cuda_ok(cudaLaunchKernelExC(&cfg, kernel, args), "cooperative launch");
 }
 

@@ -92,14 +92,19 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     __syncwarp();
   }
   __syncthreads();
-  // 2. expert counts, exclusive scan, and each warp's first position per expert
+  // 2. expert counts (one thread per expert), exclusive scan, and each warp's
+  //    first position per expert
+  for (int e = tid; e < E; e += ROUTE_THREADS) {
+    int c = 0;
+    for (int w = 0; w < ROUTE_WARPS; ++w) c += cnt[w * E + e];
+    s_toff[e] = c;  // counts, parked in the tile-offset array until step 4
+  }
+  __syncthreads();
   if (tid == 0) {
     int acc = 0;
     for (int e = 0; e < E; ++e) {
       s_off[e] = acc;
-      int c = 0;
-      for (int w = 0; w < ROUTE_WARPS; ++w) c += cnt[w * E + e];
-      acc += c;
+      acc += s_toff[e];
     }
     s_off[E] = acc;
   }
@@ -144,20 +149,19 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   __syncthreads();
   for (int e = tid; e <= E; e += ROUTE_THREADS) p.offsets[e] = s_off[e];
   const int ntiles = min(s_toff[E], p.max_tiles);
-  // 5. the tile table: rows of a tile are one expert's, tokens ascending
-  for (int t = tid; t < ntiles; t += ROUTE_THREADS) {
-    int lo_e = 0, hi_e = E - 1;  // last expert whose first tile <= t
+  // 5. the tile table, one warp per tile: rows of a tile are one expert's, tokens ascending
+  for (int t = warp; t < ntiles; t += ROUTE_WARPS) {
+    int lo_e = 0, hi_e = E - 1;  // last expert whose first tile <= t (empty experts are skipped over)
     while (lo_e < hi_e) {
       const int mid = (lo_e + hi_e + 1) >> 1;
       if (s_toff[mid] <= t) lo_e = mid; else hi_e = mid - 1;
     }
     const int e = lo_e;
-    const int j = t - s_toff[e];
-    const int row0 = s_off[e] + j * BM;
+    const int row0 = s_off[e] + (t - s_toff[e]) * BM;
     const int rows = min(BM, s_off[e + 1] - row0);
     uint32_t mask = 0;
     int blo = 0x7fffffff, bhi = -1;
-    for (int i = 0; i < rows; ++i) {
+    for (int i = lane; i < rows; i += 32) {
       const int tok = p.perm[row0 + i] / p.k;
       const int r = tok / p.T_r;
       const int b = r * p.bpr + (tok % p.T_r) / p.rpb;
@@ -165,21 +169,29 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
       blo = min(blo, b);
       bhi = max(bhi, b);
     }
-    int32_t* tr = tiles + 6 * t;
-    tr[0] = e;
-    tr[1] = row0;
-    tr[2] = rows;
-    tr[3] = blo;
-    tr[4] = bhi;
-    tr[5] = int32_t(mask);
-    // arrival key: latest position among the barriers in [blo, bhi]; barrier (r, c)
-    // arrives at ((r - self) mod R) * bpr + c
-    int key = 0;
-    for (int r = blo / p.bpr; r <= bhi / p.bpr; ++r) {
-      const int c_hi = (r == bhi / p.bpr) ? bhi % p.bpr : p.bpr - 1;
-      key = max(key, ((r - p.self + p.R) % p.R) * p.bpr + c_hi);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mask |= __shfl_xor_sync(0xffffffffu, mask, o);
+      blo = min(blo, __shfl_xor_sync(0xffffffffu, blo, o));
+      bhi = max(bhi, __shfl_xor_sync(0xffffffffu, bhi, o));
     }
-    s_key[t] = key;
+    if (lane == 0) {
+      int32_t* tr = tiles + 6 * t;
+      tr[0] = e;
+      tr[1] = row0;
+      tr[2] = rows;
+      tr[3] = blo;
+      tr[4] = bhi;
+      tr[5] = int32_t(mask);
+      // arrival key: latest position among the barriers in [blo, bhi]; barrier (r, c)
+      // arrives at ((r - self) mod R) * bpr + c
+      int key = 0;
+      for (int r = blo / p.bpr; r <= bhi / p.bpr; ++r) {
+        const int c_hi = (r == bhi / p.bpr) ? bhi % p.bpr : p.bpr - 1;
+        key = max(key, ((r - p.self + p.R) % p.R) * p.bpr + c_hi);
+      }
+      s_key[t] = key;
+    }
   }
   __syncthreads();
   // 6. consumer order: tiles by (key, index)
