@@ -132,12 +132,13 @@ tl_status tl_gemm(const tl_gemm_args* args, void* stream);
  *    `gathered` with bulk TMA copies and release one flag per row chunk
  *    (produce_tile_notify).  Pull mode first waits on the source's readiness
  *    flag of the same id (two barriers per tile); push mode has one barrier.
- *  - consumer: tcgen05 GEMM tiles of 128 x 256 acquire every flag guarding
- *    their rows (consume_tile_wait; flag id = rank * barriers_per_rank +
+ *  - consumer: tcgen05 GEMM tiles of 256 x 256 on pairs of CTAs
+ *    (cta_group::2); each CTA acquires every flag guarding its 128 rows
+ *    (consume_tile_wait; flag id = rank * barriers_per_rank +
  *    row_in_shard / rows_per_barrier, an affine map of the row) before loading
- *    A, and run in arrival order: shards self, self+1, ..., self+R-1
- *    (consume_tile_swizzle).  Tiles wholly inside the self shard read A_self in
- *    place and never wait.  Copies run in the order self+1, ..., self+R-1, self.
+ *    them, and tiles run in arrival order: shards self, self+1, ..., self+R-1
+ *    (consume_tile_swizzle).  Row halves wholly inside the self shard read
+ *    A_self in place and never wait.  Copies run in the order self+1, ..., self+R-1, self.
  * Output is independent of self_rank, mode and rows_per_barrier.
  */
 typedef struct tl_ag_gemm_args {
@@ -159,16 +160,17 @@ typedef struct tl_ag_gemm_args {
   uint32_t epoch;              /* nonzero */
   uint32_t reserved1;
   uint64_t timeout_ns;         /* 0 = 1 s */
-  int32_t* trace;              /* optional device int32 [num m tiles * num n tiles]:
-                                  trace[slot] = m_tile * n_tiles + n_tile of the tile
-                                  the consumer ran at schedule slot `slot` */
+  int32_t* trace;              /* optional device int32 [ceil(M/256) * ceil(N/256)]:
+                                  trace[slot] = m_tile * n_tiles + n_tile of the 256 x 256
+                                  tile the consumer ran at schedule slot `slot` */
 } tl_ag_gemm_args;
 
 /* Flags an AG-GEMM call needs: R * ceil(M_shard / rows_per_barrier) (after
  * replacing 0 by the default); also returns the effective rows_per_barrier. */
 int tl_ag_gemm_num_flags(int R, int M_shard, int K, int rows_per_barrier, int* effective_rpb);
 /* Host copy of the consumer's row-tile order (the swizzle): writes the
- * ceil(R*M_shard/128) m-tile indices in the order the consumer runs them. */
+ * ceil(R*M_shard/256) m-tile indices (256-row tiles) in the order the consumer
+ * runs them. */
 tl_status tl_ag_gemm_tile_order(int R, int self_rank, int M_shard, int32_t* m_order, int capacity);
 tl_status tl_ag_gemm(const tl_ag_gemm_args* args, void* stream);
 
@@ -176,16 +178,18 @@ tl_status tl_ag_gemm(const tl_ag_gemm_args* args, void* stream);
  * out[d] = rows [d*M/R, (d+1)*M/R) of S = (((P_0 + P_1) + P_2) + ...), P_r =
  * A_r . B_r (talk summary, Key Findings and Technical Deep Dive: a persistent
  * GEMM that notifies each finished partial tile, and a reduce stage that waits
- * on its own and its peers' tiles).  One launch: every 128 x 256 partial tile
- * (fp32) is pushed into a receive slot of `workspace` (a ring of two waves of
- * slots, reused as the launch proceeds) and its flag released; output tiles
- * run in destination order, m tiles innermost, and the R partial tiles of one
- * output tile are produced back to back, rank (d + 1 + tau + j) mod R at
- * position j of output tile tau.  The CTAs that computed them each reduce one
- * row slice of the tile after waiting on all R flags, adding the partials in
- * rank order 0..R-1 in fp32, and write bf16 rows into out[d].  Flags: one
- * arrival flag per (tile, rank) and one "reduced" flag per (tile, slice); a
- * pusher reuses a ring slot only after the reduced flags of its previous tile.
+ * on its own and its peers' tiles).  One launch on pairs of CTAs
+ * (cta_group::2, 256 x 256 tiles; CTA h of a pair owns rows h*128..h*128+127
+ * of every tile): every fp32 partial half-tile is pushed into a receive slot of
+ * `workspace` (a ring of two waves of slots, reused as the launch proceeds)
+ * and its arrival flag released; output tiles run in destination order, m
+ * tiles innermost, and the R partials of one output tile are produced back to
+ * back, rank (d + 1 + tau + j) mod R at position j of output tile tau.
+ * Reducer warps of the CTAs that computed them each reduce one row slice of
+ * their half after acquiring its R arrival flags, adding the partials in rank
+ * order 0..R-1 in fp32, write bf16 rows into out[d], and release a "reduced"
+ * flag; a pusher reuses a ring slot only after the reduced flags of the tile
+ * that used it before.
  */
 typedef struct tl_gemm_rs_args {
   int32_t R;                   /* ranks, 1..TL_MAX_RANKS */
@@ -201,17 +205,17 @@ typedef struct tl_gemm_rs_args {
   uint32_t epoch;              /* nonzero */
   uint32_t reserved0;
   uint64_t timeout_ns;         /* 0 = 1 s */
-  int32_t* trace;              /* optional device int32 [tl_gemm_rs_num_flags(R, M, N) / 2]:
+  int32_t* trace;              /* optional device int32 [tl_gemm_rs_num_flags(R, M, N) / 4]:
                                   trace[item] = ((d * m_tiles + m) * n_tiles + n) * R + r,
                                   the output tile and rank of each produced partial,
-                                  m_tiles = ceil(M/R/128), n_tiles = ceil(N/256) */
+                                  m_tiles = ceil(M/R/256), n_tiles = ceil(N/256) */
 } tl_gemm_rs_args;
 
-/* Workspace bytes for the current device: min(items, 2 * CTAs) slots of
- * 128 KiB, CTAs = the largest multiple of R not above the SM count. */
+/* Workspace bytes for the current device: min(items, 2 * pairs) items of two
+ * 128 KiB half-slots, pairs = half the SM count. */
 size_t tl_gemm_rs_workspace_size(int R, int M, int N);
-/* Flags a GEMM-RS call needs: 2 * R * tiles (arrival and reduced flags),
- * tiles = R * ceil(M/R/128) * ceil(N/256). */
+/* Flags a GEMM-RS call needs: 4 * R * tiles (arrival and reduced flags for
+ * both halves), tiles = R * ceil(M/R/256) * ceil(N/256). */
 int tl_gemm_rs_num_flags(int R, int M, int N);
 tl_status tl_gemm_rs(const tl_gemm_rs_args* args, void* stream);
 

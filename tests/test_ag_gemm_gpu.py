@@ -49,7 +49,7 @@ def run_ag(B, A, Bm, *, self_rank=0, mode=None, rpb=0, f32=False, notify_ready=T
             B.tl_tile_notify(ready, 0, nflags, epoch)
             if withhold is not None:
                 B.tl_tile_notify(ready, withhold, 1, epoch - 1)
-    Mt, Nt = -(-R * Ms // 128), -(-N // 256)
+    Mt, Nt = -(-R * Ms // 256), -(-N // 256)
     tr = torch.full((Mt * Nt,), -1, dtype=torch.int32, device="cuda") if trace else None
     B.tl_ag_gemm(dA, dB, G, C, sig, epoch, self_rank=self_rank, C_f32=C32, mode=mode, src_ready=ready,
                  rows_per_barrier=rpb, timeout_ns=timeout_ns, trace=tr)
@@ -70,7 +70,7 @@ def check_all(B, A, Bm, r, self_rank=0):
     assert np.all(flags[:r["nflags"]] == r["epoch"])
     if r["trace"] is not None:
         R, Ms, N = len(A), A[0].shape[0], Bm.shape[1]
-        order = oracle.ag_gemm.consumer_order(R, self_rank, Ms, N, 128, 256)
+        order = oracle.ag_gemm.consumer_order(R, self_rank, Ms, N, 256, 256)
         want_trace = [m * r["Nt"] + n for (m, n) in order]
         assert r["trace"].cpu().tolist() == want_trace
 
@@ -160,7 +160,7 @@ def test_ag_llm_full_size_sampled(B):
     check_bf16(got, want, "C sampled")
     # every element: finite (no NaN left from the poison) and the trace is the swizzle
     assert np.isfinite(to_f64(r["C"])).all()
-    order = oracle.ag_gemm.consumer_order(c["R"], 0, c["M_shard"], N, 128, 256)
+    order = oracle.ag_gemm.consumer_order(c["R"], 0, c["M_shard"], N, 256, 256)
     assert r["trace"].cpu().tolist() == [m * r["Nt"] + n for (m, n) in order]
 
 
@@ -175,5 +175,5 @@ def test_ag_sweep_points(B, R, M):
     rng = np.random.default_rng(R)
     rows, cols = rng.integers(0, M, 2000), rng.integers(0, 1024, 2000)
     check_bf16(to_f64(r["C"])[rows, cols], oracle.ag_gemm.ag_gemm_at(A, Bm, rows, cols), "C sampled")
-    order = oracle.ag_gemm.consumer_order(R, R - 1, M // R, 1024, 128, 256)
+    order = oracle.ag_gemm.consumer_order(R, R - 1, M // R, 1024, 256, 256)
     assert r["trace"].cpu().tolist() == [m * r["Nt"] + n for (m, n) in order]

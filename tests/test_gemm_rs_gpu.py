@@ -43,8 +43,8 @@ def run_rs(B, A, Bl, *, timeout_ns=0):
 
 
 def expected_trace(R, M, N):
-    Mt, Nt = -(-(M // R) // 128), -(-N // 256)
-    return [((d * Mt + m) * Nt + n) * R + r for (_, d, m, n, r) in oracle.gemm_rs.item_order(R, M, N, 128, 256)]
+    Mt, Nt = -(-(M // R) // 256), -(-N // 256)
+    return [((d * Mt + m) * Nt + n) * R + r for (_, d, m, n, r) in oracle.gemm_rs.item_order(R, M, N, 256, 256)]
 
 
 def check(B, A, Bl, r):
@@ -54,7 +54,7 @@ def check(B, A, Bl, r):
         check_bf16(to_f64(o), w, f"out[{d}]")
     assert np.all(r["sig"].read_flags()[:r["nflags"]] == r["epoch"])
     R, M, N = len(A), A[0].shape[0], Bl[0].shape[1]
-    assert r["trace"].cpu().tolist()[:r["nflags"] // 2] == expected_trace(R, M, N)
+    assert r["trace"].cpu().tolist()[:r["nflags"] // 4] == expected_trace(R, M, N)
 
 
 @pytest.mark.parametrize("R,M,K_r,N", [
@@ -132,7 +132,7 @@ def test_rs_llm_full_size_sampled(B):
     r = run_rs(B, A, Bl)
     assert r["status"] == (0, -1)
     assert np.all(r["sig"].read_flags() == r["epoch"])
-    assert r["trace"].cpu().tolist()[:r["nflags"] // 2] == expected_trace(R, M, N)
+    assert r["trace"].cpu().tolist()[:r["nflags"] // 4] == expected_trace(R, M, N)
     rng = np.random.default_rng(2)
     rows = np.concatenate([rng.integers(0, M, 2500), [0, M - 1]])
     cols = np.concatenate([rng.integers(0, N, 2500), [N - 1, 0]])

@@ -46,8 +46,8 @@ def test_ag_tile_order_matches_oracle(B):
     import oracle
     for (R, s, Ms) in [(2, 0, 128), (8, 0, 1024), (8, 3, 1024), (3, 1, 100), (5, 4, 77), (1, 0, 300), (4, 2, 256)]:
         got = B.tl_ag_gemm_tile_order(R, s, Ms)
-        Mt = -(-R * Ms // 128)
-        want = [m for (m, n) in oracle.ag_gemm.consumer_order(R, s, Ms, 256, 128, 256)]
+        Mt = -(-R * Ms // 256)
+        want = [m for (m, n) in oracle.ag_gemm.consumer_order(R, s, Ms, 256, 256, 256)]
         assert got == want[:Mt] and len(got) == Mt
 
 

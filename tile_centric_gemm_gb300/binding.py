@@ -228,7 +228,7 @@ def tl_ag_gemm_num_flags(R, M_shard, K, rows_per_barrier=0):
 
 
 def tl_ag_gemm_tile_order(R, self_rank, M_shard):
-    Mt = -(-R * M_shard // 128)
+    Mt = -(-R * M_shard // 256)
     out = (ctypes.c_int32 * Mt)()
     _check(lib.tl_ag_gemm_tile_order(R, self_rank, M_shard, out, Mt))
     return list(out)

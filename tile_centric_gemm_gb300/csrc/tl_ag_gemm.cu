@@ -8,12 +8,12 @@
 //    barrier); a wait's tile id maps affinely to (rank, barrier); consumer
 //    tiles are swizzled into data-arrival order.
 //
-// Every CTA of a persistent, cooperative grid (one CTA per SM) has:
-//   warp 0      TMA producer: acquires the arrival flags of a row tile, then
-//               streams A (gathered rows, or the self shard in place) and B
-//               k-blocks into a 4-stage shared-memory ring.
-//   warp 1      tcgen05 MMA issuer: 128x256x16 bf16 MMAs into one of two TMEM
-//               accumulators.
+// A persistent, cooperative grid of CTA pairs (clusters of two, one CTA per
+// SM) computes 256 x 256 tiles with tcgen05.mma.cta_group::2.  Every CTA has:
+//   warp 0      TMA producer: acquires the arrival flags of its 128 rows of a
+//               tile, then streams its rows of A (gathered, or the self shard in
+//               place) and its 128 columns of B into a 6-stage ring.
+//   warp 1      MMA issuer (leader CTA of the pair only).
 //   warps 2-5   epilogue: TMEM -> registers -> bf16 (and fp32) rows of C.
 //   warp 6      copy (AllGather producer): bulk-TMA copies of shard row chunks
 //               into `gathered`, then a release store of the chunk's flag.
@@ -22,23 +22,23 @@
 #include <new>
 #include <vector>
 
-#include "tl_common.cuh"
 #include "tl_internal.h"
+#include "tl_pair.cuh"
 
 namespace tl {
 namespace {
 
-constexpr int AG_MAX_MTILES = 1024;
+constexpr int AG_MAX_MTILES = 1024;  // 256-row pair tiles
 constexpr int kWarpCopy = 6;
 constexpr int AG_THREADS = 7 * 32;
-constexpr uint32_t AG_SMEM_COPY = SMEM_GEMM_END;
+constexpr uint32_t AG_SMEM_COPY = pair::SMEM_END;
 constexpr uint32_t AG_SMEM_BARS = AG_SMEM_COPY + COPY_NBUF * COPY_CHUNK;
-constexpr uint32_t AG_SMEM_BYTES = AG_SMEM_BARS + sizeof(Barriers) + 1024;
+constexpr uint32_t AG_SMEM_BYTES = AG_SMEM_BARS + sizeof(pair::Bars) + 1024;
 
 struct AgParams {
-  CUtensorMap map_g;     // gathered [M, K]
-  CUtensorMap map_self;  // A_self [M_shard, K]
-  CUtensorMap map_b;     // B [K, N]
+  CUtensorMap map_g;     // gathered [M, K], box 128 rows
+  CUtensorMap map_self;  // A_self [M_shard, K], box 128 rows
+  CUtensorMap map_b;     // B [K, N], box 64 x 64
   const uint8_t* shard[TL_MAX_RANKS];
   uint8_t* gathered;
   uint16_t* C;
@@ -63,51 +63,33 @@ __device__ __forceinline__ int row_flag(const AgParams& p, int row) {
 __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_constant__ AgParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + AG_SMEM_BARS);
+  pair::Bars* bars = reinterpret_cast<pair::Bars*>(smem + AG_SMEM_BARS);
   const int warp = int(warp_id());
   const int lane = int(lane_id());
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&bars->tmem_full[a], 1);
-      mbar_init(&bars->tmem_empty[a], kNumEpiWarps);
-    }
-    for (int b = 0; b < COPY_NBUF; ++b) mbar_init(&bars->copy[b], 1);
-    bars->abort = 0;
-    fence_mbar_init();
-  }
+  const uint32_t rank = cluster_ctarank();
+  const int pair_id = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
   if (warp == kWarpTma && lane == 0) {
     tma_prefetch_desc(&p.map_g);
     tma_prefetch_desc(&p.map_self);
     tma_prefetch_desc(&p.map_b);
   }
-  if (warp == kWarpMma) {
-    tmem_alloc(&bars->tmem_base, TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = bars->tmem_base;
+  const uint32_t tmem_base = pair::setup(bars, warp);
   volatile uint32_t* abort = &bars->abort;
+  const int my_work = pair_id < p.num_work ? (p.num_work - 1 - pair_id) / npairs + 1 : 0;
 
   if (warp == kWarpTma) {
-    // ---------------------------------------------------------------- TMA producer
-    int s = 0;
-    uint32_t ph = 0;
+    // ---------------------------------------------------------------- TMA producer (this CTA's 128 rows)
+    pair::Producer prod;
     int last_m = -1;
-    for (int w = blockIdx.x; w < p.num_work; w += gridDim.x) {
+    for (int w = pair_id; w < p.num_work; w += npairs) {
       const int n = w % p.Nt;
       const int m = p.m_order[w / p.Nt];
-      const int row0 = m * BM;
-      const int row1 = min(p.M, row0 + BM) - 1;
-      const bool local = (row0 / p.M_shard == p.self) && (row1 / p.M_shard == p.self);
-      if (!local && m != last_m) {
-        // consume_tile_wait: every flag guarding rows [row0, row1]; lanes poll in parallel
+      const int row0 = m * pair::BM + int(rank) * pair::HM;
+      const bool any = row0 < p.M;
+      const int row1 = min(p.M, row0 + pair::HM) - 1;
+      const bool local = any && (row0 / p.M_shard == p.self) && (row1 / p.M_shard == p.self);
+      if (any && !local && m != last_m) {
+        // consume_tile_wait: every flag guarding this CTA's rows; lanes poll in parallel
         const int id0 = row_flag(p, row0), id1 = row_flag(p, row1);
         for (int id = id0 + lane; id <= id1; id += 32)
           wait_flag(p.flags + id, p.epoch, p.status, p.timeout_ns, uint32_t(id), TL_ERR_TIMEOUT);
@@ -115,65 +97,28 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
       last_m = m;
       __syncwarp();
       if (lane == 0) {
-        if (p.trace) p.trace[w] = m * p.Nt + n;
+        if (p.trace && rank == 0) p.trace[w] = m * p.Nt + n;
         if (!local) fence_proxy_async_global();
-        for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort, p.status, p.pipe_timeout_ns, 1)) break;
-          mbar_arrive_expect_tx(&bars->full[s], STAGE_TX);
-          uint8_t* a_dst = smem + SMEM_A + s * A_STAGE_BYTES;
-          uint8_t* b_dst = smem + SMEM_B + s * B_STAGE_BYTES;
-          if (local)
-            tma_load_2d(a_dst, &p.map_self, &bars->full[s], kb * BK, row0 - p.self * p.M_shard);
-          else
-            tma_load_2d(a_dst, &p.map_g, &bars->full[s], kb * BK, row0);
-#pragma unroll
-          for (int i = 0; i < BN / 64; ++i)
-            tma_load_2d(b_dst + i * B_BOX_BYTES, &p.map_b, &bars->full[s], n * BN + i * 64, kb * BK);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
+        const CUtensorMap* ma = local ? &p.map_self : &p.map_g;
+        const int a_y = local ? row0 - p.self * p.M_shard : row0;
+        for (int kb = 0; kb < p.KB; ++kb)
+          if (!prod.load(smem, bars, rank, ma, kb * pair::BK, a_y, &p.map_b, n * pair::BN + int(rank) * pair::HN,
+                         kb * pair::BK, abort, p.status, p.pipe_timeout_ns))
+            break;
       }
       // warp-uniform exit decision
       if (__shfl_sync(0xffffffffu, *abort, 0)) break;
     }
   } else if (warp == kWarpMma) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
-      int j = 0;
-      for (int w = blockIdx.x; w < p.num_work && !*abort; w += gridDim.x, ++j) {
-        const int acc = j & 1;
-        const uint32_t acc_ph = uint32_t(j >> 1) & 1u;
-        if (!mbar_wait(&bars->tmem_empty[acc], acc_ph ^ 1u, abort, p.status, p.pipe_timeout_ns, 2)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
-        bool ok = true;
-        for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&bars->full[s], ph, abort, p.status, p.pipe_timeout_ns, 3)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          mma_kblock(smem, s, d_tmem, kb == 0);
-          tc_commit(&bars->empty[s]);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit(&bars->tmem_full[acc]);
-      }
-    }
+    // ---------------------------------------------------------------- MMA issuer (leader CTA)
+    if (lane == 0 && rank == 0)
+      pair::mma_loop(smem, bars, tmem_base, my_work, p.KB, abort, p.status, p.pipe_timeout_ns);
     __syncwarp();
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
-    // ---------------------------------------------------------------- epilogue
+    // ---------------------------------------------------------------- epilogue (this CTA's 128 rows)
     const int wq = warp & 3;  // TMEM lane quarter this warp may access
     int j = 0;
-    for (int w = blockIdx.x; w < p.num_work; w += gridDim.x, ++j) {
+    for (int w = pair_id; w < p.num_work; w += npairs, ++j) {
       const int acc = j & 1;
       const uint32_t acc_ph = uint32_t(j >> 1) & 1u;
       const int n = w % p.Nt;
@@ -181,13 +126,13 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
       const bool ok = mbar_wait(&bars->tmem_full[acc], acc_ph, abort, p.status, p.pipe_timeout_ns, 4);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int row = m * BM + wq * 32 + lane;
+      const int row = m * pair::BM + int(rank) * pair::HM + wq * 32 + lane;
       const bool row_ok = row < p.M;
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = n * BN + c * 32;
+      for (int c = 0; c < pair::BN / 32; ++c) {
+        const int col0 = n * pair::BN + c * 32;
         if (col0 >= p.N) break;
         uint32_t v[32];
-        tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * BN + c * 32), v);
+        tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
         if (row_ok) {
           uint16_t* crow = p.C + size_t(row) * p.N + col0;
@@ -213,7 +158,7 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tmem_empty[acc]);
+      if (lane == 0) pair::release_accumulator(bars, acc, rank);
     }
   } else if (warp == kWarpCopy) {
     // ---------------------------------------------------------------- AllGather producer
@@ -269,19 +214,7 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
     }
     __syncwarp();
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (*abort) {
-    // a pipeline wait gave up: let any TMA load still in flight land before the CTA exits
-    const uint64_t t0 = now_ns();
-    while (now_ns() - t0 < 50000) {
-    }
-  }
-  if (warp == kWarpMma) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
-  }
+  pair::teardown(bars, warp, tmem_base);
 }
 
 int default_rpb(int K, int M_shard) {
@@ -303,13 +236,13 @@ extern "C" tl_status tl_ag_gemm_tile_order(int R, int self_rank, int M_shard, in
   if (R < 1 || R > TL_MAX_RANKS || self_rank < 0 || self_rank >= R || M_shard < 1 || !m_order)
     return tl::fail(TL_ERR_INVALID, "tl_ag_gemm_tile_order: bad arguments");
   const long long M = (long long)R * M_shard;
-  const int Mt = int((M + tl::BM - 1) / tl::BM);
+  const int Mt = int((M + tl::pair::BM - 1) / tl::pair::BM);
   if (capacity < Mt) return tl::fail(TL_ERR_INVALID, "tl_ag_gemm_tile_order: capacity %d < %d tiles", capacity, Mt);
   // arrival position of shard r is (r - self) mod R; a row tile takes the latest
   // position among the shards its rows come from; stable by tile index
   std::vector<std::pair<int, int>> key(Mt);
   for (int m = 0; m < Mt; ++m) {
-    const long long r0 = (long long)m * tl::BM, r1 = std::min(M, r0 + tl::BM) - 1;
+    const long long r0 = (long long)m * tl::pair::BM, r1 = std::min(M, r0 + tl::pair::BM) - 1;
     int best = 0;
     for (long long r = r0 / M_shard; r <= r1 / M_shard; ++r) best = std::max(best, int((r - self_rank + R) % R));
     key[m] = {best, m};
@@ -338,7 +271,7 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
   if (!aligned16(a->B) || !aligned16(a->gathered) || !aligned16(a->C) || (a->C_f32 && !aligned16(a->C_f32)))
     return fail(TL_ERR_INVALID, "tl_ag_gemm: pointers must be 16-byte aligned");
   const long long M = (long long)a->R * a->M_shard;
-  const int Mt = int((M + BM - 1) / BM);
+  const int Mt = int((M + pair::BM - 1) / pair::BM);
   if (M > (1ll << 30) || Mt > AG_MAX_MTILES)
     return fail(TL_ERR_UNSUPPORTED, "tl_ag_gemm: %lld rows exceeds %d row tiles", M, AG_MAX_MTILES);
   int rpb = 0;
@@ -358,10 +291,11 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
   std::memset(p, 0, sizeof(AgParams));
   tl_status st = TL_OK;
   do {
-    if ((st = make_map_bf16(&p->map_g, a->gathered, M, a->K, size_t(a->K) * 2, BM, BK))) break;
-    if ((st = make_map_bf16(&p->map_self, a->A_shards[a->self_rank], a->M_shard, a->K, size_t(a->K) * 2, BM, BK)))
+    if ((st = make_map_bf16(&p->map_g, a->gathered, M, a->K, size_t(a->K) * 2, pair::HM, pair::BK))) break;
+    if ((st = make_map_bf16(&p->map_self, a->A_shards[a->self_rank], a->M_shard, a->K, size_t(a->K) * 2, pair::HM,
+                            pair::BK)))
       break;
-    if ((st = make_map_bf16(&p->map_b, a->B, a->K, a->N, size_t(a->N) * 2, BK, 64))) break;
+    if ((st = make_map_bf16(&p->map_b, a->B, a->K, a->N, size_t(a->N) * 2, pair::BK, 64))) break;
     for (int r = 0; r < a->R; ++r) p->shard[r] = static_cast<const uint8_t*>(a->A_shards[r]);
     p->gathered = static_cast<uint8_t*>(a->gathered);
     p->C = static_cast<uint16_t*>(a->C);
@@ -381,18 +315,18 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
     p->rpb = rpb;
     p->bpr = cdiv(a->M_shard, rpb);
     p->Mt = Mt;
-    p->Nt = cdiv(a->N, BN);
-    p->KB = cdiv(a->K, BK);
+    p->Nt = cdiv(a->N, pair::BN);
+    p->KB = cdiv(a->K, pair::BK);
     p->num_items = a->R * p->bpr;
     p->num_work = Mt * p->Nt;
     p->epoch = a->epoch;
     int32_t order[AG_MAX_MTILES];
     if ((st = tl_ag_gemm_tile_order(a->R, a->self_rank, a->M_shard, order, AG_MAX_MTILES))) break;
     for (int i = 0; i < Mt; ++i) p->m_order[i] = uint16_t(order[i]);
-    const int grid = std::max(1, std::min(di.sm_count, std::max(p->num_work, p->num_items)));
+    const int pairs = std::max(1, std::min(di.sm_count / 2, std::max(p->num_work, (p->num_items + 1) / 2)));
     void* args[] = {p};
-    st = launch_coop(reinterpret_cast<const void*>(&ag_gemm_kernel), grid, AG_THREADS, AG_SMEM_BYTES,
-                     (cudaStream_t)stream, args);
+    st = launch_coop(reinterpret_cast<const void*>(&ag_gemm_kernel), 2 * pairs, AG_THREADS, AG_SMEM_BYTES,
+                     (cudaStream_t)stream, args, 2);
   } while (false);
   delete p;
   return st;
