@@ -181,7 +181,7 @@ tl_status tl_ag_gemm(const tl_ag_gemm_args* args, void* stream);
  * on its own and its peers' tiles).  One launch on pairs of CTAs
  * (cta_group::2, 256 x 256 tiles; CTA h of a pair owns rows h*128..h*128+127
  * of every tile): every fp32 partial half-tile is pushed into a receive slot of
- * `workspace` (a ring of two waves of slots, reused as the launch proceeds)
+ * `workspace` (a ring of three waves of slots, reused as the launch proceeds)
  * and its arrival flag released; output tiles run in destination order, m
  * tiles innermost, and the R partials of one output tile are produced back to
  * back, rank (d + 1 + tau + j) mod R at position j of output tile tau.
@@ -211,7 +211,7 @@ typedef struct tl_gemm_rs_args {
                                   m_tiles = ceil(M/R/256), n_tiles = ceil(N/256) */
 } tl_gemm_rs_args;
 
-/* Workspace bytes for the current device: min(items, 2 * pairs) items of two
+/* Workspace bytes for the current device: min(items, 3 * pairs) items of two
  * 128 KiB half-slots, pairs = half the SM count. */
 size_t tl_gemm_rs_workspace_size(int R, int M, int N);
 /* Flags a GEMM-RS call needs: 4 * R * tiles (arrival and reduced flags for
@@ -262,11 +262,13 @@ tl_status tl_gemm_rs_noalloc(const tl_gemm_rs_args* args, uint32_t* dev_status, 
  * stable counting sort, tile table, tile order) and one cooperative kernel in
  * which copy warps gather the shards' token rows and scatter each to its topk
  * sorted positions (one flag per chunk of rows_per_barrier tokens of a shard,
- * shards in the order self, self+1, ...) while tcgen05 GEMM tiles wait on the
+ * shards in the order self, self+1, ...) while tcgen05 GEMM tiles of 256 rows
+ * of one expert wait on the
  * flags their lookup-table entry names and multiply their sorted rows by their
  * expert's weight.  No gate weighting, no combine.
  * Workspace layout (int32 words; read-only for the caller, documented for
- * tests), max_tiles = ceil(P/128) + E:
+ * tests), max_tiles = ceil(P/256) + E, tiles of 256 sorted rows computed by
+ * pairs of CTAs (cta_group::2):
  *   [0]                         number of tiles
  *   [16 + 6*t .. 16 + 6*t + 5]  tile t: expert, first sorted row, rows,
  *                               lowest barrier, highest barrier, source-rank mask

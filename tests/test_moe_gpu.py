@@ -38,7 +38,7 @@ def run_moe(B, X, ids, W, *, self_rank=0, rpb=0, timeout_ns=0):
     ws = torch.zeros(B.tl_moe_workspace_size(R, T_r, E, k) // 4, dtype=torch.int32, device="cuda")
     nflags, eff = B.tl_moe_num_flags(R, T_r, H, rpb)
     sig = B.Signals(nflags)
-    max_tiles = -(-P // 128) + E
+    max_tiles = -(-P // 256) + E
     Nt = -(-N // 256)
     trace = torch.full((max_tiles * Nt,), -1, dtype=torch.int32, device="cuda")
     _epoch[0] += 1
@@ -55,7 +55,7 @@ def check_moe(B, X, ids, W, r, self_rank=0, full_y=True):
     counts, offsets, perm = oracle.moe.route(ids, E)
     np.testing.assert_array_equal(r["offs"].cpu().numpy(), offsets)
     np.testing.assert_array_equal(r["perm"].cpu().numpy(), perm)
-    table = oracle.moe.tile_table(counts, offsets, 128)
+    table = oracle.moe.tile_table(counts, offsets, 256)
     sources = oracle.moe.tile_sources(perm, k, table, T_r, r["rpb"])
     ws, mt = r["ws"], r["max_tiles"]
     n = int(ws[0])

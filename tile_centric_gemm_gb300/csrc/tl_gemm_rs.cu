@@ -17,16 +17,16 @@
 // round-robin over CTA pairs (clusters of two, tcgen05.mma.cta_group::2); CTA
 // h of a pair owns rows h*128 .. h*128+127 of every tile it works on.
 //
-// Receive slots form a ring of 2 * pairs items (two 128-row halves each): item
+// Receive slots form a ring of 3 * pairs items (two 128-row halves each): item
 // i pushes half h into half-slot 2 * (i mod ring) + h, after the R reducers of
 // half h of the tile that used the slot before have released their "reduced"
-// flags.  The ring (about 38 MB for 76 pairs) stays in L2.  Deadlock freedom:
+// flags.  The ring is about 57 MB for 76 pairs.  Deadlock freedom:
 // a push of tile tau waits only on earlier tiles (slot-free flags, its own
 // pair's earlier accumulator) and a reduce of tau only on pushes of tau and
 // its own earlier reduces, so by induction on tau every tile completes.
 //
 // Per CTA: warp 0 TMA producer (its halves of A_r, B_r), warp 1 tcgen05 MMA
-// issuer (leader only), warps 2-5 pushers, warps 6-9 reducers.  For item
+// issuer (leader only), warps 2-5 pushers, warps 6-13 reducers.  For item
 // (tau, j) and half h:
 //   push:   TMEM -> registers -> fp32 receive slot of the item; release the
 //           arrival flag tau*R + r (produce_tile_notify).  Before reusing a ring
@@ -53,7 +53,7 @@ namespace {
 
 constexpr int RS_MAX_RANKS = 32;
 constexpr int kWarpRed0 = kWarpEpi0 + kNumEpiWarps;  // first reducer warp
-constexpr int kNumRedWarps = 4;
+constexpr int kNumRedWarps = 8;
 constexpr int kNumRedThreads = kNumRedWarps * 32;
 constexpr int RS_THREADS = (kWarpRed0 + kNumRedWarps) * 32;
 constexpr uint32_t RS_SMEM_BARS = pair::SMEM_END;
@@ -269,8 +269,8 @@ int rs_num_tiles(int R, int M, int N) {
 // CTA pairs of a launch: at most half the SMs, at most one per item.
 int rs_pairs(int num_items, int sm_count) { return std::max(1, std::min(sm_count / 2, num_items)); }
 
-// Items in the ring of receive slots: two waves of pairs, or every item when fewer.
-int rs_ring_items(int num_items, int pairs) { return std::min(num_items, 2 * pairs); }
+// Items in the ring of receive slots: three waves of pairs, or every item when fewer.
+int rs_ring_items(int num_items, int pairs) { return std::min(num_items, 3 * pairs); }
 
 int current_sm_count() {
   DeviceInfo di{};

@@ -12,21 +12,22 @@
 // Two stream-ordered launches:
 //  1. moe_route_kernel (one CTA): histogram of topk_ids over experts,
 //     exclusive scan, stable counting sort of the (token, slot) pairs by expert
-//     (perm and its inverse), then the tile table -- per 128-row tile its
+//     (perm and its inverse), then the tile table -- per 256-row tile its
 //     expert, first sorted row, rows, lowest and highest producer barrier and
 //     source-rank mask -- and the consumer tile order.
-//  2. moe_gemm_kernel (cooperative, one CTA per SM): copy warps gather every
-//     token row of every shard and scatter it to its k sorted positions in
-//     `sorted_tokens` (bulk TMA, one flag per chunk of rows_per_barrier tokens,
-//     shards in the order self, self+1, ...); the TMA warp of each GEMM tile
-//     acquires the flags of its barrier range, then a tcgen05 grouped GEMM
-//     multiplies the tile's sorted rows by its expert's weight.
+//  2. moe_gemm_kernel (cooperative, CTA pairs, one CTA per SM): copy warps
+//     gather every token row of every shard and scatter it to its k sorted
+//     positions in `sorted_tokens` (bulk TMA, one flag per chunk of
+//     rows_per_barrier tokens, shards in the order self, self+1, ...); the TMA
+//     warps of each 256-row expert tile acquire the flags of its barrier range,
+//     then a tcgen05.mma.cta_group::2 grouped GEMM multiplies the tile's sorted
+//     rows by its expert's weight.
 #include <algorithm>
 #include <cstring>
 #include <new>
 
-#include "tl_common.cuh"
 #include "tl_internal.h"
+#include "tl_pair.cuh"
 
 namespace tl {
 namespace {
@@ -38,9 +39,10 @@ constexpr int ROUTE_THREADS = 1024;
 constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
 constexpr int kWarpCopy = 6;
 constexpr int MOE_THREADS = 7 * 32;
-constexpr uint32_t MOE_SMEM_COPY = SMEM_GEMM_END;
+constexpr int TM = pair::BM;  // rows of an expert tile
+constexpr uint32_t MOE_SMEM_COPY = pair::SMEM_END;
 constexpr uint32_t MOE_SMEM_BARS = MOE_SMEM_COPY + COPY_NBUF * COPY_CHUNK;
-constexpr uint32_t MOE_SMEM_BYTES = MOE_SMEM_BARS + sizeof(Barriers) + 1024;
+constexpr uint32_t MOE_SMEM_BYTES = MOE_SMEM_BARS + sizeof(pair::Bars) + 1024;
 
 // Workspace layout, in int32 words (documented in tilelink.h).
 constexpr int WS_HEADER = 16;  // [0] = number of tiles
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     int acc = 0;
     for (int e = 0; e < E; ++e) {
       s_toff[e] = acc;
-      acc += (s_off[e + 1] - s_off[e] + BM - 1) / BM;
+      acc += (s_off[e + 1] - s_off[e] + TM - 1) / TM;
     }
     s_toff[E] = acc;
     p.ws[0] = min(acc, p.max_tiles);
@@ -157,8 +159,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
       if (s_toff[mid] <= t) lo_e = mid; else hi_e = mid - 1;
     }
     const int e = lo_e;
-    const int row0 = s_off[e] + (t - s_toff[e]) * BM;
-    const int rows = min(BM, s_off[e + 1] - row0);
+    const int row0 = s_off[e] + (t - s_toff[e]) * TM;
+    const int rows = min(TM, s_off[e + 1] - row0);
     uint32_t mask = 0;
     int blo = 0x7fffffff, bhi = -1;
     for (int i = lane; i < rows; i += 32) {
@@ -225,43 +227,25 @@ struct MoeParams {
 __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_constant__ MoeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  Barriers* bars = reinterpret_cast<Barriers*>(smem + MOE_SMEM_BARS);
+  pair::Bars* bars = reinterpret_cast<pair::Bars*>(smem + MOE_SMEM_BARS);
   const int warp = int(warp_id());
   const int lane = int(lane_id());
+  const uint32_t rank = cluster_ctarank();
+  const int h = int(rank);
+  const int pair_id = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
   const int32_t* tiles = p.ws + ws_tiles(p.max_tiles);
   const int32_t* order = p.ws + ws_order(p.max_tiles);
   const int32_t* inv = p.ws + ws_inv(p.max_tiles);
   const int num_work = p.ws[0] * p.Nt;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&bars->full[s], 1);
-      mbar_init(&bars->empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&bars->tmem_full[a], 1);
-      mbar_init(&bars->tmem_empty[a], kNumEpiWarps);
-    }
-    for (int b = 0; b < COPY_NBUF; ++b) mbar_init(&bars->copy[b], 1);
-    bars->abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == kWarpMma) {
-    tmem_alloc(&bars->tmem_base, TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = bars->tmem_base;
+  const uint32_t tmem_base = pair::setup(bars, warp);
   volatile uint32_t* abort = &bars->abort;
+  const int my_work = pair_id < num_work ? (num_work - 1 - pair_id) / npairs + 1 : 0;
 
   if (warp == kWarpTma) {
-    // ---------------------------------------------------------------- TMA producer
-    int s = 0;
-    uint32_t ph = 0;
+    // ---------------------------------------------------------------- TMA producer (this CTA's 128 rows)
+    pair::Producer prod;
     int last_t = -1;
-    for (int w = blockIdx.x; w < num_work; w += gridDim.x) {
+    for (int w = pair_id; w < num_work; w += npairs) {
       const int t = order[w / p.Nt];
       const int n = w % p.Nt;
       const int32_t* tr = tiles + 6 * t;
@@ -274,60 +258,25 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
       last_t = t;
       __syncwarp();
       if (lane == 0) {
-        if (p.trace) p.trace[w] = t * p.Nt + n;
+        if (p.trace && rank == 0) p.trace[w] = t * p.Nt + n;
         fence_proxy_async_global();
-        for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort, p.status, p.pipe_timeout_ns, 1)) break;
-          mbar_arrive_expect_tx(&bars->full[s], STAGE_TX);
-          tma_load_2d(smem + SMEM_A + s * A_STAGE_BYTES, &p.map_a, &bars->full[s], kb * BK, row0);
-          uint8_t* b_dst = smem + SMEM_B + s * B_STAGE_BYTES;
-#pragma unroll
-          for (int i = 0; i < BN / 64; ++i)
-            tma_load_2d(b_dst + i * B_BOX_BYTES, &p.map_w[e], &bars->full[s], n * BN + i * 64, kb * BK);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
+        for (int kb = 0; kb < p.KB; ++kb)
+          if (!prod.load(smem, bars, rank, &p.map_a, kb * pair::BK, row0 + h * pair::HM, &p.map_w[e],
+                         n * pair::BN + h * pair::HN, kb * pair::BK, abort, p.status, p.pipe_timeout_ns))
+            break;
       }
       if (__shfl_sync(0xffffffffu, *abort, 0)) break;
     }
   } else if (warp == kWarpMma) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
-      int j = 0;
-      for (int w = blockIdx.x; w < num_work && !*abort; w += gridDim.x, ++j) {
-        const int acc = j & 1;
-        const uint32_t acc_ph = uint32_t(j >> 1) & 1u;
-        if (!mbar_wait(&bars->tmem_empty[acc], acc_ph ^ 1u, abort, p.status, p.pipe_timeout_ns, 2)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
-        bool ok = true;
-        for (int kb = 0; kb < p.KB; ++kb) {
-          if (!mbar_wait(&bars->full[s], ph, abort, p.status, p.pipe_timeout_ns, 3)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          mma_kblock(smem, s, d_tmem, kb == 0);
-          tc_commit(&bars->empty[s]);
-          if (++s == STAGES) {
-            s = 0;
-            ph ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit(&bars->tmem_full[acc]);
-      }
-    }
+    // ---------------------------------------------------------------- MMA issuer (leader)
+    if (lane == 0 && rank == 0)
+      pair::mma_loop(smem, bars, tmem_base, my_work, p.KB, abort, p.status, p.pipe_timeout_ns);
     __syncwarp();
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
     // ---------------------------------------------------------------- epilogue: rows of this expert only
     const int wq = warp & 3;
     int j = 0;
-    for (int w = blockIdx.x; w < num_work; w += gridDim.x, ++j) {
+    for (int w = pair_id; w < num_work; w += npairs, ++j) {
       const int acc = j & 1;
       const uint32_t acc_ph = uint32_t(j >> 1) & 1u;
       const int32_t* tr = tiles + 6 * order[w / p.Nt];
@@ -336,13 +285,13 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
       const bool ok = mbar_wait(&bars->tmem_full[acc], acc_ph, abort, p.status, p.pipe_timeout_ns, 4);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const int lr = wq * 32 + lane;
+      const int lr = h * pair::HM + wq * 32 + lane;
       const bool row_ok = lr < rows;
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = n * BN + c * 32;
+      for (int c = 0; c < pair::BN / 32; ++c) {
+        const int col0 = n * pair::BN + c * 32;
         if (col0 >= p.N) break;
         uint32_t v[32];
-        tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * BN + c * 32), v);
+        tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
         if (row_ok) {
           uint16_t* yrow = p.Y + size_t(row0 + lr) * p.N + col0;
@@ -358,7 +307,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->tmem_empty[acc]);
+      if (lane == 0) pair::release_accumulator(bars, acc, rank);
     }
   } else if (warp == kWarpCopy) {
     // ---------------------------------------------------------------- AllGather + local scatter
@@ -413,21 +362,10 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
     }
     __syncwarp();
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (*abort) {
-    const uint64_t t0 = now_ns();
-    while (now_ns() - t0 < 50000) {
-    }
-  }
-  if (warp == kWarpMma) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
-  }
+  pair::teardown(bars, warp, tmem_base);
 }
 
-int moe_max_tiles(int P, int E) { return (P + BM - 1) / BM + E; }
+int moe_max_tiles(int P, int E) { return (P + TM - 1) / TM + E; }
 
 int moe_default_rpb(int H, int T_r) { return std::min(T_r, std::max(1, int(32768 / (size_t(H) * 2)))); }
 
@@ -524,9 +462,9 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
   std::memset(p, 0, sizeof(MoeParams));
   tl_status res = TL_OK;
   do {
-    if ((res = make_map_bf16(&p->map_a, a->sorted_tokens, P, a->H, size_t(a->H) * 2, BM, BK))) break;
+    if ((res = make_map_bf16(&p->map_a, a->sorted_tokens, P, a->H, size_t(a->H) * 2, pair::HM, pair::BK))) break;
     for (int e = 0; e < a->E && !res; ++e)
-      res = make_map_bf16(&p->map_w[e], a->W[e], a->H, a->N, size_t(a->N) * 2, BK, 64);
+      res = make_map_bf16(&p->map_w[e], a->W[e], a->H, a->N, size_t(a->N) * 2, pair::BK, 64);
     if (res) break;
     for (int r = 0; r < a->R; ++r) p->x[r] = static_cast<const uint8_t*>(a->X[r]);
     p->sorted = static_cast<uint8_t*>(a->sorted_tokens);
@@ -546,14 +484,15 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
     p->k = a->topk;
     p->rpb = rpb;
     p->bpr = cdiv(a->T_r, rpb);
-    p->Nt = cdiv(a->N, BN);
-    p->KB = cdiv(a->H, BK);
+    p->Nt = cdiv(a->N, pair::BN);
+    p->KB = cdiv(a->H, pair::BK);
     p->num_items = a->R * p->bpr;
     p->max_tiles = max_tiles;
     p->epoch = a->epoch;
-    const int grid = std::max(1, std::min(di.sm_count, std::max(max_tiles * p->Nt, p->num_items)));
+    const int pairs = std::max(1, std::min(di.sm_count / 2, std::max(max_tiles * p->Nt, (p->num_items + 1) / 2)));
     void* args[] = {p};
-    res = launch_coop(reinterpret_cast<const void*>(&moe_gemm_kernel), grid, MOE_THREADS, MOE_SMEM_BYTES, st, args);
+    res = launch_coop(reinterpret_cast<const void*>(&moe_gemm_kernel), 2 * pairs, MOE_THREADS, MOE_SMEM_BYTES, st,
+                      args, 2);
   } while (false);
   delete p;
   return res;
