@@ -237,7 +237,7 @@ class Workload:
         self.offs = torch.empty(MOE["E"] + 1, dtype=torch.int32, device=dev)
         self.ws_moe = torch.empty(B.tl_moe_workspace_size(MOE["R"], MOE["T_r"], MOE["E"], MOE["topk"]) // 4,
                                   dtype=torch.int32, device=dev)
-        self.sig_moe = B.Signals(B.tl_moe_num_flags(MOE["R"], MOE["T_r"], MOE["H"])[0])
+        self.sig_moe = B.Signals(B.tl_moe_num_flags(MOE["R"], MOE["T_r"], MOE["H"], MOE["topk"])[0])
         self.h_C = torch.empty_like(self.C, device="cpu").pin_memory()
         self.h_out = [torch.empty_like(o, device="cpu").pin_memory() for o in self.out]
         self.h_Y = torch.empty_like(self.Y, device="cpu").pin_memory()

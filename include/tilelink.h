@@ -212,7 +212,9 @@ typedef struct tl_gemm_rs_args {
 } tl_gemm_rs_args;
 
 /* Workspace bytes for the current device: min(items, 3 * pairs) items of two
- * 128 KiB half-slots, pairs = half the SM count. */
+ * half-slots of R * ceil(128/R) * 256 floats, pairs = half the SM count.
+ * A half-slot is laid out [slice][column/4][row in slice][4], one contiguous
+ * block per reducer slice. */
 size_t tl_gemm_rs_workspace_size(int R, int M, int N);
 /* Flags a GEMM-RS call needs: 4 * R * tiles (arrival and reduced flags for
  * both halves), tiles = R * ceil(M/R/256) * ceil(N/256). */
@@ -260,24 +262,31 @@ tl_status tl_gemm_rs_noalloc(const tl_gemm_rs_args* args, uint32_t* dev_status, 
  *   Y[i, :]            = sorted_tokens[i] . W_{expert of row i}   (fp32 accumulate, bf16)
  * Two stream-ordered launches: a one-CTA routing kernel (histogram, scan,
  * stable counting sort, tile table, tile order) and one cooperative kernel in
- * which copy warps gather the shards' token rows and scatter each to its topk
- * sorted positions (one flag per chunk of rows_per_barrier tokens of a shard,
- * shards in the order self, self+1, ...) while tcgen05 GEMM tiles of 256 rows
- * of one expert wait on the
- * flags their lookup-table entry names and multiply their sorted rows by their
- * expert's weight.  No gate weighting, no combine.
+ * which copy warps move token rows into `sorted_tokens` while tcgen05 GEMM
+ * tiles of 256 rows of one expert wait on the flags their lookup-table entry
+ * names and multiply their sorted rows by their expert's weight.  The two data
+ * modes of the talk summary (Technical Deep Dive: push sends, pull fetches
+ * with finer control of arrival order) move the same rows:
+ *  - push: source shards, in the order self, self+1, ..., scatter each token
+ *    to its topk sorted rows; one flag per chunk of rows_per_barrier tokens of
+ *    a shard (barrier id of token t: (t / T_r) * chunks + (t % T_r) /
+ *    rows_per_barrier, chunks = ceil(T_r / rows_per_barrier)); a tile waits on
+ *    every barrier from its tokens' lowest to highest and tiles run by the
+ *    latest arrival position among those, barrier (r, c) arriving at
+ *    ((r - self) mod R) * chunks + c;
+ *  - pull: the consumer side gathers the sorted rows in order, one flag per
+ *    chunk of rows_per_barrier sorted rows; a tile waits on its own chunks and
+ *    tiles run in sorted order.
+ * No gate weighting, no combine.
  * Workspace layout (int32 words; read-only for the caller, documented for
  * tests), max_tiles = ceil(P/256) + E, tiles of 256 sorted rows computed by
  * pairs of CTAs (cta_group::2):
  *   [0]                         number of tiles
  *   [16 + 6*t .. 16 + 6*t + 5]  tile t: expert, first sorted row, rows,
  *                               lowest barrier, highest barrier, source-rank mask
- *   [16 + 6*max_tiles + i]      i-th tile in consumer order (swizzle: tiles by
- *                               the latest arrival position among their barriers,
- *                               barrier (r, c) arriving at ((r-self) mod R)*chunks + c)
+ *   [16 + 6*max_tiles + i]      i-th tile in consumer order (the swizzle above)
  *   [16 + 7*max_tiles + q]      sorted row of pair q (the inverse of perm)
- * Barrier id of token t: (t / T_r) * chunks + (t % T_r) / rows_per_barrier,
- * chunks = ceil(T_r / rows_per_barrier).  Limits: R <= 32, E <= 64, H and N
+ * Limits: R <= 32, E <= 64, H and N
  * multiples of 8.  A topk id outside [0, E) records TL_ERR_INVALID in the
  * status word (the pair is clamped into range).
  */
@@ -289,7 +298,8 @@ typedef struct tl_moe_args {
   int32_t N;                    /* expert output columns, multiple of 8 */
   int32_t E;                    /* experts, 1..64 */
   int32_t topk;                 /* routed experts per token, 1..E */
-  int32_t rows_per_barrier;     /* tokens per producer chunk / flag; 0 = about 32 KB of rows */
+  int32_t rows_per_barrier;     /* rows per producer chunk / flag: push = tokens of a shard
+                                   (0 = about 32 KB), pull = sorted rows (0 = about 64 KB) */
   const void* const* X;         /* host array of R device pointers, bf16 [T_r, H] */
   const int32_t* topk_ids;      /* device int32 [R*T_r, topk] */
   const void* const* W;         /* host array of E device pointers, bf16 [H, N] */
@@ -301,14 +311,15 @@ typedef struct tl_moe_args {
   size_t workspace_bytes;
   tl_signals* signals;          /* >= tl_moe_num_flags(...) flags */
   uint32_t epoch;               /* nonzero */
-  uint32_t reserved0;
+  int32_t mode;                 /* tl_mode: TL_MODE_PULL (default, 0) or TL_MODE_PUSH */
   uint64_t timeout_ns;          /* 0 = 1 s */
   int32_t* trace;               /* optional device int32 [max_tiles * ceil(N/256)]:
                                    tile * n_tiles + n of the work run at each schedule slot */
 } tl_moe_args;
 
 size_t tl_moe_workspace_size(int R, int T_r, int E, int topk);
-int tl_moe_num_flags(int R, int T_r, int H, int rows_per_barrier, int* effective_rpb);
+/* Flags an MoE call needs in `mode`: push R * ceil(T_r / rpb), pull ceil(P / rpb). */
+int tl_moe_num_flags(int mode, int R, int T_r, int H, int topk, int rows_per_barrier, int* effective_rpb);
 tl_status tl_moe_ag_gemm(const tl_moe_args* args, void* stream);
 
 #ifdef __cplusplus

@@ -72,6 +72,21 @@ def tile_sources(perm, k, table, T_r, rows_per_barrier):
     return out
 
 
+def tile_sources_pull(perm, k, table, T_r, rows_per_barrier):
+    """Pull mode: the consumer side gathers sorted rows in order, one barrier per
+    chunk of rows_per_barrier sorted rows.  Per tile: (rank bitmask of its
+    tokens, first chunk, last chunk) -- the chunks holding its rows."""
+    out = []
+    for (mask, _, _), (_, start, rows) in zip(tile_sources(perm, k, table, T_r, 1), table):
+        out.append((mask, start // rows_per_barrier, (start + rows - 1) // rows_per_barrier))
+    return out
+
+
+def tile_order_pull(sources):
+    """Pull mode: chunks arrive in sorted-row order, so tiles run by their last chunk, then index."""
+    return [t for (_, t) in sorted((hi, t) for t, (_, _, hi) in enumerate(sources))]
+
+
 def tile_order(sources, R, self_rank, T_r, rows_per_barrier):
     """Consumer order of the tiles (the swizzle for a dynamic workload).
 

@@ -203,6 +203,27 @@ def check_moe_tile_order(tile_order, tile_sources):
     assert ks == sorted(ks)
 
 
+def check_moe_pull(tile_sources_pull, tile_order_pull, route, tile_table):
+    fx = golden_json("moe_routing_small.json")
+    ids = np.array(fx["topk_ids"])
+    counts, offsets, perm = route(ids, fx["E"])
+    table = tile_table(counts, offsets, fx["BM"])
+    for rpb, key in ((1, "pull_sources_rpb1"), (2, "pull_sources_rpb2")):
+        src = tile_sources_pull(perm, fx["k"], table, fx["T_r"], rpb)
+        assert [list(t) for t in src] == fx[key]
+    assert tile_order_pull([tuple(t) for t in fx["pull_sources_rpb2"]]) == fx["pull_order"]
+    # every sorted row's chunk lies in its tile's range and ranges never go backwards
+    rng = np.random.default_rng(4)
+    T, k, E = 300, 2, 9
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    counts, offsets, perm = route(ids, E)
+    table = tile_table(counts, offsets, 16)
+    src = tile_sources_pull(perm, k, table, 100, 8)
+    for (_, start, rows), (_, lo, hi) in zip(table, src):
+        assert lo == start // 8 and hi == (start + rows - 1) // 8
+    assert [h for (_, _, h) in src] == sorted(h for (_, _, h) in src)
+
+
 def check_moe_routing(route, tile_table, tile_sources):
     fx = golden_json("moe_routing_small.json")
     ids = np.array(fx["topk_ids"])

@@ -24,7 +24,7 @@ def B():
 _epoch = [0]
 
 
-def run_moe(B, X, ids, W, *, self_rank=0, rpb=0, timeout_ns=0):
+def run_moe(B, X, ids, W, *, self_rank=0, rpb=0, timeout_ns=0, mode=None):
     import torch
     R, (T_r, H), E, N, k = len(X), X[0].shape, len(W), W[0].shape[1], ids.shape[1]
     P = R * T_r * k
@@ -36,17 +36,18 @@ def run_moe(B, X, ids, W, *, self_rank=0, rpb=0, timeout_ns=0):
     perm = torch.full((P,), -1, dtype=torch.int32, device="cuda")
     offs = torch.full((E + 1,), -1, dtype=torch.int32, device="cuda")
     ws = torch.zeros(B.tl_moe_workspace_size(R, T_r, E, k) // 4, dtype=torch.int32, device="cuda")
-    nflags, eff = B.tl_moe_num_flags(R, T_r, H, rpb)
+    mode = B.TL_MODE_PULL if mode is None else mode
+    nflags, eff = B.tl_moe_num_flags(R, T_r, H, k, rpb, mode)
     sig = B.Signals(nflags)
     max_tiles = -(-P // 256) + E
     Nt = -(-N // 256)
     trace = torch.full((max_tiles * Nt,), -1, dtype=torch.int32, device="cuda")
     _epoch[0] += 1
     B.tl_moe_ag_gemm(dX, dids, dW, S, Y, perm, offs, ws, sig, _epoch[0], self_rank=self_rank,
-                     rows_per_barrier=rpb, timeout_ns=timeout_ns, trace=trace)
+                     rows_per_barrier=rpb, mode=mode, timeout_ns=timeout_ns, trace=trace)
     status = B.tl_query_status(sig)
     return dict(S=S, Y=Y, perm=perm, offs=offs, ws=ws.cpu().numpy(), sig=sig, status=status, rpb=eff,
-                nflags=nflags, epoch=_epoch[0], max_tiles=max_tiles, Nt=Nt, trace=trace)
+                nflags=nflags, epoch=_epoch[0], max_tiles=max_tiles, Nt=Nt, trace=trace, mode=mode)
 
 
 def check_moe(B, X, ids, W, r, self_rank=0, full_y=True):
@@ -56,14 +57,16 @@ def check_moe(B, X, ids, W, r, self_rank=0, full_y=True):
     np.testing.assert_array_equal(r["offs"].cpu().numpy(), offsets)
     np.testing.assert_array_equal(r["perm"].cpu().numpy(), perm)
     table = oracle.moe.tile_table(counts, offsets, 256)
-    sources = oracle.moe.tile_sources(perm, k, table, T_r, r["rpb"])
+    pull = r["mode"] == B.TL_MODE_PULL
+    sources = (oracle.moe.tile_sources_pull if pull else oracle.moe.tile_sources)(perm, k, table, T_r, r["rpb"])
     ws, mt = r["ws"], r["max_tiles"]
     n = int(ws[0])
     assert n == len(table)
     got = ws[16:16 + 6 * n].reshape(n, 6)
     want = np.array([[e, s0, rows, lo, hi, mask] for (e, s0, rows), (mask, lo, hi) in zip(table, sources)])
     np.testing.assert_array_equal(got, want)
-    order = oracle.moe.tile_order(sources, R, self_rank, T_r, r["rpb"])
+    order = (oracle.moe.tile_order_pull(sources) if pull else
+             oracle.moe.tile_order(sources, R, self_rank, T_r, r["rpb"]))
     assert ws[16 + 6 * mt:16 + 6 * mt + n].tolist() == order
     inv = ws[16 + 7 * mt:16 + 7 * mt + len(perm)]
     np.testing.assert_array_equal(inv[perm], np.arange(len(perm)))
@@ -81,9 +84,11 @@ def check_moe(B, X, ids, W, r, self_rank=0, full_y=True):
     (4, 128, 512, 512, 16, 2, 1, 16),
     (1, 200, 64, 72, 3, 1, 0, 0),      # one rank, top-1
 ])
-def test_moe_parity(B, R, T_r, H, N, E, k, self_rank, rpb):
+@pytest.mark.parametrize("mode", ["pull", "push"])
+def test_moe_parity(B, R, T_r, H, N, E, k, self_rank, rpb, mode):
     X, ids, W = inputs.moe_inputs(R, T_r, H, N, E, k, 1.2, seed=R * 31 + E)
-    r = run_moe(B, X, ids, W, self_rank=self_rank, rpb=rpb)
+    m = B.TL_MODE_PULL if mode == "pull" else B.TL_MODE_PUSH
+    r = run_moe(B, X, ids, W, self_rank=self_rank, rpb=rpb, mode=m)
     check_moe(B, X, ids, W, r, self_rank)
 
 
@@ -114,10 +119,11 @@ def test_moe_invalid_expert_id_is_reported(B):
 
 
 @pytest.mark.slow
-def test_moe_llm_full_size(B):
+@pytest.mark.parametrize("mode", ["pull", "push"])
+def test_moe_llm_full_size(B, mode):
     c = inputs.CONFIGS["moe_llm"]
     X, ids, W = inputs.moe_inputs(c["R"], c["T_r"], c["H"], c["N"], c["E"], c["topk"], c["zipf_s"], seed=0)
-    r = run_moe(B, X, ids, W)
+    r = run_moe(B, X, ids, W, mode=B.TL_MODE_PULL if mode == "pull" else B.TL_MODE_PUSH)
     check_moe(B, X, ids, W, r, full_y=False)
     rng = np.random.default_rng(8)
     P = c["R"] * c["T_r"] * c["topk"]

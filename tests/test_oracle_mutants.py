@@ -146,3 +146,9 @@ def test_pins_catch_moe_order_by_lowest_barrier():
         keys = [(((lo // bpr - s) % R) * bpr + lo % bpr, t) for t, (_, lo, hi) in enumerate(sources)]
         return [t for (_, t) in sorted(keys)]
     _fails(C.check_moe_tile_order, bad, M.tile_sources)
+
+
+def test_pins_catch_pull_range_off_by_one():
+    def bad(perm, k, table, T_r, rpb):
+        return [(m, lo, hi + 1) for (m, lo, hi) in M.tile_sources_pull(perm, k, table, T_r, rpb)]
+    _fails(C.check_moe_pull, bad, M.tile_order_pull, M.route, M.tile_table)

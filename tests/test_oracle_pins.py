@@ -112,6 +112,11 @@ def test_moe_tile_order_pins():
     C.check_moe_tile_order(oracle.moe.tile_order, oracle.moe.tile_sources)
 
 
+def test_moe_pull_pins():
+    M = oracle.moe
+    C.check_moe_pull(M.tile_sources_pull, M.tile_order_pull, M.route, M.tile_table)
+
+
 def test_moe_gemm_pins():
     M = oracle.moe
     C.check_moe_gemm(M.moe_ag_gemm, M.moe_at, M.sorted_tokens, M.route, oracle.ag_gemm.ag_gemm, bf16.decode)

@@ -77,7 +77,7 @@ class tl_moe_args(ctypes.Structure):
         ("N", ctypes.c_int32), ("E", ctypes.c_int32), ("topk", ctypes.c_int32), ("rows_per_barrier", ctypes.c_int32),
         ("X", ctypes.POINTER(_vp)), ("topk_ids", _vp), ("W", ctypes.POINTER(_vp)), ("sorted_tokens", _vp),
         ("Y", _vp), ("perm", _vp), ("expert_offsets", _vp), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
-        ("signals", _vp), ("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32),
+        ("signals", _vp), ("epoch", ctypes.c_uint32), ("mode", ctypes.c_int32),
         ("timeout_ns", ctypes.c_uint64), ("trace", _vp),
     ]
 
@@ -108,7 +108,7 @@ _decl("tl_gemm_rs_num_flags", _i, _i, _i, _i)
 _decl("tl_gemm_rs", _i, ctypes.POINTER(tl_gemm_rs_args), _vp)
 _decl("tl_gemm_rs_noalloc", _i, ctypes.POINTER(tl_gemm_rs_args), _vp, _vp)
 _decl("tl_moe_workspace_size", _sz, _i, _i, _i, _i)
-_decl("tl_moe_num_flags", _i, _i, _i, _i, _i, ctypes.POINTER(_i))
+_decl("tl_moe_num_flags", _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i))
 _decl("tl_moe_ag_gemm", _i, ctypes.POINTER(tl_moe_args), _vp)
 
 
@@ -292,14 +292,14 @@ def tl_moe_workspace_size(R, T_r, E, topk):
     return int(lib.tl_moe_workspace_size(R, T_r, E, topk))
 
 
-def tl_moe_num_flags(R, T_r, H, rows_per_barrier=0):
+def tl_moe_num_flags(R, T_r, H, topk, rows_per_barrier=0, mode=TL_MODE_PULL):
     eff = _i()
-    n = lib.tl_moe_num_flags(R, T_r, H, rows_per_barrier, ctypes.byref(eff))
+    n = lib.tl_moe_num_flags(mode, R, T_r, H, topk, rows_per_barrier, ctypes.byref(eff))
     return n, eff.value
 
 
 def tl_moe_ag_gemm(X, topk_ids, W, sorted_tokens, Y, perm, expert_offsets, workspace, signals: Signals, epoch: int,
-                   *, self_rank=0, rows_per_barrier=0, timeout_ns=0, trace=None, stream=None):
+                   *, self_rank=0, rows_per_barrier=0, mode=TL_MODE_PULL, timeout_ns=0, trace=None, stream=None):
     """AllGather + grouped MoE GEMM (see tilelink.h): Y rows in expert-sorted order."""
     R = len(X)
     T_r, H = X[0].shape
@@ -312,5 +312,5 @@ def tl_moe_ag_gemm(X, topk_ids, W, sorted_tokens, Y, perm, expert_offsets, works
                     W=ctypes.cast(pw, ctypes.POINTER(_vp)), sorted_tokens=_ptr(sorted_tokens), Y=_ptr(Y),
                     perm=_ptr(perm), expert_offsets=_ptr(expert_offsets), workspace=_ptr(workspace),
                     workspace_bytes=workspace.numel() * workspace.element_size(), signals=signals.handle,
-                    epoch=int(epoch) & 0xFFFFFFFF, reserved0=0, timeout_ns=int(timeout_ns), trace=_ptr(trace))
+                    epoch=int(epoch) & 0xFFFFFFFF, mode=mode, timeout_ns=int(timeout_ns), trace=_ptr(trace))
     _check(lib.tl_moe_ag_gemm(ctypes.byref(a), _stream(stream)))

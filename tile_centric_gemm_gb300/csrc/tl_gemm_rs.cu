@@ -58,7 +58,6 @@ constexpr int kNumRedThreads = kNumRedWarps * 32;
 constexpr int RS_THREADS = (kWarpRed0 + kNumRedWarps) * 32;
 constexpr uint32_t RS_SMEM_BARS = pair::SMEM_END;
 constexpr uint32_t RS_SMEM_BYTES = RS_SMEM_BARS + sizeof(pair::Bars) + 1024;
-constexpr int HALF_FLOATS = pair::HM * pair::BN;  // one fp32 128 x 256 half of a partial tile
 constexpr int RB = 8;                             // ranks loaded per batch in the reduce
 constexpr int QU = 2;                             // float4 elements per thread per round in the reduce
 
@@ -66,14 +65,14 @@ struct RsParams {
   CUtensorMap map_a[RS_MAX_RANKS];  // A_r [M, K_r], box 128 rows
   CUtensorMap map_b[RS_MAX_RANKS];  // B_r [K_r, N], box 64 x 64
   uint16_t* out[RS_MAX_RANKS];      // out[d] [Md, N] bf16
-  float* slots;                     // [ring_items][2][128*256] fp32 receive half-slots
+  float* slots;                     // [ring_items][2][half_floats] fp32 receive half-slots
   uint32_t* flags;                  // [2][items][2]: arrival, then reduced
   uint32_t* status;
   int32_t* trace;                   // optional: tile and rank of each item
   uint64_t timeout_ns;
   uint64_t pipe_timeout_ns;
   int32_t R, M, Md, K, N;
-  int32_t Mt_d, Nt, KB, num_tiles, num_items, slice_rows, ring_items;
+  int32_t Mt_d, Nt, KB, num_tiles, num_items, slice_rows, ring_items, half_floats;
   uint32_t epoch;
 };
 
@@ -134,6 +133,10 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
     const int wq = warp & 3;                         // TMEM lane quarter of this warp
     const int et = (warp - kWarpEpi0) * 32 + lane;  // 0..127 among pusher threads
     const int row_in_half = wq * 32 + lane;
+    // half-slot layout [slice][col/4][row in slice][4]: every slice is one contiguous block,
+    // and a warp's store covers runs of slice_rows * 16 contiguous bytes
+    const int my_slice = row_in_half / p.slice_rows, my_row = row_in_half % p.slice_rows;
+    const size_t my_base = (size_t(my_slice) * 64 * p.slice_rows + my_row) * 4;
     int jj = 0;
     for (int i = pair_id; i < p.num_items; i += npairs, ++jj) {
       const Item it = item_of(p, i);
@@ -152,8 +155,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       // all four pusher warps leave together (they meet at a named barrier below)
       if (!named_bar_and(1, kNumEpiThreads, ok)) break;
       tc_fence_after();
-      // half-slot layout [col/4][row][4]: a warp writes 512 contiguous bytes per store
-      float* slot = p.slots + (size_t(i % p.ring_items) * 2 + h) * HALF_FLOATS;
+      float* slot = p.slots + (size_t(i % p.ring_items) * 2 + h) * p.half_floats + my_base;
       for (int c = 0; c < pair::BN / 32; ++c) {
         if (it.nt * pair::BN + c * 32 >= p.N) break;
         uint32_t v[32];
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const float* f = reinterpret_cast<const float*>(v + g * 4);
-          st_global_cg_v4f(slot + (size_t(c * 8 + g) * pair::HM + row_in_half) * 4, f[0], f[1], f[2], f[3]);
+          st_global_cg_v4f(slot + size_t(c * 8 + g) * p.slice_rows * 4, f[0], f[1], f[2], f[3]);
         }
       }
       tc_fence_before();
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
         for (int u = 0; u < QU; ++u) {
           const int e = e0 + u * kNumRedThreads;
           const int c4 = e / s_rows, sr = e - c4 * s_rows;
-          off[u] = e < total ? (c4 * pair::HM + s0 + sr) * 4 : -1;
+          off[u] = e < total ? ((it.j * 64 + c4) * p.slice_rows + sr) * 4 : -1;
           orow[u] = orow_base + sr;
           ocol[u] = it.nt * pair::BN + c4 * 4;
         }
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
               j -= j >= p.R ? p.R : 0;
               int slot = ring_base + j;
               slot -= slot >= p.ring_items ? p.ring_items : 0;
-              const float* src = p.slots + (size_t(slot) * 2 + h) * HALF_FLOATS;
+              const float* src = p.slots + (size_t(slot) * 2 + h) * p.half_floats;
 #pragma unroll
               for (int u = 0; u < QU; ++u)
                 if (off[u] >= 0) v[rr][u] = __ldcg(reinterpret_cast<const float4*>(src + off[u]));
@@ -277,7 +279,10 @@ int current_sm_count() {
   return device_info(&di) == TL_OK ? di.sm_count : 0;
 }
 
-size_t rs_slots_bytes(int ring_items) { return size_t(ring_items) * 2 * HALF_FLOATS * sizeof(float); }
+// floats of one half-slot: R slices of ceil(128/R) rows x 256 columns
+int rs_half_floats(int R) { return R * cdiv(pair::HM, R) * pair::BN; }
+
+size_t rs_slots_bytes(int ring_items, int R) { return size_t(ring_items) * 2 * rs_half_floats(R) * sizeof(float); }
 
 // Validate the arguments shared by both entry points.
 tl_status rs_check(const tl_gemm_rs_args* a, const char* who) {
@@ -326,6 +331,7 @@ tl_status rs_launch(RsParams* p, const tl_gemm_rs_args* a, float* slots, uint32_
   p->num_tiles = rs_num_tiles(a->R, a->M, a->N);
   p->num_items = p->num_tiles * a->R;
   p->slice_rows = cdiv(pair::HM, a->R);
+  p->half_floats = rs_half_floats(a->R);
   p->epoch = a->epoch;
   const int pairs = rs_pairs(p->num_items, sm_count);
   p->ring_items = rs_ring_items(p->num_items, pairs);
@@ -343,7 +349,7 @@ extern "C" size_t tl_gemm_rs_workspace_size(int R, int M, int N) {
   const int sms = tl::current_sm_count();
   // without a usable device, size for every item (always enough)
   const int ring = sms >= 2 ? tl::rs_ring_items(items, tl::rs_pairs(items, sms)) : items;
-  return tl::rs_slots_bytes(ring);
+  return tl::rs_slots_bytes(ring, R);
 }
 
 extern "C" int tl_gemm_rs_num_flags(int R, int M, int N) {
@@ -453,6 +459,6 @@ size_t noalloc_scratch_needed(int R, int M, int N, int sm_count) {
   const int nitems = tl::rs_num_tiles(R, M, N) * R;
   const size_t nflags = 4 * size_t(nitems);
   const int ring = tl::rs_ring_items(nitems, tl::rs_pairs(nitems, sm_count));
-  return align_up(kNoAllocHeader + nflags * 4, 256) + tl::rs_slots_bytes(ring);
+  return align_up(kNoAllocHeader + nflags * 4, 256) + tl::rs_slots_bytes(ring, R);
 }
 }  // namespace

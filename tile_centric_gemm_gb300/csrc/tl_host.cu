@@ -111,25 +111,29 @@ tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cuda
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  int nattr = 1;
+  cudaLaunchAttribute attr[1];
   if (cluster > 1) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = unsigned(cluster);
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    nattr = 2;
-    int max_clusters = 0;
-    cfg.attrs = attr + 1;
+    // Clusters: the grid is sized to the number of clusters the device holds at
+    // once, so every CTA is resident together (the cooperative attribute is not
+    // combined with clusters: profilers cannot launch that combination).  Every
+    // cross-CTA wait in the kernels is bounded in any case.
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
     cfg.numAttrs = 1;
+    int max_clusters = 0;
     if (tl_status s = cuda_ok(cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg), "cluster occupancy"))
       return s;
     if (grid / cluster > max_clusters)
       return fail(TL_ERR_UNSUPPORTED, "%d clusters of %d CTAs cannot be co-resident (at most %d)", grid / cluster,
                   cluster, max_clusters);
-  } else {
+    return cuda_ok(cudaLaunchKernelExC(&cfg, kernel, args), "cluster launch");
+  }
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  {
     int per_sm = 0;
     if (tl_status s = cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, smem),
                               "occupancy"))
@@ -139,7 +143,7 @@ tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cuda
                   di.sm_count);
   }
   cfg.attrs = attr;
-  cfg.numAttrs = nattr;
+  cfg.numAttrs = 1;
   return cuda_ok(cudaLaunchKernelExC(&cfg, kernel, args), "cooperative launch");
 }
 

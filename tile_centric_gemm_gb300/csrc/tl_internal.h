@@ -40,9 +40,10 @@ tl_status device_info(DeviceInfo* out);
 tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                         uint64_t row_pitch_bytes, uint32_t box_rows, uint32_t box_cols);
 
-// Launch with every CTA co-resident (cooperative launch), in clusters of
-// `cluster` CTAs; fails instead of launching when the grid cannot be resident
-// at once.
+// Launch a grid whose CTAs must all be resident at once: a cooperative launch
+// for single CTAs, a cluster launch sized within the device's resident-cluster
+// capacity for clusters of `cluster` CTAs.  Fails instead of launching when the
+// grid cannot be resident at once.
 tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cudaStream_t st, void** args,
                       int cluster = 1);
 

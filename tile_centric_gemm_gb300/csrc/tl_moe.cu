@@ -50,13 +50,15 @@ __host__ __device__ inline int ws_tiles(int) { return WS_HEADER; }
 __host__ __device__ inline int ws_order(int max_tiles) { return WS_HEADER + 6 * max_tiles; }
 __host__ __device__ inline int ws_inv(int max_tiles) { return WS_HEADER + 7 * max_tiles; }
 
+constexpr int ROUTE_SMEM_PAIRS = 20480;  // topk ids and perm kept in shared memory up to this many pairs
+
 struct RouteParams {
   const int32_t* topk;    // [T, k]
   int32_t* perm;          // [P] sorted position -> token*k + slot
   int32_t* offsets;       // [E+1]
   int32_t* ws;            // workspace
   uint32_t* status;
-  int32_t T, k, E, R, T_r, rpb, bpr, self, max_tiles;
+  int32_t T, k, E, R, T_r, rpb, bpr, self, max_tiles, pull, staged;
 };
 
 // Stable counting sort of the P = T*k pairs by expert, then the tile table.
@@ -67,8 +69,19 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   int32_t* s_off = cnt + ROUTE_WARPS * E;      // [E+1]
   int32_t* s_toff = s_off + (E + 1);           // [E+1] tile offsets
   int32_t* s_key = s_toff + (E + 1);           // [max_tiles]
+  int32_t* s_ids = s_key + p.max_tiles;        // [P] when staged
+  int32_t* s_perm = s_ids + (p.staged ? p.T * p.k : 0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.T * p.k;
+  // stage the routing in shared memory (one coalesced pass) so the passes below
+  // do not chain global-memory round trips
+  const int32_t* ids = p.topk;
+  int32_t* perm = p.perm;
+  if (p.staged) {
+    for (int q = tid; q < P; q += ROUTE_THREADS) s_ids[q] = p.topk[q];
+    ids = s_ids;
+    perm = s_perm;
+  }
   const int per_warp = ((P + ROUTE_WARPS - 1) / ROUTE_WARPS + 31) / 32 * 32;
   const int q0 = warp * per_warp, q1 = min(P, q0 + per_warp);
   int32_t* tiles = p.ws + ws_tiles(p.max_tiles);
@@ -81,7 +94,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   for (int base = q0; base < q1; base += 32) {
     const int q = base + lane;
     const bool act = q < q1;
-    int e = act ? p.topk[q] : -1;
+    int e = act ? ids[q] : -1;
     if (act && (e < 0 || e >= E)) {
       record_error(p.status, TL_ERR_INVALID, uint32_t(q), uint32_t(e), uint32_t(E));
       e = min(max(e, 0), E - 1);
@@ -124,12 +137,13 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   for (int base = q0; base < q1; base += 32) {
     const int q = base + lane;
     const bool act = q < q1;
-    int e = act ? min(max(p.topk[q], 0), E - 1) : 0;
+    int e = act ? min(max(ids[q], 0), E - 1) : 0;
     const unsigned am = __ballot_sync(0xffffffffu, act);
     if (act) {
       const unsigned peers = __match_any_sync(am, e);
       const int pos = cnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
-      p.perm[pos] = q;
+      perm[pos] = q;
+      if (p.staged) p.perm[pos] = q;
       inv[q] = pos;
       __syncwarp(am);
       if (lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
@@ -164,7 +178,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     uint32_t mask = 0;
     int blo = 0x7fffffff, bhi = -1;
     for (int i = lane; i < rows; i += 32) {
-      const int tok = p.perm[row0 + i] / p.k;
+      const int tok = perm[row0 + i] / p.k;
       const int r = tok / p.T_r;
       const int b = r * p.bpr + (tok % p.T_r) / p.rpb;
       mask |= 1u << r;
@@ -178,6 +192,20 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
       bhi = max(bhi, __shfl_xor_sync(0xffffffffu, bhi, o));
     }
     if (lane == 0) {
+      int key = 0;
+      if (p.pull) {
+        // pull: the tile's own chunks of sorted rows; chunks arrive in sorted order
+        blo = row0 / p.rpb;
+        bhi = (row0 + rows - 1) / p.rpb;
+        key = bhi;
+      } else {
+        // push: latest arrival position among the source barriers in [blo, bhi];
+        // barrier (r, c) arrives at ((r - self) mod R) * bpr + c
+        for (int r = blo / p.bpr; r <= bhi / p.bpr; ++r) {
+          const int c_hi = (r == bhi / p.bpr) ? bhi % p.bpr : p.bpr - 1;
+          key = max(key, ((r - p.self + p.R) % p.R) * p.bpr + c_hi);
+        }
+      }
       int32_t* tr = tiles + 6 * t;
       tr[0] = e;
       tr[1] = row0;
@@ -185,13 +213,6 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
       tr[3] = blo;
       tr[4] = bhi;
       tr[5] = int32_t(mask);
-      // arrival key: latest position among the barriers in [blo, bhi]; barrier (r, c)
-      // arrives at ((r - self) mod R) * bpr + c
-      int key = 0;
-      for (int r = blo / p.bpr; r <= bhi / p.bpr; ++r) {
-        const int c_hi = (r == bhi / p.bpr) ? bhi % p.bpr : p.bpr - 1;
-        key = max(key, ((r - p.self + p.R) % p.R) * p.bpr + c_hi);
-      }
       s_key[t] = key;
     }
   }
@@ -220,8 +241,9 @@ struct MoeParams {
   int32_t* trace;
   uint64_t timeout_ns;
   uint64_t pipe_timeout_ns;
-  int32_t R, self, T_r, H, N, E, k, rpb, bpr, Nt, KB, num_items, max_tiles;
+  int32_t R, self, T_r, H, N, E, k, rpb, bpr, Nt, KB, num_items, max_tiles, pull, P;
   uint32_t epoch;
+  const int32_t* perm;
 };
 
 __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_constant__ MoeParams p) {
@@ -318,9 +340,12 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
       uint32_t seq = 0;  // pieces loaded by this CTA: buffer seq % NBUF, parity (seq / NBUF) & 1
       bool dead = false;
       for (int it = blockIdx.x; it < p.num_items && !dead; it += gridDim.x) {
+        // push: item = (shard r, chunk c of its tokens), each token scattered to its k sorted rows;
+        // pull: item = chunk of rpb sorted rows, each gathered from its token's shard
         const int jj = it / p.bpr, c = it % p.bpr;
-        const int r = (p.self + jj) % p.R;  // shards self, self+1, ...
-        const int t0 = c * p.rpb, t1 = min(p.T_r, t0 + p.rpb);
+        const int r = (p.self + jj) % p.R;  // push: shards self, self+1, ...
+        const int t0 = p.pull ? it * p.rpb : c * p.rpb;
+        const int t1 = p.pull ? min(p.P, t0 + p.rpb) : min(p.T_r, t0 + p.rpb);
         const int nunits = (t1 - t0) * pieces;
         int issued = 0, stored = 0;
         while (stored < nunits) {
@@ -331,8 +356,15 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
             const int tl = t0 + issued / pieces, pc = issued % pieces;
             const uint32_t off = uint32_t(pc) * COPY_CHUNK;
             const uint32_t sz = min(COPY_CHUNK, row_bytes - off);
+            const uint8_t* src;
+            if (p.pull) {
+              const int tok = p.perm[tl] / p.k;
+              src = p.x[tok / p.T_r] + size_t(tok % p.T_r) * row_bytes + off;
+            } else {
+              src = p.x[r] + size_t(tl) * row_bytes + off;
+            }
             mbar_arrive_expect_tx(&bars->copy[buf], sz);
-            bulk_g2s(stage + buf * COPY_CHUNK, p.x[r] + size_t(tl) * row_bytes + off, sz, &bars->copy[buf]);
+            bulk_g2s(stage + buf * COPY_CHUNK, src, sz, &bars->copy[buf]);
             ++issued;
           }
           const uint32_t q = seq + uint32_t(stored);
@@ -344,10 +376,14 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
           const int tl = t0 + stored / pieces, pc = stored % pieces;
           const uint32_t off = uint32_t(pc) * COPY_CHUNK;
           const uint32_t sz = min(COPY_CHUNK, row_bytes - off);
-          const int tok = r * p.T_r + tl;
-          for (int sl = 0; sl < p.k; ++sl) {
-            const int pos = inv[tok * p.k + sl];
-            bulk_s2g(p.sorted + size_t(pos) * row_bytes + off, stage + buf * COPY_CHUNK, sz);
+          if (p.pull) {
+            bulk_s2g(p.sorted + size_t(tl) * row_bytes + off, stage + buf * COPY_CHUNK, sz);
+          } else {
+            const int tok = r * p.T_r + tl;
+            for (int sl = 0; sl < p.k; ++sl) {
+              const int pos = inv[tok * p.k + sl];
+              bulk_s2g(p.sorted + size_t(pos) * row_bytes + off, stage + buf * COPY_CHUNK, sz);
+            }
           }
           bulk_commit();
           ++stored;
@@ -356,7 +392,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
         bulk_wait<0>();
         if (dead) break;
         fence_proxy_async_global();
-        st_release(p.flags + r * p.bpr + c, p.epoch);
+        st_release(p.flags + (p.pull ? it : r * p.bpr + c), p.epoch);
       }
       bulk_wait<0>();
     }
@@ -367,7 +403,11 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
 
 int moe_max_tiles(int P, int E) { return (P + TM - 1) / TM + E; }
 
-int moe_default_rpb(int H, int T_r) { return std::min(T_r, std::max(1, int(32768 / (size_t(H) * 2)))); }
+// push: tokens of a shard per flag (about 32 KB of source rows); pull: sorted rows per flag (about 64 KB)
+int moe_default_rpb(int mode, int H, int T_r, long long P) {
+  if (mode == TL_MODE_PULL) return int(std::min<long long>(P, std::max(1, int(65536 / (size_t(H) * 2)))));
+  return std::min(T_r, std::max(1, int(32768 / (size_t(H) * 2))));
+}
 
 }  // namespace
 }  // namespace tl
@@ -380,11 +420,14 @@ extern "C" size_t tl_moe_workspace_size(int R, int T_r, int E, int topk) {
   return size_t(tl::ws_inv(mt) + P) * sizeof(int32_t);
 }
 
-extern "C" int tl_moe_num_flags(int R, int T_r, int H, int rows_per_barrier, int* effective_rpb) {
-  if (R < 1 || T_r < 1 || H < 1) return -1;
-  const int rpb = rows_per_barrier > 0 ? std::min(rows_per_barrier, T_r) : tl::moe_default_rpb(H, T_r);
+extern "C" int tl_moe_num_flags(int mode, int R, int T_r, int H, int topk, int rows_per_barrier, int* effective_rpb) {
+  if (R < 1 || T_r < 1 || H < 1 || topk < 1 || (mode != TL_MODE_PULL && mode != TL_MODE_PUSH)) return -1;
+  const long long P = (long long)R * T_r * topk;
+  if (P > (1ll << 30)) return -1;
+  const int lim = mode == TL_MODE_PULL ? int(P) : T_r;
+  const int rpb = rows_per_barrier > 0 ? std::min(rows_per_barrier, lim) : tl::moe_default_rpb(mode, H, T_r, P);
   if (effective_rpb) *effective_rpb = rpb;
-  return R * tl::cdiv(T_r, rpb);
+  return mode == TL_MODE_PULL ? tl::cdiv(int(P), rpb) : R * tl::cdiv(T_r, rpb);
 }
 
 extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
@@ -423,8 +466,10 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
   const size_t need = tl_moe_workspace_size(a->R, a->T_r, a->E, a->topk);
   if (a->workspace_bytes < need)
     return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: workspace %zu bytes, need %zu", a->workspace_bytes, need);
+  if (a->mode != TL_MODE_PULL && a->mode != TL_MODE_PUSH) return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: mode %d", a->mode);
+  const bool pull = a->mode == TL_MODE_PULL;
   int rpb = 0;
-  const int nflags = tl_moe_num_flags(a->R, a->T_r, a->H, a->rows_per_barrier, &rpb);
+  const int nflags = tl_moe_num_flags(a->mode, a->R, a->T_r, a->H, a->topk, a->rows_per_barrier, &rpb);
   if (a->signals->num_flags < nflags)
     return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: signals hold %d flags, need %d", a->signals->num_flags, nflags);
   DeviceInfo di{};
@@ -448,7 +493,12 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
   rp.bpr = cdiv(a->T_r, rpb);
   rp.self = a->self_rank;
   rp.max_tiles = max_tiles;
-  const size_t route_smem = (size_t(ROUTE_WARPS) * a->E + 2 * (a->E + 1) + max_tiles) * sizeof(int32_t);
+  rp.pull = pull ? 1 : 0;
+  rp.staged = P <= ROUTE_SMEM_PAIRS ? 1 : 0;
+  const size_t route_smem =
+      (size_t(ROUTE_WARPS) * a->E + 2 * (a->E + 1) + max_tiles + (rp.staged ? 2 * P : 0)) * sizeof(int32_t);
+  if (route_smem > size_t(di.max_smem_optin))
+    return fail(TL_ERR_UNSUPPORTED, "tl_moe_ag_gemm: routing needs %zu bytes of shared memory", route_smem);
   if (tl_status s = cuda_ok(cudaFuncSetAttribute(reinterpret_cast<const void*>(&moe_route_kernel),
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(route_smem)),
                             "cudaFuncSetAttribute(route)"))
@@ -486,8 +536,11 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
     p->bpr = cdiv(a->T_r, rpb);
     p->Nt = cdiv(a->N, pair::BN);
     p->KB = cdiv(a->H, pair::BK);
-    p->num_items = a->R * p->bpr;
+    p->num_items = pull ? nflags : a->R * p->bpr;
     p->max_tiles = max_tiles;
+    p->pull = pull ? 1 : 0;
+    p->P = int(P);
+    p->perm = a->perm;
     p->epoch = a->epoch;
     const int pairs = std::max(1, std::min(di.sm_count / 2, std::max(max_tiles * p->Nt, (p->num_items + 1) / 2)));
     void* args[] = {p};
