@@ -117,7 +117,7 @@ typedef struct tl_gemm_args {
   int32_t reserved0;
   const void* A;               /* device bf16 [M, K] */
   const void* B;               /* device bf16 [K, N] */
-  void* C;                     /* device bf16 [M, N], written */
+  void* C;                     /* device bf16 [M, N], written; may be NULL when C_f32 is given */
   float* C_f32;                /* optional device float [M, N], written; NULL = none */
   tl_signals* signals;         /* receives device-side errors in its status word (any size >= 1) */
   uint64_t timeout_ns;         /* bound of the pipeline waits is 2 * timeout + 1 s; 0 = 1 s */
@@ -249,6 +249,38 @@ tl_status tl_gemm_rs(const tl_gemm_rs_args* args, void* stream);
  */
 #define TL_GEMM_RS_NOALLOC_MAX_BYTES (64ull << 20)
 tl_status tl_gemm_rs_noalloc(const tl_gemm_rs_args* args, uint32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------- communication halves alone
+ * tl_allgather: the AllGather-GEMM producer without the GEMM -- the same copy
+ * routine moves every shard into `gathered`, rows_per_barrier rows at a time,
+ * and releases one flag per chunk (flag ids and modes as for tl_ag_gemm, so a
+ * caller's own consumer can tl_tile_wait on them).  One warp on every SM.
+ * tl_reduce_scatter: the GEMM-ReduceScatter reduce stage without the GEMM --
+ * out[d] = rows [d*M/R, (d+1)*M/R) of (((P_0 + P_1) + P_2) + ...) with the fp32
+ * partials P_r [M, N] given, summed in rank order in fp32, one bf16 rounding.
+ * Both serve as the separate communication step of a decomposed schedule
+ * (talk summary, Background) and to measure the fused kernels' overlap.
+ */
+typedef struct tl_allgather_args {
+  int32_t R, self_rank, M_shard, K;  /* as tl_ag_gemm_args */
+  int32_t mode, rows_per_barrier;
+  const void* const* A_shards;       /* host array of R device pointers, bf16 [M_shard, K] */
+  void* gathered;                    /* device bf16 [R*M_shard, K], written */
+  tl_signals* signals;               /* >= tl_ag_gemm_num_flags(...) flags, released per chunk */
+  const tl_signals* src_ready;       /* pull mode readiness flags, else NULL */
+  uint32_t epoch;                    /* nonzero */
+  uint32_t reserved0;
+  uint64_t timeout_ns;               /* 0 = 1 s */
+} tl_allgather_args;
+
+typedef struct tl_reduce_scatter_args {
+  int32_t R, M, N, reserved0;        /* M multiple of R, N multiple of 8 */
+  const float* const* partials;      /* host array of R device pointers, float [M, N] */
+  void* const* out;                  /* host array of R device pointers, bf16 [M/R, N], written */
+} tl_reduce_scatter_args;
+
+tl_status tl_allgather(const tl_allgather_args* args, void* stream);
+tl_status tl_reduce_scatter(const tl_reduce_scatter_args* args, void* stream);
 
 /* ---------------------------------------------------------------- AllGather + grouped MoE GEMM
  * The AllGather + GroupGEMM part of an MoE layer (talk summary, Key Findings

@@ -29,7 +29,7 @@ EXPORTED = [
     "tl_signals_reset", "tl_tile_notify", "tl_tile_wait", "tl_query_status",
     "tl_gemm", "tl_ag_gemm_num_flags", "tl_ag_gemm_tile_order", "tl_ag_gemm",
     "tl_gemm_rs_workspace_size", "tl_gemm_rs_num_flags", "tl_gemm_rs", "tl_gemm_rs_noalloc",
-    "tl_moe_workspace_size", "tl_moe_num_flags", "tl_moe_ag_gemm",
+    "tl_moe_workspace_size", "tl_moe_num_flags", "tl_moe_ag_gemm", "tl_allgather", "tl_reduce_scatter",
 ]
 
 
@@ -82,6 +82,22 @@ class tl_moe_args(ctypes.Structure):
     ]
 
 
+class tl_allgather_args(ctypes.Structure):
+    _fields_ = [
+        ("R", ctypes.c_int32), ("self_rank", ctypes.c_int32), ("M_shard", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("mode", ctypes.c_int32), ("rows_per_barrier", ctypes.c_int32), ("A_shards", ctypes.POINTER(_vp)),
+        ("gathered", _vp), ("signals", _vp), ("src_ready", _vp), ("epoch", ctypes.c_uint32),
+        ("reserved0", ctypes.c_uint32), ("timeout_ns", ctypes.c_uint64),
+    ]
+
+
+class tl_reduce_scatter_args(ctypes.Structure):
+    _fields_ = [
+        ("R", ctypes.c_int32), ("M", ctypes.c_int32), ("N", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("partials", ctypes.POINTER(_vp)), ("out", ctypes.POINTER(_vp)),
+    ]
+
+
 def _decl(name, restype, *argtypes):
     f = getattr(lib, name)
     f.restype = restype
@@ -110,6 +126,8 @@ _decl("tl_gemm_rs_noalloc", _i, ctypes.POINTER(tl_gemm_rs_args), _vp, _vp)
 _decl("tl_moe_workspace_size", _sz, _i, _i, _i, _i)
 _decl("tl_moe_num_flags", _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i))
 _decl("tl_moe_ag_gemm", _i, ctypes.POINTER(tl_moe_args), _vp)
+_decl("tl_allgather", _i, ctypes.POINTER(tl_allgather_args), _vp)
+_decl("tl_reduce_scatter", _i, ctypes.POINTER(tl_reduce_scatter_args), _vp)
 
 
 def _check(code):
@@ -314,3 +332,27 @@ def tl_moe_ag_gemm(X, topk_ids, W, sorted_tokens, Y, perm, expert_offsets, works
                     workspace_bytes=workspace.numel() * workspace.element_size(), signals=signals.handle,
                     epoch=int(epoch) & 0xFFFFFFFF, mode=mode, timeout_ns=int(timeout_ns), trace=_ptr(trace))
     _check(lib.tl_moe_ag_gemm(ctypes.byref(a), _stream(stream)))
+
+
+def tl_allgather(A_shards, gathered, signals: Signals, epoch: int, *, self_rank=0, mode=TL_MODE_PUSH,
+                 src_ready: Signals | None = None, rows_per_barrier=0, timeout_ns=0, stream=None):
+    """Gather the shards into `gathered`, releasing one flag per chunk (see tilelink.h)."""
+    R = len(A_shards)
+    M_shard, K = A_shards[0].shape
+    ptrs = _ptr_array(A_shards)
+    a = tl_allgather_args(R=R, self_rank=self_rank, M_shard=M_shard, K=K, mode=mode,
+                          rows_per_barrier=rows_per_barrier, A_shards=ctypes.cast(ptrs, ctypes.POINTER(_vp)),
+                          gathered=_ptr(gathered), signals=signals.handle,
+                          src_ready=src_ready.handle if src_ready is not None else None,
+                          epoch=int(epoch) & 0xFFFFFFFF, reserved0=0, timeout_ns=int(timeout_ns))
+    _check(lib.tl_allgather(ctypes.byref(a), _stream(stream)))
+
+
+def tl_reduce_scatter(partials, out, *, stream=None):
+    """out[d] = rows d of the rank-ordered fp32 sum of the partials, bf16."""
+    R = len(partials)
+    M, N = partials[0].shape
+    pp, po = _ptr_array(partials), _ptr_array(out)
+    a = tl_reduce_scatter_args(R=R, M=M, N=N, reserved0=0, partials=ctypes.cast(pp, ctypes.POINTER(_vp)),
+                               out=ctypes.cast(po, ctypes.POINTER(_vp)))
+    _check(lib.tl_reduce_scatter(ctypes.byref(a), _stream(stream)))

@@ -22,6 +22,7 @@
 #include <new>
 #include <vector>
 
+#include "tl_copy.cuh"
 #include "tl_internal.h"
 #include "tl_pair.cuh"
 
@@ -163,54 +164,9 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
   } else if (warp == kWarpCopy) {
     // ---------------------------------------------------------------- AllGather producer
     if (lane == 0) {
-      uint8_t* stage = smem + AG_SMEM_COPY;
-      uint32_t seq = 0;  // chunks this CTA has loaded: buffer seq % NBUF, parity (seq / NBUF) & 1
-      bool dead = false;
-      for (int it = blockIdx.x; it < p.num_items && !dead; it += gridDim.x) {
-        // copy order: shards self+1, ..., self+R-1, then self; chunks ascending
-        const int jj = it / p.bpr, b = it % p.bpr;
-        const int r = (p.self + 1 + jj) % p.R;
-        const int lo = b * p.rpb;
-        const int rows = min(p.rpb, p.M_shard - lo);
-        const uint8_t* src = p.shard[r] + size_t(lo) * p.K * 2;
-        uint8_t* dst = p.gathered + (size_t(r) * p.M_shard + lo) * size_t(p.K) * 2;
-        const uint32_t bytes = uint32_t(rows) * uint32_t(p.K) * 2u;
-        const int flag_id = r * p.bpr + b;
-        // pull mode: the source publishes readiness first (second barrier of the pull protocol)
-        if (p.ready) wait_flag(p.ready + flag_id, p.epoch, p.status, p.timeout_ns, uint32_t(flag_id), TL_ERR_TIMEOUT);
-        const int nch = int((bytes + COPY_CHUNK - 1) / COPY_CHUNK);
-        int issued = 0, stored = 0;
-        while (stored < nch) {
-          while (issued < nch && issued - stored < COPY_NBUF) {
-            const uint32_t q = seq + uint32_t(issued);
-            const int buf = int(q % COPY_NBUF);
-            // the store that last read `buf` (chunk q - NBUF) must have finished reading it
-            bulk_wait_read_dyn(stored - issued + COPY_NBUF - 1);
-            const uint32_t off = uint32_t(issued) * COPY_CHUNK;
-            const uint32_t sz = min(COPY_CHUNK, bytes - off);
-            mbar_arrive_expect_tx(&bars->copy[buf], sz);
-            bulk_g2s(stage + buf * COPY_CHUNK, src + off, sz, &bars->copy[buf]);
-            ++issued;
-          }
-          const uint32_t q = seq + uint32_t(stored);
-          const int buf = int(q % COPY_NBUF);
-          if (!mbar_wait(&bars->copy[buf], (q / COPY_NBUF) & 1u, abort, p.status, p.pipe_timeout_ns, 5)) {
-            dead = true;
-            break;
-          }
-          const uint32_t off = uint32_t(stored) * COPY_CHUNK;
-          bulk_s2g(dst + off, stage + buf * COPY_CHUNK, min(COPY_CHUNK, bytes - off));
-          bulk_commit();
-          ++stored;
-        }
-        seq += uint32_t(nch);
-        // produce_tile_notify: writes complete -> order with the generic proxy -> release
-        bulk_wait<0>();
-        if (dead) break;
-        fence_proxy_async_global();
-        st_release(p.flags + flag_id, p.epoch);
-      }
-      bulk_wait<0>();
+      AgCopyJob job{p.shard, p.gathered, p.flags, p.ready, p.status, p.timeout_ns, p.pipe_timeout_ns,
+                    p.R, p.self, p.M_shard, p.K, p.rpb, p.bpr, p.num_items, p.epoch};
+      ag_copy_items(job, smem + AG_SMEM_COPY, bars->copy, abort, int(blockIdx.x), int(gridDim.x));
     }
     __syncwarp();
   }

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_pair_kernel(const __grid
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
-        if (row_ok) {
+        if (row_ok && p.C) {
           uint16_t* crow = p.C + size_t(row) * p.N + col0;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -85,7 +85,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_pair_kernel(const __grid
                            pack_bf16x2(f[6], f[7]));
             }
           }
-          if (p.C_f32) {
+        }
+        if (row_ok && p.C_f32) {
+          {
             float* frow = p.C_f32 + size_t(row) * p.N + col0;
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
@@ -114,8 +116,9 @@ extern "C" tl_status tl_gemm(const tl_gemm_args* a, void* stream) {
   if (a->M < 1 || a->N < 1 || a->K < 1) return fail(TL_ERR_INVALID, "tl_gemm: empty shape");
   if (a->K % 8 || a->N % 8)
     return fail(TL_ERR_UNSUPPORTED, "tl_gemm: K (%d) and N (%d) must be multiples of 8", a->K, a->N);
-  if (!a->A || !a->B || !a->C || !a->signals) return fail(TL_ERR_INVALID, "tl_gemm: NULL pointer argument");
-  if (!aligned16(a->A) || !aligned16(a->B) || !aligned16(a->C) || (a->C_f32 && !aligned16(a->C_f32)))
+  if (!a->A || !a->B || (!a->C && !a->C_f32) || !a->signals)
+    return fail(TL_ERR_INVALID, "tl_gemm: NULL pointer argument");
+  if (!aligned16(a->A) || !aligned16(a->B) || (a->C && !aligned16(a->C)) || (a->C_f32 && !aligned16(a->C_f32)))
     return fail(TL_ERR_INVALID, "tl_gemm: pointers must be 16-byte aligned");
   DeviceInfo di{};
   if (tl_status s = device_info(&di)) return s;
