@@ -52,7 +52,11 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true", help="skip the fused-vs-halves measurements")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--only", choices=["ag", "rs", "moe"],
+                    help="run one fused call of the step (W untimed, then K timed back to back) and print its "
+                         "device time; for profiling a single kernel on the bench's workload")
     return ap.parse_args()
 
 
@@ -284,6 +288,116 @@ class Workload:
                 raise RuntimeError(f"device error {code} at {where}")
 
 
+def flushed_time_us(torch, fn, flush, reps=7):
+    """Median device time (CUDA events on the current stream) of fn() over reps
+    runs, each after a write of a buffer larger than L2 (not timed; it also
+    hides the host's launch latency), after one warm-up run."""
+    fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(ts)
+
+
+def overlap_metrics(torch, B, wl):
+    """The fused kernels against their halves run alone, one after the other, and
+    (AG-GEMM) decomposed onto two streams: the copy engine gathers shard by shard
+    on a side stream while per-shard GEMMs wait on each copy's event, replayed
+    from a CUDA graph so the host's launch rate does not bound it.  Every variant
+    runs from a cold L2."""
+    R, Ms, K = AG["R"], AG["M_shard"], AG["K"]
+    A, Bm = wl.d_ag[:R], wl.d_ag[R]
+    sig1 = B.Signals(max(1, wl.sig_ag.num_flags))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ep = [10_000_000]
+
+    def copy_only():
+        ep[0] += 1
+        B.tl_allgather(A, wl.G, sig1, ep[0])
+
+    def gemm_only():
+        B.tl_gemm(wl.G, Bm, wl.C, sig1)
+
+    def seq():
+        copy_only()
+        gemm_only()
+
+    s1 = torch.cuda.Stream()
+
+    def decomposed_launches():
+        main = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(main)
+        s1.wait_event(start)
+        evs = []
+        with torch.cuda.stream(s1):
+            for j in range(1, R):
+                wl.G[j * Ms:(j + 1) * Ms].copy_(A[j], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s1)
+                evs.append(e)
+            wl.G[0:Ms].copy_(A[0], non_blocking=True)
+        B.tl_gemm(A[0], Bm, wl.C[0:Ms], sig1)
+        for j, e in zip(range(1, R), evs):
+            main.wait_event(e)
+            B.tl_gemm(wl.G[j * Ms:(j + 1) * Ms], Bm, wl.C[j * Ms:(j + 1) * Ms], sig1)
+        main.wait_stream(s1)
+
+    decomposed_launches()  # sets every kernel's launch attributes before the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        decomposed_launches()
+
+    t_copy = flushed_time_us(torch, copy_only, flush)
+    t_gemm = flushed_time_us(torch, gemm_only, flush)
+    t_seq = flushed_time_us(torch, seq, flush)
+    t_dec = flushed_time_us(torch, graph.replay, flush)
+    t_fused = flushed_time_us(torch, wl.ag, flush)
+    ag = {"t_copy_us": t_copy, "t_gemm_us": t_gemm, "t_seq_us": t_seq, "t_decomposed_us": t_dec,
+          "t_fused_us": t_fused, "speedup_vs_seq": t_seq / t_fused,
+          "speedup_vs_decomposed": t_dec / t_fused,
+          "fused_over_max_copy_gemm": t_fused / max(t_copy, t_gemm),
+          "overlap_efficiency": (t_seq - t_fused) / min(t_copy, t_gemm),
+          "copy_gbs": 2 * R * Ms * K * 2 / (t_copy * 1e-6) / 1e9}
+    # GEMM-RS: per-rank GEMMs with fp32 partials, then the rank-ordered ReduceScatter
+    Rr, M, N = RS["R"], RS["M"], RS["N"]
+    parts = [torch.empty(M, N, dtype=torch.float32, device="cuda") for _ in range(Rr)]
+
+    def rs_gemm():
+        for r in range(Rr):
+            B.tl_gemm(wl.d_rs[r], wl.d_rs[Rr + r], None, sig1, C_f32=parts[r])
+
+    def rs_reduce():
+        B.tl_reduce_scatter(parts, wl.out)
+
+    def rs_seq():
+        rs_gemm()
+        rs_reduce()
+
+    t_g = flushed_time_us(torch, rs_gemm, flush, reps=5)
+    t_r = flushed_time_us(torch, rs_reduce, flush, reps=5)
+    t_s = flushed_time_us(torch, rs_seq, flush, reps=5)
+    t_f = flushed_time_us(torch, wl.rs, flush, reps=5)
+    rs = {"t_gemm_us": t_g, "t_reduce_us": t_r, "t_seq_us": t_s, "t_fused_us": t_f,
+          "speedup_vs_seq": t_s / t_f, "fused_over_max_gemm_reduce": t_f / max(t_g, t_r),
+          "overlap_efficiency": (t_s - t_f) / min(t_g, t_r),
+          "reduce_gbs": (Rr * M * N * 4 + M * N * 2) / (t_r * 1e-6) / 1e9}
+    for s in (sig1, wl.sig_ag, wl.sig_rs):
+        code, where = B.tl_query_status(s)
+        if code:
+            raise RuntimeError(f"device error {code} at {where} in the overlap measurements")
+    del parts, flush
+    return {"ag_gemm": ag, "gemm_rs": rs}
+
+
 def main():
     args = parse()
     world, rank, local_rank = dist_env()
@@ -310,6 +424,25 @@ def main():
     peaks, peak_src = load_peaks()
     wl = Workload(B, torch)
     stream = torch.cuda.current_stream()
+    if args.only:
+        fn = {"ag": wl.ag, "rs": wl.rs, "moe": wl.moe}[args.only]
+        flops = {"ag": AG_FLOPS, "rs": RS_FLOPS, "moe": MOE_FLOPS}[args.only]
+        for _ in range(args.warmup):
+            fn()
+        barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        barrier()
+        wl.check_status()
+        us = a.elapsed_time(b) * 1e3 / max(1, args.steps)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "us_per_call": us, "tflops": flops / (us * 1e-6) / 1e12,
+                              "calls": args.steps, "warmup": args.warmup}), flush=True)
+        return
     for _ in range(max(3, args.warmup)):
         wl.ag()
         wl.rs()
@@ -398,6 +531,8 @@ def main():
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes()},
         "gpu_launches": K * wl.launches_per_step,
     }
+    if not args.no_overlap:
+        line["overlap"] = overlap_metrics(torch, B, wl)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, sample = time_oracle()
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",

@@ -98,14 +98,71 @@ tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint6
   return TL_OK;
 }
 
+namespace {
+// Per (device, kernel, block, smem, cluster): the attribute is set and the resident
+// capacity (CTAs per SM, or clusters) queried once, then reused on every launch.
+struct LaunchKey {
+  int device;
+  const void* kernel;
+  int block;
+  size_t smem;
+  int cluster;
+  bool operator==(const LaunchKey& o) const {
+    return device == o.device && kernel == o.kernel && block == o.block && smem == o.smem && cluster == o.cluster;
+  }
+};
+struct LaunchEntry {
+  LaunchKey key;
+  int capacity;
+};
+std::mutex g_launch_mu;
+LaunchEntry g_launch_cache[64];
+int g_launch_n = 0;
+}  // namespace
+
 tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cudaStream_t st, void** args,
                       int cluster) {
-  if (tl_status s = cuda_ok(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
-                            "cudaFuncSetAttribute(max dynamic smem)"))
-    return s;
   DeviceInfo di{};
   if (tl_status s = device_info(&di)) return s;
   if (cluster < 1 || grid % cluster) return fail(TL_ERR_INTERNAL, "grid %d is not a multiple of cluster %d", grid, cluster);
+  const LaunchKey key{di.device, kernel, block, smem, cluster};
+  int capacity = -1;
+  {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    for (int i = 0; i < g_launch_n; ++i)
+      if (g_launch_cache[i].key == key) capacity = g_launch_cache[i].capacity;
+  }
+  if (capacity < 0) {
+    if (tl_status s = cuda_ok(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
+                              "cudaFuncSetAttribute(max dynamic smem)"))
+      return s;
+    if (cluster > 1) {
+      cudaLaunchConfig_t q{};
+      q.gridDim = dim3(grid);
+      q.blockDim = dim3(block);
+      q.dynamicSmemBytes = smem;
+      cudaLaunchAttribute ca[1];
+      ca[0].id = cudaLaunchAttributeClusterDimension;
+      ca[0].val.clusterDim.x = unsigned(cluster);
+      ca[0].val.clusterDim.y = 1;
+      ca[0].val.clusterDim.z = 1;
+      q.attrs = ca;
+      q.numAttrs = 1;
+      if (tl_status s = cuda_ok(cudaOccupancyMaxActiveClusters(&capacity, kernel, &q), "cluster occupancy")) return s;
+      capacity *= cluster;
+    } else {
+      int per_sm = 0;
+      if (tl_status s = cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, smem),
+                                "occupancy"))
+        return s;
+      capacity = per_sm * di.sm_count;
+    }
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    if (g_launch_n < 64) g_launch_cache[g_launch_n++] = LaunchEntry{key, capacity};
+  }
+  if (grid > capacity)
+    return fail(TL_ERR_UNSUPPORTED, "grid of %d CTAs (clusters of %d) cannot be co-resident (at most %d)", grid,
+                cluster, capacity);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
@@ -123,25 +180,10 @@ tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cuda
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int max_clusters = 0;
-    if (tl_status s = cuda_ok(cudaOccupancyMaxActiveClusters(&max_clusters, kernel, &cfg), "cluster occupancy"))
-      return s;
-    if (grid / cluster > max_clusters)
-      return fail(TL_ERR_UNSUPPORTED, "%d clusters of %d CTAs cannot be co-resident (at most %d)", grid / cluster,
-                  cluster, max_clusters);
     return cuda_ok(cudaLaunchKernelExC(&cfg, kernel, args), "cluster launch");
   }
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
-  {
-    int per_sm = 0;
-    if (tl_status s = cuda_ok(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, smem),
-                              "occupancy"))
-      return s;
-    if (per_sm < 1 || grid > per_sm * di.sm_count)
-      return fail(TL_ERR_UNSUPPORTED, "grid of %d CTAs cannot be co-resident (%d per SM x %d SMs)", grid, per_sm,
-                  di.sm_count);
-  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cuda_ok(cudaLaunchKernelExC(&cfg, kernel, args), "cooperative launch");
