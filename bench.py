@@ -38,11 +38,31 @@ RS = dict(R=8, M=8192, K_r=1792, N=4096)
 MOE = dict(R=8, T_r=1024, H=4096, N=1408, E=32, topk=2, zipf_s=1.2)
 AG_FLOPS = 2 * AG["R"] * AG["M_shard"] * AG["N"] * AG["K"]
 RS_FLOPS = 2 * RS["R"] * RS["M"] * RS["N"] * RS["K_r"]
+# operands read once and the bf16 output written once (the emulated fp32 partial push and read are extra)
+RS_BYTES = RS["R"] * (RS["M"] * RS["K_r"] + RS["K_r"] * RS["N"]) * 2 + RS["M"] * RS["N"] * 2
 MOE_FLOPS = 2 * MOE["R"] * MOE["T_r"] * MOE["topk"] * MOE["N"] * MOE["H"]
 METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s on 1 GB300"
 WORKLOAD = ("AG-GEMM R=8 [8192x4096]x[4096x1792] + GEMM-RS R=8 8x[8192x1792]x[1792x4096] "
             "+ MoE AG+grouped GEMM R=8 8192 tokens top-2/32 experts [16384x4096]x[4096x1408] "
             "(TP MLP up/down projection and MoE expert up-projection, emulated ranks)")
+
+
+# DRAM traffic of one gemm_rs_kernel launch on this workload, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel's
+# sources hash to what was captured.
+RS_TRAFFIC_BYTES = 3_119_440_128 + 1_101_488_128
+RS_TRAFFIC_SOURCES = ("tl_gemm_rs.cu", "tl_pair.cuh", "tl_common.cuh", "tl_ptx.cuh")
+RS_TRAFFIC_SHA256 = "c110035e2bf9ae9a6a5e252185854e180dfeeb45eed75de905bf09b46dfc7bbc"
+
+
+def rs_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tile_centric_gemm_gb300", "csrc")
+    for f in RS_TRAFFIC_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return RS_TRAFFIC_BYTES if h.hexdigest() == RS_TRAFFIC_SHA256 else None
 
 
 def parse():
@@ -525,7 +545,8 @@ def main():
         "roofline": {"bound": "tensor", "kernel": "gemm_rs_kernel", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
                      "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),
-                     "traffic": None},
+                     "traffic": rs_traffic(), "traffic_unit": "bytes per launch (ncu DRAM read + write)",
+                     "algorithmic_bytes": RS_BYTES},
         "clocks": clocks,
         "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes()},

@@ -38,7 +38,10 @@
  *    rest of the launch, and finishes; its outputs are then undefined.
  *  - Failure: no call aborts the process; no exception crosses the ABI.
  *    tl_last_error() returns a message for the calling thread's last error.
- *  - Not capturable into CUDA graphs for replay: epochs are launch parameters.
+ *  - Calls that take an epoch are not capturable into CUDA graphs for replay:
+ *    the epoch is a launch parameter.  tl_gemm and tl_reduce_scatter take none;
+ *    they may be captured once a first call outside any capture has set up
+ *    their kernel on the device (launch attributes are set on first use).
  */
 #ifndef TILELINK_H
 #define TILELINK_H
@@ -293,7 +296,7 @@ tl_status tl_reduce_scatter(const tl_reduce_scatter_args* args, void* stream);
  *   sorted_tokens[i]   = token perm[i]/topk  (the gathered tokens, expert order)
  *   Y[i, :]            = sorted_tokens[i] . W_{expert of row i}   (fp32 accumulate, bf16)
  * Two stream-ordered launches: a one-CTA routing kernel (histogram, scan,
- * stable counting sort, tile table, tile order) and one cooperative kernel in
+ * stable counting sort, tile table, tile order) and one persistent kernel in
  * which copy warps move token rows into `sorted_tokens` while tcgen05 GEMM
  * tiles of 256 rows of one expert wait on the flags their lookup-table entry
  * names and multiply their sorted rows by their expert's weight.  The two data

@@ -8,8 +8,9 @@
 //    barrier); a wait's tile id maps affinely to (rank, barrier); consumer
 //    tiles are swizzled into data-arrival order.
 //
-// A persistent, cooperative grid of CTA pairs (clusters of two, one CTA per
-// SM) computes 256 x 256 tiles with tcgen05.mma.cta_group::2.  Every CTA has:
+// A persistent grid of CTA pairs (clusters of two, one CTA per SM, sized so
+// that every CTA is resident at once) computes 256 x 256 tiles with
+// tcgen05.mma.cta_group::2.  Every CTA has:
 //   warp 0      TMA producer: acquires the arrival flags of its 128 rows of a
 //               tile, then streams its rows of A (gathered, or the self shard in
 //               place) and its 128 columns of B into a 6-stage ring.

@@ -1,4 +1,4 @@
-// tl_host.cu -- error reporting, device queries, tensor maps, cooperative launch,
+// tl_host.cu -- error reporting, device queries, tensor maps, co-resident launches,
 // and the signal primitives of the C ABI (tl_signals_*, tl_tile_notify,
 // tl_tile_wait, tl_query_status).
 //

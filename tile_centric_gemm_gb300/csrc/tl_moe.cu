@@ -15,7 +15,7 @@
 //     (perm and its inverse), then the tile table -- per 256-row tile its
 //     expert, first sorted row, rows, lowest and highest producer barrier and
 //     source-rank mask -- and the consumer tile order.
-//  2. moe_gemm_kernel (cooperative, CTA pairs, one CTA per SM): copy warps
+//  2. moe_gemm_kernel (persistent CTA pairs, one CTA per SM): copy warps
 //     gather every token row of every shard and scatter it to its k sorted
 //     positions in `sorted_tokens` (bulk TMA, one flag per chunk of
 //     rows_per_barrier tokens, shards in the order self, self+1, ...); the TMA
