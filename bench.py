@@ -74,6 +74,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true", help="skip the fused-vs-halves measurements")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--sweep", action="store_true",
+                    help="AG-GEMM sweep (R in {2,4,8}, M in {1024..16384}, K=8192, N=1024; shards in HBM and "
+                         "peer shards in pinned host memory): copy, GEMM, sequential and fused times, one JSON line")
     ap.add_argument("--only", choices=["ag", "rs", "moe"],
                     help="run one fused call of the step (W untimed, then K timed back to back) and print its "
                          "device time; for profiling a single kernel on the bench's workload")
@@ -418,6 +421,70 @@ def overlap_metrics(torch, B, wl):
     return {"ag_gemm": ag, "gemm_rs": rs}
 
 
+SWEEP = dict(R=(2, 4, 8), M=(1024, 2048, 4096, 8192, 16384), K=8192, N=1024)
+
+
+def run_sweep(torch, B, peaks):
+    """The AG-GEMM sweep: fused time against the copy and the GEMM alone, from a cold L2."""
+    K, N = SWEEP["K"], SWEEP["N"]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    rows = []
+    for placement in ("hbm", "pinned_host"):
+        for R in SWEEP["R"]:
+            for M in SWEEP["M"]:
+                Ms = M // R
+                gen = torch.Generator(device="cuda")
+                shards = []
+                for r in range(R):
+                    gen.manual_seed(r)
+                    a = torch.randn(Ms, K, generator=gen, device="cuda").to(torch.bfloat16)
+                    # rank 0 is the caller; the others sit behind the slower link in the pinned-host case
+                    shards.append(a.cpu().pin_memory() if placement == "pinned_host" and r != 0 else a)
+                gen.manual_seed(1000)
+                Bm = (torch.randn(K, N, generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+                G = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+                C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+                sig = B.Signals(B.tl_ag_gemm_num_flags(R, Ms, K)[0])
+                ep = [0]
+
+                def copy_only():
+                    ep[0] += 1
+                    B.tl_allgather(shards, G, sig, ep[0])
+
+                def gemm_only():
+                    B.tl_gemm(G, Bm, C, sig)
+
+                def seq():
+                    copy_only()
+                    gemm_only()
+
+                def fused():
+                    ep[0] += 1
+                    B.tl_ag_gemm(shards, Bm, G, C, sig, ep[0])
+
+                t_copy = flushed_time_us(torch, copy_only, flush, reps=5)
+                t_gemm = flushed_time_us(torch, gemm_only, flush, reps=5)
+                t_seq = flushed_time_us(torch, seq, flush, reps=5)
+                t_fused = flushed_time_us(torch, fused, flush, reps=5)
+                code, where = B.tl_query_status(sig)
+                if code:
+                    raise RuntimeError(f"device error {code} at {where} in the sweep (R={R}, M={M}, {placement})")
+                flops = 2 * M * N * K
+                host_bytes = (R - 1) * Ms * K * 2 if placement == "pinned_host" else 0
+                rows.append({"placement": placement, "R": R, "M": M, "t_copy_us": t_copy, "t_gemm_us": t_gemm,
+                             "t_seq_us": t_seq, "t_fused_us": t_fused,
+                             "tflops": flops / (t_fused * 1e-6) / 1e12,
+                             "frac_of_peak": flops / (t_fused * 1e-6) / 1e12 / peaks["bf16_tflops"],
+                             "fused_over_max": t_fused / max(t_copy, t_gemm),
+                             "speedup_vs_seq": t_seq / t_fused,
+                             "overlap_efficiency": (t_seq - t_fused) / min(t_copy, t_gemm),
+                             "copy_gbs": 2 * M * K * 2 / (t_copy * 1e-6) / 1e9,
+                             "host_read_gbs": host_bytes / (t_copy * 1e-6) / 1e9 if host_bytes else None})
+                del shards, G, C, Bm, sig
+    del flush
+    return rows
+
+
 def main():
     args = parse()
     world, rank, local_rank = dist_env()
@@ -442,6 +509,12 @@ def main():
             pg.barrier()
 
     peaks, peak_src = load_peaks()
+    if args.sweep:
+        rows = run_sweep(torch, B, peaks)
+        if rank == 0:
+            print(json.dumps({"sweep": "AG-GEMM K=8192 N=1024, bf16 N(0,1) x N(0,0.02), cold L2, median of 5",
+                              "peak_tflops": peaks["bf16_tflops"], "rows": rows}), flush=True)
+        return
     wl = Workload(B, torch)
     stream = torch.cuda.current_stream()
     if args.only:

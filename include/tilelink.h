@@ -19,9 +19,15 @@
  * Conventions shared by every call
  * --------------------------------
  *  - Matrices are row-major.  bf16 = IEEE bfloat16 (uint16 storage).
- *  - Pointers named "device" must be device (or device-mapped) memory, 16-byte
- *    aligned.  Arrays of pointers (A_shards, A, B, out, X, W) are HOST arrays
- *    read during the call; the pointers in them are device pointers.
+ *  - Pointers named "device" must be device memory of the current device,
+ *    16-byte aligned; operands the kernels load with TMA are checked and any
+ *    other memory is rejected with TL_ERR_UNSUPPORTED before a launch.  Arrays
+ *    of pointers (A_shards, A, B, out, X, W) are HOST arrays read during the
+ *    call; the pointers in them are device pointers.
+ *  - AllGather shards (tl_ag_gemm other than the self shard, tl_allgather) may
+ *    also be pinned host or managed memory, the stand-in for a slower link:
+ *    those are copied with plain loads by the copy warps.  Pageable host
+ *    memory and other devices' memory are rejected (TL_ERR_UNSUPPORTED).
  *  - Ownership: the caller owns every buffer passed in.  The library allocates
  *    only the flag/status memory of a tl_signals object.
  *  - Ordering: every call that takes a stream is asynchronous and ordered on
@@ -141,7 +147,8 @@ tl_status tl_gemm(const tl_gemm_args* args, void* stream);
  *    row_in_shard / rows_per_barrier, an affine map of the row) before loading
  *    them, and tiles run in arrival order: shards self, self+1, ..., self+R-1
  *    (consume_tile_swizzle).  Row halves wholly inside the self shard read
- *    A_self in place and never wait.  Copies run in the order self+1, ..., self+R-1, self.
+ *    A_self in place and never wait, so the self shard must be device memory.
+ *    Copies run in the order self+1, ..., self+R-1, self.
  * Output is independent of self_rank, mode and rows_per_barrier.
  */
 typedef struct tl_ag_gemm_args {

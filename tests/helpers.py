@@ -22,6 +22,12 @@ def dev_bf16(bits):
     return inputs.to_torch_bf16(bits).cuda()
 
 
+def pinned_bf16(bits):
+    """bf16 bits -> a pinned host torch tensor (device-addressable: the slow-link stand-in)."""
+    from tile_centric_gemm_gb300 import inputs
+    return inputs.to_torch_bf16(bits).pin_memory()
+
+
 def to_bits(t):
     """bf16 torch tensor -> uint16 numpy bits."""
     import torch

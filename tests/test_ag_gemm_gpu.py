@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.helpers import check_bf16, check_f32, dev_bf16, to_bits, to_f64
+from tests.helpers import check_bf16, check_f32, dev_bf16, pinned_bf16, to_bits, to_f64
 from tile_centric_gemm_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -30,11 +30,11 @@ class Epoch:
 
 
 def run_ag(B, A, Bm, *, self_rank=0, mode=None, rpb=0, f32=False, notify_ready=True, timeout_ns=0,
-           withhold=None, trace=False):
+           withhold=None, trace=False, host_ranks=()):
     import torch
     R, (Ms, K), N = len(A), A[0].shape, Bm.shape[1]
     mode = B.TL_MODE_PUSH if mode is None else mode
-    dA = [dev_bf16(a) for a in A]
+    dA = [pinned_bf16(a) if r in host_ranks else dev_bf16(a) for r, a in enumerate(A)]
     dB = dev_bf16(Bm)
     G = torch.full((R * Ms, K), float("nan"), dtype=torch.bfloat16, device="cuda")
     C = torch.full((R * Ms, N), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -177,3 +177,30 @@ def test_ag_sweep_points(B, R, M):
     check_bf16(to_f64(r["C"])[rows, cols], oracle.ag_gemm.ag_gemm_at(A, Bm, rows, cols), "C sampled")
     order = oracle.ag_gemm.consumer_order(R, R - 1, M // R, 1024, 256, 256)
     assert r["trace"].cpu().tolist() == [m * r["Nt"] + n for (m, n) in order]
+
+
+@pytest.mark.parametrize("mode", ["push", "pull"])
+def test_ag_pinned_host_peer_shards(B, mode):
+    # the slower-link stand-in: every shard but the self shard in pinned host memory
+    R, Ms, K, N, self_rank = 4, 300, 520, 264, 2
+    A, Bm = inputs.ag_gemm_inputs(R, Ms, K, N, "normal", seed=41)
+    m = B.TL_MODE_PUSH if mode == "push" else B.TL_MODE_PULL
+    r = run_ag(B, A, Bm, self_rank=self_rank, mode=m, rpb=13, trace=True,
+               host_ranks=[x for x in range(R) if x != self_rank])
+    check_all(B, A, Bm, r, self_rank)
+
+
+def test_ag_rejects_host_self_shard_and_host_b(B):
+    import torch
+    R, Ms, K, N = 2, 128, 256, 256
+    A, Bm = inputs.ag_gemm_inputs(R, Ms, K, N, "normal", seed=43)
+    G = torch.zeros(R * Ms, K, dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros(R * Ms, N, dtype=torch.bfloat16, device="cuda")
+    sig = B.Signals(B.tl_ag_gemm_num_flags(R, Ms, K)[0])
+    with pytest.raises(B.TLError) as e:
+        B.tl_ag_gemm([pinned_bf16(A[0]), dev_bf16(A[1])], dev_bf16(Bm), G, C, sig, 1, self_rank=0)
+    assert e.value.code == B.TL_ERR_UNSUPPORTED and "self shard" in str(e.value)
+    with pytest.raises(B.TLError) as e:
+        B.tl_ag_gemm([dev_bf16(a) for a in A], pinned_bf16(Bm), G, C, sig, 1)
+    assert e.value.code == B.TL_ERR_UNSUPPORTED
+    assert np.all(sig.read_flags() == 0)

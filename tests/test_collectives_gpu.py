@@ -5,7 +5,7 @@ import pytest
 
 import oracle
 from oracle import bf16
-from tests.helpers import check_bf16, dev_bf16, to_bits, to_f64
+from tests.helpers import check_bf16, dev_bf16, pinned_bf16, to_bits, to_f64
 from tile_centric_gemm_gb300 import inputs
 
 pytestmark = pytest.mark.gpu
@@ -30,6 +30,35 @@ def test_allgather_bit_exact_and_flags(B, R, Ms, K, self_rank, rpb):
     assert B.tl_query_status(sig) == (0, -1)
     np.testing.assert_array_equal(to_bits(G), oracle.ag_gemm.gathered(A))
     assert np.all(sig.read_flags() == 3)
+
+
+@pytest.mark.parametrize("host_ranks", [[1, 2], [0, 1, 2, 3]])
+def test_allgather_pinned_host_shards_bit_exact(B, host_ranks):
+    # shards in pinned host memory are copied with plain loads; the result is the same gather
+    import torch
+    R, Ms, K = 4, 200, 392
+    A = [inputs.normal_bf16((Ms, K), 110 + r) for r in range(R)]
+    src = [pinned_bf16(a) if r in host_ranks else dev_bf16(a) for r, a in enumerate(A)]
+    G = torch.full((R * Ms, K), float("nan"), dtype=torch.bfloat16, device="cuda")
+    nflags, _ = B.tl_ag_gemm_num_flags(R, Ms, K, 9)
+    sig = B.Signals(nflags)
+    B.tl_allgather(src, G, sig, 5, self_rank=1, rows_per_barrier=9)
+    assert B.tl_query_status(sig) == (0, -1)
+    np.testing.assert_array_equal(to_bits(G), oracle.ag_gemm.gathered(A))
+    assert np.all(sig.read_flags() == 5)
+
+
+def test_allgather_rejects_pageable_host_shard_without_launch(B):
+    import torch
+    A = [inputs.normal_bf16((64, 256), 120 + r) for r in range(2)]
+    src = [dev_bf16(A[0]), inputs.to_torch_bf16(A[1])]  # second shard: pageable host memory
+    G = torch.zeros(128, 256, dtype=torch.bfloat16, device="cuda")
+    nflags, _ = B.tl_ag_gemm_num_flags(2, 64, 256)
+    sig = B.Signals(nflags)
+    with pytest.raises(B.TLError) as e:
+        B.tl_allgather(src, G, sig, 1)
+    assert e.value.code == B.TL_ERR_UNSUPPORTED and "pageable" in str(e.value)
+    assert np.all(sig.read_flags() == 0)
 
 
 def test_allgather_pull_waits_for_source(B):

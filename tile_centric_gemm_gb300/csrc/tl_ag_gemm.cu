@@ -54,6 +54,7 @@ struct AgParams {
   int32_t R, self, M_shard, K, N, M;
   int32_t rpb, bpr, Mt, Nt, KB, num_items, num_work;
   uint32_t epoch;
+  uint64_t host_mask;  // shards in host memory (copied with plain loads)
   uint16_t m_order[AG_MAX_MTILES];
 };
 
@@ -164,12 +165,9 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
     }
   } else if (warp == kWarpCopy) {
     // ---------------------------------------------------------------- AllGather producer
-    if (lane == 0) {
-      AgCopyJob job{p.shard, p.gathered, p.flags, p.ready, p.status, p.timeout_ns, p.pipe_timeout_ns,
-                    p.R, p.self, p.M_shard, p.K, p.rpb, p.bpr, p.num_items, p.epoch};
-      ag_copy_items(job, smem + AG_SMEM_COPY, bars->copy, abort, int(blockIdx.x), int(gridDim.x));
-    }
-    __syncwarp();
+    AgCopyJob job{p.shard, p.gathered, p.flags, p.ready, p.status, p.timeout_ns, p.pipe_timeout_ns,
+                  p.R, p.self, p.M_shard, p.K, p.rpb, p.bpr, p.num_items, p.epoch, p.host_mask};
+    ag_copy_items(job, smem + AG_SMEM_COPY, bars->copy, abort, int(blockIdx.x), int(gridDim.x));
   }
   pair::teardown(bars, warp, tmem_base);
 }
@@ -242,6 +240,11 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
   DeviceInfo di{};
   if (tl_status s = device_info(&di)) return s;
   if (a->signals->device != di.device) return fail(TL_ERR_INVALID, "tl_ag_gemm: signals belong to another device");
+  const uint8_t* shard_dev[TL_MAX_RANKS];
+  uint64_t host_mask = 0;
+  if (tl_status s = classify_shards("tl_ag_gemm", a->A_shards, a->R, di.device, shard_dev, &host_mask)) return s;
+  if ((host_mask >> a->self_rank) & 1ull)
+    return fail(TL_ERR_UNSUPPORTED, "tl_ag_gemm: the self shard is read in place by TMA and must be device memory");
 
   AgParams* p = new (std::nothrow) AgParams;
   if (!p) return fail(TL_ERR_INTERNAL, "out of host memory");
@@ -253,7 +256,8 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
                             pair::BK)))
       break;
     if ((st = make_map_bf16(&p->map_b, a->B, a->K, a->N, size_t(a->N) * 2, pair::BK, 64))) break;
-    for (int r = 0; r < a->R; ++r) p->shard[r] = static_cast<const uint8_t*>(a->A_shards[r]);
+    for (int r = 0; r < a->R; ++r) p->shard[r] = shard_dev[r];
+    p->host_mask = host_mask;
     p->gathered = static_cast<uint8_t*>(a->gathered);
     p->C = static_cast<uint16_t*>(a->C);
     p->C_f32 = a->C_f32;

@@ -34,12 +34,9 @@ __global__ void __launch_bounds__(32, 1) allgather_kernel(const __grid_constant_
     fence_mbar_init();
   }
   __syncwarp();
-  if (threadIdx.x == 0) {
-    AgCopyJob job = p.job;
-    job.shard = p.shard;
-    ag_copy_items(job, stage, bars, &abort_flag, int(blockIdx.x), int(gridDim.x));
-  }
-  __syncwarp();
+  AgCopyJob job = p.job;
+  job.shard = p.shard;
+  ag_copy_items(job, stage, bars, &abort_flag, int(blockIdx.x), int(gridDim.x));
 }
 
 struct ReduceParams {
@@ -96,7 +93,8 @@ extern "C" tl_status tl_allgather(const tl_allgather_args* a, void* stream) {
   DeviceInfo di{};
   if (tl_status s = device_info(&di)) return s;
   AllgatherParams p{};
-  for (int r = 0; r < a->R; ++r) p.shard[r] = static_cast<const uint8_t*>(a->A_shards[r]);
+  if (tl_status s = classify_shards("tl_allgather", a->A_shards, a->R, di.device, p.shard, &p.job.host_mask))
+    return s;
   p.job.gathered = static_cast<uint8_t*>(a->gathered);
   p.job.flags = a->signals->flags;
   p.job.ready = a->mode == TL_MODE_PULL ? a->src_ready->flags : nullptr;
@@ -112,13 +110,9 @@ extern "C" tl_status tl_allgather(const tl_allgather_args* a, void* stream) {
   p.job.num_items = a->R * p.job.bpr;
   p.job.epoch = a->epoch;
   const int grid = std::max(1, std::min(di.sm_count, p.job.num_items));
-  const void* kernel = reinterpret_cast<const void*>(&allgather_kernel);
-  if (tl_status s = cuda_ok(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 int(AGC_SMEM_BYTES)),
-                            "cudaFuncSetAttribute(allgather)"))
-    return s;
-  allgather_kernel<<<grid, 32, AGC_SMEM_BYTES, (cudaStream_t)stream>>>(p);
-  return cuda_ok(cudaGetLastError(), "allgather launch");
+  void* args[] = {&p};
+  return launch_coop(reinterpret_cast<const void*>(&allgather_kernel), grid, 32, AGC_SMEM_BYTES,
+                     (cudaStream_t)stream, args);
 }
 
 extern "C" tl_status tl_reduce_scatter(const tl_reduce_scatter_args* a, void* stream) {

@@ -1,9 +1,13 @@
 // tl_copy.cuh -- the AllGather producer shared by the fused AllGather-GEMM
-// kernel and the stand-alone AllGather: one warp lane moves row chunks of the
-// shards into the gathered buffer through a ring of shared-memory buffers with
-// bulk TMA copies, and releases one flag per chunk once its writes are
+// kernel and the stand-alone AllGather: one warp moves row chunks of the shards
+// into the gathered buffer and releases one flag per chunk once its writes are
 // complete (produce_tile_notify).  Pull mode first acquires the source's
 // readiness flag of the same chunk.
+//  * Shards in device memory: one lane streams the chunk through a ring of
+//    shared-memory buffers with bulk TMA copies (global -> shared -> global).
+//  * Shards in pinned host (or managed) memory -- the stand-in for a slower
+//    link: all 32 lanes copy 16-byte vectors with plain loads and stores, many
+//    loads in flight per lane, then fence before the release.
 #pragma once
 
 #include "tilelink.h"
@@ -21,16 +25,40 @@ struct AgCopyJob {
   uint64_t pipe_timeout_ns;
   int R, self, M_shard, K, rpb, bpr, num_items;
   uint32_t epoch;
+  uint64_t host_mask;  // bit r: shard r is host (or managed) memory, copied with plain loads
 };
 
+// Copy `bytes` (a multiple of 16) from host-resident src to dst with every lane
+// of the warp: kVec 16-byte loads in flight per lane.
+__device__ __forceinline__ void copy_rows_plain(const uint8_t* src, uint8_t* dst, uint32_t bytes, int lane) {
+  constexpr int kVec = 8;
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  const uint32_t n = bytes / 16u;
+  for (uint32_t base = 0; base < n; base += 32u * kVec) {
+    uint4 v[kVec];
+#pragma unroll
+    for (int u = 0; u < kVec; ++u) {
+      const uint32_t i = base + uint32_t(u) * 32u + uint32_t(lane);
+      if (i < n) v[u] = __ldcg(s + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kVec; ++u) {
+      const uint32_t i = base + uint32_t(u) * 32u + uint32_t(lane);
+      if (i < n) __stcg(d + i, v[u]);
+    }
+  }
+}
+
 // Items first, first + stride, ... in copy order: shards self+1, ..., self+R-1,
-// then self; chunks ascending.  `stage` holds COPY_NBUF buffers of COPY_CHUNK
-// bytes; `bars` COPY_NBUF mbarriers initialised with count 1.
+// then self; chunks ascending.  Called by all 32 lanes of one warp.  `stage`
+// holds COPY_NBUF buffers of COPY_CHUNK bytes; `bars` COPY_NBUF mbarriers
+// initialised with count 1.
 __device__ __forceinline__ void ag_copy_items(const AgCopyJob& j, uint8_t* stage, uint64_t* bars,
                                               volatile uint32_t* abort, int first, int stride) {
-  uint32_t seq = 0;  // chunks loaded so far: buffer seq % NBUF, parity (seq / NBUF) & 1
-  bool dead = false;
-  for (int it = first; it < j.num_items && !dead; it += stride) {
+  const int lane = int(lane_id());
+  uint32_t seq = 0;  // lane 0: chunks loaded so far: buffer seq % NBUF, parity (seq / NBUF) & 1
+  for (int it = first; it < j.num_items; it += stride) {
     const int jj = it / j.bpr, b = it % j.bpr;
     const int r = (j.self + 1 + jj) % j.R;
     const int lo = b * j.rpb;
@@ -41,41 +69,57 @@ __device__ __forceinline__ void ag_copy_items(const AgCopyJob& j, uint8_t* stage
     const int flag_id = r * j.bpr + b;
     // pull mode: the source publishes readiness first (first barrier of the pull protocol);
     // a chunk whose source never became ready is neither copied nor announced
-    if (j.ready && !wait_flag(j.ready + flag_id, j.epoch, j.status, j.timeout_ns, uint32_t(flag_id), TL_ERR_TIMEOUT))
+    bool ready = true;
+    if (j.ready && lane == 0)
+      ready = wait_flag(j.ready + flag_id, j.epoch, j.status, j.timeout_ns, uint32_t(flag_id), TL_ERR_TIMEOUT);
+    if (!__shfl_sync(0xffffffffu, ready, 0)) continue;
+    if ((j.host_mask >> r) & 1ull) {
+      copy_rows_plain(src, dst, bytes, lane);
+      // produce_tile_notify: every lane's stores are ordered before lane 0's release
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) st_release(j.flags + flag_id, j.epoch);
       continue;
-    const int nch = int((bytes + COPY_CHUNK - 1) / COPY_CHUNK);
-    int issued = 0, stored = 0;
-    while (stored < nch) {
-      while (issued < nch && issued - stored < COPY_NBUF) {
-        const uint32_t q = seq + uint32_t(issued);
-        const int buf = int(q % COPY_NBUF);
-        // the store that last read `buf` (chunk q - NBUF) must have finished reading it
-        bulk_wait_read_dyn(stored - issued + COPY_NBUF - 1);
-        const uint32_t off = uint32_t(issued) * COPY_CHUNK;
-        const uint32_t sz = min(COPY_CHUNK, bytes - off);
-        mbar_arrive_expect_tx(&bars[buf], sz);
-        bulk_g2s(stage + buf * COPY_CHUNK, src + off, sz, &bars[buf]);
-        ++issued;
-      }
-      const uint32_t q = seq + uint32_t(stored);
-      const int buf = int(q % COPY_NBUF);
-      if (!mbar_wait(&bars[buf], (q / COPY_NBUF) & 1u, abort, j.status, j.pipe_timeout_ns, 5)) {
-        dead = true;
-        break;
-      }
-      const uint32_t off = uint32_t(stored) * COPY_CHUNK;
-      bulk_s2g(dst + off, stage + buf * COPY_CHUNK, min(COPY_CHUNK, bytes - off));
-      bulk_commit();
-      ++stored;
     }
-    seq += uint32_t(nch);
-    // produce_tile_notify: writes complete -> order with the generic proxy -> release
-    bulk_wait<0>();
-    if (dead) break;
-    fence_proxy_async_global();
-    st_release(j.flags + flag_id, j.epoch);
+    bool dead = false;
+    if (lane == 0) {
+      const int nch = int((bytes + COPY_CHUNK - 1) / COPY_CHUNK);
+      int issued = 0, stored = 0;
+      while (stored < nch) {
+        while (issued < nch && issued - stored < COPY_NBUF) {
+          const uint32_t q = seq + uint32_t(issued);
+          const int buf = int(q % COPY_NBUF);
+          // the store that last read `buf` (chunk q - NBUF) must have finished reading it
+          bulk_wait_read_dyn(stored - issued + COPY_NBUF - 1);
+          const uint32_t off = uint32_t(issued) * COPY_CHUNK;
+          const uint32_t sz = min(COPY_CHUNK, bytes - off);
+          mbar_arrive_expect_tx(&bars[buf], sz);
+          bulk_g2s(stage + buf * COPY_CHUNK, src + off, sz, &bars[buf]);
+          ++issued;
+        }
+        const uint32_t q = seq + uint32_t(stored);
+        const int buf = int(q % COPY_NBUF);
+        if (!mbar_wait(&bars[buf], (q / COPY_NBUF) & 1u, abort, j.status, j.pipe_timeout_ns, 5)) {
+          dead = true;
+          break;
+        }
+        const uint32_t off = uint32_t(stored) * COPY_CHUNK;
+        bulk_s2g(dst + off, stage + buf * COPY_CHUNK, min(COPY_CHUNK, bytes - off));
+        bulk_commit();
+        ++stored;
+      }
+      seq += uint32_t(nch);
+      // produce_tile_notify: writes complete -> order with the generic proxy -> release
+      bulk_wait<0>();
+      if (!dead) {
+        fence_proxy_async_global();
+        st_release(j.flags + flag_id, j.epoch);
+      }
+    }
+    if (__shfl_sync(0xffffffffu, dead, 0)) break;
   }
-  bulk_wait<0>();
+  if (lane == 0) bulk_wait<0>();
+  __syncwarp();
 }
 
 }  // namespace tl

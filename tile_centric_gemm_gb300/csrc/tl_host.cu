@@ -85,6 +85,15 @@ tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint6
                         uint32_t box_rows, uint32_t box_cols) {
   auto fn = encode_fn();
   if (!fn) return fail(TL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  // TMA operands must be memory of the current device
+  cudaPointerAttributes at{};
+  int dev = -1;
+  if (cudaPointerGetAttributes(&at, base) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(TL_ERR_UNSUPPORTED, "tensor operand %p is not memory the device can address", base);
+  }
+  if (at.type != cudaMemoryTypeDevice || at.device != dev)
+    return fail(TL_ERR_UNSUPPORTED, "tensor operand %p must be device memory of device %d (TMA-loaded)", base, dev);
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_pitch_bytes};
   cuuint32_t box[2] = {box_cols, box_rows};
@@ -95,6 +104,36 @@ tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint6
   if (r != CUDA_SUCCESS)
     return fail(TL_ERR_INVALID, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] pitch %llu", int(r),
                 (unsigned long long)rows, (unsigned long long)cols, (unsigned long long)row_pitch_bytes);
+  return TL_OK;
+}
+
+tl_status classify_shards(const char* who, const void* const* shards, int R, int device, const uint8_t** dev,
+                          uint64_t* host_mask) {
+  *host_mask = 0;
+  for (int r = 0; r < R; ++r) {
+    cudaPointerAttributes at{};
+    const cudaError_t e = cudaPointerGetAttributes(&at, shards[r]);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return fail(TL_ERR_UNSUPPORTED, "%s: shard %d is not memory the device can address (%s)", who, r,
+                  cudaGetErrorName(e));
+    }
+    if (at.type == cudaMemoryTypeDevice) {
+      if (at.device != device)
+        return fail(TL_ERR_UNSUPPORTED, "%s: shard %d lives on device %d, the call runs on device %d", who, r,
+                    at.device, device);
+      dev[r] = static_cast<const uint8_t*>(shards[r]);
+    } else if (at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeManaged) {
+      if (!at.devicePointer)
+        return fail(TL_ERR_UNSUPPORTED, "%s: host shard %d is not mapped into the device's address space", who, r);
+      dev[r] = static_cast<const uint8_t*>(at.devicePointer);
+      *host_mask |= 1ull << r;
+    } else {
+      return fail(TL_ERR_UNSUPPORTED, "%s: shard %d is pageable host memory; pin it (cudaHostAlloc / "
+                                      "cudaHostRegister) or place it on the device", who, r);
+    }
+    if (!aligned16(dev[r])) return fail(TL_ERR_INVALID, "%s: shard %d device address is not 16-byte aligned", who, r);
+  }
   return TL_OK;
 }
 

@@ -47,6 +47,13 @@ tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint6
 tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cudaStream_t st, void** args,
                       int cluster = 1);
 
+// Where each of R shard pointers lives: device memory of `device` (bulk TMA
+// copies), or pinned host / managed memory (plain loads; bit r of *host_mask).
+// dev[r] receives the address the device uses.  Pageable host memory and other
+// devices' memory are rejected (TL_ERR_UNSUPPORTED) before any launch.
+tl_status classify_shards(const char* who, const void* const* shards, int R, int device, const uint8_t** dev,
+                          uint64_t* host_mask);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 

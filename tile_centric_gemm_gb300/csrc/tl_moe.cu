@@ -475,6 +475,13 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
   DeviceInfo di{};
   if (tl_status s = device_info(&di)) return s;
   if (a->signals->device != di.device) return fail(TL_ERR_INVALID, "tl_moe_ag_gemm: signals belong to another device");
+  {
+    // the token shards are moved with bulk TMA copies: device memory only
+    const uint8_t* xdev[TL_MAX_RANKS];
+    uint64_t host_mask = 0;
+    if (tl_status s = classify_shards("tl_moe_ag_gemm", a->X, a->R, di.device, xdev, &host_mask)) return s;
+    if (host_mask) return fail(TL_ERR_UNSUPPORTED, "tl_moe_ag_gemm: token shards must be device memory");
+  }
   cudaStream_t st = (cudaStream_t)stream;
 
   // 1. routing and lookup tables
