@@ -39,7 +39,7 @@ def run_rs(B, A, Bl, *, timeout_ns=0):
     _epoch[0] += 1
     B.tl_gemm_rs(dA, dB, out, ws, sig, _epoch[0], timeout_ns=timeout_ns, trace=trace)
     status = B.tl_query_status(sig)
-    return dict(out=out, sig=sig, status=status, epoch=_epoch[0], nflags=nflags, trace=trace)
+    return dict(out=out, sig=sig, status=status, epoch=_epoch[0], nflags=nflags, items=nflags // 4, trace=trace)
 
 
 def expected_trace(R, M, N):
@@ -47,14 +47,19 @@ def expected_trace(R, M, N):
     return [((d * Mt + m) * Nt + n) * R + r for (_, d, m, n, r) in oracle.gemm_rs.item_order(R, M, N, 256, 256)]
 
 
+def check_flags(r):
+    """Every arrival and reduced flag holds the call's epoch."""
+    assert np.all(r["sig"].read_flags()[:r["nflags"]] == r["epoch"])
+
+
 def check(B, A, Bl, r):
     assert r["status"] == (0, -1), r["status"]
     want = oracle.gemm_rs.gemm_rs(A, Bl)
     for d, (o, w) in enumerate(zip(r["out"], want)):
         check_bf16(to_f64(o), w, f"out[{d}]")
-    assert np.all(r["sig"].read_flags()[:r["nflags"]] == r["epoch"])
+    check_flags(r)
     R, M, N = len(A), A[0].shape[0], Bl[0].shape[1]
-    assert r["trace"].cpu().tolist()[:r["nflags"] // 4] == expected_trace(R, M, N)
+    assert r["trace"].cpu().tolist()[:r["items"]] == expected_trace(R, M, N)
 
 
 @pytest.mark.parametrize("R,M,K_r,N", [
@@ -102,13 +107,31 @@ def test_rs_repeated_calls_reuse_signals(B):
     ws = torch.empty(B.tl_gemm_rs_workspace_size(R, M, N) // 4, dtype=torch.float32, device="cuda")
     sig = B.Signals(B.tl_gemm_rs_num_flags(R, M, N))
     want = oracle.gemm_rs.gemm_rs(A, Bl)
-    for e in (1, 2, 3):
+    # epochs need only increase between calls on the same signals
+    for e in (1, 2, 5, 9):
         ws.fill_(float("nan"))
         out = [torch.full((M // R, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(R)]
         B.tl_gemm_rs(dA, dB, out, ws, sig, e)
         assert B.tl_query_status(sig) == (0, -1)
         for d in range(R):
             check_bf16(to_f64(out[d]), want[d], f"epoch {e} out[{d}]")
+
+
+def test_rs_workspace_aligned_to_16_bytes_only(B):
+    # the workspace needs only 16-byte alignment
+    import torch
+    R, M, K_r, N = 4, 1024, 192, 512
+    A, Bl = inputs.gemm_rs_inputs(R, M, K_r, N, seed=21)
+    n = B.tl_gemm_rs_workspace_size(R, M, N) // 4
+    ws = torch.full((n + 64,), float("nan"), dtype=torch.float32, device="cuda")[4:4 + n]
+    assert ws.data_ptr() % 128 == 16
+    out = [torch.full((M // R, N), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    sig = B.Signals(B.tl_gemm_rs_num_flags(R, M, N))
+    B.tl_gemm_rs([dev_bf16(a) for a in A], [dev_bf16(b) for b in Bl], out, ws, sig, 1)
+    assert B.tl_query_status(sig) == (0, -1)
+    want = oracle.gemm_rs.gemm_rs(A, Bl)
+    for d in range(R):
+        check_bf16(to_f64(out[d]), want[d], f"out[{d}]")
 
 
 def test_rs_rejects_bad_arguments(B):
@@ -131,8 +154,8 @@ def test_rs_llm_full_size_sampled(B):
     A, Bl = inputs.gemm_rs_inputs(R, M, K_r, N, seed=0)
     r = run_rs(B, A, Bl)
     assert r["status"] == (0, -1)
-    assert np.all(r["sig"].read_flags() == r["epoch"])
-    assert r["trace"].cpu().tolist()[:r["nflags"] // 4] == expected_trace(R, M, N)
+    check_flags(r)
+    assert r["trace"].cpu().tolist()[:r["items"]] == expected_trace(R, M, N)
     rng = np.random.default_rng(2)
     rows = np.concatenate([rng.integers(0, M, 2500), [0, M - 1]])
     cols = np.concatenate([rng.integers(0, N, 2500), [N - 1, 0]])

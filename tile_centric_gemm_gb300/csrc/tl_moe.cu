@@ -24,6 +24,7 @@
 //     rows by its expert's weight.
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "tl_internal.h"
@@ -59,7 +60,21 @@ struct RouteParams {
   int32_t* ws;            // workspace
   uint32_t* status;
   int32_t T, k, E, R, T_r, rpb, bpr, self, max_tiles, pull, staged;
+  int32_t k_shift;  // log2(k) when k is a power of two, else -1
+  int32_t use_tb;   // token -> (barrier, rank) table in shared memory (staged runs)
 };
+
+// Lanes of `am` whose expert equals this lane's (e < 64): one ballot per bit of e.
+__device__ __forceinline__ unsigned same_expert_lanes(unsigned am, int e) {
+  unsigned peers = am;
+#pragma unroll
+  for (int b = 0; b < 6; ++b) {
+    const bool bit = (e >> b) & 1;
+    const unsigned bb = __ballot_sync(am, bit);
+    peers &= bit ? bb : ~bb;
+  }
+  return peers;
+}
 
 // Stable counting sort of the P = T*k pairs by expert, then the tile table.
 __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const RouteParams p) {
@@ -71,6 +86,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   int32_t* s_key = s_toff + (E + 1);           // [max_tiles]
   int32_t* s_ids = s_key + p.max_tiles;        // [P] when staged
   int32_t* s_perm = s_ids + (p.staged ? p.T * p.k : 0);
+  int32_t* s_tb = s_perm + (p.staged ? p.T * p.k : 0);  // [T] when use_tb: (barrier << 6) | rank
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int P = p.T * p.k;
   // stage the routing in shared memory (one coalesced pass) so the passes below
@@ -81,6 +97,13 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     for (int q = tid; q < P; q += ROUTE_THREADS) s_ids[q] = p.topk[q];
     ids = s_ids;
     perm = s_perm;
+  }
+  // the producer barrier and rank of every token, once (the tile table reads them per row)
+  if (p.use_tb) {
+    for (int t = tid; t < p.T; t += ROUTE_THREADS) {
+      const int r = t / p.T_r;
+      s_tb[t] = ((r * p.bpr + (t - r * p.T_r) / p.rpb) << 6) | r;
+    }
   }
   const int per_warp = ((P + ROUTE_WARPS - 1) / ROUTE_WARPS + 31) / 32 * 32;
   const int q0 = warp * per_warp, q1 = min(P, q0 + per_warp);
@@ -101,7 +124,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     }
     const unsigned am = __ballot_sync(0xffffffffu, act);
     if (act) {
-      const unsigned peers = __match_any_sync(am, e);
+      const unsigned peers = same_expert_lanes(am, e);
       if (lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
     }
     __syncwarp();
@@ -140,7 +163,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     int e = act ? min(max(ids[q], 0), E - 1) : 0;
     const unsigned am = __ballot_sync(0xffffffffu, act);
     if (act) {
-      const unsigned peers = __match_any_sync(am, e);
+      const unsigned peers = same_expert_lanes(am, e);
       const int pos = cnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
       perm[pos] = q;
       if (p.staged) p.perm[pos] = q;
@@ -178,9 +201,17 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     uint32_t mask = 0;
     int blo = 0x7fffffff, bhi = -1;
     for (int i = lane; i < rows; i += 32) {
-      const int tok = perm[row0 + i] / p.k;
-      const int r = tok / p.T_r;
-      const int b = r * p.bpr + (tok % p.T_r) / p.rpb;
+      const int q = perm[row0 + i];
+      const int tok = p.k_shift >= 0 ? (q >> p.k_shift) : q / p.k;
+      int r, b;
+      if (p.use_tb) {
+        const int v = s_tb[tok];
+        r = v & 63;
+        b = v >> 6;
+      } else {
+        r = tok / p.T_r;
+        b = r * p.bpr + (tok % p.T_r) / p.rpb;
+      }
       mask |= 1u << r;
       blo = min(blo, b);
       bhi = max(bhi, b);
@@ -502,14 +533,27 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
   rp.max_tiles = max_tiles;
   rp.pull = pull ? 1 : 0;
   rp.staged = P <= ROUTE_SMEM_PAIRS ? 1 : 0;
-  const size_t route_smem =
-      (size_t(ROUTE_WARPS) * a->E + 2 * (a->E + 1) + max_tiles + (rp.staged ? 2 * P : 0)) * sizeof(int32_t);
+  rp.use_tb = rp.staged;
+  rp.k_shift = (a->topk & (a->topk - 1)) == 0 ? __builtin_ctz(unsigned(a->topk)) : -1;
+  const size_t route_smem = (size_t(ROUTE_WARPS) * a->E + 2 * (a->E + 1) + max_tiles + (rp.staged ? 2 * P : 0) +
+                             (rp.use_tb ? T : 0)) *
+                            sizeof(int32_t);
   if (route_smem > size_t(di.max_smem_optin))
     return fail(TL_ERR_UNSUPPORTED, "tl_moe_ag_gemm: routing needs %zu bytes of shared memory", route_smem);
-  if (tl_status s = cuda_ok(cudaFuncSetAttribute(reinterpret_cast<const void*>(&moe_route_kernel),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, int(route_smem)),
-                            "cudaFuncSetAttribute(route)"))
-    return s;
+  {
+    // the routing kernel's shared-memory limit is raised once per device to the most asked for so far
+    static std::mutex mu;
+    static int route_smem_set[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (di.device < 0 || di.device >= 64) return fail(TL_ERR_UNSUPPORTED, "device ordinal %d", di.device);
+    if (int(route_smem) > route_smem_set[di.device]) {
+      if (tl_status s = cuda_ok(cudaFuncSetAttribute(reinterpret_cast<const void*>(&moe_route_kernel),
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, int(route_smem)),
+                                "cudaFuncSetAttribute(route)"))
+        return s;
+      route_smem_set[di.device] = int(route_smem);
+    }
+  }
   moe_route_kernel<<<1, ROUTE_THREADS, route_smem, st>>>(rp);
   if (tl_status s = cuda_ok(cudaGetLastError(), "route launch")) return s;
 
