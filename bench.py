@@ -315,31 +315,75 @@ def flushed_time_us(torch, fn, flush, reps=7):
     """Median device time (CUDA events on the current stream) of fn() over reps
     runs, each after a write of a buffer larger than L2 (not timed; it also
     hides the host's launch latency), after one warm-up run."""
+    return time_variants(torch, fn, flush, reps)["cold"]
+
+
+def time_variants(torch, fn, flush, reps=7):
+    """Device times of fn() in microseconds: 'cold' (median) and 'cold_min' with
+    L2 flushed before every run by a write larger than L2, and 'warm' (median)
+    with runs back to back, each bracketed by its own events."""
     fn()
-    ts = []
-    for _ in range(reps):
-        flush.zero_()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        b.synchronize()
-        ts.append(a.elapsed_time(b) * 1e3)
-    return statistics.median(ts)
+    cold, warm = [], []
+    for flushed in (True, False):
+        for _ in range(reps):
+            if flushed:
+                flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            (cold if flushed else warm).append(a.elapsed_time(b) * 1e3)
+    return {"cold": statistics.median(cold), "cold_min": min(cold), "warm": statistics.median(warm)}
+
+
+def decomposed_graph(torch, B, shards, Bm, G, C, sig):
+    """The prior-art decomposed schedule as a CUDA graph: the copy engine gathers
+    shard after shard (rank 0 last) on a side stream while the main stream runs
+    one GEMM per shard, the local shard 0 first, each after its copy's event."""
+    R, Ms = len(shards), shards[0].shape[0]
+    s1 = torch.cuda.Stream()
+
+    def launches():
+        main = torch.cuda.current_stream()
+        start = torch.cuda.Event()
+        start.record(main)
+        s1.wait_event(start)
+        evs = []
+        with torch.cuda.stream(s1):
+            for j in range(1, R):
+                G[j * Ms:(j + 1) * Ms].copy_(shards[j], non_blocking=True)
+                e = torch.cuda.Event()
+                e.record(s1)
+                evs.append(e)
+            G[0:Ms].copy_(shards[0], non_blocking=True)
+        B.tl_gemm(shards[0], Bm, C[0:Ms], sig)
+        for j, e in zip(range(1, R), evs):
+            main.wait_event(e)
+            B.tl_gemm(G[j * Ms:(j + 1) * Ms], Bm, C[j * Ms:(j + 1) * Ms], sig)
+        main.wait_stream(s1)
+
+    launches()  # sets every kernel's launch attributes before the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        launches()
+    return graph
 
 
 def overlap_metrics(torch, B, wl):
     """The fused kernels against their halves run alone, one after the other, and
-    (AG-GEMM) decomposed onto two streams: the copy engine gathers shard by shard
-    on a side stream while per-shard GEMMs wait on each copy's event, replayed
-    from a CUDA graph so the host's launch rate does not bound it.  Every variant
-    runs from a cold L2."""
+    (AG-GEMM) decomposed onto two streams (the copy engine and per-shard GEMMs,
+    replayed from a CUDA graph so the host's launch rate does not bound it), plus
+    torch.matmul on the same operands as a library reference.  The metrics use
+    the cold-L2 medians; warm medians and cold minima are reported beside them."""
     R, Ms, K = AG["R"], AG["M_shard"], AG["K"]
     A, Bm = wl.d_ag[:R], wl.d_ag[R]
     sig1 = B.Signals(max(1, wl.sig_ag.num_flags))
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     ep = [10_000_000]
+    C_lib = torch.empty_like(wl.C)
 
     def copy_only():
         ep[0] += 1
@@ -352,44 +396,22 @@ def overlap_metrics(torch, B, wl):
         copy_only()
         gemm_only()
 
-    s1 = torch.cuda.Stream()
-
-    def decomposed_launches():
-        main = torch.cuda.current_stream()
-        start = torch.cuda.Event()
-        start.record(main)
-        s1.wait_event(start)
-        evs = []
-        with torch.cuda.stream(s1):
-            for j in range(1, R):
-                wl.G[j * Ms:(j + 1) * Ms].copy_(A[j], non_blocking=True)
-                e = torch.cuda.Event()
-                e.record(s1)
-                evs.append(e)
-            wl.G[0:Ms].copy_(A[0], non_blocking=True)
-        B.tl_gemm(A[0], Bm, wl.C[0:Ms], sig1)
-        for j, e in zip(range(1, R), evs):
-            main.wait_event(e)
-            B.tl_gemm(wl.G[j * Ms:(j + 1) * Ms], Bm, wl.C[j * Ms:(j + 1) * Ms], sig1)
-        main.wait_stream(s1)
-
-    decomposed_launches()  # sets every kernel's launch attributes before the capture
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        decomposed_launches()
-
-    t_copy = flushed_time_us(torch, copy_only, flush)
-    t_gemm = flushed_time_us(torch, gemm_only, flush)
-    t_seq = flushed_time_us(torch, seq, flush)
-    t_dec = flushed_time_us(torch, graph.replay, flush)
-    t_fused = flushed_time_us(torch, wl.ag, flush)
+    graph = decomposed_graph(torch, B, A, Bm, wl.G, wl.C, sig1)
+    ag_t = {"copy": time_variants(torch, copy_only, flush), "gemm": time_variants(torch, gemm_only, flush),
+            "seq": time_variants(torch, seq, flush), "decomposed": time_variants(torch, graph.replay, flush),
+            "fused": time_variants(torch, wl.ag, flush),
+            "torch_matmul": time_variants(torch, lambda: torch.matmul(wl.G, Bm, out=C_lib), flush)}
+    t_copy, t_gemm, t_seq = ag_t["copy"]["cold"], ag_t["gemm"]["cold"], ag_t["seq"]["cold"]
+    t_dec, t_fused = ag_t["decomposed"]["cold"], ag_t["fused"]["cold"]
     ag = {"t_copy_us": t_copy, "t_gemm_us": t_gemm, "t_seq_us": t_seq, "t_decomposed_us": t_dec,
-          "t_fused_us": t_fused, "speedup_vs_seq": t_seq / t_fused,
+          "t_fused_us": t_fused, "t_torch_matmul_us": ag_t["torch_matmul"]["cold"],
+          "speedup_vs_seq": t_seq / t_fused,
           "speedup_vs_decomposed": t_dec / t_fused,
           "fused_over_max_copy_gemm": t_fused / max(t_copy, t_gemm),
           "overlap_efficiency": (t_seq - t_fused) / min(t_copy, t_gemm),
-          "copy_gbs": 2 * R * Ms * K * 2 / (t_copy * 1e-6) / 1e9}
+          "copy_gbs": 2 * R * Ms * K * 2 / (t_copy * 1e-6) / 1e9,
+          "warm_us": {k: v["warm"] for k, v in ag_t.items()},
+          "cold_min_us": {k: v["cold_min"] for k, v in ag_t.items()}}
     # GEMM-RS: per-rank GEMMs with fp32 partials, then the rank-ordered ReduceScatter
     Rr, M, N = RS["R"], RS["M"], RS["N"]
     parts = [torch.empty(M, N, dtype=torch.float32, device="cuda") for _ in range(Rr)]
@@ -405,14 +427,25 @@ def overlap_metrics(torch, B, wl):
         rs_gemm()
         rs_reduce()
 
-    t_g = flushed_time_us(torch, rs_gemm, flush, reps=5)
-    t_r = flushed_time_us(torch, rs_reduce, flush, reps=5)
-    t_s = flushed_time_us(torch, rs_seq, flush, reps=5)
-    t_f = flushed_time_us(torch, wl.rs, flush, reps=5)
+    lib_out = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for _ in range(Rr)]
+
+    def rs_torch_matmul():
+        for r in range(Rr):
+            torch.matmul(wl.d_rs[r], wl.d_rs[Rr + r], out=lib_out[r])
+
+    rs_t = {"gemm": time_variants(torch, rs_gemm, flush, reps=5),
+            "reduce": time_variants(torch, rs_reduce, flush, reps=5),
+            "seq": time_variants(torch, rs_seq, flush, reps=5), "fused": time_variants(torch, wl.rs, flush, reps=5),
+            "torch_matmul": time_variants(torch, rs_torch_matmul, flush, reps=5)}
+    t_g, t_r, t_s, t_f = (rs_t[k]["cold"] for k in ("gemm", "reduce", "seq", "fused"))
     rs = {"t_gemm_us": t_g, "t_reduce_us": t_r, "t_seq_us": t_s, "t_fused_us": t_f,
+          "t_torch_matmul_us": rs_t["torch_matmul"]["cold"],
           "speedup_vs_seq": t_s / t_f, "fused_over_max_gemm_reduce": t_f / max(t_g, t_r),
           "overlap_efficiency": (t_s - t_f) / min(t_g, t_r),
-          "reduce_gbs": (Rr * M * N * 4 + M * N * 2) / (t_r * 1e-6) / 1e9}
+          "reduce_gbs": (Rr * M * N * 4 + M * N * 2) / (t_r * 1e-6) / 1e9,
+          "warm_us": {k: v["warm"] for k, v in rs_t.items()},
+          "cold_min_us": {k: v["cold_min"] for k, v in rs_t.items()}}
+    del lib_out
     for s in (sig1, wl.sig_ag, wl.sig_rs):
         code, where = B.tl_query_status(s)
         if code:
@@ -462,17 +495,23 @@ def run_sweep(torch, B, peaks):
                     ep[0] += 1
                     B.tl_ag_gemm(shards, Bm, G, C, sig, ep[0])
 
+                C_lib = torch.empty_like(C)
+                graph = decomposed_graph(torch, B, shards, Bm, G, C, sig)
                 t_copy = flushed_time_us(torch, copy_only, flush, reps=5)
                 t_gemm = flushed_time_us(torch, gemm_only, flush, reps=5)
                 t_seq = flushed_time_us(torch, seq, flush, reps=5)
+                t_dec = flushed_time_us(torch, graph.replay, flush, reps=5)
                 t_fused = flushed_time_us(torch, fused, flush, reps=5)
+                t_lib = flushed_time_us(torch, lambda: torch.matmul(G, Bm, out=C_lib), flush, reps=5)
+                del graph
                 code, where = B.tl_query_status(sig)
                 if code:
                     raise RuntimeError(f"device error {code} at {where} in the sweep (R={R}, M={M}, {placement})")
                 flops = 2 * M * N * K
                 host_bytes = (R - 1) * Ms * K * 2 if placement == "pinned_host" else 0
                 rows.append({"placement": placement, "R": R, "M": M, "t_copy_us": t_copy, "t_gemm_us": t_gemm,
-                             "t_seq_us": t_seq, "t_fused_us": t_fused,
+                             "t_seq_us": t_seq, "t_decomposed_us": t_dec, "t_fused_us": t_fused,
+                             "t_torch_matmul_us": t_lib, "speedup_vs_decomposed": t_dec / t_fused,
                              "tflops": flops / (t_fused * 1e-6) / 1e12,
                              "frac_of_peak": flops / (t_fused * 1e-6) / 1e12 / peaks["bf16_tflops"],
                              "fused_over_max": t_fused / max(t_copy, t_gemm),
@@ -480,7 +519,7 @@ def run_sweep(torch, B, peaks):
                              "overlap_efficiency": (t_seq - t_fused) / min(t_copy, t_gemm),
                              "copy_gbs": 2 * M * K * 2 / (t_copy * 1e-6) / 1e9,
                              "host_read_gbs": host_bytes / (t_copy * 1e-6) / 1e9 if host_bytes else None})
-                del shards, G, C, Bm, sig
+                del shards, G, C, C_lib, Bm, sig
     del flush
     return rows
 
