@@ -13,6 +13,14 @@ Compute-Communication Overlapping Kernels using Tile-Centric Primitives"):
 
 The sum runs in fixed rank order, S = (((P_0 + P_1) + P_2) + ... ), P_r in
 float64 from exactly decoded bf16 inputs.
+
+Two variants closer to a real ReduceScatter's traffic (the options of the
+library's GEMM-RS):
+* bf16 partials -- every partial is rounded to bf16 (round to nearest even)
+  before it is summed, as a rank that sends its partial in the output type;
+* ring order -- destination d sums the partials in the order a ring
+  ReduceScatter accumulates them, ranks d+1, d+2, ..., d (mod R): the running
+  sum starts next to d and travels around the ring back to d.
 """
 from __future__ import annotations
 
@@ -44,6 +52,50 @@ def gemm_rs(A_list, B_list):
     Md = M // R
     S = reduced(A_list, B_list)
     return [S[d * Md:(d + 1) * Md, :] for d in range(R)]
+
+
+def summation_order(R, d, order="rank"):
+    """Ranks in the order destination d adds their partials."""
+    if order == "rank":
+        return list(range(R))
+    if order == "ring":
+        return [(d + 1 + i) % R for i in range(R)]
+    raise ValueError(order)
+
+
+def gemm_rs_variant(A_list, B_list, partials="f32", order="rank"):
+    """Row shards out[d] (float64) with the partials optionally rounded to bf16
+    first and summed in rank or ring order; the float64 sum follows that order."""
+    R = len(A_list)
+    M = A_list[0].shape[0]
+    if M % R:
+        raise ValueError("M must be a multiple of R")
+    Md = M // R
+    P = []
+    for A_r, B_r in zip(A_list, B_list):
+        p = partial(A_r, B_r)
+        if partials == "bf16":
+            p = bf16.decode(bf16.encode_rne(p))
+        elif partials != "f32":
+            raise ValueError(partials)
+        P.append(p)
+    out = []
+    for d in range(R):
+        S = None
+        for r in summation_order(R, d, order):
+            blk = P[r][d * Md:(d + 1) * Md, :]
+            S = blk if S is None else S + blk
+        out.append(S)
+    return out
+
+
+def partial_abs_sum(A_list, B_list):
+    """sum_r |P_r| (float64), full [M, N]: scales the rounding error of bf16 partials."""
+    S = None
+    for A_r, B_r in zip(A_list, B_list):
+        P = np.abs(partial(A_r, B_r))
+        S = P if S is None else S + P
+    return S
 
 
 def gemm_rs_at(A_list, B_list, rows, cols):

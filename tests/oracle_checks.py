@@ -292,3 +292,37 @@ def check_moe_gemm(moe_ag_gemm, moe_at, sorted_tokens, route, ag_gemm, decode):
         np.testing.assert_array_equal(Gs[i], G[perm[i] // 2])
     ii, jj = np.meshgrid(np.arange(12), np.arange(3), indexing="ij")
     np.testing.assert_array_equal(moe_at(X, ids, W, ii.ravel(), jj.ravel()), Y.ravel())
+
+
+def check_gemm_rs_variant(variant, gemm_rs):
+    """Pins of the bf16-partial / ring-order GEMM-RS variant."""
+    rng = np.random.default_rng(19)
+    # f32 partials in rank order are the plain definition
+    R, M, Kr, N = 3, 6, 4, 5
+    A = [_rand_bits(rng, (M, Kr)) for _ in range(R)]
+    B = [_rand_bits(rng, (Kr, N)) for _ in range(R)]
+    for a, b in zip(variant(A, B, "f32", "rank"), gemm_rs(A, B)):
+        np.testing.assert_array_equal(a, b)
+    # bf16 rounding of each partial: P_0 = 1 + 2^-8 is a tie between 1 and 1 + 2^-7
+    # and rounds to the even 1.0; P_1 = 1 is exact.  bf16 partials sum to 2, fp32 ones
+    # to 2 + 2^-8.  Partials that bf16 holds exactly are not changed.
+    A = [_bits(np.array([[1.0, 2.0 ** -8]] * 2)), _bits(np.array([[1.0, 0.0]] * 2))]
+    B = [_bits(np.array([[1.0], [1.0]]))] * 2
+    for o in variant(A, B, "bf16", "rank"):
+        np.testing.assert_array_equal(o, [[2.0]])
+    for o in variant(A, B, "f32", "rank"):
+        np.testing.assert_array_equal(o, [[2.0 + 2.0 ** -8]])
+    A = [_bits(np.array([[1.5, 0.25]] * 2)), _bits(np.array([[3.0, -1.0]] * 2))]
+    for x, y in zip(variant(A, B, "bf16", "rank"), variant(A, B, "f32", "rank")):
+        np.testing.assert_array_equal(x, y)
+    # ring order, by hand: R = 4 partials 1, 2^53, -2^53, 0 on every row; destination d
+    # adds ranks d+1, d+2, d+3, d.  In float64 (1 + 2^53) rounds to 2^53, so a row sums
+    # to 0 exactly when 1 and 2^53 are both added before -2^53:
+    #   d=0: 2^53, -2^53, 0, 1 -> 1     d=1: -2^53, 0, 1, 2^53 -> 1
+    #   d=2: 0, 1, 2^53, -2^53 -> 0     d=3: 1, 2^53, -2^53, 0 -> 0
+    # (rank order gives 0 everywhere; the reversed ring gives 1, 1, 0, 1)
+    vals = [1.0, 2.0 ** 53, -(2.0 ** 53), 0.0]
+    A = [_bits(np.full((4, 1), v)) for v in vals]
+    B = [_bits(np.array([[1.0]]))] * 4
+    np.testing.assert_array_equal([o[0, 0] for o in variant(A, B, "f32", "ring")], [1.0, 1.0, 0.0, 0.0])
+    np.testing.assert_array_equal([o[0, 0] for o in variant(A, B, "f32", "rank")], [0.0, 0.0, 0.0, 0.0])

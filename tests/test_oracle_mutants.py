@@ -152,3 +152,27 @@ def test_pins_catch_pull_range_off_by_one():
     def bad(perm, k, table, T_r, rpb):
         return [(m, lo, hi + 1) for (m, lo, hi) in M.tile_sources_pull(perm, k, table, T_r, rpb)]
     _fails(C.check_moe_pull, bad, M.tile_order_pull, M.route, M.tile_table)
+
+
+def test_pins_catch_reversed_ring():
+    def bad(A, B, partials="f32", order="rank"):
+        if order != "ring":
+            return G.gemm_rs_variant(A, B, partials, order)
+        R = len(A)
+        Md = A[0].shape[0] // R
+        P = [G.partial(a, b) for a, b in zip(A, B)]
+        out = []
+        for d in range(R):
+            S = None
+            for r in [(d - 1 - i) % R for i in range(R)]:
+                blk = P[r][d * Md:(d + 1) * Md]
+                S = blk if S is None else S + blk
+            out.append(S)
+        return out
+    _fails(C.check_gemm_rs_variant, bad, G.gemm_rs)
+
+
+def test_pins_catch_unrounded_bf16_partials():
+    def bad(A, B, partials="f32", order="rank"):
+        return G.gemm_rs_variant(A, B, "f32", order)
+    _fails(C.check_gemm_rs_variant, bad, G.gemm_rs)

@@ -132,3 +132,16 @@ def test_gemm_matches_float32_library_matmul_mid_size():
     tB = inputs.to_torch_bf16(B).float()
     got = (tA @ tB).double().numpy()
     assert np.max(np.abs(got - want)) <= 1e-5 * np.max(np.abs(want))
+
+
+def test_gemm_rs_variant_pins():
+    C.check_gemm_rs_variant(oracle.gemm_rs.gemm_rs_variant, oracle.gemm_rs.gemm_rs)
+
+
+def test_gemm_rs_partial_abs_sum_bounds_the_sum():
+    from tile_centric_gemm_gb300 import inputs
+    A = [inputs.normal_bf16((8, 16), 300 + r) for r in range(3)]
+    B = [inputs.normal_bf16((16, 4), 400 + r) for r in range(3)]
+    S = oracle.gemm_rs.reduced(A, B)
+    T = oracle.gemm_rs.partial_abs_sum(A, B)
+    assert np.all(np.abs(S) <= T * (1 + 1e-12)) and np.all(T >= 0)
