@@ -412,6 +412,16 @@ def overlap_metrics(torch, B, wl):
           "copy_gbs": 2 * R * Ms * K * 2 / (t_copy * 1e-6) / 1e9,
           "warm_us": {k: v["warm"] for k, v in ag_t.items()},
           "cold_min_us": {k: v["cold_min"] for k, v in ag_t.items()}}
+    # swizzle ablation: the fused kernel with its consumer in arrival order and in plain row
+    # order, for the calling rank 0 (the two orders coincide) and a rank in the middle
+    abl = {}
+    for self_rank in (0, R // 2):
+        for name, sw in (("arrival", B.TL_SWIZZLE_ARRIVAL), ("rows", B.TL_SWIZZLE_ROWS)):
+            def fused_sw(self_rank=self_rank, sw=sw):
+                ep[0] += 1
+                B.tl_ag_gemm(A, Bm, wl.G, wl.C, sig1, ep[0], self_rank=self_rank, swizzle=sw)
+            abl[f"self{self_rank}_{name}_us"] = flushed_time_us(torch, fused_sw, flush)
+    ag["swizzle_ablation"] = abl
     # GEMM-RS: per-rank GEMMs with fp32 partials, then the rank-ordered ReduceScatter
     Rr, M, N = RS["R"], RS["M"], RS["N"]
     parts = [torch.empty(M, N, dtype=torch.float32, device="cuda") for _ in range(Rr)]
@@ -446,7 +456,18 @@ def overlap_metrics(torch, B, wl):
           "warm_us": {k: v["warm"] for k, v in rs_t.items()},
           "cold_min_us": {k: v["cold_min"] for k, v in rs_t.items()}}
     del lib_out
-    for s in (sig1, wl.sig_ag, wl.sig_rs):
+    # the fused kernel with bf16 partials (half the emulated partial traffic) and with
+    # the ring summation order, beside the default fp32 partials in rank order
+    abl = {}
+    sig_rs2 = B.Signals(wl.sig_rs.num_flags)
+    for name, opt in (("bf16_partials", B.TL_RS_BF16_PARTIALS), ("ring_order", B.TL_RS_RING_ORDER),
+                      ("bf16_partials_ring_order", B.TL_RS_BF16_PARTIALS | B.TL_RS_RING_ORDER)):
+        def rs_opt(opt=opt):
+            ep[0] += 1
+            B.tl_gemm_rs(wl.d_rs[:Rr], wl.d_rs[Rr:], wl.out, wl.ws, sig_rs2, ep[0], options=opt)
+        abl[f"{name}_us"] = flushed_time_us(torch, rs_opt, flush, reps=5)
+    rs["options_ablation"] = abl
+    for s in (sig1, sig_rs2, wl.sig_ag, wl.sig_rs):
         code, where = B.tl_query_status(s)
         if code:
             raise RuntimeError(f"device error {code} at {where} in the overlap measurements")

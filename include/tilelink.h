@@ -74,6 +74,14 @@ typedef enum {
 
 typedef enum { TL_MODE_PULL = 0, TL_MODE_PUSH = 1 } tl_mode;
 
+/* Consumer row-tile order of AllGather-GEMM (talk summary, Technical Deep Dive:
+ * swizzling lines the consumption order up with the arrival order). */
+typedef enum {
+  TL_SWIZZLE_ARRIVAL = 0, /* row tiles in the order their shards arrive: self, self+1, ... (default) */
+  TL_SWIZZLE_ROWS = 1     /* row tiles in index order 0, 1, ..., whatever the arrival order
+                             (the unswizzled schedule, kept for comparison) */
+} tl_swizzle;
+
 /* Opaque per-tile signal buffer: device uint32 flags plus a device status word. */
 typedef struct tl_signals tl_signals;
 
@@ -146,7 +154,7 @@ tl_status tl_gemm(const tl_gemm_args* args, void* stream);
  *    (consume_tile_wait; flag id = rank * barriers_per_rank +
  *    row_in_shard / rows_per_barrier, an affine map of the row) before loading
  *    them, and tiles run in arrival order: shards self, self+1, ..., self+R-1
- *    (consume_tile_swizzle).  Row halves wholly inside the self shard read
+ *    (consume_tile_swizzle; TL_SWIZZLE_ROWS runs them in index order instead).  Row halves wholly inside the self shard read
  *    A_self in place and never wait, so the self shard must be device memory.
  *    Copies run in the order self+1, ..., self+R-1, self.
  * Output is independent of self_rank, mode and rows_per_barrier.
@@ -159,7 +167,7 @@ typedef struct tl_ag_gemm_args {
   int32_t N;                   /* output columns, >= 8, multiple of 8 */
   int32_t mode;                /* tl_mode */
   int32_t rows_per_barrier;    /* rows per producer tile / flag; 0 = about 32 KB of A */
-  int32_t reserved0;
+  int32_t swizzle;             /* tl_swizzle: consumer row-tile order; 0 = arrival order */
   const void* const* A_shards; /* host array of R device pointers, bf16 [M_shard, K] */
   const void* B;               /* device bf16 [K, N] */
   void* gathered;              /* device bf16 [R*M_shard, K], written (the gathered A) */
@@ -201,6 +209,11 @@ tl_status tl_ag_gemm(const tl_ag_gemm_args* args, void* stream);
  * flag; a pusher reuses a ring slot only after the reduced flags of the tile
  * that used it before.
  */
+/* GEMM-RS options (bits of tl_gemm_rs_args.options), closer to a real
+ * ReduceScatter's traffic; the default (0) is fp32 partials summed in rank order. */
+#define TL_RS_BF16_PARTIALS 1u /* round each partial to bf16 (RNE) before it is pushed */
+#define TL_RS_RING_ORDER 2u    /* destination d sums ranks d+1, d+2, ..., d (mod R) */
+
 typedef struct tl_gemm_rs_args {
   int32_t R;                   /* ranks, 1..TL_MAX_RANKS */
   int32_t M;                   /* rows of every A_r; multiple of R */
@@ -213,7 +226,7 @@ typedef struct tl_gemm_rs_args {
   size_t workspace_bytes;
   tl_signals* signals;         /* >= tl_gemm_rs_num_flags(R, M, N) flags */
   uint32_t epoch;              /* nonzero */
-  uint32_t reserved0;
+  uint32_t options;            /* TL_RS_* bits; 0 = fp32 partials, rank order */
   uint64_t timeout_ns;         /* 0 = 1 s */
   int32_t* trace;              /* optional device int32 [tl_gemm_rs_num_flags(R, M, N) / 4]:
                                   trace[item] = ((d * m_tiles + m) * n_tiles + n) * R + r,

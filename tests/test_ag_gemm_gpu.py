@@ -30,7 +30,7 @@ class Epoch:
 
 
 def run_ag(B, A, Bm, *, self_rank=0, mode=None, rpb=0, f32=False, notify_ready=True, timeout_ns=0,
-           withhold=None, trace=False, host_ranks=()):
+           withhold=None, trace=False, host_ranks=(), swizzle=0):
     import torch
     R, (Ms, K), N = len(A), A[0].shape, Bm.shape[1]
     mode = B.TL_MODE_PUSH if mode is None else mode
@@ -52,7 +52,7 @@ def run_ag(B, A, Bm, *, self_rank=0, mode=None, rpb=0, f32=False, notify_ready=T
     Mt, Nt = -(-R * Ms // 256), -(-N // 256)
     tr = torch.full((Mt * Nt,), -1, dtype=torch.int32, device="cuda") if trace else None
     B.tl_ag_gemm(dA, dB, G, C, sig, epoch, self_rank=self_rank, C_f32=C32, mode=mode, src_ready=ready,
-                 rows_per_barrier=rpb, timeout_ns=timeout_ns, trace=tr)
+                 rows_per_barrier=rpb, timeout_ns=timeout_ns, trace=tr, swizzle=swizzle)
     status = B.tl_query_status(sig)
     out = dict(G=G, C=C, C32=C32, sig=sig, ready=ready, epoch=epoch, status=status, nflags=nflags,
                rpb=eff_rpb, trace=tr, Mt=Mt, Nt=Nt)
@@ -204,3 +204,14 @@ def test_ag_rejects_host_self_shard_and_host_b(B):
         B.tl_ag_gemm([dev_bf16(a) for a in A], pinned_bf16(Bm), G, C, sig, 1)
     assert e.value.code == B.TL_ERR_UNSUPPORTED
     assert np.all(sig.read_flags() == 0)
+
+
+def test_ag_rows_swizzle_runs_tiles_in_index_order(B):
+    # the unswizzled schedule: same result, row tiles 0, 1, ... whatever the arrival order
+    R, Ms, K, N, self_rank = 4, 300, 520, 264, 2
+    A, Bm = inputs.ag_gemm_inputs(R, Ms, K, N, "normal", seed=47)
+    r = run_ag(B, A, Bm, self_rank=self_rank, rpb=11, trace=True, swizzle=B.TL_SWIZZLE_ROWS)
+    assert r["status"] == (0, -1)
+    check_bf16(to_f64(r["C"]), oracle.ag_gemm.ag_gemm(A, Bm), "C")
+    np.testing.assert_array_equal(to_bits(r["G"]), oracle.ag_gemm.gathered(A))
+    assert r["trace"].cpu().tolist() == [m * r["Nt"] + n for m in range(r["Mt"]) for n in range(r["Nt"])]

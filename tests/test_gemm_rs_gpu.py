@@ -23,7 +23,7 @@ def B():
 _epoch = [0]
 
 
-def run_rs(B, A, Bl, *, timeout_ns=0):
+def run_rs(B, A, Bl, *, timeout_ns=0, options=0):
     import torch
     R = len(A)
     M, K_r = A[0].shape
@@ -37,7 +37,7 @@ def run_rs(B, A, Bl, *, timeout_ns=0):
     sig = B.Signals(nflags)
     trace = torch.full((nflags,), -1, dtype=torch.int32, device="cuda")
     _epoch[0] += 1
-    B.tl_gemm_rs(dA, dB, out, ws, sig, _epoch[0], timeout_ns=timeout_ns, trace=trace)
+    B.tl_gemm_rs(dA, dB, out, ws, sig, _epoch[0], timeout_ns=timeout_ns, trace=trace, options=options)
     status = B.tl_query_status(sig)
     return dict(out=out, sig=sig, status=status, epoch=_epoch[0], nflags=nflags, items=nflags // 4, trace=trace)
 
@@ -180,3 +180,58 @@ def test_rs_mid_size_sampled(B):
     Md = M // R
     full = [to_f64(o) for o in r["out"]]
     check_bf16(np.array([full[row // Md][row % Md, col] for row, col in zip(rows, cols)]), want, "sampled")
+
+
+def test_rs_ring_order_sums_from_the_next_rank(B):
+    # P_0 = 1, P_1 = 2^24, P_2 = -2^24, P_3 = 0 in every element.  Destination d adds
+    # ranks d+1, d+2, d+3, d; in fp32 (1 + 2^24) rounds to 2^24, so a row is 0 exactly
+    # when 1 and 2^24 are both added before -2^24:
+    #   d=0: 2^24, -2^24, 0, 1 -> 1     d=1: -2^24, 0, 1, 2^24 -> 1
+    #   d=2: 0, 1, 2^24, -2^24 -> 0     d=3: 1, 2^24, -2^24, 0 -> 0
+    R, M, K_r, N = 4, 1024, 8, 256
+    vals = [(1.0, 1.0), (2.0 ** 12, 2.0 ** 12), (-(2.0 ** 12), 2.0 ** 12), (0.0, 0.0)]
+    A, Bl = [], []
+    for a, b in vals:
+        Am = np.zeros((M, K_r), np.float32)
+        Am[:, 0] = a
+        Bm = np.zeros((K_r, N), np.float32)
+        Bm[0, :] = b
+        A.append(inputs.bf16_bits_from_f32(Am))
+        Bl.append(inputs.bf16_bits_from_f32(Bm))
+    r = run_rs(B, A, Bl, options=B.TL_RS_RING_ORDER)
+    assert r["status"] == (0, -1)
+    p = [np.float32(a * b) for a, b in vals]
+    for d, want in enumerate([1.0, 1.0, 0.0, 0.0]):
+        acc = None
+        for i in range(R):
+            x = p[(d + 1 + i) % R]
+            acc = x if acc is None else np.float32(acc + x)
+        assert float(acc) == want
+        assert np.all(to_f64(r["out"][d]) == want), d
+    check_flags(r)
+
+
+@pytest.mark.parametrize("R,M,K_r,N,options", [(4, 1024, 256, 512, 1), (3, 300, 72, 264, 1), (4, 1024, 256, 512, 3),
+                                               (8, 2048, 128, 264, 2)])
+def test_rs_bf16_partials_and_ring_order_parity(B, R, M, K_r, N, options):
+    A, Bl = inputs.gemm_rs_inputs(R, M, K_r, N, seed=60 + R + options)
+    r = run_rs(B, A, Bl, options=options)
+    assert r["status"] == (0, -1)
+    parts = "bf16" if options & B.TL_RS_BF16_PARTIALS else "f32"
+    order = "ring" if options & B.TL_RS_RING_ORDER else "rank"
+    want = oracle.gemm_rs.gemm_rs_variant(A, Bl, parts, order)
+    mag = oracle.gemm_rs.partial_abs_sum(A, Bl)
+    Md = M // R
+    for d in range(R):
+        got, o = to_f64(r["out"][d]), want[d]
+        assert np.isfinite(got).all()
+        if parts == "f32":
+            check_bf16(got, o, f"out[{d}]")
+            continue
+        # a partial rounded to bf16 on the GPU (from an fp32 accumulation) may land one
+        # bf16 step away from the exact partial rounded, 2^-8 |P_r| at most; the final
+        # rounding adds 2^-9 |o|
+        bound = 2.0 ** -8 * (np.abs(o) + mag[d * Md:(d + 1) * Md]) + 1e-3 * np.abs(o).max()
+        assert np.all(np.abs(got - o) <= bound), f"out[{d}]: max excess {np.max(np.abs(got - o) - bound):.3e}"
+        assert np.abs(got - o).max() / np.abs(o).max() <= 2e-2
+    check_flags(r)

@@ -66,3 +66,23 @@ def test_invalid_arguments_fail_without_launch(B):
     h = ctypes.c_void_p()
     assert B.lib.tl_signals_create(0, ctypes.byref(h)) == B.TL_ERR_INVALID
     assert "num_flags" in B.tl_last_error()
+
+
+def test_ag_gemm_rejects_unknown_swizzle_without_launch(B):
+    # argument checks run before any device query, so this needs no GPU
+    ptrs = (ctypes.c_void_p * 2)(16, 32)
+    a = B.tl_ag_gemm_args(R=2, self_rank=0, M_shard=128, K=256, N=256, mode=B.TL_MODE_PUSH, rows_per_barrier=0,
+                          swizzle=7, A_shards=ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)), B=48,
+                          gathered=64, C=80, C_f32=None, signals=96, src_ready=None, epoch=1, reserved1=0,
+                          timeout_ns=0, trace=None)
+    assert B.lib.tl_ag_gemm(ctypes.byref(a), None) == B.TL_ERR_INVALID
+    assert "swizzle" in B.tl_last_error()
+
+
+def test_gemm_rs_rejects_unknown_options_without_launch(B):
+    ptrs = (ctypes.c_void_p * 2)(16, 32)
+    pp = ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p))
+    a = B.tl_gemm_rs_args(R=2, M=256, K_r=64, N=256, A=pp, B=pp, out=pp, workspace=48, workspace_bytes=1 << 30,
+                          signals=64, epoch=1, options=8, timeout_ns=0, trace=None)
+    assert B.lib.tl_gemm_rs(ctypes.byref(a), None) == B.TL_ERR_INVALID
+    assert "options" in B.tl_last_error()

@@ -61,7 +61,7 @@ def test_noalloc_rejects_a_problem_beyond_the_static_scratch(B):
     ptrs = (ctypes.c_void_p * R)(*([t.data_ptr()] * R))
     pp = ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p))
     a = B.tl_gemm_rs_args(R=R, M=M, K_r=K_r, N=N, A=pp, B=pp, out=pp, workspace=None, workspace_bytes=0,
-                          signals=None, epoch=1, reserved0=0, timeout_ns=0, trace=None)
+                          signals=None, epoch=1, options=0, timeout_ns=0, trace=None)
     rc = B.lib.tl_gemm_rs_noalloc(ctypes.byref(a), None, torch.cuda.current_stream().cuda_stream)
     assert rc == B.TL_ERR_UNSUPPORTED
     assert "static scratch" in B.tl_last_error()
@@ -79,6 +79,6 @@ def test_noalloc_rejects_workspace_or_signals(B):
     a = B.tl_gemm_rs_args(R=2, M=256, K_r=64, N=256, A=ctypes.cast(pa, ctypes.POINTER(ctypes.c_void_p)),
                           B=ctypes.cast(pb, ctypes.POINTER(ctypes.c_void_p)),
                           out=ctypes.cast(po, ctypes.POINTER(ctypes.c_void_p)), workspace=ws.data_ptr(),
-                          workspace_bytes=ws.numel() * 4, signals=None, epoch=1, reserved0=0, timeout_ns=0,
+                          workspace_bytes=ws.numel() * 4, signals=None, epoch=1, options=0, timeout_ns=0,
                           trace=None)
     assert B.lib.tl_gemm_rs_noalloc(ctypes.byref(a), None, None) == B.TL_ERR_INVALID

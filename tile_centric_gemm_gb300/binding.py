@@ -20,6 +20,8 @@ lib = ctypes.CDLL(_LIB_PATH)
 
 TL_OK, TL_ERR_INVALID, TL_ERR_CUDA, TL_ERR_TIMEOUT, TL_ERR_UNSUPPORTED, TL_ERR_INTERNAL = range(6)
 TL_MODE_PULL, TL_MODE_PUSH = 0, 1
+TL_SWIZZLE_ARRIVAL, TL_SWIZZLE_ROWS = 0, 1
+TL_RS_BF16_PARTIALS, TL_RS_RING_ORDER = 1, 2
 STATUS_NAMES = {0: "TL_OK", 1: "TL_ERR_INVALID", 2: "TL_ERR_CUDA", 3: "TL_ERR_TIMEOUT",
                 4: "TL_ERR_UNSUPPORTED", 5: "TL_ERR_INTERNAL"}
 
@@ -46,7 +48,7 @@ class tl_ag_gemm_args(ctypes.Structure):
     _fields_ = [
         ("R", ctypes.c_int32), ("self_rank", ctypes.c_int32), ("M_shard", ctypes.c_int32),
         ("K", ctypes.c_int32), ("N", ctypes.c_int32), ("mode", ctypes.c_int32),
-        ("rows_per_barrier", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("rows_per_barrier", ctypes.c_int32), ("swizzle", ctypes.c_int32),
         ("A_shards", ctypes.POINTER(_vp)), ("B", _vp), ("gathered", _vp), ("C", _vp), ("C_f32", _vp),
         ("signals", _vp), ("src_ready", _vp),
         ("epoch", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
@@ -66,7 +68,7 @@ class tl_gemm_rs_args(ctypes.Structure):
         ("R", ctypes.c_int32), ("M", ctypes.c_int32), ("K_r", ctypes.c_int32), ("N", ctypes.c_int32),
         ("A", ctypes.POINTER(_vp)), ("B", ctypes.POINTER(_vp)), ("out", ctypes.POINTER(_vp)),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("signals", _vp),
-        ("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32), ("timeout_ns", ctypes.c_uint64),
+        ("epoch", ctypes.c_uint32), ("options", ctypes.c_uint32), ("timeout_ns", ctypes.c_uint64),
         ("trace", _vp),
     ]
 
@@ -254,14 +256,14 @@ def tl_ag_gemm_tile_order(R, self_rank, M_shard):
 
 def tl_ag_gemm(A_shards, B, gathered, C, signals: Signals, epoch: int, *, self_rank=0, C_f32=None,
                mode=TL_MODE_PUSH, src_ready: Signals | None = None, rows_per_barrier=0, timeout_ns=0,
-               trace=None, stream=None):
+               trace=None, swizzle=TL_SWIZZLE_ARRIVAL, stream=None):
     """C = [A_0; ...; A_{R-1}] . B, gathered rows written to `gathered` (see tilelink.h)."""
     R = len(A_shards)
     M_shard, K = A_shards[0].shape
     N = B.shape[1]
     ptrs = _ptr_array(A_shards)
     a = tl_ag_gemm_args(R=R, self_rank=self_rank, M_shard=M_shard, K=K, N=N, mode=mode,
-                        rows_per_barrier=rows_per_barrier, reserved0=0,
+                        rows_per_barrier=rows_per_barrier, swizzle=int(swizzle),
                         A_shards=ctypes.cast(ptrs, ctypes.POINTER(_vp)), B=_ptr(B), gathered=_ptr(gathered),
                         C=_ptr(C), C_f32=_ptr(C_f32), signals=signals.handle,
                         src_ready=src_ready.handle if src_ready is not None else None,
@@ -277,8 +279,9 @@ def tl_gemm_rs_num_flags(R, M, N):
     return int(lib.tl_gemm_rs_num_flags(R, M, N))
 
 
-def tl_gemm_rs(A, B, out, workspace, signals: Signals, epoch: int, *, timeout_ns=0, trace=None, stream=None):
-    """out[d] = rows d of sum_r A_r . B_r in rank order (see tilelink.h)."""
+def tl_gemm_rs(A, B, out, workspace, signals: Signals, epoch: int, *, timeout_ns=0, trace=None, options=0,
+               stream=None):
+    """out[d] = rows d of sum_r A_r . B_r, rank order unless options say otherwise (see tilelink.h)."""
     R = len(A)
     M, K_r = A[0].shape
     N = B[0].shape[1]
@@ -286,12 +289,12 @@ def tl_gemm_rs(A, B, out, workspace, signals: Signals, epoch: int, *, timeout_ns
     a = tl_gemm_rs_args(R=R, M=M, K_r=K_r, N=N, A=ctypes.cast(pa, ctypes.POINTER(_vp)),
                         B=ctypes.cast(pb, ctypes.POINTER(_vp)), out=ctypes.cast(po, ctypes.POINTER(_vp)),
                         workspace=_ptr(workspace), workspace_bytes=workspace.numel() * workspace.element_size(),
-                        signals=signals.handle, epoch=int(epoch) & 0xFFFFFFFF, reserved0=0,
+                        signals=signals.handle, epoch=int(epoch) & 0xFFFFFFFF, options=int(options),
                         timeout_ns=int(timeout_ns), trace=_ptr(trace))
     _check(lib.tl_gemm_rs(ctypes.byref(a), _stream(stream)))
 
 
-def tl_gemm_rs_noalloc(A, B, out, epoch: int, *, dev_status=None, timeout_ns=0, stream=None):
+def tl_gemm_rs_noalloc(A, B, out, epoch: int, *, dev_status=None, timeout_ns=0, options=0, stream=None):
     """GEMM-RS for callers that cannot allocate device memory: the library's
     static device scratch replaces the workspace and the signals object.
     dev_status: optional int32 CUDA tensor of 4 words that receives device errors."""
@@ -302,7 +305,7 @@ def tl_gemm_rs_noalloc(A, B, out, epoch: int, *, dev_status=None, timeout_ns=0, 
     a = tl_gemm_rs_args(R=R, M=M, K_r=K_r, N=N, A=ctypes.cast(pa, ctypes.POINTER(_vp)),
                         B=ctypes.cast(pb, ctypes.POINTER(_vp)), out=ctypes.cast(po, ctypes.POINTER(_vp)),
                         workspace=None, workspace_bytes=0, signals=None, epoch=int(epoch) & 0xFFFFFFFF,
-                        reserved0=0, timeout_ns=int(timeout_ns), trace=None)
+                        options=int(options), timeout_ns=int(timeout_ns), trace=None)
     _check(lib.tl_gemm_rs_noalloc(ctypes.byref(a), _ptr(dev_status), _stream(stream)))
 
 

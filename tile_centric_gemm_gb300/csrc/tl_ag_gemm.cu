@@ -218,6 +218,8 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
   if (a->mode != TL_MODE_PULL && a->mode != TL_MODE_PUSH) return fail(TL_ERR_INVALID, "tl_ag_gemm: mode %d", a->mode);
   if (a->mode == TL_MODE_PULL && !a->src_ready)
     return fail(TL_ERR_INVALID, "tl_ag_gemm: pull mode needs src_ready flags");
+  if (a->swizzle != TL_SWIZZLE_ARRIVAL && a->swizzle != TL_SWIZZLE_ROWS)
+    return fail(TL_ERR_INVALID, "tl_ag_gemm: swizzle %d", a->swizzle);
   if (!a->A_shards || !a->B || !a->gathered || !a->C || !a->signals)
     return fail(TL_ERR_INVALID, "tl_ag_gemm: NULL pointer argument");
   if (a->epoch == 0) return fail(TL_ERR_INVALID, "tl_ag_gemm: epoch must be nonzero");
@@ -283,7 +285,7 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
     p->epoch = a->epoch;
     int32_t order[AG_MAX_MTILES];
     if ((st = tl_ag_gemm_tile_order(a->R, a->self_rank, a->M_shard, order, AG_MAX_MTILES))) break;
-    for (int i = 0; i < Mt; ++i) p->m_order[i] = uint16_t(order[i]);
+    for (int i = 0; i < Mt; ++i) p->m_order[i] = uint16_t(a->swizzle == TL_SWIZZLE_ROWS ? i : order[i]);
     const int pairs = std::max(1, std::min(di.sm_count / 2, std::max(p->num_work, (p->num_items + 1) / 2)));
     void* args[] = {p};
     st = launch_coop(reinterpret_cast<const void*>(&ag_gemm_kernel), 2 * pairs, AG_THREADS, AG_SMEM_BYTES,

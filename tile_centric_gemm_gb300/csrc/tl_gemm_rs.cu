@@ -73,6 +73,8 @@ struct RsParams {
   uint64_t pipe_timeout_ns;
   int32_t R, M, Md, K, N;
   int32_t Mt_d, Nt, KB, num_tiles, num_items, slice_rows, ring_items, half_floats;
+  int32_t bf16_parts;  // partials travel as bf16 (half the bytes of a slot)
+  int32_t ring_order;  // destination d sums ranks d+1, ..., d instead of 0, ..., R-1
   uint32_t epoch;
 };
 
@@ -155,16 +157,29 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       // all four pusher warps leave together (they meet at a named barrier below)
       if (!named_bar_and(1, kNumEpiThreads, ok)) break;
       tc_fence_after();
-      float* slot = p.slots + (size_t(i % p.ring_items) * 2 + h) * p.half_floats + my_base;
+      // element offset of this thread's first value in its half-slot (4-byte floats, or
+      // 2-byte bf16 values in half the bytes)
+      const size_t slot_el = (size_t(i % p.ring_items) * 2 + h) * p.half_floats + my_base;
       for (int c = 0; c < pair::BN / 32; ++c) {
         if (it.nt * pair::BN + c * 32 >= p.N) break;
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
+        if (p.bf16_parts) {
+          uint16_t* slot16 = reinterpret_cast<uint16_t*>(p.slots) + slot_el;
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float* f = reinterpret_cast<const float*>(v + g * 4);
-          st_global_cg_v4f(slot + size_t(c * 8 + g) * p.slice_rows * 4, f[0], f[1], f[2], f[3]);
+          for (int g = 0; g < 8; ++g) {
+            const float* f = reinterpret_cast<const float*>(v + g * 4);
+            st_global_cg_v2u(slot16 + size_t(c * 8 + g) * p.slice_rows * 4, pack_bf16x2(f[0], f[1]),
+                             pack_bf16x2(f[2], f[3]));
+          }
+        } else {
+          float* slot = p.slots + slot_el;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const float* f = reinterpret_cast<const float*>(v + g * 4);
+            st_global_cg_v4f(slot + size_t(c * 8 + g) * p.slice_rows * 4, f[0], f[1], f[2], f[3]);
+          }
         }
       }
       tc_fence_before();
@@ -216,17 +231,32 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
 #pragma unroll
           for (int rr = 0; rr < RB; ++rr) {
             if (rb + rr < p.R) {
-              int j = jbase + rb + rr;
+              // position rb + rr of the summation order: rank rb + rr, or d + 1 + rb + rr around the ring
+              int rank_r = rb + rr;
+              if (p.ring_order) {
+                rank_r += it.d + 1;
+                rank_r -= rank_r >= p.R ? p.R : 0;
+                rank_r -= rank_r >= p.R ? p.R : 0;
+              }
+              int j = jbase + rank_r;
               j -= j >= p.R ? p.R : 0;
               int slot = ring_base + j;
               slot -= slot >= p.ring_items ? p.ring_items : 0;
-              const float* src = p.slots + (size_t(slot) * 2 + h) * p.half_floats;
+              const size_t base_el = (size_t(slot) * 2 + h) * p.half_floats;
+              if (p.bf16_parts) {
+                const uint16_t* src16 = reinterpret_cast<const uint16_t*>(p.slots) + base_el;
 #pragma unroll
-              for (int u = 0; u < QU; ++u)
-                if (off[u] >= 0) v[rr][u] = __ldcg(reinterpret_cast<const float4*>(src + off[u]));
+                for (int u = 0; u < QU; ++u)
+                  if (off[u] >= 0) v[rr][u] = unpack_bf16x4(__ldcg(reinterpret_cast<const uint2*>(src16 + off[u])));
+              } else {
+                const float* src = p.slots + base_el;
+#pragma unroll
+                for (int u = 0; u < QU; ++u)
+                  if (off[u] >= 0) v[rr][u] = __ldcg(reinterpret_cast<const float4*>(src + off[u]));
+              }
             }
           }
-          // fixed rank order: acc = ((P_0 + P_1) + P_2) + ...
+          // fixed order (rank order, or ring order): acc = ((P_a + P_b) + P_c) + ...
 #pragma unroll
           for (int rr = 0; rr < RB; ++rr) {
             if (rb + rr < p.R) {
@@ -296,6 +326,8 @@ tl_status rs_check(const tl_gemm_rs_args* a, const char* who) {
     return fail(TL_ERR_UNSUPPORTED, "%s: K_r (%d) and N (%d) must be multiples of 8", who, a->K_r, a->N);
   if (!a->A || !a->B || !a->out) return fail(TL_ERR_INVALID, "%s: NULL pointer argument", who);
   if (a->epoch == 0) return fail(TL_ERR_INVALID, "%s: epoch must be nonzero", who);
+  if (a->options & ~(TL_RS_BF16_PARTIALS | TL_RS_RING_ORDER))
+    return fail(TL_ERR_INVALID, "%s: unknown options 0x%x", who, a->options);
   for (int r = 0; r < a->R; ++r) {
     if (!a->A[r] || !a->B[r] || !a->out[r] || !aligned16(a->A[r]) || !aligned16(a->B[r]) || !aligned16(a->out[r]))
       return fail(TL_ERR_INVALID, "%s: rank %d pointer NULL or not 16-byte aligned", who, r);
@@ -333,6 +365,8 @@ tl_status rs_launch(RsParams* p, const tl_gemm_rs_args* a, float* slots, uint32_
   p->slice_rows = cdiv(pair::HM, a->R);
   p->half_floats = rs_half_floats(a->R);
   p->epoch = a->epoch;
+  p->bf16_parts = (a->options & TL_RS_BF16_PARTIALS) ? 1 : 0;
+  p->ring_order = (a->options & TL_RS_RING_ORDER) ? 1 : 0;
   const int pairs = rs_pairs(p->num_items, sm_count);
   p->ring_items = rs_ring_items(p->num_items, pairs);
   void* args[] = {p};
