@@ -73,7 +73,6 @@ struct RsParams {
   uint64_t pipe_timeout_ns;
   int32_t R, M, Md, K, N;
   int32_t Mt_d, Nt, KB, num_tiles, num_items, slice_rows, ring_items, half_floats;
-  int32_t bf16_parts;  // partials travel as bf16 (half the bytes of a slot)
   int32_t ring_order;  // destination d sums ranks d+1, ..., d instead of 0, ..., R-1
   uint32_t epoch;
 };
@@ -95,6 +94,8 @@ __device__ __forceinline__ Item item_of(const RsParams& p, int i) {
   return it;
 }
 
+// kBf16: partials travel as bf16 (TL_RS_BF16_PARTIALS); one instantiation per partial type.
+template <bool kBf16>
 __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_constant__ RsParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
-        if (p.bf16_parts) {
+        if (kBf16) {
           uint16_t* slot16 = reinterpret_cast<uint16_t*>(p.slots) + slot_el;
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
@@ -243,11 +244,15 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
               int slot = ring_base + j;
               slot -= slot >= p.ring_items ? p.ring_items : 0;
               const size_t base_el = (size_t(slot) * 2 + h) * p.half_floats;
-              if (p.bf16_parts) {
+              if (kBf16) {
+                // raw words now, widened below, so every load of the batch is in flight together
                 const uint16_t* src16 = reinterpret_cast<const uint16_t*>(p.slots) + base_el;
 #pragma unroll
                 for (int u = 0; u < QU; ++u)
-                  if (off[u] >= 0) v[rr][u] = unpack_bf16x4(__ldcg(reinterpret_cast<const uint2*>(src16 + off[u])));
+                  if (off[u] >= 0) {
+                    const uint2 w = __ldcg(reinterpret_cast<const uint2*>(src16 + off[u]));
+                    v[rr][u] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), 0.f, 0.f);
+                  }
               } else {
                 const float* src = p.slots + base_el;
 #pragma unroll
@@ -255,6 +260,13 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
                   if (off[u] >= 0) v[rr][u] = __ldcg(reinterpret_cast<const float4*>(src + off[u]));
               }
             }
+          }
+          if (kBf16) {
+#pragma unroll
+            for (int rr = 0; rr < RB; ++rr)
+#pragma unroll
+              for (int u = 0; u < QU; ++u)
+                v[rr][u] = unpack_bf16x4(make_uint2(__float_as_uint(v[rr][u].x), __float_as_uint(v[rr][u].y)));
           }
           // fixed order (rank order, or ring order): acc = ((P_a + P_b) + P_c) + ...
 #pragma unroll
@@ -365,13 +377,13 @@ tl_status rs_launch(RsParams* p, const tl_gemm_rs_args* a, float* slots, uint32_
   p->slice_rows = cdiv(pair::HM, a->R);
   p->half_floats = rs_half_floats(a->R);
   p->epoch = a->epoch;
-  p->bf16_parts = (a->options & TL_RS_BF16_PARTIALS) ? 1 : 0;
   p->ring_order = (a->options & TL_RS_RING_ORDER) ? 1 : 0;
   const int pairs = rs_pairs(p->num_items, sm_count);
   p->ring_items = rs_ring_items(p->num_items, pairs);
   void* args[] = {p};
-  return launch_coop(reinterpret_cast<const void*>(&gemm_rs_kernel), 2 * pairs, RS_THREADS, RS_SMEM_BYTES, st, args,
-                     2);
+  const void* kernel = (a->options & TL_RS_BF16_PARTIALS) ? reinterpret_cast<const void*>(&gemm_rs_kernel<true>)
+                                                           : reinterpret_cast<const void*>(&gemm_rs_kernel<false>);
+  return launch_coop(kernel, 2 * pairs, RS_THREADS, RS_SMEM_BYTES, st, args, 2);
 }
 
 }  // namespace
