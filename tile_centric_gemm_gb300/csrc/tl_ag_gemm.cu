@@ -24,6 +24,7 @@
 #include <vector>
 
 #include "tl_copy.cuh"
+#include "tl_epilogue.cuh"
 #include "tl_internal.h"
 #include "tl_pair.cuh"
 
@@ -33,14 +34,19 @@ namespace {
 constexpr int AG_MAX_MTILES = 1024;  // 256-row pair tiles
 constexpr int kWarpCopy = 6;
 constexpr int AG_THREADS = 7 * 32;
+// shared memory: the pipeline stages, the copy warp's staging (three buffers),
+// then one 32 x 32 C box per epilogue warp for the TMA-store epilogue
+constexpr int AG_COPY_NBUF = 3;
 constexpr uint32_t AG_SMEM_COPY = pair::SMEM_END;
-constexpr uint32_t AG_SMEM_BARS = AG_SMEM_COPY + COPY_NBUF * COPY_CHUNK;
+constexpr uint32_t AG_SMEM_CSTAGE = AG_SMEM_COPY + AG_COPY_NBUF * COPY_CHUNK;
+constexpr uint32_t AG_SMEM_BARS = AG_SMEM_CSTAGE + kNumEpiWarps * C_BOX_BYTES;
 constexpr uint32_t AG_SMEM_BYTES = AG_SMEM_BARS + sizeof(pair::Bars) + 1024;
 
 struct AgParams {
   CUtensorMap map_g;     // gathered [M, K], box 128 rows
   CUtensorMap map_self;  // A_self [M_shard, K], box 128 rows
   CUtensorMap map_b;     // B [K, N], box 64 x 64
+  CUtensorMap map_c;     // C [M, N], box 32 x 32, 64-byte swizzle (TMA stores)
   const uint8_t* shard[TL_MAX_RANKS];
   uint8_t* gathered;
   uint16_t* C;
@@ -120,6 +126,7 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
     // ---------------------------------------------------------------- epilogue (this CTA's 128 rows)
     const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    uint8_t* cbox = smem + AG_SMEM_CSTAGE + uint32_t(wq) * C_BOX_BYTES;
     int j = 0;
     for (int w = pair_id; w < p.num_work; w += npairs, ++j) {
       const int acc = j & 1;
@@ -137,16 +144,10 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
+        // bf16 C: this warp's 32 x 32 box with one TMA store (rows past M are not written)
+        const int row_base = m * pair::BM + int(rank) * pair::HM + wq * 32;
+        if (row_base < p.M) store_box_bf16(&p.map_c, cbox, 1, lane, v, col0, row_base);
         if (row_ok) {
-          uint16_t* crow = p.C + size_t(row) * p.N + col0;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (col0 + g * 8 < p.N) {
-              const float* f = reinterpret_cast<const float*>(v + g * 8);
-              st_global_v4(crow + g * 8, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                           pack_bf16x2(f[6], f[7]));
-            }
-          }
           if (p.C_f32) {
             float* frow = p.C_f32 + size_t(row) * p.N + col0;
 #pragma unroll
@@ -163,11 +164,13 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
       __syncwarp();
       if (lane == 0) pair::release_accumulator(bars, acc, rank);
     }
+    if (lane == 0) bulk_wait<0>();  // every store of this warp is complete
+    __syncwarp();
   } else if (warp == kWarpCopy) {
     // ---------------------------------------------------------------- AllGather producer
     AgCopyJob job{p.shard, p.gathered, p.flags, p.ready, p.status, p.timeout_ns, p.pipe_timeout_ns,
                   p.R, p.self, p.M_shard, p.K, p.rpb, p.bpr, p.num_items, p.epoch, p.host_mask};
-    ag_copy_items(job, smem + AG_SMEM_COPY, bars->copy, abort, int(blockIdx.x), int(gridDim.x));
+    ag_copy_items<AG_COPY_NBUF>(job, smem + AG_SMEM_COPY, bars->copy, abort, int(blockIdx.x), int(gridDim.x));
   }
   pair::teardown(bars, warp, tmem_base);
 }
@@ -258,6 +261,7 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
                             pair::BK)))
       break;
     if ((st = make_map_bf16(&p->map_b, a->B, a->K, a->N, size_t(a->N) * 2, pair::BK, 64))) break;
+    if ((st = make_map_bf16(&p->map_c, a->C, M, a->N, size_t(a->N) * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))) break;
     for (int r = 0; r < a->R; ++r) p->shard[r] = shard_dev[r];
     p->host_mask = host_mask;
     p->gathered = static_cast<uint8_t*>(a->gathered);

@@ -52,10 +52,12 @@ __device__ __forceinline__ void copy_rows_plain(const uint8_t* src, uint8_t* dst
 
 // Items first, first + stride, ... in copy order: shards self+1, ..., self+R-1,
 // then self; chunks ascending.  Called by all 32 lanes of one warp.  `stage`
-// holds COPY_NBUF buffers of COPY_CHUNK bytes; `bars` COPY_NBUF mbarriers
-// initialised with count 1.
+// holds NBUF buffers of COPY_CHUNK bytes; `bars` NBUF mbarriers initialised
+// with count 1.
+template <int NBUF = COPY_NBUF>
 __device__ __forceinline__ void ag_copy_items(const AgCopyJob& j, uint8_t* stage, uint64_t* bars,
                                               volatile uint32_t* abort, int first, int stride) {
+  static_assert(NBUF >= 1 && NBUF <= COPY_NBUF, "staging buffers");
   const int lane = int(lane_id());
   uint32_t seq = 0;  // lane 0: chunks loaded so far: buffer seq % NBUF, parity (seq / NBUF) & 1
   for (int it = first; it < j.num_items; it += stride) {
@@ -86,11 +88,11 @@ __device__ __forceinline__ void ag_copy_items(const AgCopyJob& j, uint8_t* stage
       const int nch = int((bytes + COPY_CHUNK - 1) / COPY_CHUNK);
       int issued = 0, stored = 0;
       while (stored < nch) {
-        while (issued < nch && issued - stored < COPY_NBUF) {
+        while (issued < nch && issued - stored < NBUF) {
           const uint32_t q = seq + uint32_t(issued);
-          const int buf = int(q % COPY_NBUF);
+          const int buf = int(q % NBUF);
           // the store that last read `buf` (chunk q - NBUF) must have finished reading it
-          bulk_wait_read_dyn(stored - issued + COPY_NBUF - 1);
+          bulk_wait_read_dyn(stored - issued + NBUF - 1);
           const uint32_t off = uint32_t(issued) * COPY_CHUNK;
           const uint32_t sz = min(COPY_CHUNK, bytes - off);
           mbar_arrive_expect_tx(&bars[buf], sz);
@@ -98,8 +100,8 @@ __device__ __forceinline__ void ag_copy_items(const AgCopyJob& j, uint8_t* stage
           ++issued;
         }
         const uint32_t q = seq + uint32_t(stored);
-        const int buf = int(q % COPY_NBUF);
-        if (!mbar_wait(&bars[buf], (q / COPY_NBUF) & 1u, abort, j.status, j.pipe_timeout_ns, 5)) {
+        const int buf = int(q % NBUF);
+        if (!mbar_wait(&bars[buf], (q / NBUF) & 1u, abort, j.status, j.pipe_timeout_ns, 5)) {
           dead = true;
           break;
         }

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <new>
 
+#include "tl_epilogue.cuh"
 #include "tl_internal.h"
 #include "tl_pair.cuh"
 
@@ -16,12 +17,15 @@ namespace tl {
 namespace {
 
 constexpr int GEMM_THREADS = 6 * 32;
-constexpr uint32_t GEMM_SMEM_BARS = pair::SMEM_END;
+// C staging for TMA stores: per epilogue warp two buffers of one 32 x 32 box
+constexpr uint32_t GEMM_SMEM_CSTAGE = pair::SMEM_END;
+constexpr uint32_t GEMM_SMEM_BARS = GEMM_SMEM_CSTAGE + kNumEpiWarps * 2 * C_BOX_BYTES;
 constexpr uint32_t GEMM_SMEM_BYTES = GEMM_SMEM_BARS + sizeof(pair::Bars) + 1024;
 
 struct GemmParams {
   CUtensorMap map_a;  // A [M, K]
   CUtensorMap map_b;  // B [K, N]
+  CUtensorMap map_c;  // C [M, N], box 32 x 32, 64-byte swizzle (TMA stores)
   uint16_t* C;
   float* C_f32;
   uint32_t* status;
@@ -59,6 +63,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_pair_kernel(const __grid
     __syncwarp();
   } else {
     const int wq = warp & 3;
+    uint8_t* cstage = smem + GEMM_SMEM_CSTAGE + uint32_t(wq) * 2 * C_BOX_BYTES;
+    int nbox = 0;  // boxes this warp has stored (buffer nbox & 1)
     int j = 0;
     for (int t = pair_id; t < p.num_tiles; t += npairs, ++j) {
       const int acc = j & 1;
@@ -75,16 +81,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_pair_kernel(const __grid
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
-        if (row_ok && p.C) {
-          uint16_t* crow = p.C + size_t(row) * p.N + col0;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            if (col0 + g * 8 < p.N) {
-              const float* f = reinterpret_cast<const float*>(v + g * 8);
-              st_global_v4(crow + g * 8, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
-                           pack_bf16x2(f[6], f[7]));
-            }
-          }
+        const int row_base = m * pair::BM + int(rank) * pair::HM + wq * 32;
+        if (p.C && row_base < p.M) {
+          // this warp's 32 x 32 box through shared memory, one TMA store (rows and
+          // columns past the matrix are not written)
+          store_box_bf16(&p.map_c, cstage + (nbox & 1) * C_BOX_BYTES, 2, lane, v, col0, row_base);
+          ++nbox;
         }
         if (row_ok && p.C_f32) {
           {
@@ -103,6 +105,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_pair_kernel(const __grid
       __syncwarp();
       if (lane == 0) pair::release_accumulator(bars, acc, rank);
     }
+    if (lane == 0) bulk_wait<0>();  // every store of this warp is complete
+    __syncwarp();
   }
   pair::teardown(bars, warp, tmem_base);
 }
@@ -129,6 +133,9 @@ extern "C" tl_status tl_gemm(const tl_gemm_args* a, void* stream) {
   do {
     if ((st = make_map_bf16(&p->map_a, a->A, a->M, a->K, size_t(a->K) * 2, pair::HM, pair::BK))) break;
     if ((st = make_map_bf16(&p->map_b, a->B, a->K, a->N, size_t(a->N) * 2, pair::BK, 64))) break;
+    if (a->C && (st = make_map_bf16(&p->map_c, a->C, a->M, a->N, size_t(a->N) * 2, 32, 32,
+                                    CU_TENSOR_MAP_SWIZZLE_64B)))
+      break;
     p->C = static_cast<uint16_t*>(a->C);
     p->C_f32 = a->C_f32;
     p->status = a->signals->status;

@@ -82,7 +82,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t row_pitch_bytes,
-                        uint32_t box_rows, uint32_t box_cols) {
+                        uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn) return fail(TL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   // TMA operands must be memory of the current device
@@ -99,7 +99,7 @@ tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint6
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(TL_ERR_INVALID, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] pitch %llu", int(r),

@@ -35,10 +35,11 @@ struct DeviceInfo {
 tl_status device_info(DeviceInfo* out);
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix with the given row
-// pitch; box = box_rows x box_cols elements; 128-byte swizzle; out-of-range
-// elements read as zero.
+// pitch; box = box_rows x box_cols elements; 128-byte swizzle unless given;
+// out-of-range elements read as zero (and are not written by stores).
 tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
-                        uint64_t row_pitch_bytes, uint32_t box_rows, uint32_t box_cols);
+                        uint64_t row_pitch_bytes, uint32_t box_rows, uint32_t box_cols,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
 // Launch a grid whose CTAs must all be resident at once: a cooperative launch
 // for single CTAs, a cluster launch sized within the device's resident-cluster

@@ -27,6 +27,7 @@
 #include <mutex>
 #include <new>
 
+#include "tl_epilogue.cuh"
 #include "tl_internal.h"
 #include "tl_pair.cuh"
 
@@ -41,8 +42,12 @@ constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
 constexpr int kWarpCopy = 6;
 constexpr int MOE_THREADS = 7 * 32;
 constexpr int TM = pair::BM;  // rows of an expert tile
+// shared memory: the pipeline stages, the copy warp's staging (three buffers),
+// then one 32 x 32 Y box per epilogue warp for the TMA-store epilogue
+constexpr int MOE_COPY_NBUF = 3;
 constexpr uint32_t MOE_SMEM_COPY = pair::SMEM_END;
-constexpr uint32_t MOE_SMEM_BARS = MOE_SMEM_COPY + COPY_NBUF * COPY_CHUNK;
+constexpr uint32_t MOE_SMEM_CSTAGE = MOE_SMEM_COPY + MOE_COPY_NBUF * COPY_CHUNK;
+constexpr uint32_t MOE_SMEM_BARS = MOE_SMEM_CSTAGE + kNumEpiWarps * C_BOX_BYTES;
 constexpr uint32_t MOE_SMEM_BYTES = MOE_SMEM_BARS + sizeof(pair::Bars) + 1024;
 
 // Workspace layout, in int32 words (documented in tilelink.h).
@@ -262,6 +267,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
 
 struct MoeParams {
   CUtensorMap map_a;               // sorted tokens [P, H]
+  CUtensorMap map_y;               // Y [P, N], box 32 x 32, 64-byte swizzle (TMA stores)
   CUtensorMap map_w[MOE_MAX_E];    // W_e [H, N]
   const uint8_t* x[MOE_MAX_R];     // shards [T_r, H]
   uint8_t* sorted;
@@ -328,6 +334,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
     // ---------------------------------------------------------------- epilogue: rows of this expert only
     const int wq = warp & 3;
+    uint8_t* cbox = smem + MOE_SMEM_CSTAGE + uint32_t(wq) * C_BOX_BYTES;
     int j = 0;
     for (int w = pair_id; w < num_work; w += npairs, ++j) {
       const int acc = j & 1;
@@ -340,13 +347,19 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
       tc_fence_after();
       const int lr = h * pair::HM + wq * 32 + lane;
       const bool row_ok = lr < rows;
+      // this warp's 32 rows: all of this expert's (one TMA store per 32 x 32 box), some of them
+      // (plain stores: the rows after them belong to the next tile), or none
+      const int box_r0 = h * pair::HM + wq * 32;
+      const bool whole = box_r0 + 32 <= rows;
       for (int c = 0; c < pair::BN / 32; ++c) {
         const int col0 = n * pair::BN + c * 32;
         if (col0 >= p.N) break;
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
-        if (row_ok) {
+        if (whole) {
+          store_box_bf16(&p.map_y, cbox, 1, lane, v, col0, row0 + box_r0);
+        } else if (row_ok) {
           uint16_t* yrow = p.Y + size_t(row0 + lr) * p.N + col0;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -362,6 +375,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) pair::release_accumulator(bars, acc, rank);
     }
+    if (lane == 0) bulk_wait<0>();  // every store of this warp is complete
+    __syncwarp();
   } else if (warp == kWarpCopy) {
     // ---------------------------------------------------------------- AllGather + local scatter
     if (lane == 0) {
@@ -380,10 +395,10 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
         const int nunits = (t1 - t0) * pieces;
         int issued = 0, stored = 0;
         while (stored < nunits) {
-          while (issued < nunits && issued - stored < COPY_NBUF) {
+          while (issued < nunits && issued - stored < MOE_COPY_NBUF) {
             const uint32_t q = seq + uint32_t(issued);
-            const int buf = int(q % COPY_NBUF);
-            bulk_wait_read_dyn(stored - issued + COPY_NBUF - 1);
+            const int buf = int(q % MOE_COPY_NBUF);
+            bulk_wait_read_dyn(stored - issued + MOE_COPY_NBUF - 1);
             const int tl = t0 + issued / pieces, pc = issued % pieces;
             const uint32_t off = uint32_t(pc) * COPY_CHUNK;
             const uint32_t sz = min(COPY_CHUNK, row_bytes - off);
@@ -399,8 +414,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
             ++issued;
           }
           const uint32_t q = seq + uint32_t(stored);
-          const int buf = int(q % COPY_NBUF);
-          if (!mbar_wait(&bars->copy[buf], (q / COPY_NBUF) & 1u, abort, p.status, p.pipe_timeout_ns, 5)) {
+          const int buf = int(q % MOE_COPY_NBUF);
+          if (!mbar_wait(&bars->copy[buf], (q / MOE_COPY_NBUF) & 1u, abort, p.status, p.pipe_timeout_ns, 5)) {
             dead = true;
             break;
           }
@@ -564,6 +579,7 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
   tl_status res = TL_OK;
   do {
     if ((res = make_map_bf16(&p->map_a, a->sorted_tokens, P, a->H, size_t(a->H) * 2, pair::HM, pair::BK))) break;
+    if ((res = make_map_bf16(&p->map_y, a->Y, P, a->N, size_t(a->N) * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))) break;
     for (int e = 0; e < a->E && !res; ++e)
       res = make_map_bf16(&p->map_w[e], a->W[e], a->H, a->N, size_t(a->N) * 2, pair::BK, 64);
     if (res) break;
