@@ -138,8 +138,11 @@ tl_status classify_shards(const char* who, const void* const* shards, int R, int
 }
 
 namespace {
-// Per (device, kernel, block, smem, cluster): the attribute is set and the resident
-// capacity (CTAs per SM, or clusters) queried once, then reused on every launch.
+// The dynamic shared-memory limit of a kernel is raised per device to the most
+// any launch has asked for (never lowered: a kernel whose launches ask for
+// different sizes keeps a limit that fits them all); the resident capacity
+// (CTAs per SM, or clusters) is queried once per (device, kernel, block, smem,
+// cluster) and reused.
 struct LaunchKey {
   int device;
   const void* kernel;
@@ -154,9 +157,31 @@ struct LaunchEntry {
   LaunchKey key;
   int capacity;
 };
+struct SmemLimit {
+  int device;
+  const void* kernel;
+  size_t smem;
+};
 std::mutex g_launch_mu;
 LaunchEntry g_launch_cache[64];
 int g_launch_n = 0;
+SmemLimit g_smem_limit[64];
+int g_smem_n = 0;
+
+// Raise `kernel`'s dynamic shared-memory limit on `device` to at least `smem`.
+tl_status ensure_smem_limit(int device, const void* kernel, size_t smem) {
+  std::lock_guard<std::mutex> lock(g_launch_mu);
+  int slot = -1;
+  for (int i = 0; i < g_smem_n; ++i)
+    if (g_smem_limit[i].device == device && g_smem_limit[i].kernel == kernel) slot = i;
+  if (slot >= 0 && g_smem_limit[slot].smem >= smem) return TL_OK;
+  if (tl_status s = cuda_ok(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
+                            "cudaFuncSetAttribute(max dynamic smem)"))
+    return s;
+  if (slot >= 0) g_smem_limit[slot].smem = smem;
+  else if (g_smem_n < 64) g_smem_limit[g_smem_n++] = SmemLimit{device, kernel, smem};
+  return TL_OK;
+}
 }  // namespace
 
 tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cudaStream_t st, void** args,
@@ -164,6 +189,7 @@ tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cuda
   DeviceInfo di{};
   if (tl_status s = device_info(&di)) return s;
   if (cluster < 1 || grid % cluster) return fail(TL_ERR_INTERNAL, "grid %d is not a multiple of cluster %d", grid, cluster);
+  if (tl_status s = ensure_smem_limit(di.device, kernel, smem)) return s;
   const LaunchKey key{di.device, kernel, block, smem, cluster};
   int capacity = -1;
   {
@@ -172,9 +198,6 @@ tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cuda
       if (g_launch_cache[i].key == key) capacity = g_launch_cache[i].capacity;
   }
   if (capacity < 0) {
-    if (tl_status s = cuda_ok(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)),
-                              "cudaFuncSetAttribute(max dynamic smem)"))
-      return s;
     if (cluster > 1) {
       cudaLaunchConfig_t q{};
       q.gridDim = dim3(grid);

@@ -38,6 +38,7 @@ constexpr int MOE_MAX_E = 64;
 constexpr int MOE_MAX_R = 32;
 constexpr int MOE_MAX_TILES = 8192;
 constexpr int ROUTE_THREADS = 1024;
+constexpr uint32_t ROUTE_CTAS = 8;  // the routing kernel's cluster
 constexpr int ROUTE_WARPS = ROUTE_THREADS / 32;
 constexpr int kWarpCopy = 6;
 constexpr int MOE_THREADS = 7 * 32;
@@ -56,7 +57,6 @@ __host__ __device__ inline int ws_tiles(int) { return WS_HEADER; }
 __host__ __device__ inline int ws_order(int max_tiles) { return WS_HEADER + 6 * max_tiles; }
 __host__ __device__ inline int ws_inv(int max_tiles) { return WS_HEADER + 7 * max_tiles; }
 
-constexpr int ROUTE_SMEM_PAIRS = 20480;  // topk ids and perm kept in shared memory up to this many pairs
 
 struct RouteParams {
   const int32_t* topk;    // [T, k]
@@ -64,9 +64,8 @@ struct RouteParams {
   int32_t* offsets;       // [E+1]
   int32_t* ws;            // workspace
   uint32_t* status;
-  int32_t T, k, E, R, T_r, rpb, bpr, self, max_tiles, pull, staged;
+  int32_t T, k, E, R, T_r, rpb, bpr, self, max_tiles, pull;
   int32_t k_shift;  // log2(k) when k is a power of two, else -1
-  int32_t use_tb;   // token -> (barrier, rank) table in shared memory (staged runs)
 };
 
 // Lanes of `am` whose expert equals this lane's (e < 64): one ballot per bit of e.
@@ -81,37 +80,32 @@ __device__ __forceinline__ unsigned same_expert_lanes(unsigned am, int e) {
   return peers;
 }
 
-// Stable counting sort of the P = T*k pairs by expert, then the tile table.
+// Routing on a cluster of ROUTE_CTAS CTAs: CTA c owns the c-th contiguous range
+// of the P = T*k (token, slot) pairs, and its warps own consecutive sub-ranges.
+//  1. per-warp expert counts over the warp's pairs;
+//  2. (cluster barrier) every CTA reads every CTA's per-expert totals from
+//     distributed shared memory: expert offsets (exclusive scan) and, for a
+//     stable sort, the base of each of its warps per expert = offset + the counts
+//     of every lower CTA and every lower warp of this CTA; stable scatter of the
+//     pairs (perm and its inverse, in global memory);
+//  3. (cluster barrier) the tile table, one tile per warp across the cluster,
+//     the tile keys gathered in CTA 0's shared memory;
+//  4. (cluster barrier) CTA 0 ranks the tiles by (key, index): the consumer order.
 __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const RouteParams p) {
   extern __shared__ int32_t sm[];
   const int E = p.E;
-  int32_t* cnt = sm;                           // [ROUTE_WARPS][E] per-warp counts, then bases
-  int32_t* s_off = cnt + ROUTE_WARPS * E;      // [E+1]
-  int32_t* s_toff = s_off + (E + 1);           // [E+1] tile offsets
-  int32_t* s_key = s_toff + (E + 1);           // [max_tiles]
-  int32_t* s_ids = s_key + p.max_tiles;        // [P] when staged
-  int32_t* s_perm = s_ids + (p.staged ? p.T * p.k : 0);
-  int32_t* s_tb = s_perm + (p.staged ? p.T * p.k : 0);  // [T] when use_tb: (barrier << 6) | rank
+  int32_t* cnt = sm;                       // [ROUTE_WARPS][E] per-warp counts, then per-warp bases
+  int32_t* ctot = cnt + ROUTE_WARPS * E;   // [E] this CTA's per-expert totals (read by the cluster)
+  int32_t* s_off = ctot + E;               // [E+1] expert offsets
+  int32_t* s_toff = s_off + (E + 1);       // [E+1] first tile of each expert
+  int32_t* s_key = s_toff + (E + 1);       // [max_tiles] tile keys (CTA 0)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = cluster_ctarank();
   const int P = p.T * p.k;
-  // stage the routing in shared memory (one coalesced pass) so the passes below
-  // do not chain global-memory round trips
-  const int32_t* ids = p.topk;
-  int32_t* perm = p.perm;
-  if (p.staged) {
-    for (int q = tid; q < P; q += ROUTE_THREADS) s_ids[q] = p.topk[q];
-    ids = s_ids;
-    perm = s_perm;
-  }
-  // the producer barrier and rank of every token, once (the tile table reads them per row)
-  if (p.use_tb) {
-    for (int t = tid; t < p.T; t += ROUTE_THREADS) {
-      const int r = t / p.T_r;
-      s_tb[t] = ((r * p.bpr + (t - r * p.T_r) / p.rpb) << 6) | r;
-    }
-  }
-  const int per_warp = ((P + ROUTE_WARPS - 1) / ROUTE_WARPS + 31) / 32 * 32;
-  const int q0 = warp * per_warp, q1 = min(P, q0 + per_warp);
+  const int per_cta = ((P + ROUTE_CTAS - 1) / ROUTE_CTAS + 31) / 32 * 32;
+  const int c0 = min(P, int(crank) * per_cta), c1 = min(P, c0 + per_cta);
+  const int per_warp = ((c1 - c0 + ROUTE_WARPS - 1) / ROUTE_WARPS + 31) / 32 * 32;
+  const int q0 = min(c1, c0 + warp * per_warp), q1 = min(c1, q0 + per_warp);
   int32_t* tiles = p.ws + ws_tiles(p.max_tiles);
   int32_t* order = p.ws + ws_order(p.max_tiles);
   int32_t* inv = p.ws + ws_inv(p.max_tiles);
@@ -122,7 +116,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   for (int base = q0; base < q1; base += 32) {
     const int q = base + lane;
     const bool act = q < q1;
-    int e = act ? ids[q] : -1;
+    int e = act ? p.topk[q] : -1;
     if (act && (e < 0 || e >= E)) {
       record_error(p.status, TL_ERR_INVALID, uint32_t(q), uint32_t(e), uint32_t(E));
       e = min(max(e, 0), E - 1);
@@ -135,25 +129,43 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     __syncwarp();
   }
   __syncthreads();
-  // 2. expert counts (one thread per expert), exclusive scan, and each warp's
-  //    first position per expert
   for (int e = tid; e < E; e += ROUTE_THREADS) {
     int c = 0;
     for (int w = 0; w < ROUTE_WARPS; ++w) c += cnt[w * E + e];
-    s_toff[e] = c;  // counts, parked in the tile-offset array until step 4
+    ctot[e] = c;
   }
-  __syncthreads();
-  if (tid == 0) {
-    int acc = 0;
-    for (int e = 0; e < E; ++e) {
-      s_off[e] = acc;
-      acc += s_toff[e];
+  cluster_sync();
+  // 2. expert totals and offsets from every CTA's totals, this CTA's bases
+  if (tid < 32) {
+    // one lane per expert (E <= 64 in two rounds): totals, then a warp scan for the offsets
+    int carry = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      int tot = 0, below = 0;
+      if (e < E) {
+        for (uint32_t c = 0; c < ROUTE_CTAS; ++c) {
+          const int v = int(ld_shared_cluster_u32(map_to_rank(&ctot[e], c)));
+          tot += v;
+          below += c < crank ? v : 0;
+        }
+      }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (e < E) {
+        s_off[e] = carry + incl - tot;
+        s_toff[e] = below;  // parked: the counts of lower CTAs
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    s_off[E] = acc;
+    if (lane == 0) s_off[E] = carry;
   }
   __syncthreads();
   for (int e = tid; e < E; e += ROUTE_THREADS) {
-    int run = s_off[e];
+    int run = s_off[e] + s_toff[e];
     for (int w = 0; w < ROUTE_WARPS; ++w) {
       const int c = cnt[w * E + e];
       cnt[w * E + e] = run;
@@ -161,25 +173,23 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     }
   }
   __syncthreads();
-  // 3. stable scatter: pairs keep their (token, slot) order inside an expert
+  // stable scatter: pairs keep their (token, slot) order inside an expert
   for (int base = q0; base < q1; base += 32) {
     const int q = base + lane;
     const bool act = q < q1;
-    int e = act ? min(max(ids[q], 0), E - 1) : 0;
+    const int e = act ? min(max(p.topk[q], 0), E - 1) : 0;
     const unsigned am = __ballot_sync(0xffffffffu, act);
     if (act) {
       const unsigned peers = same_expert_lanes(am, e);
       const int pos = cnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
-      perm[pos] = q;
-      if (p.staged) p.perm[pos] = q;
+      p.perm[pos] = q;
       inv[q] = pos;
       __syncwarp(am);
       if (lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
     }
     __syncwarp();
   }
-  __syncthreads();
-  // 4. tiles per expert and their offsets
+  // tiles per expert and their offsets (every CTA, from the same totals)
   if (tid == 0) {
     int acc = 0;
     for (int e = 0; e < E; ++e) {
@@ -187,14 +197,20 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
       acc += (s_off[e + 1] - s_off[e] + TM - 1) / TM;
     }
     s_toff[E] = acc;
-    p.ws[0] = min(acc, p.max_tiles);
-    if (acc > p.max_tiles) record_error(p.status, TL_ERR_INTERNAL, 0xFFFE0000u, uint32_t(acc), uint32_t(p.max_tiles));
+    if (crank == 0) {
+      p.ws[0] = min(acc, p.max_tiles);
+      if (acc > p.max_tiles)
+        record_error(p.status, TL_ERR_INTERNAL, 0xFFFE0000u, uint32_t(acc), uint32_t(p.max_tiles));
+    }
   }
-  __syncthreads();
-  for (int e = tid; e <= E; e += ROUTE_THREADS) p.offsets[e] = s_off[e];
+  if (crank == 0)
+    for (int e = tid; e <= E; e += ROUTE_THREADS) p.offsets[e] = s_off[e];
+  // every CTA's perm and inverse are in global memory before any tile reads them
+  cluster_sync();
+  // 3. the tile table, one warp per tile across the cluster: rows of a tile are one
+  //    expert's, tokens ascending
   const int ntiles = min(s_toff[E], p.max_tiles);
-  // 5. the tile table, one warp per tile: rows of a tile are one expert's, tokens ascending
-  for (int t = warp; t < ntiles; t += ROUTE_WARPS) {
+  for (int t = int(crank) * ROUTE_WARPS + warp; t < ntiles; t += ROUTE_CTAS * ROUTE_WARPS) {
     int lo_e = 0, hi_e = E - 1;  // last expert whose first tile <= t (empty experts are skipped over)
     while (lo_e < hi_e) {
       const int mid = (lo_e + hi_e + 1) >> 1;
@@ -206,17 +222,10 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     uint32_t mask = 0;
     int blo = 0x7fffffff, bhi = -1;
     for (int i = lane; i < rows; i += 32) {
-      const int q = perm[row0 + i];
+      const int q = p.perm[row0 + i];
       const int tok = p.k_shift >= 0 ? (q >> p.k_shift) : q / p.k;
-      int r, b;
-      if (p.use_tb) {
-        const int v = s_tb[tok];
-        r = v & 63;
-        b = v >> 6;
-      } else {
-        r = tok / p.T_r;
-        b = r * p.bpr + (tok % p.T_r) / p.rpb;
-      }
+      const int r = tok / p.T_r;
+      const int b = r * p.bpr + (tok - r * p.T_r) / p.rpb;
       mask |= 1u << r;
       blo = min(blo, b);
       bhi = max(bhi, b);
@@ -249,19 +258,21 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
       tr[3] = blo;
       tr[4] = bhi;
       tr[5] = int32_t(mask);
-      s_key[t] = key;
+      st_shared_cluster_u32(map_to_rank(&s_key[t], 0), uint32_t(key));
     }
   }
-  __syncthreads();
-  // 6. consumer order: tiles by (key, index)
-  for (int t = tid; t < ntiles; t += ROUTE_THREADS) {
-    const int kt = s_key[t];
-    int rank = 0;
-    for (int u = 0; u < ntiles; ++u) {
-      const int ku = s_key[u];
-      rank += (ku < kt) || (ku == kt && u < t);
+  cluster_sync();
+  // 4. consumer order: tiles by (key, index)
+  if (crank == 0) {
+    for (int t = tid; t < ntiles; t += ROUTE_THREADS) {
+      const int kt = s_key[t];
+      int rank = 0;
+      for (int u = 0; u < ntiles; ++u) {
+        const int ku = s_key[u];
+        rank += (ku < kt) || (ku == kt && u < t);
+      }
+      order[rank] = t;
     }
-    order[rank] = t;
   }
 }
 
@@ -547,30 +558,16 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
   rp.self = a->self_rank;
   rp.max_tiles = max_tiles;
   rp.pull = pull ? 1 : 0;
-  rp.staged = P <= ROUTE_SMEM_PAIRS ? 1 : 0;
-  rp.use_tb = rp.staged;
   rp.k_shift = (a->topk & (a->topk - 1)) == 0 ? __builtin_ctz(unsigned(a->topk)) : -1;
-  const size_t route_smem = (size_t(ROUTE_WARPS) * a->E + 2 * (a->E + 1) + max_tiles + (rp.staged ? 2 * P : 0) +
-                             (rp.use_tb ? T : 0)) *
-                            sizeof(int32_t);
+  const size_t route_smem = (size_t(ROUTE_WARPS) * a->E + a->E + 2 * (a->E + 1) + max_tiles) * sizeof(int32_t);
   if (route_smem > size_t(di.max_smem_optin))
     return fail(TL_ERR_UNSUPPORTED, "tl_moe_ag_gemm: routing needs %zu bytes of shared memory", route_smem);
   {
-    // the routing kernel's shared-memory limit is raised once per device to the most asked for so far
-    static std::mutex mu;
-    static int route_smem_set[64] = {};
-    std::lock_guard<std::mutex> lock(mu);
-    if (di.device < 0 || di.device >= 64) return fail(TL_ERR_UNSUPPORTED, "device ordinal %d", di.device);
-    if (int(route_smem) > route_smem_set[di.device]) {
-      if (tl_status s = cuda_ok(cudaFuncSetAttribute(reinterpret_cast<const void*>(&moe_route_kernel),
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, int(route_smem)),
-                                "cudaFuncSetAttribute(route)"))
-        return s;
-      route_smem_set[di.device] = int(route_smem);
-    }
+    void* rargs[] = {&rp};
+    if (tl_status s = launch_coop(reinterpret_cast<const void*>(&moe_route_kernel), int(ROUTE_CTAS), ROUTE_THREADS,
+                                  route_smem, st, rargs, int(ROUTE_CTAS)))
+      return s;
   }
-  moe_route_kernel<<<1, ROUTE_THREADS, route_smem, st>>>(rp);
-  if (tl_status s = cuda_ok(cudaGetLastError(), "route launch")) return s;
 
   // 2. AllGather + scatter and grouped GEMM
   MoeParams* p = new (std::nothrow) MoeParams;
