@@ -10,6 +10,11 @@ Compute-Communication Overlapping Kernels using Tile-Centric Primitives"):
 * Technical Deep Dive, dynamic workloads: routing makes the tile -> rank
   dependencies data dependent, so they are handed to the kernel as lookup
   tables built from the routing.
+* Key Findings / Experimental Setup & Results, the rest of the MoE layer (the
+  down-projection side): a GroupGEMM per rank over the expert-sorted rows, a
+  ReduceScatter of the ranks' partial outputs, a TopK-reduce that combines
+  each token's k expert outputs with its gate weights, and a scatter back to
+  the token order on the token's own rank (moe_down).
 
 Routing bookkeeping (integer, plain loops):
   counts[e]   number of (token, slot) pairs routed to expert e
@@ -138,3 +143,37 @@ def moe_at(X_shards, topk_ids, W, rows, cols, route_result=None):
         x = bf16.decode(X_shards[tok // T_r][tok % T_r, :])
         out[i] = np.dot(x, bf16.decode(W[e][:, col]))
     return out
+
+
+def moe_down(H_list, W2_list, topk_ids, gates, E, T_r):
+    """The down-projection side of the MoE layer, float64.
+
+    Every expert's weights are split over the R ranks along the intermediate
+    dimension: rank r holds H_r [P, I_r] (the intermediate activations of the
+    P = T*k routed rows, in expert-sorted order) and W2_r [E*I_r, Hd] (expert
+    e's slice at rows e*I_r .. (e+1)*I_r - 1).  With i a sorted row of expert e,
+      Y[i]   = sum over ranks r = 0..R-1, in order, of H_r[i] . W2_r[e slice]
+      out[t] = sum over slots s = 0..k-1, in order, of gates[t, s] * Y[pos(t, s)]
+    where pos(t, s) is the sorted row of pair t*k + s; row shard d of out
+    (tokens d*T_r .. (d+1)*T_r - 1) is returned as out[d]."""
+    R = len(H_list)
+    ids = np.asarray(topk_ids)
+    T, k = ids.shape
+    counts, offsets, perm = route(ids, E)
+    I_r = H_list[0].shape[1]
+    Hd = W2_list[0].shape[1]
+    P = T * k
+    Y = np.zeros((P, Hd), dtype=np.float64)
+    for H_r, W2_r in zip(H_list, W2_list):
+        Hr, Wr = bf16.decode(H_r), bf16.decode(W2_r)
+        for e in range(E):
+            lo, hi = int(offsets[e]), int(offsets[e + 1])
+            if hi > lo:
+                Y[lo:hi] = Y[lo:hi] + Hr[lo:hi] @ Wr[e * I_r:(e + 1) * I_r]
+    pos = np.empty(P, dtype=np.int64)
+    pos[np.asarray(perm, dtype=np.int64)] = np.arange(P)
+    g = np.asarray(gates, dtype=np.float64)
+    out = np.zeros((T, Hd), dtype=np.float64)
+    for s in range(k):
+        out = out + g[:, s:s + 1] * Y[pos[np.arange(T) * k + s]]
+    return [out[d * T_r:(d + 1) * T_r] for d in range(T // T_r)]

@@ -326,3 +326,54 @@ def check_gemm_rs_variant(variant, gemm_rs):
     B = [_bits(np.array([[1.0]]))] * 4
     np.testing.assert_array_equal([o[0, 0] for o in variant(A, B, "f32", "ring")], [1.0, 1.0, 0.0, 0.0])
     np.testing.assert_array_equal([o[0, 0] for o in variant(A, B, "f32", "rank")], [0.0, 0.0, 0.0, 0.0])
+
+
+def check_moe_down(moe_down, route):
+    """Pins of the MoE down-projection side: brute force on a tiny case, the
+    plain-GEMM special case, and linearity in the ranks and in the gates."""
+    rng = np.random.default_rng(23)
+    # brute force: R = 2 ranks, T = 6 tokens of T_r = 3, top-2 of E = 3, I_r = 2, Hd = 3
+    R, T_r, E, k, I_r, Hd = 2, 3, 3, 2, 2, 3
+    T, P = R * T_r, R * T_r * k
+    ids = np.array([[0, 2], [1, 0], [2, 1], [0, 1], [2, 0], [1, 2]], dtype=np.int32)
+    H = [_rand_bits(rng, (P, I_r)) for _ in range(R)]
+    W2 = [_rand_bits(rng, (E * I_r, Hd)) for _ in range(R)]
+    gates = rng.uniform(0.0, 1.0, (T, k)).astype(np.float32)
+    out = moe_down(H, W2, ids, gates, E, T_r)
+    # sorted rows by (expert, token, slot), written out by hand from ids
+    sorted_pairs = [(e, t, s) for e in range(E) for t in range(T) for s in range(k) if ids[t, s] == e]
+    pos = {(t, s): i for i, (_, t, s) in enumerate(sorted_pairs)}
+    dec = lambda b: np.asarray(b, dtype=np.uint32).astype(np.uint32) << 16
+    Hf = [dec(h).view(np.float32).astype(np.float64) for h in H]
+    Wf = [dec(w).view(np.float32).astype(np.float64) for w in W2]
+    for t in range(T):
+        for c in range(Hd):
+            want = 0.0
+            for s in range(k):
+                i = pos[(t, s)]
+                e = ids[t, s]
+                y = 0.0
+                for r in range(R):
+                    for j in range(I_r):
+                        y += Hf[r][i, j] * Wf[r][e * I_r + j, c]
+                want += float(gates[t, s]) * y
+            assert abs(out[t // T_r][t % T_r, c] - want) <= 1e-12 * max(1.0, abs(want)), (t, c)
+    # E = 1, k = 1, R = 1, gate 1: sorted rows are the tokens in order, out = H . W2
+    H1 = [_rand_bits(rng, (4, 3))]
+    W1 = [_rand_bits(rng, (3, 5))]
+    o = moe_down(H1, W1, np.zeros((4, 1), np.int32), np.ones((4, 1), np.float32), 1, 4)
+    Hf1, Wf1 = dec(H1[0]).view(np.float32).astype(np.float64), dec(W1[0]).view(np.float32).astype(np.float64)
+    np.testing.assert_allclose(o[0], Hf1 @ Wf1, rtol=1e-12, atol=0)
+    # linearity in the ranks: the R-rank result is the sum of the one-rank results
+    parts = [moe_down([H[r]], [W2[r]], ids, gates, E, T) for r in range(R)]
+    whole = np.concatenate(out)
+    np.testing.assert_allclose(whole, parts[0][0] + parts[1][0], rtol=1e-12, atol=1e-12)
+    # gates: zeroing slot 1 leaves only slot 0's expert output
+    g0 = gates.copy()
+    g0[:, 1] = 0.0
+    o0 = np.concatenate(moe_down(H, W2, ids, g0, E, T_r))
+    for t in range(T):
+        i = pos[(t, 0)]
+        e = ids[t, 0]
+        y = sum(Hf[r][i] @ Wf[r][e * I_r:(e + 1) * I_r] for r in range(R))
+        np.testing.assert_allclose(o0[t], float(gates[t, 0]) * y, rtol=1e-12, atol=1e-12)

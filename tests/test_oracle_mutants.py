@@ -176,3 +176,31 @@ def test_pins_catch_unrounded_bf16_partials():
     def bad(A, B, partials="f32", order="rank"):
         return G.gemm_rs_variant(A, B, "f32", order)
     _fails(C.check_gemm_rs_variant, bad, G.gemm_rs)
+
+
+def test_pins_catch_swapped_gates():
+    def bad(H, W2, ids, gates, E, T_r):
+        return M.moe_down(H, W2, ids, np.ascontiguousarray(gates[:, ::-1]), E, T_r)
+    _fails(C.check_moe_down, bad, M.route)
+
+
+def test_pins_catch_wrong_expert_slice():
+    def bad(H, W2, ids, gates, E, T_r):
+        I_r = H[0].shape[1]
+        rolled = [np.roll(w, I_r, axis=0) for w in W2]
+        return M.moe_down(H, rolled, ids, gates, E, T_r)
+    _fails(C.check_moe_down, bad, M.route)
+
+
+def test_pins_catch_sorted_row_for_pair_index():
+    def bad(H, W2, ids, gates, E, T_r):
+        # reads row t*k + s of Y instead of the pair's sorted position
+        T, k = np.asarray(ids).shape
+        ident = np.arange(T * k)
+        old_route = M.route
+        try:
+            M.route = lambda i, e: (lambda c, o, p: (c, o, ident))(*old_route(i, e))
+            return M.moe_down(H, W2, ids, gates, E, T_r)
+        finally:
+            M.route = old_route
+    _fails(C.check_moe_down, bad, M.route)

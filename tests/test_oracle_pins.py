@@ -145,3 +145,7 @@ def test_gemm_rs_partial_abs_sum_bounds_the_sum():
     S = oracle.gemm_rs.reduced(A, B)
     T = oracle.gemm_rs.partial_abs_sum(A, B)
     assert np.all(np.abs(S) <= T * (1 + 1e-12)) and np.all(T >= 0)
+
+
+def test_moe_down_pins():
+    C.check_moe_down(oracle.moe.moe_down, oracle.moe.route)
