@@ -377,6 +377,51 @@ size_t tl_moe_workspace_size(int R, int T_r, int E, int topk);
 int tl_moe_num_flags(int mode, int R, int T_r, int H, int topk, int rows_per_barrier, int* effective_rpb);
 tl_status tl_moe_ag_gemm(const tl_moe_args* args, void* stream);
 
+/* ---------------------------------------------------------------- MoE down-projection side
+ * The rest of the MoE layer after the up-projection (talk summary, Key Findings
+ * and Experimental Setup & Results: GroupGEMM, ReduceScatter, TopK-reduce and a
+ * scatter back to the token order).  Every expert's weights are split over the R
+ * ranks along the intermediate dimension: rank r holds H_r [P, I_r], the
+ * intermediate activations of the P = R*T_r*topk routed rows in expert-sorted
+ * order, and W2_r [E*I_r, Hd] with expert e's slice at rows e*I_r.  With i a
+ * sorted row of expert e and pos(t, s) the sorted row of pair t*topk + s:
+ *   Y[i]      = sum over ranks r = 0..R-1, in order, of H_r[i] . W2_r[e slice]   (fp32)
+ *   out[d][u] = bf16( sum over slots s = 0..topk-1, in order, of
+ *                     gates[t, s] * Y[pos(t, s)] ),   t = d*T_r + u          (fp32)
+ * Two stream-ordered launches: a grouped GEMM-ReduceScatter on pairs of CTAs
+ * (items = (expert tile, 256-column tile, rank), the R partials of a tile pushed
+ * into receive slots, reducers summing them in rank order into Y, as in
+ * tl_gemm_rs), then the TopK-reduce that combines and scatters.  The routing
+ * (sorted rows, tile table, inverse permutation) is the workspace a
+ * tl_moe_ag_gemm call on the same topk_ids, R, T_r, E and topk left behind.
+ * Limits: R <= 32, E <= 64, I_r and Hd multiples of 8.
+ */
+typedef struct tl_moe_down_args {
+  int32_t R;                   /* ranks, 1..32 */
+  int32_t T_r;                 /* tokens per rank */
+  int32_t topk;                /* routed experts per token */
+  int32_t E;                   /* experts, 1..64 */
+  int32_t I_r;                 /* intermediate columns per rank (contraction), multiple of 8 */
+  int32_t Hd;                  /* output hidden size, multiple of 8 */
+  const void* const* H;        /* host array of R device pointers, bf16 [P, I_r], expert-sorted rows */
+  const void* const* W2;       /* host array of R device pointers, bf16 [E*I_r, Hd] */
+  const float* gates;          /* device fp32 [R*T_r, topk] */
+  const int32_t* routing;      /* device: the workspace of the matching tl_moe_ag_gemm call */
+  void* const* out;            /* host array of R device pointers, bf16 [T_r, Hd], written */
+  void* workspace;             /* device, >= tl_moe_down_workspace_size(...) bytes, 16-byte aligned */
+  size_t workspace_bytes;
+  tl_signals* signals;         /* >= tl_moe_down_num_flags(...) flags */
+  uint32_t epoch;              /* nonzero */
+  uint32_t reserved0;
+  uint64_t timeout_ns;         /* 0 = 1 s */
+} tl_moe_down_args;
+
+/* Workspace bytes: the fp32 receive ring (as for GEMM-RS) and Y [P, Hd] fp32. */
+size_t tl_moe_down_workspace_size(int R, int T_r, int topk, int E, int Hd);
+/* Flags: 4 * R * max_tiles * ceil(Hd/256), max_tiles = ceil(P/256) + E. */
+int tl_moe_down_num_flags(int R, int T_r, int topk, int E, int Hd);
+tl_status tl_moe_down(const tl_moe_down_args* args, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -177,3 +177,26 @@ def moe_down(H_list, W2_list, topk_ids, gates, E, T_r):
     for s in range(k):
         out = out + g[:, s:s + 1] * Y[pos[np.arange(T) * k + s]]
     return [out[d * T_r:(d + 1) * T_r] for d in range(T // T_r)]
+
+
+def moe_down_at(H_list, W2_list, topk_ids, gates, E, toks, cols, route_result=None):
+    """out[toks[i], cols[i]] (global token index) one element at a time."""
+    ids = np.asarray(topk_ids)
+    T, k = ids.shape
+    counts, offsets, perm = route_result if route_result is not None else route(ids, E)
+    P = T * k
+    pos = np.empty(P, dtype=np.int64)
+    pos[np.asarray(perm, dtype=np.int64)] = np.arange(P)
+    I_r = H_list[0].shape[1]
+    out = np.empty(len(toks), dtype=np.float64)
+    for n, (t, c) in enumerate(zip(toks, cols)):
+        acc = 0.0
+        for s in range(k):
+            i = int(pos[int(t) * k + s])
+            e = int(ids[int(t), s])
+            y = 0.0
+            for H_r, W2_r in zip(H_list, W2_list):
+                y += float(np.dot(bf16.decode(H_r[i, :]), bf16.decode(W2_r[e * I_r:(e + 1) * I_r, int(c)])))
+            acc += float(gates[int(t), s]) * y
+        out[n] = acc
+    return out

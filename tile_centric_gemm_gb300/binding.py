@@ -32,6 +32,7 @@ EXPORTED = [
     "tl_gemm", "tl_ag_gemm_num_flags", "tl_ag_gemm_tile_order", "tl_ag_gemm",
     "tl_gemm_rs_workspace_size", "tl_gemm_rs_num_flags", "tl_gemm_rs", "tl_gemm_rs_noalloc",
     "tl_moe_workspace_size", "tl_moe_num_flags", "tl_moe_ag_gemm", "tl_allgather", "tl_reduce_scatter",
+    "tl_moe_down_workspace_size", "tl_moe_down_num_flags", "tl_moe_down",
 ]
 
 
@@ -84,6 +85,16 @@ class tl_moe_args(ctypes.Structure):
     ]
 
 
+class tl_moe_down_args(ctypes.Structure):
+    _fields_ = [
+        ("R", ctypes.c_int32), ("T_r", ctypes.c_int32), ("topk", ctypes.c_int32), ("E", ctypes.c_int32),
+        ("I_r", ctypes.c_int32), ("Hd", ctypes.c_int32),
+        ("H", ctypes.POINTER(_vp)), ("W2", ctypes.POINTER(_vp)), ("gates", _vp), ("routing", _vp),
+        ("out", ctypes.POINTER(_vp)), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("signals", _vp),
+        ("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32), ("timeout_ns", ctypes.c_uint64),
+    ]
+
+
 class tl_allgather_args(ctypes.Structure):
     _fields_ = [
         ("R", ctypes.c_int32), ("self_rank", ctypes.c_int32), ("M_shard", ctypes.c_int32), ("K", ctypes.c_int32),
@@ -122,6 +133,9 @@ _decl("tl_ag_gemm_num_flags", _i, _i, _i, _i, _i, ctypes.POINTER(_i))
 _decl("tl_ag_gemm_tile_order", _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int32), _i)
 _decl("tl_ag_gemm", _i, ctypes.POINTER(tl_ag_gemm_args), _vp)
 _decl("tl_gemm_rs_workspace_size", _sz, _i, _i, _i)
+_decl("tl_moe_down_workspace_size", _sz, _i, _i, _i, _i, _i)
+_decl("tl_moe_down_num_flags", _i, _i, _i, _i, _i, _i)
+_decl("tl_moe_down", _i, ctypes.POINTER(tl_moe_down_args), _vp)
 _decl("tl_gemm_rs_num_flags", _i, _i, _i, _i)
 _decl("tl_gemm_rs", _i, ctypes.POINTER(tl_gemm_rs_args), _vp)
 _decl("tl_gemm_rs_noalloc", _i, ctypes.POINTER(tl_gemm_rs_args), _vp, _vp)
@@ -359,3 +373,28 @@ def tl_reduce_scatter(partials, out, *, stream=None):
     a = tl_reduce_scatter_args(R=R, M=M, N=N, reserved0=0, partials=ctypes.cast(pp, ctypes.POINTER(_vp)),
                                out=ctypes.cast(po, ctypes.POINTER(_vp)))
     _check(lib.tl_reduce_scatter(ctypes.byref(a), _stream(stream)))
+
+
+def tl_moe_down_workspace_size(R, T_r, topk, E, Hd):
+    return int(lib.tl_moe_down_workspace_size(R, T_r, topk, E, Hd))
+
+
+def tl_moe_down_num_flags(R, T_r, topk, E, Hd):
+    return int(lib.tl_moe_down_num_flags(R, T_r, topk, E, Hd))
+
+
+def tl_moe_down(H, W2, gates, routing, out, workspace, signals: Signals, epoch: int, *, topk, E, timeout_ns=0,
+                stream=None):
+    """out[d] = the gate-weighted combine of each token's expert outputs, Y summed over ranks
+    (see tilelink.h); routing is the workspace of the matching tl_moe_ag_gemm call."""
+    R = len(H)
+    P, I_r = H[0].shape
+    Hd = W2[0].shape[1]
+    T_r = out[0].shape[0]
+    ph, pw, po = _ptr_array(H), _ptr_array(W2), _ptr_array(out)
+    a = tl_moe_down_args(R=R, T_r=T_r, topk=topk, E=E, I_r=I_r, Hd=Hd, H=ctypes.cast(ph, ctypes.POINTER(_vp)),
+                         W2=ctypes.cast(pw, ctypes.POINTER(_vp)), gates=_ptr(gates), routing=_ptr(routing),
+                         out=ctypes.cast(po, ctypes.POINTER(_vp)), workspace=_ptr(workspace),
+                         workspace_bytes=workspace.numel() * workspace.element_size(), signals=signals.handle,
+                         epoch=int(epoch) & 0xFFFFFFFF, reserved0=0, timeout_ns=int(timeout_ns))
+    _check(lib.tl_moe_down(ctypes.byref(a), _stream(stream)))

@@ -29,6 +29,7 @@
 
 #include "tl_epilogue.cuh"
 #include "tl_internal.h"
+#include "tl_moe_ws.cuh"
 #include "tl_pair.cuh"
 
 namespace tl {
@@ -51,11 +52,7 @@ constexpr uint32_t MOE_SMEM_CSTAGE = MOE_SMEM_COPY + MOE_COPY_NBUF * COPY_CHUNK;
 constexpr uint32_t MOE_SMEM_BARS = MOE_SMEM_CSTAGE + kNumEpiWarps * C_BOX_BYTES;
 constexpr uint32_t MOE_SMEM_BYTES = MOE_SMEM_BARS + sizeof(pair::Bars) + 1024;
 
-// Workspace layout, in int32 words (documented in tilelink.h).
-constexpr int WS_HEADER = 16;  // [0] = number of tiles
-__host__ __device__ inline int ws_tiles(int) { return WS_HEADER; }
-__host__ __device__ inline int ws_order(int max_tiles) { return WS_HEADER + 6 * max_tiles; }
-__host__ __device__ inline int ws_inv(int max_tiles) { return WS_HEADER + 7 * max_tiles; }
+static_assert(TM == MOE_TILE_ROWS, "expert tiles are CTA-pair tiles");
 
 
 struct RouteParams {
@@ -458,7 +455,6 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
   pair::teardown(bars, warp, tmem_base);
 }
 
-int moe_max_tiles(int P, int E) { return (P + TM - 1) / TM + E; }
 
 // push: tokens of a shard per flag (about 32 KB of source rows); pull: sorted rows per flag (about 64 KB)
 int moe_default_rpb(int mode, int H, int T_r, long long P) {

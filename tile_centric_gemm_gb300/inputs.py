@@ -114,3 +114,16 @@ def to_torch_bf16(bits: np.ndarray):
     """Reinterpret a uint16 bit array as a torch.bfloat16 CPU tensor (no copy of values)."""
     import torch
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def moe_down_inputs(R: int, T_r: int, topk: int, E: int, I_r: int, Hd: int, seed: int = 0):
+    """The down-projection side of the MoE layer: per-rank intermediate activations
+    H_r [R*T_r*topk, I_r] ~ N(0,1) in expert-sorted row order, per-rank weights
+    W2_r [E*I_r, Hd] ~ N(0,0.02) (expert e's slice at rows e*I_r), bf16 bits, and
+    gate weights [R*T_r, topk] float32, uniform(0,1) normalised to sum 1 per token."""
+    P = R * T_r * topk
+    H = [normal_bf16((P, I_r), seed + 4000 + r, 1.0) for r in range(R)]
+    W2 = [normal_bf16((E * I_r, Hd), seed + 5000 + r, 0.02) for r in range(R)]
+    g = np.random.Generator(np.random.PCG64(seed + 6000)).uniform(0.0, 1.0, (R * T_r, topk)).astype(np.float32)
+    gates = (g / g.sum(axis=1, keepdims=True)).astype(np.float32)
+    return H, W2, gates
