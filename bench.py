@@ -77,7 +77,8 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="AG-GEMM sweep (R in {2,4,8}, M in {1024..16384}, K=8192, N=1024; shards in HBM and "
                          "peer shards in pinned host memory): copy, GEMM, sequential and fused times, one JSON line")
-    ap.add_argument("--only", choices=["ag", "rs", "moe"],
+    ap.add_argument("--no-extras", action="store_true", help="skip the measurements outside the step")
+    ap.add_argument("--only", choices=["ag", "rs", "moe", "moe_down"],
                     help="run one fused call of the step (W untimed, then K timed back to back) and print its "
                          "device time; for profiling a single kernel on the bench's workload")
     return ap.parse_args()
@@ -545,6 +546,50 @@ def run_sweep(torch, B, peaks):
     return rows
 
 
+# the down side of the step's MoE layer: same routing; I_r = the up side's per-rank columns, Hd = its hidden size
+MOE_DOWN = dict(R=MOE["R"], T_r=MOE["T_r"], topk=MOE["topk"], E=MOE["E"], I_r=MOE["N"], Hd=MOE["H"])
+MOE_DOWN_FLOPS = 2 * MOE_DOWN["R"] * (MOE_DOWN["R"] * MOE_DOWN["T_r"] * MOE_DOWN["topk"]) * MOE_DOWN["Hd"] * \
+    MOE_DOWN["I_r"]
+
+
+class MoeDown:
+    """The MoE layer's down-projection side on the bench's routing (the step's MoE
+    call leaves it in its workspace): per-rank H_r [P, I_r] ~ N(0,1), W2_r
+    [E*I_r, Hd] ~ N(0,0.02), gates uniform and normalised per token, drawn on the
+    device from seeded generators (the weights alone are 3 GB)."""
+
+    def __init__(self, B, torch, wl):
+        c = MOE_DOWN
+        self.B, self.torch, self.wl = B, torch, wl
+        P = c["R"] * c["T_r"] * c["topk"]
+        g = torch.Generator(device="cuda")
+        self.H, self.W2 = [], []
+        for r in range(c["R"]):
+            g.manual_seed(4000 + r)
+            self.H.append(torch.randn(P, c["I_r"], generator=g, device="cuda").to(torch.bfloat16))
+            g.manual_seed(5000 + r)
+            self.W2.append((torch.randn(c["E"] * c["I_r"], c["Hd"], generator=g, device="cuda") * 0.02)
+                           .to(torch.bfloat16))
+        g.manual_seed(6000)
+        gates = torch.rand(c["R"] * c["T_r"], c["topk"], generator=g, device="cuda")
+        self.gates = (gates / gates.sum(dim=1, keepdim=True)).contiguous()
+        self.out = [torch.empty(c["T_r"], c["Hd"], dtype=torch.bfloat16, device="cuda") for _ in range(c["R"])]
+        nbytes = B.tl_moe_down_workspace_size(c["R"], c["T_r"], c["topk"], c["E"], c["Hd"])
+        self.work = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
+        self.sig = B.Signals(B.tl_moe_down_num_flags(c["R"], c["T_r"], c["topk"], c["E"], c["Hd"]))
+        self.epoch = 0
+
+    def run(self):
+        self.epoch += 1
+        self.B.tl_moe_down(self.H, self.W2, self.gates, self.wl.ws_moe, self.out, self.work, self.sig, self.epoch,
+                           topk=MOE_DOWN["topk"], E=MOE_DOWN["E"])
+
+    def check_status(self):
+        code, where = self.B.tl_query_status(self.sig)
+        if code:
+            raise RuntimeError(f"device error {code} at {where} in the MoE down projection")
+
+
 def main():
     args = parse()
     world, rank, local_rank = dist_env()
@@ -578,8 +623,13 @@ def main():
     wl = Workload(B, torch)
     stream = torch.cuda.current_stream()
     if args.only:
-        fn = {"ag": wl.ag, "rs": wl.rs, "moe": wl.moe}[args.only]
-        flops = {"ag": AG_FLOPS, "rs": RS_FLOPS, "moe": MOE_FLOPS}[args.only]
+        if args.only == "moe_down":
+            wl.moe()  # the routing the down projection reads
+            down = MoeDown(B, torch, wl)
+            fn, flops = down.run, MOE_DOWN_FLOPS
+        else:
+            fn = {"ag": wl.ag, "rs": wl.rs, "moe": wl.moe}[args.only]
+            flops = {"ag": AG_FLOPS, "rs": RS_FLOPS, "moe": MOE_FLOPS}[args.only]
         for _ in range(args.warmup):
             fn()
         barrier()
@@ -687,6 +737,16 @@ def main():
     }
     if not args.no_overlap:
         line["overlap"] = overlap_metrics(torch, B, wl)
+    if not args.no_extras:
+        # outside the step: the MoE layer's down-projection side on the step's routing
+        down = MoeDown(B, torch, wl)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        t = flushed_time_us(torch, down.run, flush, reps=5)
+        down.check_status()
+        line["extras"] = {"moe_down": {"us": t, "tflops": MOE_DOWN_FLOPS / (t * 1e-6) / 1e12, "config": MOE_DOWN,
+                                       "what": "grouped GEMM -> ReduceScatter over ranks -> gate-weighted "
+                                               "TopK-reduce -> scatter, one call (two launches)"}}
+        del down, flush
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, sample = time_oracle()
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",

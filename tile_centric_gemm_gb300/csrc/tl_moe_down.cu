@@ -13,7 +13,8 @@
 //    tiles come from a lookup table built from the routing.
 //
 // Launch 1, moe_down_kernel (CTA pairs, tcgen05.mma.cta_group::2): output tile
-// tau = (expert tile t of the routing's tile table, 256-column tile n), t-major;
+// tau = (expert tile t of the routing's tile table, 256-column tile n), column
+// tiles in groups of four with the tiles inside a group (weight panel reuse);
 // its R partials P_r = H_r[rows of t] . W2_r[expert slice, cols of n] are items
 // tau*R + j, rank r = (tau + j) mod R, taken round-robin by the CTA pairs.
 // Per CTA: warp 0 TMA producer, warp 1 MMA issuer (leader), warps 2-5 pushers
@@ -57,7 +58,7 @@ struct MdParams {
   const int32_t* ws;                // routing workspace: tile count, tile table
   uint64_t timeout_ns;
   uint64_t pipe_timeout_ns;
-  int32_t R, P, I_r, Hd, Nt, KB, max_tiles, max_items, slice_rows, ring_items, half_floats;
+  int32_t R, P, I_r, Hd, Nt, G, KB, max_tiles, max_items, slice_rows, ring_items, half_floats;
   uint32_t epoch;
 };
 
@@ -65,12 +66,18 @@ struct MdItem {
   int tau, t, n, r, j, e, row0, rows;
 };
 
-__device__ __forceinline__ MdItem md_item(const MdParams& p, int i) {
+// Output tile tau -> (expert tile t, column tile n): column tiles in groups of G,
+// every tile (in expert order) inside a group, the group's column tiles innermost,
+// so an expert's weight panels for a group are reused by all its tiles and a
+// tile's rows by the group's column tiles.
+__device__ __forceinline__ MdItem md_item(const MdParams& p, int i, int ntiles) {
   MdItem it;
   it.tau = i / p.R;
   it.j = i % p.R;
-  it.t = it.tau / p.Nt;
-  it.n = it.tau % p.Nt;
+  const int per_group = ntiles * p.G;
+  const int g = it.tau / per_group, rem = it.tau - g * per_group;
+  it.t = rem / p.G;
+  it.n = g * p.G + rem % p.G;
   it.r = (it.tau + it.j) % p.R;
   const int32_t* tr = p.ws + ws_tiles(p.max_tiles) + 6 * it.t;
   it.e = tr[0];
@@ -90,7 +97,8 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
   const int pair_id = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
   const uint32_t tmem_base = pair::setup(bars, warp);
   volatile uint32_t* abort = &bars->abort;
-  const int num_items = min(p.ws[0], p.max_tiles) * p.Nt * p.R;
+  const int ntiles = min(p.ws[0], p.max_tiles);
+  const int num_items = ntiles * p.Nt * p.R;
   const int my_items = pair_id < num_items ? (num_items - 1 - pair_id) / npairs + 1 : 0;
   uint32_t* arrived = p.flags;                         // 2*(tau*R + r) + h
   uint32_t* reduced = p.flags + 2 * size_t(p.max_items);  // 2*(tau*R + j) + h
@@ -100,7 +108,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
     if (lane == 0) {
       pair::Producer prod;
       for (int i = pair_id; i < num_items && !*abort; i += npairs) {
-        const MdItem it = md_item(p, i);
+        const MdItem it = md_item(p, i, ntiles);
         for (int kb = 0; kb < p.KB; ++kb)
           if (!prod.load(smem, bars, rank, &p.map_h[it.r], kb * pair::BK, it.row0 + h * pair::HM, &p.map_w[it.r],
                          it.n * pair::BN + h * pair::HN, it.e * p.I_r + kb * pair::BK, abort, p.status,
@@ -124,7 +132,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
     const size_t my_base = (size_t(my_slice) * 64 * p.slice_rows + my_row) * 4;
     int jj = 0;
     for (int i = pair_id; i < num_items; i += npairs, ++jj) {
-      const MdItem it = md_item(p, i);
+      const MdItem it = md_item(p, i, ntiles);
       const int acc = jj & 1;
       const uint32_t acc_ph = uint32_t(jj >> 1) & 1u;
       // slot free: the R reducers of this half of the tile that last used the slot are done with it
@@ -162,7 +170,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
     // ---------------------------------------------------------------- reducers (this CTA's half)
     const int et = (warp - kWarpRed0) * 32 + lane;
     for (int i = pair_id; i < num_items; i += npairs) {
-      const MdItem it = md_item(p, i);
+      const MdItem it = md_item(p, i, ntiles);
       // consume_tile_wait / peer_tile_wait: all R partials of this half have arrived
       if (lane == 0) {
         for (int r = 0; r < p.R; ++r) {
@@ -364,6 +372,7 @@ extern "C" tl_status tl_moe_down(const tl_moe_down_args* a, void* stream) {
     p->I_r = a->I_r;
     p->Hd = a->Hd;
     p->Nt = cdiv(a->Hd, pair::BN);
+    p->G = p->Nt % 4 == 0 ? 4 : (p->Nt % 2 == 0 ? 2 : 1);
     p->KB = cdiv(a->I_r, pair::BK);
     p->max_tiles = max_tiles;
     p->max_items = max_items;
