@@ -1,5 +1,6 @@
-"""Oracle for the tile-centric AllGather-GEMM, GEMM-ReduceScatter and MoE
-AllGather + grouped GEMM path.
+"""Oracle for the tile-centric AllGather-GEMM, GEMM-ReduceScatter, MoE
+(AllGather + grouped GEMM, and the down-projection side) and AllGather-KV
+attention path.
 
 TEST INFRASTRUCTURE ONLY.  A plain, slow CPU restatement of what the path
 computes, written from the TileLink talk summary ("TileLink: Generating
@@ -20,4 +21,4 @@ closed forms, invariants, hand-worked fixtures under ``tests/golden/`` and,
 for bf16 rounding, the float32 -> bfloat16 conversion of an independent
 library.
 """
-from . import bf16, ag_gemm, gemm_rs, moe  # noqa: F401
+from . import bf16, ag_gemm, gemm_rs, moe, attention  # noqa: F401

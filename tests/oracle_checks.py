@@ -7,6 +7,7 @@ loops, closed forms, invariants that a plausible mistake breaks, or the
 hand-worked fixtures in tests/golden/.
 """
 import itertools
+import math
 import json
 import os
 
@@ -377,3 +378,95 @@ def check_moe_down(moe_down, route):
         e = ids[t, 0]
         y = sum(Hf[r][i] @ Wf[r][e * I_r:(e + 1) * I_r] for r in range(R))
         np.testing.assert_allclose(o0[t], float(gates[t, 0]) * y, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------ AllGather-KV attention
+
+def check_ag_attention(attn, gather):
+    """Pins of the AllGather-KV attention oracle.
+
+    * the gather: explicit row copying, shards in rank order;
+    * non-causal, grouped heads: torch's scaled_dot_product_attention in
+      float64 on the CPU (an independent library routine; default scale and an
+      explicit one);
+    * closed forms: values constant per key/value head give that constant;
+      zero queries give the mean of the visible values and LSE = log(count);
+      the first query of rank 0 under the causal mask sees one key;
+    * the causal result of a query equals the non-causal result over the
+      gathered prefix up to its position;
+    * the Ring-Attention merge: the attention over all shards equals the
+      exp(lse_r - lse)-weighted sum of the per-shard results;
+    * the error scale sum_j softmax_j |v_j| is 1 when every |v| is 1.
+    """
+    import torch
+    import torch.nn.functional as F
+    rng = np.random.default_rng(29)
+    R, S, H, Hkv, D = 3, 5, 4, 2, 8
+    g = H // Hkv
+    dec = lambda b: (np.asarray(b, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+    Q = _rand_bits(rng, (S, H, D), -2, 2)
+    K = [_rand_bits(rng, (S, Hkv, D), -2, 2) for _ in range(R)]
+    V = [_rand_bits(rng, (S, Hkv, D), -4, 4) for _ in range(R)]
+    # gather by explicit copying
+    Kg = gather(K)
+    assert Kg.shape == (R * S, Hkv, D)
+    for r in range(R):
+        for u in range(S):
+            np.testing.assert_array_equal(Kg[r * S + u], K[r][u])
+    Kf, Vf = dec(gather(K)), dec(gather(V))
+    q_t = torch.from_numpy(dec(Q)).permute(1, 0, 2).contiguous()
+    k_t = torch.from_numpy(Kf).permute(1, 0, 2).contiguous()
+    v_t = torch.from_numpy(Vf).permute(1, 0, 2).contiguous()
+    for scale in (None, 0.3):
+        want = F.scaled_dot_product_attention(q_t, k_t, v_t, scale=scale, enable_gqa=True).permute(1, 0, 2).numpy()
+        for self_rank in (0, 2):
+            O, L, A = attn(Q, K, V, self_rank, scale=scale, causal=False)
+            np.testing.assert_allclose(O, want, rtol=1e-10, atol=1e-12)
+    # constant values per key/value head
+    c = np.array([[1.5] * D, [-0.25] * D])
+    Vc = [_bits(np.broadcast_to(c, (S, Hkv, D)).copy()) for _ in range(R)]
+    for causal in (False, True):
+        O, _, _ = attn(Q, K, Vc, 1, causal=causal)
+        for h in range(H):
+            np.testing.assert_allclose(O[:, h, :], np.broadcast_to(c[h // g], (S, D)), rtol=1e-13, atol=0)
+    # zero queries: uniform weights over the visible keys
+    Z = _bits(np.zeros((S, H, D), dtype=np.float32))
+    for causal in (False, True):
+        for self_rank in (0, 1, 2):
+            O, L, _ = attn(Z, K, V, self_rank, causal=causal)
+            for t in range(S):
+                n = (self_rank * S + t + 1) if causal else R * S
+                for h in range(H):
+                    want = sum(Vf[j, h // g] for j in range(n)) / n
+                    np.testing.assert_allclose(O[t, h], want, rtol=1e-12, atol=1e-13)
+                    assert abs(L[h, t] - math.log(n)) <= 1e-12, (causal, self_rank, t, h)
+    # first query of rank 0, causal: one visible key (K_0 row 0)
+    O, L, _ = attn(Q, K, V, 0, causal=True)
+    qf = dec(Q)
+    for h in range(H):
+        np.testing.assert_allclose(O[0, h], dec(V[0])[0, h // g], rtol=0, atol=0)
+        dot = 0.0
+        for e in range(D):
+            dot += qf[0, h, e] * dec(K[0])[0, h // g, e]
+        assert abs(L[h, 0] - dot / math.sqrt(D)) <= 1e-12
+    # causal = non-causal over the prefix up to the query's position
+    for self_rank in (1, 2):
+        O, L, _ = attn(Q, K, V, self_rank, causal=True)
+        for t in range(S):
+            n = self_rank * S + t + 1
+            Kp, Vp = [Kg[:n]], [gather(V)[:n]]
+            o1, l1, _ = attn(Q[t:t + 1], Kp, Vp, 0, causal=False)
+            np.testing.assert_allclose(O[t], o1[0], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(L[:, t], l1[:, 0], rtol=1e-12, atol=1e-13)
+    # Ring-Attention merge of per-shard results (pins LSE, including its scale)
+    for scale in (None, 0.7):
+        O, L, _ = attn(Q, K, V, 1, scale=scale, causal=False)
+        parts = [attn(Q, [K[r]], [V[r]], 0, scale=scale, causal=False) for r in range(R)]
+        lse = np.logaddexp.reduce(np.stack([p[1] for p in parts]), axis=0)
+        np.testing.assert_allclose(L, lse, rtol=1e-12, atol=1e-12)
+        merged = sum(np.exp(p[1] - lse).T[:, :, None] * p[0] for p in parts)
+        np.testing.assert_allclose(O, merged, rtol=1e-10, atol=1e-12)
+    # error scale with |v| = 1 everywhere
+    Vs = [_bits(np.where(rng.integers(0, 2, (S, Hkv, D)) == 1, 1.0, -1.0).astype(np.float32)) for _ in range(R)]
+    _, _, A = attn(Q, K, Vs, 2, causal=True)
+    np.testing.assert_allclose(A, 1.0, rtol=1e-13, atol=0)

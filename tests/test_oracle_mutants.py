@@ -204,3 +204,37 @@ def test_pins_catch_sorted_row_for_pair_index():
         finally:
             M.route = old_route
     _fails(C.check_moe_down, bad, M.route)
+
+
+def _mutated_attention(old, new):
+    """A copy of the attention oracle with one source substitution, loaded as a
+    fresh module (the oracle itself is untouched)."""
+    import importlib.util
+    import inspect
+    import types
+    src = inspect.getsource(oracle.attention)
+    assert src.count(old) == 1, old
+    mod = types.ModuleType("attention_mutant")
+    mod.__dict__["__package__"] = "oracle"
+    exec(compile(src.replace(old, new), "attention_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("old,new", [
+    ("o, lse, a = _attend(q[:, h, :], k[:, h // g, :], v[:, h // g, :], vis, scale)",
+     "o, lse, a = _attend(q[:, h, :], k[:, h % Hkv, :], v[:, h % Hkv, :], vis, scale)"),  # head grouping
+    ("s = (q_rows @ k.T) * scale", "s = (q_rows @ k.T)"),                                # dropped scale
+    ("return keys[None, :] <= pos[:, None]", "return keys[None, :] < pos[:, None]"),     # causal off by one
+    ("pos = self_rank * S_kv + np.asarray(t_rows)", "pos = np.asarray(t_rows)"),         # rank offset lost
+    ("lse = m + np.log(l)", "lse = np.log(l)"),                                          # LSE without the max
+    ("o = (w @ v) / l[:, None]", "o = (w @ v)"),                                         # no normalisation
+    ("for s in shards], axis=0)", "for s in shards[::-1]], axis=0)"),                    # reversed gather
+    ("o, lse, a = _attend(q[:, h, :], k[:, h // g, :], v[:, h // g, :], vis, scale)",
+     "o, lse, a = _attend(q[:, h, :], k[:, h // g, :], k[:, h // g, :], vis, scale)"),  # keys as values
+    ("a = (w @ np.abs(v)) / l[:, None]", "a = (w @ v) / l[:, None]"),                    # error scale signed
+    ("scale = 1.0 / math.sqrt(D)", "scale = 1.0 / D"),                                    # default scale
+])
+def test_pins_catch_attention_mistakes(old, new):
+    m = _mutated_attention(old, new)
+    with np.errstate(all="ignore"):
+        _fails(C.check_ag_attention, m.ag_kv_attention, m.gather)

@@ -149,3 +149,20 @@ def test_gemm_rs_partial_abs_sum_bounds_the_sum():
 
 def test_moe_down_pins():
     C.check_moe_down(oracle.moe.moe_down, oracle.moe.route)
+
+
+def test_ag_attention_pins():
+    C.check_ag_attention(oracle.attention.ag_kv_attention, oracle.attention.gather)
+
+
+def test_ag_attention_sampled_matches_full():
+    from tile_centric_gemm_gb300 import inputs
+    Q, K, V = inputs.ag_attention_inputs(R=3, S_shard=37, H=4, H_kv=2, D=16, seed=3)
+    for causal in (False, True):
+        O, L, A = oracle.attention.ag_kv_attention(Q, K, V, 1, causal=causal)
+        rows, heads = [0, 5, 36, 17], [0, 3, 1, 2]
+        o, l, a = oracle.attention.ag_kv_attention_at(Q, K, V, 1, rows, heads, causal=causal)
+        for i, (t, h) in enumerate(zip(rows, heads)):
+            np.testing.assert_allclose(o[i], O[t, h], rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(a[i], A[t, h], rtol=1e-12, atol=1e-14)
+            assert abs(l[i] - L[h, t]) <= 1e-12

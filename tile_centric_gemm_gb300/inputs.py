@@ -9,7 +9,9 @@ Conventions
 -----------
 * Every tensor is drawn from its own ``numpy.random.Generator(PCG64(seed))``.
   Seeds: shard r -> base+r; B (or B_r) -> base+1000(+r); expert weight W_e ->
-  base+2000+e; routing -> base+3000.  numpy's PCG64 bit stream is stable across
+  base+2000+e; routing -> base+3000; MoE down side -> base+4000..6000;
+  attention Q -> base+7000, K_r -> base+8000+r, V_r -> base+9000+r.
+  numpy's PCG64 bit stream is stable across
   platforms, so x86 and aarch64 hosts draw identical inputs.
 * Values are drawn in float32 and rounded to bfloat16 with round-to-nearest-even
   (the packing step of the bfloat16 storage format: keep the top 16 bits of the
@@ -28,7 +30,7 @@ import numpy as np
 __all__ = [
     "CONFIGS", "bf16_bits_from_f32", "uniform_bf16", "normal_bf16",
     "ag_gemm_inputs", "gemm_rs_inputs", "moe_inputs", "zipf_topk",
-    "to_torch_bf16",
+    "to_torch_bf16", "moe_down_inputs", "ag_attention_inputs",
 ]
 
 # The five workloads (shapes, value distributions).  Names describe the workload.
@@ -127,3 +129,14 @@ def moe_down_inputs(R: int, T_r: int, topk: int, E: int, I_r: int, Hd: int, seed
     g = np.random.Generator(np.random.PCG64(seed + 6000)).uniform(0.0, 1.0, (R * T_r, topk)).astype(np.float32)
     gates = (g / g.sum(axis=1, keepdims=True)).astype(np.float32)
     return H, W2, gates
+
+
+def ag_attention_inputs(R: int, S_shard: int, H: int, H_kv: int, D: int = 128, seed: int = 0):
+    """Sequence-parallel attention inputs: this rank's queries Q [S_shard, H, D]
+    and every rank's keys and values K_r, V_r [S_shard, H_kv, D], all N(0,1)
+    bf16 bits (unit-variance activations after the projections).  Seeds: Q ->
+    base+7000, K_r -> base+8000+r, V_r -> base+9000+r."""
+    Q = normal_bf16((S_shard, H, D), seed + 7000)
+    K = [normal_bf16((S_shard, H_kv, D), seed + 8000 + r) for r in range(R)]
+    V = [normal_bf16((S_shard, H_kv, D), seed + 9000 + r) for r in range(R)]
+    return Q, K, V
