@@ -52,7 +52,7 @@ WORKLOAD = ("AG-GEMM R=8 [8192x4096]x[4096x1792] + GEMM-RS R=8 8x[8192x1792]x[17
 # sources hash to what was captured.
 RS_TRAFFIC_BYTES = 3_134_247_168 + 1_101_220_608
 RS_TRAFFIC_SOURCES = ("tl_gemm_rs.cu", "tl_pair.cuh", "tl_common.cuh", "tl_ptx.cuh")
-RS_TRAFFIC_SHA256 = "474002386a3515a8daa3e843a12abd2b9160c7bf8a38264e52534cf283cf180e"
+RS_TRAFFIC_SHA256 = "7708242702455653f22cbe5377b45ddb7f42d9d563826e988f86049295a141bc"
 
 
 def rs_traffic():

@@ -422,6 +422,63 @@ size_t tl_moe_down_workspace_size(int R, int T_r, int topk, int E, int Hd);
 int tl_moe_down_num_flags(int R, int T_r, int topk, int E, int Hd);
 tl_status tl_moe_down(const tl_moe_down_args* args, void* stream);
 
+/* ---------------------------------------------------------------- AllGather-KV attention
+ * Sequence-parallel attention with the key/value AllGather overlapped with the
+ * attention that consumes it (talk summary, Key Findings and Experimental Setup
+ * & Results: attention layers, AllGather-KV against Ring Attention).  Rank
+ * `self_rank` holds the queries Q of its S_shard tokens; every rank r holds the
+ * keys K_r and values V_r of its own tokens.  With Kg, Vg the shards gathered in
+ * rank order (token self_rank*S_shard + t is query t's global position), for
+ * every query t and head h, with kv head hk = h / (H / H_kv):
+ *   s_j   = scale * <Q[t, h], Kg[j, hk]>        over the visible keys j
+ *           (all keys; causal: j <= self_rank*S_shard + t)
+ *   O[t, h] = bf16( sum_j exp(s_j - lse) Vg[j, hk] ),  lse[h, t] = log sum_j exp(s_j)
+ * One launch on pairs of CTAs (cta_group::2):
+ *  - producer: a copy warp per CTA moves the peers' key and value shards, 128
+ *    tokens at a time, into K_gathered / V_gathered (bulk TMA copies; plain
+ *    loads for pinned-host shards) and releases one flag per chunk of each
+ *    (produce_tile_notify), shards self+1, ..., self+R-1, then self;
+ *  - consumer: work units of one head and 512 query rows (two 256-row tiles
+ *    that share every key/value tile); each unit streams its own shard's keys
+ *    and values first (in place, no wait), then the peers' in copy order,
+ *    acquiring each chunk's flags before loading it (consume_tile_wait).
+ *    S = Q K^T and O += P V run on the tensor cores with S and O in tensor
+ *    memory; the online softmax (running max, rescaling of O only when the max
+ *    grows by more than 2^8) runs in between on the CTAs' softmax warps.
+ * The result does not depend on the copy order or the schedule; it is one
+ * evaluation of the formula above with P rounded to bf16 for the P V product.
+ * Flags: K chunk (r, c) uses flag r * ceil(S_shard/128) + c, V chunk the same
+ * id plus R * ceil(S_shard/128).
+ * Limits: head_dim = 128; R <= TL_MAX_RANKS; H % H_kv == 0; the self shards and
+ * Q, O, K_gathered, V_gathered must be device memory; peer shards device or
+ * pinned host memory.
+ */
+typedef struct tl_ag_attn_args {
+  int32_t R;                   /* ranks, 1..TL_MAX_RANKS */
+  int32_t self_rank;           /* 0..R-1 */
+  int32_t S_shard;             /* tokens per rank, >= 1 */
+  int32_t H;                   /* query heads, >= 1 */
+  int32_t H_kv;                /* key/value heads, divides H */
+  int32_t head_dim;            /* 128 */
+  int32_t causal;              /* 0 = every key, 1 = keys at or before the query's position */
+  float scale;                 /* softmax scale; 0 = 1/sqrt(head_dim) */
+  const void* Q;               /* device bf16 [S_shard, H, head_dim] */
+  const void* const* K_shards; /* host array of R pointers, bf16 [S_shard, H_kv, head_dim] */
+  const void* const* V_shards; /* host array of R pointers, bf16 [S_shard, H_kv, head_dim] */
+  void* K_gathered;            /* device bf16 [R*S_shard, H_kv, head_dim], written */
+  void* V_gathered;            /* device bf16 [R*S_shard, H_kv, head_dim], written */
+  void* O;                     /* device bf16 [S_shard, H, head_dim], written */
+  float* lse;                  /* optional device float [H, S_shard] (natural log), written; NULL = none */
+  tl_signals* signals;         /* >= tl_ag_attn_num_flags(R, S_shard) flags */
+  uint32_t epoch;              /* nonzero */
+  uint32_t reserved0;
+  uint64_t timeout_ns;         /* 0 = 1 s */
+} tl_ag_attn_args;
+
+/* Flags an AllGather-KV attention call needs: 2 * R * ceil(S_shard / 128). */
+int tl_ag_attn_num_flags(int R, int S_shard);
+tl_status tl_ag_attn(const tl_ag_attn_args* args, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

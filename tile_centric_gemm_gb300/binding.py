@@ -33,6 +33,7 @@ EXPORTED = [
     "tl_gemm_rs_workspace_size", "tl_gemm_rs_num_flags", "tl_gemm_rs", "tl_gemm_rs_noalloc",
     "tl_moe_workspace_size", "tl_moe_num_flags", "tl_moe_ag_gemm", "tl_allgather", "tl_reduce_scatter",
     "tl_moe_down_workspace_size", "tl_moe_down_num_flags", "tl_moe_down",
+    "tl_ag_attn_num_flags", "tl_ag_attn",
 ]
 
 
@@ -54,6 +55,17 @@ class tl_ag_gemm_args(ctypes.Structure):
         ("signals", _vp), ("src_ready", _vp),
         ("epoch", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
         ("timeout_ns", ctypes.c_uint64), ("trace", _vp),
+    ]
+
+
+class tl_ag_attn_args(ctypes.Structure):
+    _fields_ = [
+        ("R", ctypes.c_int32), ("self_rank", ctypes.c_int32), ("S_shard", ctypes.c_int32),
+        ("H", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("causal", ctypes.c_int32), ("scale", ctypes.c_float),
+        ("Q", _vp), ("K_shards", ctypes.POINTER(_vp)), ("V_shards", ctypes.POINTER(_vp)),
+        ("K_gathered", _vp), ("V_gathered", _vp), ("O", _vp), ("lse", _vp), ("signals", _vp),
+        ("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32), ("timeout_ns", ctypes.c_uint64),
     ]
 
 
@@ -144,6 +156,8 @@ _decl("tl_moe_num_flags", _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i))
 _decl("tl_moe_ag_gemm", _i, ctypes.POINTER(tl_moe_args), _vp)
 _decl("tl_allgather", _i, ctypes.POINTER(tl_allgather_args), _vp)
 _decl("tl_reduce_scatter", _i, ctypes.POINTER(tl_reduce_scatter_args), _vp)
+_decl("tl_ag_attn_num_flags", _i, _i, _i)
+_decl("tl_ag_attn", _i, ctypes.POINTER(tl_ag_attn_args), _vp)
 
 
 def _check(code):
@@ -398,3 +412,25 @@ def tl_moe_down(H, W2, gates, routing, out, workspace, signals: Signals, epoch: 
                          workspace_bytes=workspace.numel() * workspace.element_size(), signals=signals.handle,
                          epoch=int(epoch) & 0xFFFFFFFF, reserved0=0, timeout_ns=int(timeout_ns))
     _check(lib.tl_moe_down(ctypes.byref(a), _stream(stream)))
+
+
+def tl_ag_attn_num_flags(R, S_shard):
+    return int(lib.tl_ag_attn_num_flags(R, S_shard))
+
+
+def tl_ag_attn(Q, K_shards, V_shards, K_gathered, V_gathered, O, signals: Signals, epoch: int, *, self_rank=0,
+               causal=False, scale=0.0, lse=None, timeout_ns=0, stream=None):
+    """O = softmax(scale Q Kg^T) Vg per head over the gathered key/value shards,
+    K_gathered / V_gathered written (see tilelink.h).  Q [S_shard, H, D],
+    K_r / V_r [S_shard, H_kv, D], lse optional float [H, S_shard]."""
+    R = len(K_shards)
+    S_shard, H, D = Q.shape
+    H_kv = K_shards[0].shape[1]
+    pk, pv = _ptr_array(K_shards), _ptr_array(V_shards)
+    a = tl_ag_attn_args(R=R, self_rank=self_rank, S_shard=S_shard, H=H, H_kv=H_kv, head_dim=D,
+                        causal=int(bool(causal)), scale=float(scale), Q=_ptr(Q),
+                        K_shards=ctypes.cast(pk, ctypes.POINTER(_vp)), V_shards=ctypes.cast(pv, ctypes.POINTER(_vp)),
+                        K_gathered=_ptr(K_gathered), V_gathered=_ptr(V_gathered), O=_ptr(O), lse=_ptr(lse),
+                        signals=signals.handle, epoch=int(epoch) & 0xFFFFFFFF, reserved0=0,
+                        timeout_ns=int(timeout_ns))
+    _check(lib.tl_ag_attn(ctypes.byref(a), _stream(stream)))

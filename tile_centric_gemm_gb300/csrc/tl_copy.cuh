@@ -50,77 +50,87 @@ __device__ __forceinline__ void copy_rows_plain(const uint8_t* src, uint8_t* dst
   }
 }
 
+// Copy item `it` of the job (shard (self + 1 + it / bpr) mod R, row chunk
+// it % bpr) into the gathered buffer and release its flag.  Called by all 32
+// lanes of one warp.  `stage` holds NBUF buffers of COPY_CHUNK bytes; `bars`
+// NBUF mbarriers initialised with count 1; `seq` (lane 0's count of chunks
+// staged so far: buffer seq % NBUF, parity (seq / NBUF) & 1) carries the
+// staging ring's state from one call to the next.  Returns true (on every
+// lane) if a pipeline wait gave up.
+template <int NBUF = COPY_NBUF>
+__device__ __forceinline__ bool ag_copy_one(const AgCopyJob& j, int it, uint8_t* stage, uint64_t* bars,
+                                            volatile uint32_t* abort, uint32_t& seq) {
+  static_assert(NBUF >= 1 && NBUF <= COPY_NBUF, "staging buffers");
+  const int lane = int(lane_id());
+  const int jj = it / j.bpr, b = it % j.bpr;
+  const int r = (j.self + 1 + jj) % j.R;
+  const int lo = b * j.rpb;
+  const int rows = min(j.rpb, j.M_shard - lo);
+  const uint8_t* src = j.shard[r] + size_t(lo) * j.K * 2;
+  uint8_t* dst = j.gathered + (size_t(r) * j.M_shard + lo) * size_t(j.K) * 2;
+  const uint32_t bytes = uint32_t(rows) * uint32_t(j.K) * 2u;
+  const int flag_id = r * j.bpr + b;
+  // pull mode: the source publishes readiness first (first barrier of the pull protocol);
+  // a chunk whose source never became ready is neither copied nor announced
+  bool ready = true;
+  if (j.ready && lane == 0)
+    ready = wait_flag(j.ready + flag_id, j.epoch, j.status, j.timeout_ns, uint32_t(flag_id), TL_ERR_TIMEOUT);
+  if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
+  if ((j.host_mask >> r) & 1ull) {
+    copy_rows_plain(src, dst, bytes, lane);
+    // produce_tile_notify: every lane's stores are ordered before lane 0's release
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) st_release(j.flags + flag_id, j.epoch);
+    return false;
+  }
+  bool dead = false;
+  if (lane == 0) {
+    const int nch = int((bytes + COPY_CHUNK - 1) / COPY_CHUNK);
+    int issued = 0, stored = 0;
+    while (stored < nch) {
+      while (issued < nch && issued - stored < NBUF) {
+        const uint32_t q = seq + uint32_t(issued);
+        const int buf = int(q % NBUF);
+        // the store that last read `buf` (chunk q - NBUF) must have finished reading it
+        bulk_wait_read_dyn(stored - issued + NBUF - 1);
+        const uint32_t off = uint32_t(issued) * COPY_CHUNK;
+        const uint32_t sz = min(COPY_CHUNK, bytes - off);
+        mbar_arrive_expect_tx(&bars[buf], sz);
+        bulk_g2s(stage + buf * COPY_CHUNK, src + off, sz, &bars[buf]);
+        ++issued;
+      }
+      const uint32_t q = seq + uint32_t(stored);
+      const int buf = int(q % NBUF);
+      if (!mbar_wait(&bars[buf], (q / NBUF) & 1u, abort, j.status, j.pipe_timeout_ns, 5)) {
+        dead = true;
+        break;
+      }
+      const uint32_t off = uint32_t(stored) * COPY_CHUNK;
+      bulk_s2g(dst + off, stage + buf * COPY_CHUNK, min(COPY_CHUNK, bytes - off));
+      bulk_commit();
+      ++stored;
+    }
+    seq += uint32_t(nch);
+    // produce_tile_notify: writes complete -> order with the generic proxy -> release
+    bulk_wait<0>();
+    if (!dead) {
+      fence_proxy_async_global();
+      st_release(j.flags + flag_id, j.epoch);
+    }
+  }
+  return __shfl_sync(0xffffffffu, dead, 0);
+}
+
 // Items first, first + stride, ... in copy order: shards self+1, ..., self+R-1,
-// then self; chunks ascending.  Called by all 32 lanes of one warp.  `stage`
-// holds NBUF buffers of COPY_CHUNK bytes; `bars` NBUF mbarriers initialised
-// with count 1.
+// then self; chunks ascending.  Called by all 32 lanes of one warp.
 template <int NBUF = COPY_NBUF>
 __device__ __forceinline__ void ag_copy_items(const AgCopyJob& j, uint8_t* stage, uint64_t* bars,
                                               volatile uint32_t* abort, int first, int stride) {
-  static_assert(NBUF >= 1 && NBUF <= COPY_NBUF, "staging buffers");
-  const int lane = int(lane_id());
-  uint32_t seq = 0;  // lane 0: chunks loaded so far: buffer seq % NBUF, parity (seq / NBUF) & 1
-  for (int it = first; it < j.num_items; it += stride) {
-    const int jj = it / j.bpr, b = it % j.bpr;
-    const int r = (j.self + 1 + jj) % j.R;
-    const int lo = b * j.rpb;
-    const int rows = min(j.rpb, j.M_shard - lo);
-    const uint8_t* src = j.shard[r] + size_t(lo) * j.K * 2;
-    uint8_t* dst = j.gathered + (size_t(r) * j.M_shard + lo) * size_t(j.K) * 2;
-    const uint32_t bytes = uint32_t(rows) * uint32_t(j.K) * 2u;
-    const int flag_id = r * j.bpr + b;
-    // pull mode: the source publishes readiness first (first barrier of the pull protocol);
-    // a chunk whose source never became ready is neither copied nor announced
-    bool ready = true;
-    if (j.ready && lane == 0)
-      ready = wait_flag(j.ready + flag_id, j.epoch, j.status, j.timeout_ns, uint32_t(flag_id), TL_ERR_TIMEOUT);
-    if (!__shfl_sync(0xffffffffu, ready, 0)) continue;
-    if ((j.host_mask >> r) & 1ull) {
-      copy_rows_plain(src, dst, bytes, lane);
-      // produce_tile_notify: every lane's stores are ordered before lane 0's release
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) st_release(j.flags + flag_id, j.epoch);
-      continue;
-    }
-    bool dead = false;
-    if (lane == 0) {
-      const int nch = int((bytes + COPY_CHUNK - 1) / COPY_CHUNK);
-      int issued = 0, stored = 0;
-      while (stored < nch) {
-        while (issued < nch && issued - stored < NBUF) {
-          const uint32_t q = seq + uint32_t(issued);
-          const int buf = int(q % NBUF);
-          // the store that last read `buf` (chunk q - NBUF) must have finished reading it
-          bulk_wait_read_dyn(stored - issued + NBUF - 1);
-          const uint32_t off = uint32_t(issued) * COPY_CHUNK;
-          const uint32_t sz = min(COPY_CHUNK, bytes - off);
-          mbar_arrive_expect_tx(&bars[buf], sz);
-          bulk_g2s(stage + buf * COPY_CHUNK, src + off, sz, &bars[buf]);
-          ++issued;
-        }
-        const uint32_t q = seq + uint32_t(stored);
-        const int buf = int(q % NBUF);
-        if (!mbar_wait(&bars[buf], (q / NBUF) & 1u, abort, j.status, j.pipe_timeout_ns, 5)) {
-          dead = true;
-          break;
-        }
-        const uint32_t off = uint32_t(stored) * COPY_CHUNK;
-        bulk_s2g(dst + off, stage + buf * COPY_CHUNK, min(COPY_CHUNK, bytes - off));
-        bulk_commit();
-        ++stored;
-      }
-      seq += uint32_t(nch);
-      // produce_tile_notify: writes complete -> order with the generic proxy -> release
-      bulk_wait<0>();
-      if (!dead) {
-        fence_proxy_async_global();
-        st_release(j.flags + flag_id, j.epoch);
-      }
-    }
-    if (__shfl_sync(0xffffffffu, dead, 0)) break;
-  }
-  if (lane == 0) bulk_wait<0>();
+  uint32_t seq = 0;
+  for (int it = first; it < j.num_items; it += stride)
+    if (ag_copy_one<NBUF>(j, it, stage, bars, abort, seq)) break;
+  if (lane_id() == 0) bulk_wait<0>();
   __syncwarp();
 }
 

@@ -107,6 +107,32 @@ tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint6
   return TL_OK;
 }
 
+tl_status make_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t planes, uint64_t rows, uint64_t cols,
+                           uint64_t row_pitch_bytes, uint64_t plane_pitch_bytes, uint32_t box_rows,
+                           uint32_t box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return fail(TL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cudaPointerAttributes at{};
+  int dev = -1;
+  if (cudaPointerGetAttributes(&at, base) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(TL_ERR_UNSUPPORTED, "tensor operand %p is not memory the device can address", base);
+  }
+  if (at.type != cudaMemoryTypeDevice || at.device != dev)
+    return fail(TL_ERR_UNSUPPORTED, "tensor operand %p must be device memory of device %d (TMA-loaded)", base, dev);
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {row_pitch_bytes, plane_pitch_bytes};
+  cuuint32_t box[3] = {box_cols, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(TL_ERR_INVALID, "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu x %llu]", int(r),
+                (unsigned long long)planes, (unsigned long long)rows, (unsigned long long)cols);
+  return TL_OK;
+}
+
 tl_status classify_shards(const char* who, const void* const* shards, int R, int device, const uint8_t** dev,
                           uint64_t* host_mask) {
   *host_mask = 0;

@@ -41,6 +41,14 @@ tl_status make_map_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint6
                         uint64_t row_pitch_bytes, uint32_t box_rows, uint32_t box_cols,
                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B);
 
+// 3-D bf16 tensor map over `planes` stacked row-major [rows, cols] matrices
+// (plane pitch in bytes); box = box_rows x box_cols elements of one plane,
+// 128-byte swizzle.  Rows past `rows` read as zero, so a box never reaches
+// into the next plane.
+tl_status make_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t planes, uint64_t rows, uint64_t cols,
+                           uint64_t row_pitch_bytes, uint64_t plane_pitch_bytes, uint32_t box_rows,
+                           uint32_t box_cols);
+
 // Launch a grid whose CTAs must all be resident at once: a cooperative launch
 // for single CTAs, a cluster launch sized within the device's resident-cluster
 // capacity for clusters of `cluster` CTAs.  Fails instead of launching when the
