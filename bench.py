@@ -78,7 +78,7 @@ def parse():
                     help="AG-GEMM sweep (R in {2,4,8}, M in {1024..16384}, K=8192, N=1024; shards in HBM and "
                          "peer shards in pinned host memory): copy, GEMM, sequential and fused times, one JSON line")
     ap.add_argument("--no-extras", action="store_true", help="skip the measurements outside the step")
-    ap.add_argument("--only", choices=["ag", "rs", "moe", "moe_down"],
+    ap.add_argument("--only", choices=["ag", "rs", "moe", "moe_down", "ag_attn"],
                     help="run one fused call of the step (W untimed, then K timed back to back) and print its "
                          "device time; for profiling a single kernel on the bench's workload")
     return ap.parse_args()
@@ -590,6 +590,103 @@ class MoeDown:
             raise RuntimeError(f"device error {code} at {where} in the MoE down projection")
 
 
+# AllGather-KV attention (sequence parallel): 8 ranks x 8192 tokens (a 64K context), 32 query heads
+# over 8 key/value heads, head dim 128; rank 0's view (every rank does the same work when not causal)
+AG_ATTN = dict(R=8, S_shard=8192, H=32, H_kv=8, D=128)
+
+
+def attn_flops(c, causal, self_rank):
+    """4 * D flops per visible (query, key) pair and head (S = Q K^T and O = P V)."""
+    S = c["S_shard"]
+    pairs = S * (self_rank * S) + S * (S + 1) // 2 if causal else S * c["R"] * S
+    return 4 * c["D"] * c["H"] * pairs
+
+
+class AgAttn:
+    """AllGather-KV attention on the device: Q [S, H, D], K_r / V_r [S, H_kv, D]
+    ~ N(0,1), drawn on the device from seeded generators."""
+
+    def __init__(self, B, torch):
+        c = AG_ATTN
+        self.B, self.torch = B, torch
+        g = torch.Generator(device="cuda")
+        g.manual_seed(7000)
+        self.Q = torch.randn(c["S_shard"], c["H"], c["D"], generator=g, device="cuda").to(torch.bfloat16)
+        self.K, self.V = [], []
+        for r in range(c["R"]):
+            g.manual_seed(8000 + r)
+            self.K.append(torch.randn(c["S_shard"], c["H_kv"], c["D"], generator=g, device="cuda").to(torch.bfloat16))
+            g.manual_seed(9000 + r)
+            self.V.append(torch.randn(c["S_shard"], c["H_kv"], c["D"], generator=g, device="cuda").to(torch.bfloat16))
+        self.Kg = torch.empty(c["R"] * c["S_shard"], c["H_kv"], c["D"], dtype=torch.bfloat16, device="cuda")
+        self.Vg = torch.empty_like(self.Kg)
+        self.O = torch.empty(c["S_shard"], c["H"], c["D"], dtype=torch.bfloat16, device="cuda")
+        self.L = torch.empty(c["H"], c["S_shard"], dtype=torch.float32, device="cuda")
+        self.sig = B.Signals(B.tl_ag_attn_num_flags(c["R"], c["S_shard"]))
+        self.sig_ag = B.Signals(B.tl_ag_gemm_num_flags(c["R"], c["S_shard"], c["H_kv"] * c["D"], 0)[0])
+        self.epoch = 0
+
+    def run(self, causal=False, self_rank=0):
+        self.epoch += 1
+        self.B.tl_ag_attn(self.Q, self.K, self.V, self.Kg, self.Vg, self.O, self.sig, self.epoch,
+                          self_rank=self_rank, causal=causal, lse=self.L)
+
+    def copy_only(self):
+        """The key and value AllGathers alone (the stand-alone AllGather, two calls)."""
+        c = AG_ATTN
+        flat = lambda ts: [t.view(c["S_shard"], c["H_kv"] * c["D"]) for t in ts]
+        self.epoch += 1
+        self.B.tl_allgather(flat(self.K), self.Kg.view(-1, c["H_kv"] * c["D"]), self.sig_ag, self.epoch)
+        self.epoch += 1
+        self.B.tl_allgather(flat(self.V), self.Vg.view(-1, c["H_kv"] * c["D"]), self.sig_ag, self.epoch)
+
+    def torch_decomposed(self):
+        """torch: gather by concatenation, then scaled_dot_product_attention with grouped heads."""
+        F = self.torch.nn.functional
+        q = self.Q.permute(1, 0, 2).unsqueeze(0)
+        k = self.torch.cat(self.K).permute(1, 0, 2).unsqueeze(0)
+        v = self.torch.cat(self.V).permute(1, 0, 2).unsqueeze(0)
+        return F.scaled_dot_product_attention(q, k, v, enable_gqa=True)
+
+    def check_status(self):
+        for s in (self.sig, self.sig_ag):
+            code, where = self.B.tl_query_status(s)
+            if code:
+                raise RuntimeError(f"device error {code} at {where} in the AllGather-KV attention")
+
+
+def attn_extras(torch, B, peaks, peak_src):
+    a = AgAttn(B, torch)
+    c = AG_ATTN
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    out = {"config": c, "what": "AllGather of the key/value shards fused with the attention over them, one launch; "
+                                "flops = 4 * D * H * visible (query, key) pairs",
+           "peak_tflops": peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16 burst"}
+    for name, causal, self_rank in (("full", False, 0), ("causal_last_rank", True, c["R"] - 1),
+                                    ("causal_middle_rank", True, c["R"] // 2 - 1)):
+        t = flushed_time_us(torch, lambda: a.run(causal, self_rank), flush, reps=5)
+        fl = attn_flops(c, causal, self_rank)
+        out[name] = {"us": t, "tflops": fl / (t * 1e-6) / 1e12, "self_rank": self_rank, "causal": causal,
+                     "frac": fl / (t * 1e-6) / 1e12 / peaks["bf16_tflops"]}
+    a.check_status()
+    t_copy = flushed_time_us(torch, a.copy_only, flush, reps=5)
+    a.check_status()
+    kv_bytes = 2 * c["R"] * c["S_shard"] * c["H_kv"] * c["D"] * 2
+    out["copy_only"] = {"us": t_copy, "gbs": 2 * kv_bytes / (t_copy * 1e-6) / 1e9,
+                        "what": "tl_allgather of K then V (read + write bytes / time)"}
+    try:
+        t_torch = flushed_time_us(torch, a.torch_decomposed, flush, reps=3)
+        fl = attn_flops(c, False, 0)
+        out["torch_cat_sdpa"] = {"us": t_torch, "tflops": fl / (t_torch * 1e-6) / 1e12,
+                                 "speedup_of_fused": t_torch / out["full"]["us"]}
+    except Exception as ex:  # a torch build without a fused attention for this device
+        out["torch_cat_sdpa"] = {"unavailable": str(ex).splitlines()[0][:200]}
+    # the copy runs inside the fused launch; alone it would add this much to a copy-then-attend schedule
+    out["copy_frac_of_fused"] = t_copy / out["full"]["us"]
+    del a, flush
+    return out
+
+
 def main():
     args = parse()
     world, rank, local_rank = dist_env()
@@ -627,6 +724,9 @@ def main():
             wl.moe()  # the routing the down projection reads
             down = MoeDown(B, torch, wl)
             fn, flops = down.run, MOE_DOWN_FLOPS
+        elif args.only == "ag_attn":
+            attn = AgAttn(B, torch)
+            fn, flops = attn.run, attn_flops(AG_ATTN, False, 0)
         else:
             fn = {"ag": wl.ag, "rs": wl.rs, "moe": wl.moe}[args.only]
             flops = {"ag": AG_FLOPS, "rs": RS_FLOPS, "moe": MOE_FLOPS}[args.only]
@@ -747,6 +847,7 @@ def main():
                                        "what": "grouped GEMM -> ReduceScatter over ranks -> gate-weighted "
                                                "TopK-reduce -> scatter, one call (two launches)"}}
         del down, flush
+        line["extras"]["ag_attn"] = attn_extras(torch, B, peaks, peak_src)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, sample = time_oracle()
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",

@@ -162,6 +162,12 @@ __device__ __forceinline__ void issue_pv(uint8_t* smem, int X, int vs, uint32_t 
   }
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank) {
   if (rank == 0) mbar_arrive(bar);
   else mbar_arrive_cluster(map_to_rank(bar, 0));
@@ -403,11 +409,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i >= lim) v[c][i] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // row max in eight independent chains (a single chain would serialise 128 dependent maxima)
+        float mq[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t* x = &v[q >> 1][(q & 1) * 16];
+          float a = fmax3(__uint_as_float(x[0]), __uint_as_float(x[1]), __uint_as_float(x[2]));
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(v[c][i]));
+          for (int i = 3; i < 15; i += 2) a = fmax3(a, __uint_as_float(x[i]), __uint_as_float(x[i + 1]));
+          mq[q] = fmaxf(a, __uint_as_float(x[15]));
+        }
+        const float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]), fmax3(fmax3(mq[3], mq[4], mq[5]), mq[6], mq[7]));
         const float mnew = fmaxf(m, mx * p.scale_log2);
         const bool resc = mnew > m + kRescaleLog2;
         float alpha = 1.0f;
@@ -417,7 +429,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
           l *= alpha;
         }
         const float neg_m = (m == -INFINITY) ? 0.0f : -m;
-        float sum = 0.0f;
+        float sq[8];  // eight partial row sums
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sq[q] = 0.0f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -427,7 +441,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
             for (int e = 0; e < 4; ++e) {
               const float p0 = ex2_approx(fmaf(__uint_as_float(v[c][k * 8 + 2 * e]), p.scale_log2, neg_m));
               const float p1 = ex2_approx(fmaf(__uint_as_float(v[c][k * 8 + 2 * e + 1]), p.scale_log2, neg_m));
-              sum += p0 + p1;
+              sq[(k & 1) * 4 + e] += p0 + p1;
               w[e] = pack_bf16x2(p0, p1);
             }
             const uint32_t chunk = uint32_t(c * 4 + k);  // 16-byte chunk of the row: keys 8*chunk..
@@ -435,7 +449,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
             st_shared_v4(addr, w[0], w[1], w[2], w[3]);
           }
         }
-        l += sum;
+        l += ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
