@@ -89,6 +89,16 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(pg, x):
+    """The slowest rank's time: all-reduce MAX over the process group (None = one rank)."""
+    if pg is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t[0])
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -779,10 +789,7 @@ def main():
     rs_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     moe_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
     ms_per_step = total_ms / K
-    if pg:
-        t = torch.tensor([ms_per_step])
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms_per_step = float(t[0])
+    ms_per_step = max_over_ranks(pg, ms_per_step)
     step_flops = AG_FLOPS + RS_FLOPS + MOE_FLOPS
     value = world * step_flops / (ms_per_step * 1e-3) / 1e12
 
@@ -803,10 +810,7 @@ def main():
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / E
-    if pg:
-        t = torch.tensor([e2e_ms])
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    e2e_ms = max_over_ranks(pg, e2e_ms)
     wl.check_status()
 
     rs_avg = statistics.mean(rs_ms)
