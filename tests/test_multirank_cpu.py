@@ -34,7 +34,7 @@ def test_max_over_ranks_gloo_two_ranks():
     import torch.multiprocessing as mp
     port = _free_port()
     values = [3.25, 7.5]
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_max_worker, args=(2, port, values, out), nprocs=2, join=True)
         assert dict(out) == {0: 7.5, 1: 7.5}
