@@ -279,35 +279,47 @@ class Workload:
         self.h_C = torch.empty_like(self.C, device="cpu").pin_memory()
         self.h_out = [torch.empty_like(o, device="cpu").pin_memory() for o in self.out]
         self.h_Y = torch.empty_like(self.Y, device="cpu").pin_memory()
+        # set 0 = the tensors above; set 1 = a second copy of every input and of every
+        # output read back, so that the end-to-end loop can copy one step's inputs in
+        # while the previous step computes and its outputs go out
+        self.sets = [dict(ag=self.d_ag, rs=self.d_rs, moe=self.d_moe, C=self.C, out=self.out, Y=self.Y),
+                     dict(ag=[torch.empty_like(t) for t in self.d_ag], rs=[torch.empty_like(t) for t in self.d_rs],
+                          moe=[torch.empty_like(t) for t in self.d_moe], C=torch.empty_like(self.C),
+                          out=[torch.empty_like(o) for o in self.out], Y=torch.empty_like(self.Y))]
         self.epoch = 0
         self.launches_per_step = 4  # ag_gemm, gemm_rs, moe route, moe gemm
 
-    def ag(self):
+    def ag(self, b=0):
         self.epoch += 1
         R = AG["R"]
-        self.B.tl_ag_gemm(self.d_ag[:R], self.d_ag[R], self.G, self.C, self.sig_ag, self.epoch)
+        d = self.sets[b]
+        self.B.tl_ag_gemm(d["ag"][:R], d["ag"][R], self.G, d["C"], self.sig_ag, self.epoch)
 
-    def rs(self):
+    def rs(self, b=0):
         self.epoch += 1
         R = RS["R"]
-        self.B.tl_gemm_rs(self.d_rs[:R], self.d_rs[R:], self.out, self.ws, self.sig_rs, self.epoch)
+        d = self.sets[b]
+        self.B.tl_gemm_rs(d["rs"][:R], d["rs"][R:], d["out"], self.ws, self.sig_rs, self.epoch)
 
-    def moe(self):
+    def moe(self, b=0):
         self.epoch += 1
         R, E = MOE["R"], MOE["E"]
-        d = self.d_moe
-        self.B.tl_moe_ag_gemm(d[:R], d[R + E], d[R:R + E], self.S, self.Y, self.perm, self.offs, self.ws_moe,
+        d = self.sets[b]
+        m = d["moe"]
+        self.B.tl_moe_ag_gemm(m[:R], m[R + E], m[R:R + E], self.S, d["Y"], self.perm, self.offs, self.ws_moe,
                               self.sig_moe, self.epoch)
 
-    def h2d(self):
-        for h, d in zip(self.h_ag + self.h_rs + self.h_moe, self.d_ag + self.d_rs + self.d_moe):
-            d.copy_(h, non_blocking=True)
+    def h2d(self, b=0):
+        d = self.sets[b]
+        for h, t in zip(self.h_ag + self.h_rs + self.h_moe, d["ag"] + d["rs"] + d["moe"]):
+            t.copy_(h, non_blocking=True)
 
-    def d2h(self):
-        self.h_C.copy_(self.C, non_blocking=True)
-        for h, d in zip(self.h_out, self.out):
-            h.copy_(d, non_blocking=True)
-        self.h_Y.copy_(self.Y, non_blocking=True)
+    def d2h(self, b=0):
+        d = self.sets[b]
+        self.h_C.copy_(d["C"], non_blocking=True)
+        for h, t in zip(self.h_out, d["out"]):
+            h.copy_(t, non_blocking=True)
+        self.h_Y.copy_(d["Y"], non_blocking=True)
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.h_ag + self.h_rs + self.h_moe)
@@ -320,6 +332,69 @@ class Workload:
             code, where = self.B.tl_query_status(s)
             if code:
                 raise RuntimeError(f"device error {code} at {where}")
+
+
+def e2e_serial(torch, wl, E, stream, barrier):
+    """ms per step with the copies and the calls in one stream: H2D inputs, the three
+    calls, D2H outputs, one step after the other."""
+    for _ in range(2):
+        wl.h2d(); wl.ag(); wl.rs(); wl.moe(); wl.d2h()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        wl.h2d(); wl.ag(); wl.rs(); wl.moe(); wl.d2h()
+    e1.record(stream)
+    barrier()
+    return e0.elapsed_time(e1) / E
+
+
+def e2e_pipelined(torch, wl, E, stream, barrier):
+    """ms per step over E steps, each copying all of its inputs in and all of its
+    outputs back, with two device sets: step i computes on set i % 2 while step
+    i+1's inputs copy into the other set (copy-in stream) and step i-1's outputs
+    copy out (copy-out stream).  The timed region runs from before the first
+    copy-in to after the last copy-out."""
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]
+
+    def run(n, e0=None):
+        inputs_free, inputs_ready, outputs_ready, outputs_read = ev(), ev(), ev(), ev()
+        if e0 is not None:
+            e0.record(stream)
+        cin.wait_stream(stream)
+        cout.wait_stream(stream)
+        for i in range(n):
+            b = i & 1
+            with torch.cuda.stream(cin):
+                if i >= 2:
+                    cin.wait_event(inputs_free[b])
+                wl.h2d(b)
+                inputs_ready[b].record(cin)
+            stream.wait_event(inputs_ready[b])
+            if i >= 2:
+                stream.wait_event(outputs_read[b])
+            wl.ag(b)
+            wl.rs(b)
+            wl.moe(b)
+            inputs_free[b].record(stream)
+            outputs_ready[b].record(stream)
+            with torch.cuda.stream(cout):
+                cout.wait_event(outputs_ready[b])
+                wl.d2h(b)
+                outputs_read[b].record(cout)
+        stream.wait_stream(cin)
+        stream.wait_stream(cout)
+
+    run(2)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    run(E, e0)
+    e1.record(stream)
+    barrier()
+    return e0.elapsed_time(e1) / E
 
 
 def flushed_time_us(torch, fn, flush, reps=7):
@@ -793,24 +868,11 @@ def main():
     step_flops = AG_FLOPS + RS_FLOPS + MOE_FLOPS
     value = world * step_flops / (ms_per_step * 1e-3) / 1e12
 
-    # end to end through the public API with host buffers: H2D inputs, both calls, D2H outputs
+    # end to end through the public API with host buffers: every step copies its inputs in
+    # from pinned host memory, runs the three calls and reads its outputs back
     E = max(3, args.e2e_steps)
-    for _ in range(2):
-        wl.h2d(); wl.ag(); wl.rs(); wl.moe(); wl.d2h()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(E):
-        wl.h2d()
-        wl.ag()
-        wl.rs()
-        wl.moe()
-        wl.d2h()
-    e1.record(stream)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / E
-    e2e_ms = max_over_ranks(pg, e2e_ms)
+    e2e_serial_ms = max_over_ranks(pg, e2e_serial(torch, wl, E, stream, barrier))
+    e2e_ms = max_over_ranks(pg, e2e_pipelined(torch, wl, E, stream, barrier))
     wl.check_status()
 
     rs_avg = statistics.mean(rs_ms)
@@ -836,7 +898,11 @@ def main():
                      "algorithmic_bytes": RS_BYTES},
         "clocks": clocks,
         "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes()},
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes(),
+                "how": "double-buffered: step i+1's inputs copy in on a copy stream while step i computes, "
+                       "step i's outputs copy out on a third stream",
+                "serial_ms_per_step": e2e_serial_ms,
+                "serial_value": world * step_flops / (e2e_serial_ms * 1e-3) / 1e12},
         "gpu_launches": K * wl.launches_per_step,
     }
     if not args.no_overlap:
