@@ -166,7 +166,7 @@ typedef struct tl_ag_gemm_args {
   int32_t K;                   /* contraction, >= 8, multiple of 8 */
   int32_t N;                   /* output columns, >= 8, multiple of 8 */
   int32_t mode;                /* tl_mode */
-  int32_t rows_per_barrier;    /* rows per producer tile / flag; 0 = about 32 KB of A */
+  int32_t rows_per_barrier;    /* rows per producer tile / flag; 0 = about 128 KB of A */
   int32_t swizzle;             /* tl_swizzle: consumer row-tile order; 0 = arrival order */
   const void* const* A_shards; /* host array of R device pointers, bf16 [M_shard, K] */
   const void* B;               /* device bf16 [K, N] */
@@ -354,7 +354,7 @@ typedef struct tl_moe_args {
   int32_t E;                    /* experts, 1..64 */
   int32_t topk;                 /* routed experts per token, 1..E */
   int32_t rows_per_barrier;     /* rows per producer chunk / flag: push = tokens of a shard
-                                   (0 = about 32 KB), pull = sorted rows (0 = about 64 KB) */
+                                   (0 = about 128 KB), pull = sorted rows (0 = about 64 KB) */
   const void* const* X;         /* host array of R device pointers, bf16 [T_r, H] */
   const int32_t* topk_ids;      /* device int32 [R*T_r, topk] */
   const void* const* W;         /* host array of E device pointers, bf16 [H, N] */

@@ -52,8 +52,8 @@ def test_ag_tile_order_matches_oracle(B):
 
 
 def test_ag_num_flags(B):
-    assert B.tl_ag_gemm_num_flags(8, 1024, 4096) == (8 * 256, 4)
-    assert B.tl_ag_gemm_num_flags(2, 128, 512) == (2 * 4, 32)
+    assert B.tl_ag_gemm_num_flags(8, 1024, 4096) == (8 * 64, 16)   # default: about 128 KB of A per chunk
+    assert B.tl_ag_gemm_num_flags(2, 128, 512) == (2 * 1, 128)
     assert B.tl_ag_gemm_num_flags(3, 100, 136, 16) == (3 * 7, 16)
     assert B.tl_ag_gemm_num_flags(2, 10, 8, 0)[1] == 10   # capped at the shard
 

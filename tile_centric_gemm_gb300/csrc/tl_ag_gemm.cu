@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
 }
 
 int default_rpb(int K, int M_shard) {
-  int rpb = std::max(1, int(32768 / (size_t(K) * 2)));
+  int rpb = std::max(1, int(131072 / (size_t(K) * 2)));  // about 128 KB of A per chunk
   return std::min(rpb, M_shard);
 }
 

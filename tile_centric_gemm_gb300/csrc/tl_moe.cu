@@ -456,10 +456,10 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
 }
 
 
-// push: tokens of a shard per flag (about 32 KB of source rows); pull: sorted rows per flag (about 64 KB)
+// push: tokens of a shard per flag (about 128 KB of source rows); pull: sorted rows per flag (about 64 KB)
 int moe_default_rpb(int mode, int H, int T_r, long long P) {
   if (mode == TL_MODE_PULL) return int(std::min<long long>(P, std::max(1, int(65536 / (size_t(H) * 2)))));
-  return std::min(T_r, std::max(1, int(32768 / (size_t(H) * 2))));
+  return std::min(T_r, std::max(1, int(131072 / (size_t(H) * 2))));
 }
 
 }  // namespace
