@@ -115,13 +115,17 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
     // ---------------------------------------------------------------- TMA producer (this CTA's halves)
     if (lane == 0) {
       pair::Producer prod;
+      // operands stay in L2 ahead of the streamed partials: A rows are reused across a
+      // destination's n tiles and B columns across its m tiles
+      const uint64_t keep = l2_policy_evict_last();
       for (int i = pair_id; i < p.num_items && !*abort; i += npairs) {
         const Item it = item_of(p, i);
         if (p.trace && rank == 0) p.trace[i] = ((it.d * p.Mt_d + it.mt) * p.Nt + it.nt) * p.R + it.r;
         const int row0 = it.d * p.Md + it.mt * pair::BM + h * pair::HM;
         for (int kb = 0; kb < p.KB; ++kb)
-          if (!prod.load(smem, bars, rank, &p.map_a[it.r], kb * pair::BK, row0, &p.map_b[it.r],
-                         it.nt * pair::BN + h * pair::HN, kb * pair::BK, abort, p.status, p.pipe_timeout_ns))
+          if (!prod.load_hint(smem, bars, rank, &p.map_a[it.r], kb * pair::BK, row0, &p.map_b[it.r],
+                              it.nt * pair::BN + h * pair::HN, kb * pair::BK, keep, abort, p.status,
+                              p.pipe_timeout_ns))
             break;
       }
     }
@@ -161,6 +165,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       // element offset of this thread's first value in its half-slot (4-byte floats, or
       // 2-byte bf16 values in half the bytes)
       const size_t slot_el = (size_t(i % p.ring_items) * 2 + h) * p.half_floats + my_base;
+      const uint64_t stream = l2_policy_evict_first();  // partial lines: written once, read once
       for (int c = 0; c < pair::BN / 32; ++c) {
         if (it.nt * pair::BN + c * 32 >= p.N) break;
         uint32_t v[32];
@@ -171,15 +176,15 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
             const float* f = reinterpret_cast<const float*>(v + g * 4);
-            st_global_cg_v2u(slot16 + size_t(c * 8 + g) * p.slice_rows * 4, pack_bf16x2(f[0], f[1]),
-                             pack_bf16x2(f[2], f[3]));
+            st_global_cg_v2u_hint(slot16 + size_t(c * 8 + g) * p.slice_rows * 4, pack_bf16x2(f[0], f[1]),
+                                  pack_bf16x2(f[2], f[3]), stream);
           }
         } else {
           float* slot = p.slots + slot_el;
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
             const float* f = reinterpret_cast<const float*>(v + g * 4);
-            st_global_cg_v4f(slot + size_t(c * 8 + g) * p.slice_rows * 4, f[0], f[1], f[2], f[3]);
+            st_global_cg_v4f_hint(slot + size_t(c * 8 + g) * p.slice_rows * 4, f[0], f[1], f[2], f[3], stream);
           }
         }
       }
