@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       const int total = s_rows * (n_cols / 4);                   // float4 elements of the slice
       // rank r's partial was pushed by item tau*R + j(r), j(r) = (r - d - 1 - tau) mod R,
       // into half-slot 2 * ((tau*R + j(r)) mod ring_items) + h
+      const uint64_t drop = l2_policy_evict_first();  // each partial line is read once, here
       const int jbase = ((-(it.d + 1 + it.tau)) % p.R + p.R) % p.R;
       const int ring_base = int((size_t(it.tau) * p.R) % size_t(p.ring_items));
       uint16_t* out = p.out[it.d];
@@ -255,14 +256,14 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
 #pragma unroll
                 for (int u = 0; u < QU; ++u)
                   if (off[u] >= 0) {
-                    const uint2 w = __ldcg(reinterpret_cast<const uint2*>(src16 + off[u]));
+                    const uint2 w = ld_global_cg_v2u_hint(src16 + off[u], drop);
                     v[rr][u] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), 0.f, 0.f);
                   }
               } else {
                 const float* src = p.slots + base_el;
 #pragma unroll
                 for (int u = 0; u < QU; ++u)
-                  if (off[u] >= 0) v[rr][u] = __ldcg(reinterpret_cast<const float4*>(src + off[u]));
+                  if (off[u] >= 0) v[rr][u] = ld_global_cg_v4f_hint(src + off[u], drop);
               }
             }
           }

@@ -305,6 +305,18 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+__device__ __forceinline__ float4 ld_global_cg_v4f_hint(const float* p, uint64_t pol) {
+  float4 r;
+  asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+__device__ __forceinline__ uint2 ld_global_cg_v2u_hint(const void* p, uint64_t pol) {
+  uint2 r;
+  asm volatile("ld.global.cg.L2::cache_hint.v2.b32 {%0, %1}, [%2], %3;" : "=r"(r.x), "=r"(r.y) : "l"(p), "l"(pol));
+  return r;
+}
 __device__ __forceinline__ void st_global_cg_v4f_hint(float* p, float a, float b, float c, float d, uint64_t pol) {
   asm volatile("st.global.cg.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a), "f"(b), "f"(c),
                "f"(d), "l"(pol)
