@@ -107,12 +107,14 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
     // ---------------------------------------------------------------- TMA producer (this CTA's halves)
     if (lane == 0) {
       pair::Producer prod;
+      // operands stay in L2 ahead of the streamed partials (as in the GEMM-RS kernel)
+      const uint64_t keep = l2_policy_evict_last();
       for (int i = pair_id; i < num_items && !*abort; i += npairs) {
         const MdItem it = md_item(p, i, ntiles);
         for (int kb = 0; kb < p.KB; ++kb)
-          if (!prod.load(smem, bars, rank, &p.map_h[it.r], kb * pair::BK, it.row0 + h * pair::HM, &p.map_w[it.r],
-                         it.n * pair::BN + h * pair::HN, it.e * p.I_r + kb * pair::BK, abort, p.status,
-                         p.pipe_timeout_ns))
+          if (!prod.load_hint(smem, bars, rank, &p.map_h[it.r], kb * pair::BK, it.row0 + h * pair::HM,
+                              &p.map_w[it.r], it.n * pair::BN + h * pair::HN, it.e * p.I_r + kb * pair::BK, keep,
+                              abort, p.status, p.pipe_timeout_ns))
             break;
       }
     }
@@ -148,6 +150,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
       if (!named_bar_and(1, kNumEpiThreads, ok)) break;
       tc_fence_after();
       float* slot = p.slots + (size_t(i % p.ring_items) * 2 + h) * p.half_floats + my_base;
+      const uint64_t stream = l2_policy_evict_first();  // partial lines: written once, read once
       for (int c = 0; c < pair::BN / 32; ++c) {
         if (it.n * pair::BN + c * 32 >= p.Hd) break;
         uint32_t v[32];
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           const float* f = reinterpret_cast<const float*>(v + g * 4);
-          st_global_cg_v4f(slot + size_t(c * 8 + g) * p.slice_rows * 4, f[0], f[1], f[2], f[3]);
+          st_global_cg_v4f_hint(slot + size_t(c * 8 + g) * p.slice_rows * 4, f[0], f[1], f[2], f[3], stream);
         }
       }
       tc_fence_before();
@@ -184,6 +187,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
       const int n_cols = min(pair::BN, p.Hd - it.n * pair::BN);
       const int total = s_rows * (n_cols / 4);
       // rank r's partial was pushed by item tau*R + j(r), j(r) = (r - tau) mod R
+      const uint64_t drop = l2_policy_evict_first();  // each partial line is read once, here
       const int jbase = ((-it.tau) % p.R + p.R) % p.R;
       const int ring_base = int((size_t(it.tau) * p.R) % size_t(p.ring_items));
       const int lrow_base = h * pair::HM + s0;  // row of the tile
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
               const float* src = p.slots + (size_t(slot) * 2 + h) * p.half_floats;
 #pragma unroll
               for (int u = 0; u < QU; ++u)
-                if (off[u] >= 0) v[rr][u] = __ldcg(reinterpret_cast<const float4*>(src + off[u]));
+                if (off[u] >= 0) v[rr][u] = ld_global_cg_v4f_hint(src + off[u], drop);
             }
           }
           // fixed rank order: ((P_0 + P_1) + P_2) + ...
