@@ -52,7 +52,7 @@ WORKLOAD = ("AG-GEMM R=8 [8192x4096]x[4096x1792] + GEMM-RS R=8 8x[8192x1792]x[17
 # sources hash to what was captured.
 RS_TRAFFIC_BYTES = 2_683_271_680 + 1_071_377_920
 RS_TRAFFIC_SOURCES = ("tl_gemm_rs.cu", "tl_pair.cuh", "tl_common.cuh", "tl_ptx.cuh")
-RS_TRAFFIC_SHA256 = "e06408a4f6ee740736d19c95077e28250876afb709bab5cb3de928994d2f1426"
+RS_TRAFFIC_SHA256 = "b4a600b8c3d11b2735e64d04b394448f494bd4580cbaa6101f9dfb798dd6fdf7"
 
 
 def rs_traffic():

@@ -4,7 +4,8 @@
 // complete (produce_tile_notify).  Pull mode first acquires the source's
 // readiness flag of the same chunk.
 //  * Shards in device memory: one lane streams the chunk through a ring of
-//    shared-memory buffers with bulk TMA copies (global -> shared -> global).
+//    shared-memory buffers with bulk TMA copies (global -> shared -> global),
+//    the source lines marked evict-first in L2 (they are read once).
 //  * Shards in pinned host (or managed) memory -- the stand-in for a slower
 //    link: all 32 lanes copy 16-byte vectors with plain loads and stores, many
 //    loads in flight per lane, then fence before the release.
@@ -86,6 +87,8 @@ __device__ __forceinline__ bool ag_copy_one(const AgCopyJob& j, int it, uint8_t*
   }
   bool dead = false;
   if (lane == 0) {
+    // each source line is read once: let it leave L2 before the gathered rows and B
+    const uint64_t once = l2_policy_evict_first();
     const int nch = int((bytes + COPY_CHUNK - 1) / COPY_CHUNK);
     int issued = 0, stored = 0;
     while (stored < nch) {
@@ -97,7 +100,7 @@ __device__ __forceinline__ bool ag_copy_one(const AgCopyJob& j, int it, uint8_t*
         const uint32_t off = uint32_t(issued) * COPY_CHUNK;
         const uint32_t sz = min(COPY_CHUNK, bytes - off);
         mbar_arrive_expect_tx(&bars[buf], sz);
-        bulk_g2s(stage + buf * COPY_CHUNK, src + off, sz, &bars[buf]);
+        bulk_g2s_hint(stage + buf * COPY_CHUNK, src + off, sz, &bars[buf], once);
         ++issued;
       }
       const uint32_t q = seq + uint32_t(stored);
