@@ -40,6 +40,8 @@ AG_FLOPS = 2 * AG["R"] * AG["M_shard"] * AG["N"] * AG["K"]
 RS_FLOPS = 2 * RS["R"] * RS["M"] * RS["N"] * RS["K_r"]
 # operands read once and the bf16 output written once (the emulated fp32 partial push and read are extra)
 RS_BYTES = RS["R"] * (RS["M"] * RS["K_r"] + RS["K_r"] * RS["N"]) * 2 + RS["M"] * RS["N"] * 2
+# the reduce-scatter's own data movement on emulated ranks: every fp32 partial written once and read once
+RS_PARTIAL_BYTES = 2 * RS["R"] * RS["M"] * RS["N"] * 4
 MOE_FLOPS = 2 * MOE["R"] * MOE["T_r"] * MOE["topk"] * MOE["N"] * MOE["H"]
 METRIC = "fused AG-GEMM / GEMM-RS TFLOP/s on 1 GB300"
 WORKLOAD = ("AG-GEMM R=8 [8192x4096]x[4096x1792] + GEMM-RS R=8 8x[8192x1792]x[1792x4096] "
@@ -895,7 +897,8 @@ def main():
                      "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": f"{peak_src} bf16 burst",
                      "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),
                      "traffic": rs_traffic(), "traffic_unit": "bytes per launch (ncu DRAM read + write)",
-                     "algorithmic_bytes": RS_BYTES},
+                     "algorithmic_bytes": RS_BYTES,
+                     "algorithmic_bytes_with_partials": RS_BYTES + RS_PARTIAL_BYTES},
         "clocks": clocks,
         "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes(),
