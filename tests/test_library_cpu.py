@@ -58,6 +58,22 @@ def test_ag_num_flags(B):
     assert B.tl_ag_gemm_num_flags(2, 10, 8, 0)[1] == 10   # capped at the shard
 
 
+def test_ag_attn_num_flags(B):
+    # one K and one V flag per 128-token chunk of every rank's shard
+    assert B.tl_ag_attn_num_flags(8, 8192) == 2 * 8 * 64
+    assert B.tl_ag_attn_num_flags(3, 300) == 2 * 3 * 3
+    assert B.tl_ag_attn_num_flags(8, 1) == 2 * 8
+    assert B.tl_ag_attn_num_flags(0, 5) == -1 and B.tl_ag_attn_num_flags(2, 0) == -1
+
+
+def test_ag_attn_rejects_null_and_empty_without_launch(B):
+    a = B.tl_ag_attn_args(R=2, self_rank=0, S_shard=0, H=4, H_kv=2, head_dim=128, causal=0, scale=0.0, epoch=1)
+    assert B.lib.tl_ag_attn(ctypes.byref(a), None) == B.TL_ERR_INVALID
+    a.S_shard = 16
+    assert B.lib.tl_ag_attn(ctypes.byref(a), None) == B.TL_ERR_INVALID  # NULL tensors
+    assert B.lib.tl_ag_attn(None, None) == B.TL_ERR_INVALID
+
+
 def test_invalid_arguments_fail_without_launch(B):
     with pytest.raises(B.TLError) as e:
         B.lib_call = B.lib.tl_ag_gemm(None, None)
