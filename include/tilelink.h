@@ -215,7 +215,7 @@ tl_status tl_ag_gemm(const tl_ag_gemm_args* args, void* stream);
 #define TL_RS_RING_ORDER 2u    /* destination d sums ranks d+1, d+2, ..., d (mod R) */
 
 typedef struct tl_gemm_rs_args {
-  int32_t R;                   /* ranks, 1..TL_MAX_RANKS */
+  int32_t R;                   /* ranks, 1..32 (TL_ERR_UNSUPPORTED above) */
   int32_t M;                   /* rows of every A_r; multiple of R */
   int32_t K_r;                 /* per-rank contraction, >= 8, multiple of 8 */
   int32_t N;                   /* >= 8, multiple of 8 */

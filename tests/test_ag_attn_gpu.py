@@ -89,6 +89,8 @@ def check_full(res, self_rank, causal, scale=None):
     (4, 64, 8, 1, 3, False),    # shard shorter than a tile, 8 query heads on one kv head
     (8, 1, 4, 4, 5, True),      # one token per rank
     (5, 200, 2, 1, 2, False),   # odd rank count
+    (64, 8, 2, 1, 63, True),    # the largest rank count, causal on the last rank
+    (64, 3, 2, 2, 10, False),   # 64 ranks of three tokens
 ])
 def test_attn_parity(B, R, S, H, Hkv, self_rank, causal):
     res = run_attn(B, R, S, H, Hkv, self_rank=self_rank, causal=causal, seed=R * 100 + S)

@@ -215,3 +215,11 @@ def test_ag_rows_swizzle_runs_tiles_in_index_order(B):
     check_bf16(to_f64(r["C"]), oracle.ag_gemm.ag_gemm(A, Bm), "C")
     np.testing.assert_array_equal(to_bits(r["G"]), oracle.ag_gemm.gathered(A))
     assert r["trace"].cpu().tolist() == [m * r["Nt"] + n for m in range(r["Mt"]) for n in range(r["Nt"])]
+
+
+def test_ag_max_ranks(B):
+    # TL_MAX_RANKS = 64 shards of 16 rows: 64 flags, one 256-row tile per 16 shards
+    R, Ms, K, N = 64, 16, 64, 64
+    A, Bm = inputs.ag_gemm_inputs(R, Ms, K, N, "normal", seed=64)
+    r = run_ag(B, A, Bm, self_rank=37, trace=True)
+    check_all(B, A, Bm, r, self_rank=37)

@@ -19,7 +19,8 @@ def B():
     return binding
 
 
-@pytest.mark.parametrize("R,Ms,K,self_rank,rpb", [(2, 128, 512, 0, 0), (3, 100, 136, 2, 7), (8, 1024, 4096, 5, 0)])
+@pytest.mark.parametrize("R,Ms,K,self_rank,rpb", [(2, 128, 512, 0, 0), (3, 100, 136, 2, 7), (8, 1024, 4096, 5, 0),
+                                                   (64, 8, 64, 40, 0)])
 def test_allgather_bit_exact_and_flags(B, R, Ms, K, self_rank, rpb):
     import torch
     A = [inputs.normal_bf16((Ms, K), 70 + r) for r in range(R)]

@@ -235,3 +235,16 @@ def test_rs_bf16_partials_and_ring_order_parity(B, R, M, K_r, N, options):
         assert np.all(np.abs(got - o) <= bound), f"out[{d}]: max excess {np.max(np.abs(got - o) - bound):.3e}"
         assert np.abs(got - o).max() / np.abs(o).max() <= 2e-2
     check_flags(r)
+
+
+def test_rs_max_ranks(B):
+    # the largest rank count, 32: four rows per reducer slice of a 128-row half tile;
+    # one more rank is rejected before any launch
+    R, M, K_r, N = 32, 1024, 32, 256
+    A, Bl = inputs.gemm_rs_inputs(R, M, K_r, N, seed=320)
+    r = run_rs(B, A, Bl)
+    check(B, A, Bl, r)
+    A, Bl = inputs.gemm_rs_inputs(33, 33 * 8, 32, 256, seed=330)
+    with pytest.raises(B.TLError) as e:
+        run_rs(B, A, Bl)
+    assert e.value.code == B.TL_ERR_UNSUPPORTED

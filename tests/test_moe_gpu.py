@@ -62,7 +62,8 @@ def check_moe(B, X, ids, W, r, self_rank=0, full_y=True):
     ws, mt = r["ws"], r["max_tiles"]
     n = int(ws[0])
     assert n == len(table)
-    got = ws[16:16 + 6 * n].reshape(n, 6)
+    got = ws[16:16 + 6 * n].reshape(n, 6).astype(np.int64)
+    got[:, 5] &= 0xFFFFFFFF  # the source-rank mask is a 32-bit word (bit 31 = rank 31)
     want = np.array([[e, s0, rows, lo, hi, mask] for (e, s0, rows), (mask, lo, hi) in zip(table, sources)])
     np.testing.assert_array_equal(got, want)
     order = (oracle.moe.tile_order_pull(sources) if pull else
@@ -83,6 +84,7 @@ def check_moe(B, X, ids, W, r, self_rank=0, full_y=True):
     (3, 50, 136, 264, 7, 3, 2, 8),     # ragged everything, three slots per token
     (4, 128, 512, 512, 16, 2, 1, 16),
     (1, 200, 64, 72, 3, 1, 0, 0),      # one rank, top-1
+    (32, 8, 128, 256, 8, 2, 31, 0),    # the largest rank count, 8 tokens per rank
 ])
 @pytest.mark.parametrize("mode", ["pull", "push"])
 def test_moe_parity(B, R, T_r, H, N, E, k, self_rank, rpb, mode):
