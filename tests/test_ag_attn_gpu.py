@@ -91,6 +91,8 @@ def check_full(res, self_rank, causal, scale=None):
     (5, 200, 2, 1, 2, False),   # odd rank count
     (64, 8, 2, 1, 63, True),    # the largest rank count, causal on the last rank
     (64, 3, 2, 2, 10, False),   # 64 ranks of three tokens
+    (1, 1, 1, 1, 0, False),     # one token, one head
+    (1, 1, 1, 1, 0, True),
 ])
 def test_attn_parity(B, R, S, H, Hkv, self_rank, causal):
     res = run_attn(B, R, S, H, Hkv, self_rank=self_rank, causal=causal, seed=R * 100 + S)

@@ -96,6 +96,7 @@ def test_ag_identity_b_returns_gathered_rows_exactly(B):
     (5, 77, 64, 8, 4, 0),          # tiny N, ragged everything
     (1, 300, 520, 512, 0, 0),      # one rank: plain GEMM
     (4, 256, 1024, 768, 2, 32),    # several tiles per shard, rotation from rank 2
+    (2, 1, 8, 8, 1, 0),            # smallest shapes: one row per shard, K = N = 8
 ])
 def test_ag_ragged_shapes(B, R, Ms, K, N, self_rank, rpb):
     A, Bm = inputs.ag_gemm_inputs(R, Ms, K, N, "normal", seed=R * 100 + Ms)

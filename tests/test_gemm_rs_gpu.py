@@ -68,6 +68,7 @@ def check(B, A, Bl, r):
     (8, 2048, 256, 512),
     (1, 200, 64, 136),      # one rank: plain GEMM, bf16 out
     (5, 5 * 130, 520, 72),  # R that does not divide the tile height
+    (4, 4, 8, 8),           # smallest shapes: one row per destination, K_r = N = 8
 ])
 def test_rs_parity(B, R, M, K_r, N):
     A, Bl = inputs.gemm_rs_inputs(R, M, K_r, N, seed=R * 7 + M)

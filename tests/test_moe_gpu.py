@@ -85,6 +85,7 @@ def check_moe(B, X, ids, W, r, self_rank=0, full_y=True):
     (4, 128, 512, 512, 16, 2, 1, 16),
     (1, 200, 64, 72, 3, 1, 0, 0),      # one rank, top-1
     (32, 8, 128, 256, 8, 2, 31, 0),    # the largest rank count, 8 tokens per rank
+    (2, 1, 8, 8, 64, 2, 1, 0),         # 64 experts (the most) for 4 routed rows: nearly all empty
 ])
 @pytest.mark.parametrize("mode", ["pull", "push"])
 def test_moe_parity(B, R, T_r, H, N, E, k, self_rank, rpb, mode):
