@@ -53,6 +53,17 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
+    # one build at a time (several ranks of one job may start together); the
+    # ones that waited find the library fresh and return
+    import fcntl
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and up_to_date():
+            return LIB
+        return _build_locked(verbose, extra_flags)
+
+
+def _build_locked(verbose, extra_flags) -> str:
     srcs = _sources()
 
     def compile_one(src):
