@@ -433,18 +433,19 @@ tl_status tl_moe_down(const tl_moe_down_args* args, void* stream);
  *   s_j   = scale * <Q[t, h], Kg[j, hk]>        over the visible keys j
  *           (all keys; causal: j <= self_rank*S_shard + t)
  *   O[t, h] = bf16( sum_j exp(s_j - lse) Vg[j, hk] ),  lse[h, t] = log sum_j exp(s_j)
- * One launch on pairs of CTAs (cta_group::2):
+ * One launch of single CTAs, one per SM (tcgen05.mma.cta_group::1):
  *  - producer: a copy warp per CTA moves the peers' key and value shards, 128
  *    tokens at a time, into K_gathered / V_gathered (bulk TMA copies; plain
  *    loads for pinned-host shards) and releases one flag per chunk of each
  *    (produce_tile_notify), shards self+1, ..., self+R-1, then self;
- *  - consumer: work units of one head and 512 query rows (two 256-row tiles
+ *  - consumer: work units of one head and 256 query rows (two 128-row tiles
  *    that share every key/value tile); each unit streams its own shard's keys
  *    and values first (in place, no wait), then the peers' in copy order,
  *    acquiring each chunk's flags before loading it (consume_tile_wait).
  *    S = Q K^T and O += P V run on the tensor cores with S and O in tensor
- *    memory; the online softmax (running max, rescaling of O only when the max
- *    grows by more than 2^8) runs in between on the CTAs' softmax warps.
+ *    memory and P written back into tensor memory over S; the online softmax
+ *    (running max, rescaling of O only when the max grows by more than 2^8)
+ *    runs in between on the CTA's softmax warps.
  * The result does not depend on the copy order or the schedule; it is one
  * evaluation of the formula above with P rounded to bf16 for the P V product.
  * Flags: K chunk (r, c) uses flag r * ceil(S_shard/128) + c, V chunk the same

@@ -9,28 +9,30 @@
 //  * Technical Deep Dive -- produce_tile_notify / consume_tile_wait: the copy
 //    of a chunk releases its flag; the consumer acquires it before loading.
 //
-// A persistent grid of CTA pairs (clusters of two, one CTA per SM) runs work
-// units of (head h, 512 query rows): two 256-row query tiles A and B that
-// share every key/value tile.  Every CTA holds 128 rows of each tile:
+// A persistent grid of single CTAs (one per SM) runs work units of (head h,
+// 256 query rows): two 128-row query tiles A and B that share every key/value
+// tile.
 //   warp 0      TMA producer: the unit's Q tiles, then per key/value tile its
-//               arrival flags (peers' shards only) and this CTA's halves of K
-//               (64 keys x 128 dims) and V (128 keys x 64 dims) into
-//               two-stage rings.
-//   warp 1      MMA issuer (leader CTA only): S_X = Q_X K^T and
-//               O_X += P_X V with tcgen05.mma.cta_group::2 (M = 256, N = 128),
-//               in the order QK_A(0) QK_B(0) | PV_A(j) QK_A(j+1) PV_B(j)
-//               QK_B(j+1) | ..., so that one tile's softmax runs while the
-//               tensor cores work on the other tile.
+//               arrival flags (peers' shards only), K (128 keys x 128 dims)
+//               and V (128 keys x 128 dims) into two-stage rings.
+//   warp 1      MMA issuer: S_X = Q_X K^T and O_X += P_X V with
+//               tcgen05.mma.cta_group::1 (M = 128, N = 128), in the order
+//               QK_A(0) QK_B(0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...,
+//               so that one tile's softmax runs while the tensor cores work on
+//               the other tile.  P V takes its A operand (P) from TMEM.
 //   warp 2      copy warp (AllGather producer), as in the AllGather-GEMM.
 //   warp 3      idle.
 //   warps 4-7   softmax of tile A, warps 8-11 of tile B, one query row per
 //               thread: S from TMEM, running max m and sum l (base 2), P as
-//               bf16 into shared memory (the A operand of P V), O in TMEM
-//               rescaled only when m grows by more than 8 (P <= 2^8 between
-//               rescales), and the final O / l and LSE.
+//               bf16 pairs written back over the first 64 columns of the
+//               row's S (tcgen05.st), O in TMEM rescaled only when m grows by
+//               more than 8 (P <= 2^8 between rescales), and the final O / l
+//               and LSE.
 //
-// TMEM (per CTA, lane = its query row): S_A cols 0-127, S_B 128-255,
-// O_A 256-383, O_B 384-511.
+// TMEM (lane = query row of the tile): S_A cols 0-127 (P_A in 0-63), S_B
+// 128-255 (P_B in 128-191), O_A 256-383, O_B 384-511.  The tensor pipe runs
+// one thread's MMAs in issue order, so the QK that overwrites S_X with the
+// next tile's scores follows the P V that reads P_X from the same columns.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -44,8 +46,8 @@ namespace {
 
 constexpr int HD = 128;          // head dim
 constexpr int KV_TILE = 128;     // keys per tile (the flag granularity too)
-constexpr int Q_ROWS = 128;      // query rows per CTA per tile
-constexpr int UNIT_ROWS = 512;   // two 256-row tiles per unit
+constexpr int Q_ROWS = 128;      // query rows per tile
+constexpr int UNIT_ROWS = 256;   // two 128-row tiles per unit
 constexpr int KST = 2;           // K ring stages
 constexpr int VST = 2;           // V ring stages
 constexpr int ATT_COPY_NBUF = 3;
@@ -54,22 +56,18 @@ constexpr int kWarpCopyA = 2;
 constexpr int kWarpSoftmax0 = 4;
 constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the running max grows by more than this
 
-constexpr uint32_t Q_BOX = Q_ROWS * 64 * 2;    // 16 KB: 128 rows x 64 dims
-constexpr uint32_t Q_TILE = 2 * Q_BOX;         // 32 KB
-constexpr uint32_t K_BOX = 64 * 64 * 2;        // 8 KB: 64 keys x 64 dims
-constexpr uint32_t K_STAGE = 2 * K_BOX;        // 16 KB: this CTA's 64 keys x 128 dims
-constexpr uint32_t V_STAGE = KV_TILE * 64 * 2; // 16 KB: 128 keys x this CTA's 64 dims
-constexpr uint32_t P_ATOM = Q_ROWS * 64 * 2;   // 16 KB: 128 rows x 64 keys
-constexpr uint32_t P_TILE = 2 * P_ATOM;        // 32 KB
+constexpr uint32_t BOX = 128 * 64 * 2;         // 16 KB: 128 rows x 64 dims, one 128-byte swizzle span wide
+constexpr uint32_t Q_TILE = 2 * BOX;           // 32 KB: 128 query rows x 128 dims (K-major)
+constexpr uint32_t K_STAGE = 2 * BOX;          // 32 KB: 128 keys x 128 dims (K-major)
+constexpr uint32_t V_STAGE = 2 * BOX;          // 32 KB: 128 keys x 128 dims (dims contiguous)
 constexpr uint32_t SMEM_Q = 0;
 constexpr uint32_t SMEM_K = SMEM_Q + 2 * Q_TILE;
 constexpr uint32_t SMEM_V = SMEM_K + KST * K_STAGE;
-constexpr uint32_t SMEM_P = SMEM_V + VST * V_STAGE;
-constexpr uint32_t SMEM_COPY = SMEM_P + 2 * P_TILE;
+constexpr uint32_t SMEM_COPY = SMEM_V + VST * V_STAGE;
 constexpr uint32_t SMEM_BARS = SMEM_COPY + ATT_COPY_NBUF * COPY_CHUNK;
 
-constexpr uint32_t IDESC_QK = idesc_bf16_f32(256, KV_TILE, false);  // B = K rows, K-major
-constexpr uint32_t IDESC_PV = idesc_bf16_f32(256, HD, true);        // B = V [keys, dims], dims contiguous
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(Q_ROWS, KV_TILE, false);  // B = K rows, K-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(Q_ROWS, HD, true);        // B = V [keys, dims], dims contiguous
 
 struct __align__(8) AttnBars {
   uint64_t q_full[2], q_empty[2];
@@ -82,10 +80,11 @@ struct __align__(8) AttnBars {
   uint32_t abort;
 };
 constexpr uint32_t ATT_SMEM_BYTES = SMEM_BARS + sizeof(AttnBars) + 1024;
+static_assert(ATT_SMEM_BYTES <= 232448, "attention shared memory above the per-CTA limit");
 
 struct AttnParams {
   CUtensorMap map_q;   // Q [S, H*D], box 128 rows x 64 dims
-  CUtensorMap map_kg;  // gathered K [R][S][Hkv*D], box 64 keys x 64 dims
+  CUtensorMap map_kg;  // gathered K [R][S][Hkv*D], box 128 keys x 64 dims
   CUtensorMap map_vg;  // gathered V, box 128 keys x 64 dims
   CUtensorMap map_ks;  // self K shard [1][S][Hkv*D]
   CUtensorMap map_vs;  // self V shard
@@ -101,7 +100,7 @@ struct AttnParams {
   uint64_t pipe_timeout_ns;
   int32_t R, self, S, H, Hkv, group, causal;
   int32_t T;   // key tiles per shard
-  int32_t QB;  // 512-row query blocks
+  int32_t QB;  // 256-row query blocks
   int32_t num_units, num_items;
   float scale_log2;
   uint32_t epoch;
@@ -140,25 +139,46 @@ __device__ __forceinline__ void tile_of(const AttnParams& p, int qb, int j, int&
   }
 }
 
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t x, int32_t y,
+                                            int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] . B[smem]: A's rows in TMEM lanes, its K elements packed
+// two bf16 per 32-bit column (16 elements = 8 columns per instruction).
+__device__ __forceinline__ void tc_mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void issue_qk(uint8_t* smem, int X, int ks, uint32_t d_tmem) {
   const uint32_t q0 = smem_u32(smem + SMEM_Q + X * Q_TILE);
   const uint32_t k0 = smem_u32(smem + SMEM_K + ks * K_STAGE);
 #pragma unroll
   for (int kk = 0; kk < HD / UMMA_K; ++kk) {
-    const uint64_t ad = sdesc_sw128(q0 + (kk >> 2) * Q_BOX + (kk & 3) * 32, 16, 1024);
-    const uint64_t bd = sdesc_sw128(k0 + (kk >> 2) * K_BOX + (kk & 3) * 32, 16, 1024);
-    tc_mma_bf16_pair(d_tmem, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+    const uint64_t ad = sdesc_sw128(q0 + (kk >> 2) * BOX + (kk & 3) * 32, 16, 1024);
+    const uint64_t bd = sdesc_sw128(k0 + (kk >> 2) * BOX + (kk & 3) * 32, 16, 1024);
+    tc_mma_bf16(d_tmem, ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
   }
 }
 
-__device__ __forceinline__ void issue_pv(uint8_t* smem, int X, int vs, uint32_t d_tmem, bool accumulate) {
-  const uint32_t p0 = smem_u32(smem + SMEM_P + X * P_TILE);
+// O += P V, P in the first 64 TMEM columns of the tile's S (keys 2c, 2c+1 in column c);
+// V's two 64-dim halves are 128-byte swizzle spans BOX bytes apart.
+__device__ __forceinline__ void issue_pv(uint8_t* smem, uint32_t p_tmem, int vs, uint32_t d_tmem, bool accumulate) {
   const uint32_t v0 = smem_u32(smem + SMEM_V + vs * V_STAGE);
 #pragma unroll
   for (int kk = 0; kk < KV_TILE / UMMA_K; ++kk) {
-    const uint64_t ad = sdesc_sw128(p0 + (kk >> 2) * P_ATOM + (kk & 3) * 32, 16, 1024);
-    const uint64_t bd = sdesc_sw128(v0 + kk * 2048, V_STAGE, 1024);
-    tc_mma_bf16_pair(d_tmem, ad, bd, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+    const uint64_t bd = sdesc_sw128(v0 + kk * 2048, BOX, 1024);
+    tc_mma_bf16_tmem_a(d_tmem, p_tmem + uint32_t(kk * 8), bd, IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -168,19 +188,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-__device__ __forceinline__ void arrive_leader(uint64_t* bar, uint32_t rank) {
-  if (rank == 0) mbar_arrive(bar);
-  else mbar_arrive_cluster(map_to_rank(bar, 0));
-}
-
 __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   AttnBars* bars = reinterpret_cast<AttnBars*>(smem + SMEM_BARS);
   const int warp = int(warp_id());
   const int lane = int(lane_id());
-  const uint32_t rank = cluster_ctarank();
-  const int pair_id = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
+  const int cta = int(blockIdx.x), nctas = int(gridDim.x);
   volatile uint32_t* abort = &bars->abort;
 
   if (warp == 0 && lane == 0) {
@@ -195,9 +209,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
       mbar_init(&bars->q_full[x], 1);
       mbar_init(&bars->q_empty[x], 1);
       mbar_init(&bars->s_full[x], 1);
-      mbar_init(&bars->p_full[x], 8);  // 4 softmax warps x 2 CTAs
+      mbar_init(&bars->p_full[x], 4);
       mbar_init(&bars->o_full[x], 1);
-      mbar_init(&bars->o_empty[x], 8);
+      mbar_init(&bars->o_empty[x], 4);
     }
     for (int s = 0; s < KST; ++s) {
       mbar_init(&bars->k_full[s], 1);
@@ -212,21 +226,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc_pair(&bars->tmem_base, TMEM_COLS);
-    tmem_relinquish_pair();
+    tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = bars->tmem_base;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer (this CTA's halves)
+    // ---------------------------------------------------------------- TMA producer
     int ks = 0, vs = 0;
     uint32_t kph = 0, vph = 0;
     int iu = 0;
-    for (int u = pair_id; u < p.num_units; u += npairs, ++iu) {
+    for (int u = cta; u < p.num_units; u += nctas, ++iu) {
       int h, qb;
       unit_of(p, u, h, qb);
       const int hk = h / p.group;
@@ -234,12 +247,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
       if (lane == 0) {
         for (int X = 0; X < 2; ++X) {
           if (!mbar_wait(&bars->q_empty[X], uint32_t(iu & 1) ^ 1u, abort, p.status, p.pipe_timeout_ns, 11)) break;
-          if (rank == 0) mbar_arrive_expect_tx(&bars->q_full[X], 2 * Q_TILE);
-          const uint32_t full = map_to_rank(&bars->q_full[X], 0);
-          const int y = qb * UNIT_ROWS + X * 256 + int(rank) * Q_ROWS;
+          mbar_arrive_expect_tx(&bars->q_full[X], Q_TILE);
+          const int y = qb * UNIT_ROWS + X * Q_ROWS;
           uint8_t* dst = smem + SMEM_Q + X * Q_TILE;
-          tma_load_2d_pair(dst, &p.map_q, full, h * HD, y);
-          tma_load_2d_pair(dst + Q_BOX, &p.map_q, full, h * HD + 64, y);
+          tma_load_2d(dst, &p.map_q, &bars->q_full[X], h * HD, y);
+          tma_load_2d(dst + BOX, &p.map_q, &bars->q_full[X], h * HD + 64, y);
         }
       }
       for (int j = 0; j < nkv; ++j) {
@@ -258,21 +270,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
           const CUtensorMap* mv = peer ? &p.map_vg : &p.map_vs;
           const int z = peer ? r : 0;
           if (mbar_wait(&bars->k_empty[ks], kph ^ 1u, abort, p.status, p.pipe_timeout_ns, 12)) {
-            if (rank == 0) mbar_arrive_expect_tx(&bars->k_full[ks], 2 * K_STAGE);
-            const uint32_t full = map_to_rank(&bars->k_full[ks], 0);
+            mbar_arrive_expect_tx(&bars->k_full[ks], K_STAGE);
             uint8_t* dst = smem + SMEM_K + ks * K_STAGE;
-            const int y = t * KV_TILE + int(rank) * 64;
-            tma_load_3d_pair(dst, mk, full, hk * HD, y, z);
-            tma_load_3d_pair(dst + K_BOX, mk, full, hk * HD + 64, y, z);
+            tma_load_3d(dst, mk, &bars->k_full[ks], hk * HD, t * KV_TILE, z);
+            tma_load_3d(dst + BOX, mk, &bars->k_full[ks], hk * HD + 64, t * KV_TILE, z);
             if (++ks == KST) {
               ks = 0;
               kph ^= 1u;
             }
           }
           if (mbar_wait(&bars->v_empty[vs], vph ^ 1u, abort, p.status, p.pipe_timeout_ns, 13)) {
-            if (rank == 0) mbar_arrive_expect_tx(&bars->v_full[vs], 2 * V_STAGE);
-            const uint32_t full = map_to_rank(&bars->v_full[vs], 0);
-            tma_load_3d_pair(smem + SMEM_V + vs * V_STAGE, mv, full, hk * HD + int(rank) * 64, t * KV_TILE, z);
+            mbar_arrive_expect_tx(&bars->v_full[vs], V_STAGE);
+            uint8_t* dst = smem + SMEM_V + vs * V_STAGE;
+            tma_load_3d(dst, mv, &bars->v_full[vs], hk * HD, t * KV_TILE, z);
+            tma_load_3d(dst + BOX, mv, &bars->v_full[vs], hk * HD + 64, t * KV_TILE, z);
             if (++vs == VST) {
               vs = 0;
               vph ^= 1u;
@@ -284,15 +295,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
       if (__shfl_sync(0xffffffffu, *abort, 0)) break;
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer (leader CTA)
-    if (lane == 0 && rank == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
       int ks = 0, vs = 0;
       uint32_t kph = 0, vph = 0;
       uint32_t pcount[2] = {0, 0};
       int iu = 0;
       const uint32_t s_tmem[2] = {tmem_base, tmem_base + 128};
       const uint32_t o_tmem[2] = {tmem_base + 256, tmem_base + 384};
-      for (int u = pair_id; u < p.num_units && !*abort; u += npairs, ++iu) {
+      for (int u = cta; u < p.num_units && !*abort; u += nctas, ++iu) {
         int h, qb;
         unit_of(p, u, h, qb);
         const int nkv = unit_tiles(p, qb);
@@ -304,10 +315,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
         tc_fence_after();
         for (int X = 0; X < 2; ++X) {
           issue_qk(smem, X, ks, s_tmem[X]);
-          tc_commit_pair(&bars->s_full[X], 0x3);
-          if (nkv == 1) tc_commit_pair(&bars->q_empty[X], 0x3);
+          tc_commit(&bars->s_full[X]);
+          if (nkv == 1) tc_commit(&bars->q_empty[X]);
         }
-        tc_commit_pair(&bars->k_empty[ks], 0x3);
+        tc_commit(&bars->k_empty[ks]);
         if (++ks == KST) {
           ks = 0;
           kph ^= 1u;
@@ -320,9 +331,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
             if (ok && j == 0) ok = mbar_wait(&bars->o_empty[X], uph ^ 1u, abort, p.status, p.pipe_timeout_ns, 25);
             if (!ok) break;
             tc_fence_after();
-            issue_pv(smem, X, vs, o_tmem[X], j > 0);
+            issue_pv(smem, s_tmem[X], vs, o_tmem[X], j > 0);
             if (X == 1) {
-              tc_commit_pair(&bars->v_empty[vs], 0x3);
+              tc_commit(&bars->v_empty[vs]);
               if (++vs == VST) {
                 vs = 0;
                 vph ^= 1u;
@@ -334,17 +345,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
                 tc_fence_after();
               }
               issue_qk(smem, X, ks, s_tmem[X]);
-              tc_commit_pair(&bars->s_full[X], 0x3);
-              if (j + 2 == nkv) tc_commit_pair(&bars->q_empty[X], 0x3);
+              tc_commit(&bars->s_full[X]);
+              if (j + 2 == nkv) tc_commit(&bars->q_empty[X]);
               if (X == 1) {
-                tc_commit_pair(&bars->k_empty[ks], 0x3);
+                tc_commit(&bars->k_empty[ks]);
                 if (++ks == KST) {
                   ks = 0;
                   kph ^= 1u;
                 }
               }
             } else {
-              tc_commit_pair(&bars->o_full[X], 0x3);
+              tc_commit(&bars->o_full[X]);
             }
           }
         }
@@ -360,7 +371,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
                  p.R, p.self, p.S, p.Hkv * HD, KV_TILE, p.T, p.num_items, p.epoch, p.host_mask_v};
     uint32_t seq = 0;
     uint8_t* stage = smem + SMEM_COPY;
-    for (int it = int(blockIdx.x); it < p.num_items; it += int(gridDim.x)) {
+    for (int it = cta; it < p.num_items; it += nctas) {
       if (ag_copy_one<ATT_COPY_NBUF>(jk, it, stage, bars->copy, abort, seq)) break;
       if (ag_copy_one<ATT_COPY_NBUF>(jv, it, stage, bars->copy, abort, seq)) break;
     }
@@ -370,20 +381,18 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
     // ---------------------------------------------------------------- softmax warps (one row per thread)
     const int X = (warp - kWarpSoftmax0) >> 2;
     const int wq = warp & 3;
-    const int row = wq * 32 + lane;  // this CTA's row of the tile = TMEM lane
+    const int row = wq * 32 + lane;  // row of the tile = TMEM lane
     const uint32_t lane_base = uint32_t(wq * 32) << 16;
     const uint32_t s_addr = tmem_base + lane_base + uint32_t(X * 128);
     const uint32_t o_addr = tmem_base + lane_base + uint32_t(256 + X * 128);
-    const uint32_t p_base = smem_u32(smem + SMEM_P + X * P_TILE) + uint32_t(row) * 128u;
-    const uint32_t swz = uint32_t(row & 7);
     uint32_t sc = 0;
     int iu = 0;
     bool ok = true;
-    for (int u = pair_id; u < p.num_units && ok; u += npairs, ++iu) {
+    for (int u = cta; u < p.num_units && ok; u += nctas, ++iu) {
       int h, qb;
       unit_of(p, u, h, qb);
       const int nkv = unit_tiles(p, qb);
-      const int qrow = qb * UNIT_ROWS + X * 256 + int(rank) * Q_ROWS + row;  // row in the shard
+      const int qrow = qb * UNIT_ROWS + X * Q_ROWS + row;  // row in the shard
       float m = -INFINITY, l = 0.0f;
       for (int j = 0; j < nkv; ++j) {
         int r, t;
@@ -432,41 +441,38 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
         float sq[8];  // eight partial row sums
 #pragma unroll
         for (int q = 0; q < 8; ++q) sq[q] = 0.0f;
+        // P as bf16 pairs over the first 64 columns of S (all of S is in registers by now)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
+          uint32_t w[32];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint32_t w[4];
+          for (int i = 0; i < 32; ++i) {
+            const int key = c * 64 + 2 * i;
+            const float p0 = ex2_approx(fmaf(__uint_as_float(v[key >> 5][key & 31]), p.scale_log2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(v[(key + 1) >> 5][(key + 1) & 31]), p.scale_log2, neg_m));
+            sq[i & 7] += p0 + p1;
+            w[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st_32cols(s_addr + uint32_t(c * 32), w);
+          if (c == 0 && j > 0 && __any_sync(0xffffffffu, resc)) {
+            // O rescale, here where half of S is dead (fewer live registers)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float p0 = ex2_approx(fmaf(__uint_as_float(v[c][k * 8 + 2 * e]), p.scale_log2, neg_m));
-              const float p1 = ex2_approx(fmaf(__uint_as_float(v[c][k * 8 + 2 * e + 1]), p.scale_log2, neg_m));
-              sq[(k & 1) * 4 + e] += p0 + p1;
-              w[e] = pack_bf16x2(p0, p1);
+            for (int q = 0; q < 4; ++q) {
+              uint32_t o[32];
+              tmem_ld_32cols(o_addr + uint32_t(q * 32), o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              tmem_st_32cols(o_addr + uint32_t(q * 32), o);
             }
-            const uint32_t chunk = uint32_t(c * 4 + k);  // 16-byte chunk of the row: keys 8*chunk..
-            const uint32_t addr = p_base + (chunk >> 3) * P_ATOM + (((chunk & 7u) ^ swz) << 4);
-            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
           }
         }
         l += ((sq[0] + sq[1]) + (sq[2] + sq[3])) + ((sq[4] + sq[5]) + (sq[6] + sq[7]));
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tmem_ld_32cols(o_addr + uint32_t(c * 32), o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st_32cols(o_addr + uint32_t(c * 32), o);
-          }
-          tmem_st_wait();
-        }
-        // P (generic-proxy stores) and O (TMEM stores) are visible to the next MMAs
-        fence_proxy_async_shared();
+        // P and the rescaled O are in TMEM before the next MMAs read them
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) arrive_leader(&bars->p_full[X], rank);
+        if (lane == 0) mbar_arrive(&bars->p_full[X]);
       }
       if (!ok) break;
       ok = mbar_wait(&bars->o_full[X], uint32_t(iu & 1), abort, p.status, p.pipe_timeout_ns, 32);
@@ -497,11 +503,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
       if (row_ok && p.lse) p.lse[size_t(h) * p.S + qrow] = (m + log2f(l)) * 0.69314718055994531f;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) arrive_leader(&bars->o_empty[X], rank);
+      if (lane == 0) mbar_arrive(&bars->o_empty[X]);
     }
   }
 
-  // teardown: every thread of both CTAs is done with TMEM and with the peer's barriers
+  // teardown: every thread is done with TMEM; after an abort, TMA loads that
+  // nobody waits for land before the CTA's shared memory is released
   tc_fence_before();
   __syncthreads();
   if (bars->abort) {
@@ -509,10 +516,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
     while (now_ns() - t0 < 50000) {
     }
   }
-  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -572,10 +578,12 @@ extern "C" tl_status tl_ag_attn(const tl_ag_attn_args* a, void* stream) {
   const uint64_t kv_pitch = kv_cols * 2;
   do {
     if ((st = make_map_bf16(&p->map_q, a->Q, S, uint64_t(a->H) * HD, uint64_t(a->H) * HD * 2, Q_ROWS, 64))) break;
-    if ((st = make_map_bf16_3d(&p->map_kg, a->K_gathered, a->R, S, kv_cols, kv_pitch, S * kv_pitch, 64, 64))) break;
+    if ((st = make_map_bf16_3d(&p->map_kg, a->K_gathered, a->R, S, kv_cols, kv_pitch, S * kv_pitch, KV_TILE, 64)))
+      break;
     if ((st = make_map_bf16_3d(&p->map_vg, a->V_gathered, a->R, S, kv_cols, kv_pitch, S * kv_pitch, KV_TILE, 64)))
       break;
-    if ((st = make_map_bf16_3d(&p->map_ks, a->K_shards[a->self_rank], 1, S, kv_cols, kv_pitch, S * kv_pitch, 64, 64)))
+    if ((st = make_map_bf16_3d(&p->map_ks, a->K_shards[a->self_rank], 1, S, kv_cols, kv_pitch, S * kv_pitch, KV_TILE,
+                               64)))
       break;
     if ((st = make_map_bf16_3d(&p->map_vs, a->V_shards[a->self_rank], 1, S, kv_cols, kv_pitch, S * kv_pitch, KV_TILE,
                                64)))
@@ -608,10 +616,10 @@ extern "C" tl_status tl_ag_attn(const tl_ag_attn_args* a, void* stream) {
     const float scale = a->scale > 0.0f ? a->scale : 1.0f / std::sqrt(float(HD));
     p->scale_log2 = scale * 1.4426950408889634f;
     p->epoch = a->epoch;
-    const int pairs = std::max(1, std::min(di.sm_count / 2, std::max(p->num_units, (p->num_items + 1) / 2)));
+    const int ctas = std::max(1, std::min(di.sm_count, std::max(p->num_units, p->num_items)));
     void* args[] = {p};
-    st = launch_coop(reinterpret_cast<const void*>(&ag_attn_kernel), 2 * pairs, ATT_THREADS, ATT_SMEM_BYTES,
-                     (cudaStream_t)stream, args, 2);
+    st = launch_coop(reinterpret_cast<const void*>(&ag_attn_kernel), ctas, ATT_THREADS, ATT_SMEM_BYTES,
+                     (cudaStream_t)stream, args, 1);
   } while (false);
   delete p;
   return st;
