@@ -90,6 +90,7 @@ def check_full(res, self_rank, causal, scale=None):
     (8, 1, 4, 4, 5, True),      # one token per rank
     (5, 200, 2, 1, 2, False),   # odd rank count
     (64, 8, 2, 1, 63, True),    # the largest rank count, causal on the last rank
+    (2, 1100, 40, 8, 1, True),  # 200 work units on 152 SMs: CTAs run two units (barrier phases across units)
     (64, 3, 2, 2, 10, False),   # 64 ranks of three tokens
     (1, 1, 1, 1, 0, False),     # one token, one head
     (1, 1, 1, 1, 0, True),
