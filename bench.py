@@ -426,7 +426,7 @@ def time_variants(torch, fn, flush, reps=7):
     return {"cold": statistics.median(cold), "cold_min": min(cold), "warm": statistics.median(warm)}
 
 
-def decomposed_graph(torch, B, shards, Bm, G, C, sig):
+def decomposed_graph(torch, B, shards, Bm, G, C, sig, ws=None):
     """The prior-art decomposed schedule as a CUDA graph: the copy engine gathers
     shard after shard (rank 0 last) on a side stream while the main stream runs
     one GEMM per shard, the local shard 0 first, each after its copy's event."""
@@ -446,10 +446,10 @@ def decomposed_graph(torch, B, shards, Bm, G, C, sig):
                 e.record(s1)
                 evs.append(e)
             G[0:Ms].copy_(shards[0], non_blocking=True)
-        B.tl_gemm(shards[0], Bm, C[0:Ms], sig)
+        B.tl_gemm(shards[0], Bm, C[0:Ms], sig, workspace=ws)
         for j, e in zip(range(1, R), evs):
             main.wait_event(e)
-            B.tl_gemm(G[j * Ms:(j + 1) * Ms], Bm, C[j * Ms:(j + 1) * Ms], sig)
+            B.tl_gemm(G[j * Ms:(j + 1) * Ms], Bm, C[j * Ms:(j + 1) * Ms], sig, workspace=ws)
         main.wait_stream(s1)
 
     launches()  # sets every kernel's launch attributes before the capture
@@ -588,13 +588,18 @@ def run_sweep(torch, B, peaks):
                 C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
                 sig = B.Signals(B.tl_ag_gemm_num_flags(R, Ms, K)[0])
                 ep = [0]
+                # split-K workspaces (zeroed; None where the tiles already fill the SMs); the
+                # per-shard GEMMs of the decomposed schedule run one after another on one stream
+                ws_ag, ws_gemm, ws_shard = (torch.zeros(n, dtype=torch.uint8, device="cuda") if n else None for n in (
+                    B.tl_ag_gemm_workspace_size(R, Ms, K, N), B.tl_gemm_workspace_size(M, N, K),
+                    B.tl_gemm_workspace_size(Ms, N, K)))
 
                 def copy_only():
                     ep[0] += 1
                     B.tl_allgather(shards, G, sig, ep[0])
 
                 def gemm_only():
-                    B.tl_gemm(G, Bm, C, sig)
+                    B.tl_gemm(G, Bm, C, sig, workspace=ws_gemm)
 
                 def seq():
                     copy_only()
@@ -602,10 +607,10 @@ def run_sweep(torch, B, peaks):
 
                 def fused():
                     ep[0] += 1
-                    B.tl_ag_gemm(shards, Bm, G, C, sig, ep[0])
+                    B.tl_ag_gemm(shards, Bm, G, C, sig, ep[0], workspace=ws_ag)
 
                 C_lib = torch.empty_like(C)
-                graph = decomposed_graph(torch, B, shards, Bm, G, C, sig)
+                graph = decomposed_graph(torch, B, shards, Bm, G, C, sig, ws_shard)
                 t_copy = flushed_time_us(torch, copy_only, flush, reps=5)
                 t_gemm = flushed_time_us(torch, gemm_only, flush, reps=5)
                 t_seq = flushed_time_us(torch, seq, flush, reps=5)
@@ -618,7 +623,10 @@ def run_sweep(torch, B, peaks):
                     raise RuntimeError(f"device error {code} at {where} in the sweep (R={R}, M={M}, {placement})")
                 flops = 2 * M * N * K
                 host_bytes = (R - 1) * Ms * K * 2 if placement == "pinned_host" else 0
-                rows.append({"placement": placement, "R": R, "M": M, "t_copy_us": t_copy, "t_gemm_us": t_gemm,
+                splits = (B.tl_ag_gemm_workspace_size(R, Ms, K, N) - 1024) // (-(-M // 256) * -(-N // 256) * 262144) \
+                    if ws_ag is not None else 1
+                rows.append({"placement": placement, "R": R, "M": M, "splits": int(splits),
+                             "t_copy_us": t_copy, "t_gemm_us": t_gemm,
                              "t_seq_us": t_seq, "t_decomposed_us": t_dec, "t_fused_us": t_fused,
                              "t_torch_matmul_us": t_lib, "speedup_vs_decomposed": t_dec / t_fused,
                              "tflops": flops / (t_fused * 1e-6) / 1e12,
@@ -628,7 +636,7 @@ def run_sweep(torch, B, peaks):
                              "overlap_efficiency": (t_seq - t_fused) / min(t_copy, t_gemm),
                              "copy_gbs": 2 * M * K * 2 / (t_copy * 1e-6) / 1e9,
                              "host_read_gbs": host_bytes / (t_copy * 1e-6) / 1e9 if host_bytes else None})
-                del shards, G, C, C_lib, Bm, sig
+                del shards, G, C, C_lib, Bm, sig, ws_ag, ws_gemm, ws_shard
     del flush
     return rows
 

@@ -138,8 +138,12 @@ typedef struct tl_gemm_args {
   float* C_f32;                /* optional device float [M, N], written; NULL = none */
   tl_signals* signals;         /* receives device-side errors in its status word (any size >= 1) */
   uint64_t timeout_ns;         /* bound of the pipeline waits is 2 * timeout + 1 s; 0 = 1 s */
+  void* workspace;             /* optional device scratch for split-K (see tl_ag_gemm_workspace_size),
+                                  16-byte aligned, zeroed before its first use; NULL = no split */
+  size_t workspace_bytes;      /* >= tl_gemm_workspace_size(M, N, K, 0) when workspace is given */
 } tl_gemm_args;
 
+size_t tl_gemm_workspace_size(int M, int N, int K, int sm_count);
 tl_status tl_gemm(const tl_gemm_args* args, void* stream);
 
 /* ---------------------------------------------------------------- AllGather-GEMM
@@ -181,8 +185,26 @@ typedef struct tl_ag_gemm_args {
   int32_t* trace;              /* optional device int32 [ceil(M/256) * ceil(N/256)]:
                                   trace[slot] = m_tile * n_tiles + n_tile of the 256 x 256
                                   tile the consumer ran at schedule slot `slot` */
+  void* workspace;             /* optional device scratch for split-K, 16-byte aligned; NULL = no split */
+  size_t workspace_bytes;      /* >= tl_ag_gemm_workspace_size(...) when workspace is given */
 } tl_ag_gemm_args;
 
+/* Split-K (both AG-GEMM and GEMM): when the 256 x 256 tiles are fewer than the
+ * CTA pairs (SMs / 2) and a workspace is given, every tile's k-blocks are cut
+ * into S equal ranges (the largest S <= 16 that divides ceil(K/64), keeps at
+ * least 8 k-blocks per range and keeps tiles * S <= pairs), run on S pairs at
+ * once; each writes an fp32 partial tile to the workspace, and once all S have
+ * (a bounded wait, TL_ERR_TIMEOUT) each adds the S partials of 1/S of the
+ * tile's columns in range order 0..S-1 and writes them to C.  Results are
+ * deterministic (fixed order) and differ from the unsplit product only by fp32
+ * rounding.  The workspace's counters are left zeroed by every call that
+ * completes; an AG-GEMM tags them with its epoch, a GEMM with a fixed tag, so
+ * after a tl_gemm call that reported a device error the first 2 KB of its
+ * workspace must be zeroed before it is used again.  Calls sharing a workspace
+ * must not run concurrently.
+ * Workspace bytes for a shape: 0 when no split would be used.  sm_count 0 =
+ * the current device's SM count (the launch uses the device's own count). */
+size_t tl_ag_gemm_workspace_size(int R, int M_shard, int K, int N, int sm_count);
 /* Flags an AG-GEMM call needs: R * ceil(M_shard / rows_per_barrier) (after
  * replacing 0 by the default); also returns the effective rows_per_barrier. */
 int tl_ag_gemm_num_flags(int R, int M_shard, int K, int rows_per_barrier, int* effective_rpb);

@@ -120,6 +120,21 @@ def test_attn_repeated_calls_same_signals(B):
     np.testing.assert_array_equal(to_bits(r2["O"]), o1)
 
 
+def test_attn_without_lse(B):
+    # the LSE output is optional; O must not depend on whether it is written
+    import torch
+    R, S, H, Hkv = 2, 300, 4, 2
+    res = run_attn(B, R, S, H, Hkv, self_rank=1, causal=True, seed=17)
+    check_full(res, 1, True)
+    O2 = torch.full_like(res["O"], float("nan"))
+    sig = B.Signals(B.tl_ag_attn_num_flags(R, S))
+    B.tl_ag_attn(dev_bf16(res["Q"]), [dev_bf16(k) for k in res["K"]], [dev_bf16(v) for v in res["V"]],
+                 res["Kg"], res["Vg"], O2, sig, 1, self_rank=1, causal=True)
+    torch.cuda.synchronize()
+    assert B.tl_query_status(sig) == (0, -1)
+    np.testing.assert_array_equal(to_bits(O2), to_bits(res["O"]))
+
+
 def test_attn_full_size_sampled(B):
     # the sequence-parallel layer size: 8 ranks x 8192 tokens (64K context),
     # 32 query heads over 8 key/value heads, head dim 128, non-causal and causal

@@ -30,7 +30,7 @@ class Epoch:
 
 
 def run_ag(B, A, Bm, *, self_rank=0, mode=None, rpb=0, f32=False, notify_ready=True, timeout_ns=0,
-           withhold=None, trace=False, host_ranks=(), swizzle=0):
+           withhold=None, trace=False, host_ranks=(), swizzle=0, ws=None):
     import torch
     R, (Ms, K), N = len(A), A[0].shape, Bm.shape[1]
     mode = B.TL_MODE_PUSH if mode is None else mode
@@ -52,7 +52,7 @@ def run_ag(B, A, Bm, *, self_rank=0, mode=None, rpb=0, f32=False, notify_ready=T
     Mt, Nt = -(-R * Ms // 256), -(-N // 256)
     tr = torch.full((Mt * Nt,), -1, dtype=torch.int32, device="cuda") if trace else None
     B.tl_ag_gemm(dA, dB, G, C, sig, epoch, self_rank=self_rank, C_f32=C32, mode=mode, src_ready=ready,
-                 rows_per_barrier=rpb, timeout_ns=timeout_ns, trace=tr, swizzle=swizzle)
+                 rows_per_barrier=rpb, timeout_ns=timeout_ns, trace=tr, swizzle=swizzle, workspace=ws)
     status = B.tl_query_status(sig)
     out = dict(G=G, C=C, C32=C32, sig=sig, ready=ready, epoch=epoch, status=status, nflags=nflags,
                rpb=eff_rpb, trace=tr, Mt=Mt, Nt=Nt)
@@ -168,9 +168,10 @@ def test_ag_llm_full_size_sampled(B):
 @pytest.mark.slow
 @pytest.mark.parametrize("R,M", [(4, 4096), (2, 1024), (8, 16384)])
 def test_ag_sweep_points(B, R, M):
-    # AG sweep workload: K=8192, N=1024, activations N(0,1), weights N(0,0.02)
+    # AG sweep workload: K=8192, N=1024, activations N(0,1), weights N(0,0.02),
+    # with the split-K workspace the sweep gives (M=1024: 16 tiles split 4 ways)
     A, Bm = inputs.ag_gemm_inputs(R, M // R, 8192, 1024, "normal", seed=M + R)
-    r = run_ag(B, A, Bm, self_rank=R - 1, trace=True)
+    r = run_ag(B, A, Bm, self_rank=R - 1, trace=True, ws=splitk_ws(B, R, M // R, 8192, 1024))
     assert r["status"] == (0, -1)
     np.testing.assert_array_equal(to_bits(r["G"]), oracle.ag_gemm.gathered(A))
     rng = np.random.default_rng(R)
@@ -216,6 +217,56 @@ def test_ag_rows_swizzle_runs_tiles_in_index_order(B):
     check_bf16(to_f64(r["C"]), oracle.ag_gemm.ag_gemm(A, Bm), "C")
     np.testing.assert_array_equal(to_bits(r["G"]), oracle.ag_gemm.gathered(A))
     assert r["trace"].cpu().tolist() == [m * r["Nt"] + n for m in range(r["Mt"]) for n in range(r["Nt"])]
+
+
+def splitk_ws(B, R, Ms, K, N):
+    import torch
+    n = B.tl_ag_gemm_workspace_size(R, Ms, K, N)
+    return torch.zeros(max(n, 16), dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("R,Ms,K,N,self_rank,splits", [
+    (2, 300, 2048, 520, 1, 4),     # 3 x 3 ragged tiles, 32 k-blocks in 4 ranges of 8
+    (8, 128, 8192, 1024, 7, 4),    # the smallest sweep point: 16 tiles, 128 k-blocks
+    (1, 256, 1024, 256, 0, 2),     # one tile, 16 k-blocks in two ranges
+    (3, 100, 1000, 264, 2, 2),     # K tail inside the last range (16 k-blocks, the last partial)
+    (3, 100, 136, 264, 1, 1),      # too few k-blocks to split: the workspace is left unused
+])
+def test_ag_splitk_parity(B, R, Ms, K, N, self_rank, splits):
+    n = B.tl_ag_gemm_workspace_size(R, Ms, K, N)
+    tiles = -(-R * Ms // 256) * -(-N // 256)
+    assert n == (0 if splits == 1 else 1024 + tiles * splits * 256 * 256 * 4)
+    A, Bm = inputs.ag_gemm_inputs(R, Ms, K, N, "normal", seed=R * 31 + Ms + K)
+    r = run_ag(B, A, Bm, self_rank=self_rank, f32=True, trace=True, ws=splitk_ws(B, R, Ms, K, N))
+    check_all(B, A, Bm, r, self_rank)
+
+
+def test_ag_splitk_deterministic_and_stale_counters(B):
+    # the sum of the ranges runs in range order whichever finishes last, so two
+    # calls give the same bits; counters left at another epoch's values (an
+    # aborted call) start over instead of miscounting
+    R, Ms, K, N = 2, 300, 2048, 520
+    A, Bm = inputs.ag_gemm_inputs(R, Ms, K, N, "normal", seed=5)
+    ws = splitk_ws(B, R, Ms, K, N)
+    r1 = run_ag(B, A, Bm, self_rank=0, ws=ws)
+    check_all(B, A, Bm, r1)
+    c1 = to_bits(r1["C"]).copy()
+    ws[:1024] = 0x37  # every counter 0x37373737: a foreign tag with 0x37 arrivals
+    r2 = run_ag(B, A, Bm, self_rank=0, ws=ws)
+    check_all(B, A, Bm, r2)
+    np.testing.assert_array_equal(to_bits(r2["C"]), c1)
+    r3 = run_ag(B, A, Bm, self_rank=0)  # unsplit: the same product up to fp32 rounding
+    check_all(B, A, Bm, r3)
+
+
+def test_ag_splitk_rejects_small_workspace(B):
+    import torch
+    R, Ms, K, N = 2, 300, 2048, 520
+    A, Bm = inputs.ag_gemm_inputs(R, Ms, K, N, "normal", seed=6)
+    small = torch.zeros(B.tl_ag_gemm_workspace_size(R, Ms, K, N) - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(B.TLError) as e:
+        run_ag(B, A, Bm, ws=small)
+    assert e.value.code == B.TL_ERR_INVALID
 
 
 def test_ag_max_ranks(B):

@@ -18,14 +18,14 @@ def B():
     return binding
 
 
-def run_gemm(B, A, Bm, f32=True):
+def run_gemm(B, A, Bm, f32=True, ws=None):
     import torch
     M, K = A.shape
     N = Bm.shape[1]
     C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
     C32 = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda") if f32 else None
     sig = B.Signals(1)
-    B.tl_gemm(dev_bf16(A), dev_bf16(Bm), C, sig, C_f32=C32)
+    B.tl_gemm(dev_bf16(A), dev_bf16(Bm), C, sig, C_f32=C32, workspace=ws)
     assert B.tl_query_status(sig) == (0, -1)
     return C, C32
 
@@ -38,6 +38,27 @@ def test_gemm_parity(B, M, N, K):
     want = oracle.ag_gemm.ag_gemm(A, Bm)
     check_bf16(to_f64(C), want, "C")
     check_f32(to_f64(C32), want, "C_f32")
+
+
+@pytest.mark.parametrize("M,N,K,splits", [
+    (1024, 1024, 8192, 4),   # 16 tiles, 128 k-blocks
+    (300, 264, 2048, 4),     # 2 x 2 ragged tiles, 32 k-blocks
+    (104, 104, 1000, 2),     # one tile, 16 k-blocks with a K tail
+])
+def test_gemm_splitk_parity(B, M, N, K, splits):
+    import torch
+    n = B.tl_gemm_workspace_size(M, N, K)
+    assert n == 1024 + -(-M // 256) * -(-N // 256) * splits * 256 * 256 * 4
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    A, Bm = inputs.ag_gemm_inputs(1, M, K, N, "normal", seed=M + N + K + 1)
+    C, C32 = run_gemm(B, A[0], Bm, ws=ws)
+    want = oracle.ag_gemm.ag_gemm(A, Bm)
+    check_bf16(to_f64(C), want, "C")
+    check_f32(to_f64(C32), want, "C_f32")
+    # the counters reset themselves; a second call gives the same bits
+    assert int(ws[:1024].count_nonzero()) == 0
+    C2, _ = run_gemm(B, A[0], Bm, f32=False, ws=ws)
+    np.testing.assert_array_equal(to_bits(C2), to_bits(C))
 
 
 def test_gemm_identity_exact(B):

@@ -58,6 +58,30 @@ def test_ag_num_flags(B):
     assert B.tl_ag_gemm_num_flags(2, 10, 8, 0)[1] == 10   # capped at the shard
 
 
+def test_splitk_workspace_sizes(B):
+    # 152 SMs = 76 CTA pairs; tiles are 256 x 256, k-blocks 64 deep.  The split S
+    # is the largest <= 16 dividing the k-blocks with >= 8 k-blocks per split and
+    # tiles * S <= 76; the workspace is 1 KB of counters plus tiles * S fp32 tiles.
+    tile_bytes = 256 * 256 * 4
+    # M=1024, N=1024: 16 tiles; K=8192: 128 k-blocks -> S=4 (16 * 4 = 64 <= 76)
+    assert B.tl_gemm_workspace_size(1024, 1024, 8192, 152) == 1024 + 16 * 4 * tile_bytes
+    assert B.tl_ag_gemm_workspace_size(8, 128, 8192, 1024, 152) == 1024 + 16 * 4 * tile_bytes
+    # 32 tiles -> S=2
+    assert B.tl_gemm_workspace_size(2048, 1024, 8192, 152) == 1024 + 32 * 2 * tile_bytes
+    # ragged: 600 x 520 is 3 x 3 tiles; K=2048 is 32 k-blocks -> S=4 (S=8 would leave 4 k-blocks)
+    assert B.tl_ag_gemm_workspace_size(2, 300, 2048, 520, 152) == 1024 + 9 * 4 * tile_bytes
+    # K=1000: 16 k-blocks -> S=2 (16 / 2 = 8), even for one tile
+    assert B.tl_gemm_workspace_size(104, 104, 1000, 152) == 1024 + 1 * 2 * tile_bytes
+    # no split: tiles fill the pairs, or too few k-blocks, or bad shapes
+    assert B.tl_gemm_workspace_size(8192, 1792, 4096, 152) == 0      # 224 tiles
+    assert B.tl_gemm_workspace_size(4096, 1024, 8192, 152) == 0      # 64 tiles: S=2 would need 128 units
+    assert B.tl_gemm_workspace_size(1024, 1024, 512, 152) == 0       # 8 k-blocks
+    assert B.tl_gemm_workspace_size(0, 1024, 8192, 152) == 0
+    assert B.tl_ag_gemm_workspace_size(0, 128, 8192, 1024, 152) == 0
+    # fewer SMs, fewer splits: 20 SMs = 10 pairs, 4 tiles -> S=2
+    assert B.tl_gemm_workspace_size(512, 512, 8192, 20) == 1024 + 4 * 2 * tile_bytes
+
+
 def test_ag_attn_num_flags(B):
     # one K and one V flag per 128-token chunk of every rank's shard
     assert B.tl_ag_attn_num_flags(8, 8192) == 2 * 8 * 64

@@ -29,7 +29,8 @@ STATUS_NAMES = {0: "TL_OK", 1: "TL_ERR_INVALID", 2: "TL_ERR_CUDA", 3: "TL_ERR_TI
 EXPORTED = [
     "tl_version", "tl_last_error", "tl_signals_create", "tl_signals_destroy", "tl_signals_flags",
     "tl_signals_reset", "tl_tile_notify", "tl_tile_wait", "tl_query_status",
-    "tl_gemm", "tl_ag_gemm_num_flags", "tl_ag_gemm_tile_order", "tl_ag_gemm",
+    "tl_gemm_workspace_size", "tl_gemm", "tl_ag_gemm_workspace_size", "tl_ag_gemm_num_flags",
+    "tl_ag_gemm_tile_order", "tl_ag_gemm",
     "tl_gemm_rs_workspace_size", "tl_gemm_rs_num_flags", "tl_gemm_rs", "tl_gemm_rs_noalloc",
     "tl_moe_workspace_size", "tl_moe_num_flags", "tl_moe_ag_gemm", "tl_allgather", "tl_reduce_scatter",
     "tl_moe_down_workspace_size", "tl_moe_down_num_flags", "tl_moe_down",
@@ -55,6 +56,7 @@ class tl_ag_gemm_args(ctypes.Structure):
         ("signals", _vp), ("src_ready", _vp),
         ("epoch", ctypes.c_uint32), ("reserved1", ctypes.c_uint32),
         ("timeout_ns", ctypes.c_uint64), ("trace", _vp),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -73,6 +75,7 @@ class tl_gemm_args(ctypes.Structure):
     _fields_ = [
         ("M", ctypes.c_int32), ("N", ctypes.c_int32), ("K", ctypes.c_int32), ("reserved0", ctypes.c_int32),
         ("A", _vp), ("B", _vp), ("C", _vp), ("C_f32", _vp), ("signals", _vp), ("timeout_ns", ctypes.c_uint64),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -140,7 +143,9 @@ _decl("tl_signals_reset", _i, _vp, _vp)
 _decl("tl_tile_notify", _i, _vp, _i, _i, _u32, _vp)
 _decl("tl_tile_wait", _i, _vp, _i, _i, _u32, _u64, _vp)
 _decl("tl_query_status", _i, _vp, _vp, ctypes.POINTER(_i), ctypes.POINTER(_i))
+_decl("tl_gemm_workspace_size", _sz, _i, _i, _i, _i)
 _decl("tl_gemm", _i, ctypes.POINTER(tl_gemm_args), _vp)
+_decl("tl_ag_gemm_workspace_size", _sz, _i, _i, _i, _i, _i)
 _decl("tl_ag_gemm_num_flags", _i, _i, _i, _i, _i, ctypes.POINTER(_i))
 _decl("tl_ag_gemm_tile_order", _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int32), _i)
 _decl("tl_ag_gemm", _i, ctypes.POINTER(tl_ag_gemm_args), _vp)
@@ -260,12 +265,26 @@ def tl_query_status(sig: Signals, stream=None):
     return code.value, where.value
 
 
-def tl_gemm(A, B, C, signals: Signals, *, C_f32=None, timeout_ns=0, stream=None):
-    """C = A . B (bf16 in, fp32 accumulate) with no communication."""
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def tl_gemm_workspace_size(M, N, K, sm_count=0):
+    return int(lib.tl_gemm_workspace_size(M, N, K, sm_count))
+
+
+def tl_ag_gemm_workspace_size(R, M_shard, K, N, sm_count=0):
+    return int(lib.tl_ag_gemm_workspace_size(R, M_shard, K, N, sm_count))
+
+
+def tl_gemm(A, B, C, signals: Signals, *, C_f32=None, timeout_ns=0, workspace=None, stream=None):
+    """C = A . B (bf16 in, fp32 accumulate) with no communication; split over K
+    when the tiles leave SMs idle and a (zeroed) workspace is given."""
     M, K = A.shape
     N = B.shape[1]
     a = tl_gemm_args(M=M, N=N, K=K, reserved0=0, A=_ptr(A), B=_ptr(B), C=_ptr(C), C_f32=_ptr(C_f32),
-                     signals=signals.handle, timeout_ns=int(timeout_ns))
+                     signals=signals.handle, timeout_ns=int(timeout_ns), workspace=_ptr(workspace),
+                     workspace_bytes=_nbytes(workspace))
     _check(lib.tl_gemm(ctypes.byref(a), _stream(stream)))
 
 
@@ -284,7 +303,7 @@ def tl_ag_gemm_tile_order(R, self_rank, M_shard):
 
 def tl_ag_gemm(A_shards, B, gathered, C, signals: Signals, epoch: int, *, self_rank=0, C_f32=None,
                mode=TL_MODE_PUSH, src_ready: Signals | None = None, rows_per_barrier=0, timeout_ns=0,
-               trace=None, swizzle=TL_SWIZZLE_ARRIVAL, stream=None):
+               trace=None, swizzle=TL_SWIZZLE_ARRIVAL, workspace=None, stream=None):
     """C = [A_0; ...; A_{R-1}] . B, gathered rows written to `gathered` (see tilelink.h)."""
     R = len(A_shards)
     M_shard, K = A_shards[0].shape
@@ -295,7 +314,8 @@ def tl_ag_gemm(A_shards, B, gathered, C, signals: Signals, epoch: int, *, self_r
                         A_shards=ctypes.cast(ptrs, ctypes.POINTER(_vp)), B=_ptr(B), gathered=_ptr(gathered),
                         C=_ptr(C), C_f32=_ptr(C_f32), signals=signals.handle,
                         src_ready=src_ready.handle if src_ready is not None else None,
-                        epoch=int(epoch) & 0xFFFFFFFF, reserved1=0, timeout_ns=int(timeout_ns), trace=_ptr(trace))
+                        epoch=int(epoch) & 0xFFFFFFFF, reserved1=0, timeout_ns=int(timeout_ns), trace=_ptr(trace),
+                        workspace=_ptr(workspace), workspace_bytes=_nbytes(workspace))
     _check(lib.tl_ag_gemm(ctypes.byref(a), _stream(stream)))
 
 

@@ -18,6 +18,9 @@
 //   warps 2-5   epilogue: TMEM -> registers -> bf16 (and fp32) rows of C.
 //   warp 6      copy (AllGather producer): bulk-TMA copies of shard row chunks
 //               into `gathered`, then a release store of the chunk's flag.
+// When the tiles would leave pairs idle and the caller gives a workspace, each
+// tile's k-blocks are split over S units on S pairs (split-K, tl_splitk.cuh);
+// the tile's rows are waited for by every unit of the tile.
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -27,6 +30,7 @@
 #include "tl_epilogue.cuh"
 #include "tl_internal.h"
 #include "tl_pair.cuh"
+#include "tl_splitk.cuh"
 
 namespace tl {
 namespace {
@@ -58,7 +62,9 @@ struct AgParams {
   uint64_t timeout_ns;       // bound of each flag wait
   uint64_t pipe_timeout_ns;  // bound of each pipeline (mbarrier) wait: 2 x flag bound + 1 s
   int32_t R, self, M_shard, K, N, M;
-  int32_t rpb, bpr, Mt, Nt, KB, num_items, num_work;
+  int32_t rpb, bpr, Mt, Nt, KB, num_items;
+  int32_t S, KBs, num_work;  // splits per tile, k-blocks per split, work units (tiles * S)
+  splitk::Work sk;
   uint32_t epoch;
   uint64_t host_mask;  // shards in host memory (copied with plain loads)
   uint16_t m_order[AG_MAX_MTILES];
@@ -91,8 +97,9 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
     pair::Producer prod;
     int last_m = -1;
     for (int w = pair_id; w < p.num_work; w += npairs) {
-      const int n = w % p.Nt;
-      const int m = p.m_order[w / p.Nt];
+      const int t = w / p.S, split = w % p.S;  // schedule slot of the tile, k range
+      const int n = t % p.Nt;
+      const int m = p.m_order[t / p.Nt];
       const int row0 = m * pair::BM + int(rank) * pair::HM;
       const bool any = row0 < p.M;
       const int row1 = min(p.M, row0 + pair::HM) - 1;
@@ -106,11 +113,11 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
       last_m = m;
       __syncwarp();
       if (lane == 0) {
-        if (p.trace && rank == 0) p.trace[w] = m * p.Nt + n;
+        if (p.trace && rank == 0 && split == 0) p.trace[t] = m * p.Nt + n;
         if (!local) fence_proxy_async_global();
         const CUtensorMap* ma = local ? &p.map_self : &p.map_g;
         const int a_y = local ? row0 - p.self * p.M_shard : row0;
-        for (int kb = 0; kb < p.KB; ++kb)
+        for (int kb = split * p.KBs; kb < (split + 1) * p.KBs; ++kb)
           if (!prod.load(smem, bars, rank, ma, kb * pair::BK, a_y, &p.map_b, n * pair::BN + int(rank) * pair::HN,
                          kb * pair::BK, abort, p.status, p.pipe_timeout_ns))
             break;
@@ -121,7 +128,7 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA issuer (leader CTA)
     if (lane == 0 && rank == 0)
-      pair::mma_loop(smem, bars, tmem_base, my_work, p.KB, abort, p.status, p.pipe_timeout_ns);
+      pair::mma_loop(smem, bars, tmem_base, my_work, p.KBs, abort, p.status, p.pipe_timeout_ns);
     __syncwarp();
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
     // ---------------------------------------------------------------- epilogue (this CTA's 128 rows)
@@ -131,33 +138,42 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
     for (int w = pair_id; w < p.num_work; w += npairs, ++j) {
       const int acc = j & 1;
       const uint32_t acc_ph = uint32_t(j >> 1) & 1u;
-      const int n = w % p.Nt;
-      const int m = p.m_order[w / p.Nt];
+      const int t = w / p.S, split = w % p.S;
+      const int n = t % p.Nt;
+      const int m = p.m_order[t / p.Nt];
       const bool ok = mbar_wait(&bars->tmem_full[acc], acc_ph, abort, p.status, p.pipe_timeout_ns, 4);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      // split-K epilogues meet at named barriers, so all four warps leave together
+      if (!(p.S > 1 ? named_bar_and(splitk::kBarrier, kNumEpiThreads, ok) : __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       const int row = m * pair::BM + int(rank) * pair::HM + wq * 32 + lane;
       const bool row_ok = row < p.M;
-      for (int c = 0; c < pair::BN / 32; ++c) {
+      const int row_base = m * pair::BM + int(rank) * pair::HM + wq * 32;
+      const int nchunks = min(pair::BN / 32, (p.N - n * pair::BN + 31) / 32);
+      const uint32_t tacc = tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN);
+      // chunk c of the finished tile (fp32 bits) to C and C_f32
+      auto write_c = [&](int c, const uint32_t* v) {
         const int col0 = n * pair::BN + c * 32;
-        if (col0 >= p.N) break;
-        uint32_t v[32];
-        tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
-        tmem_ld_wait();
         // bf16 C: this warp's 32 x 32 box with one TMA store (rows past M are not written)
-        const int row_base = m * pair::BM + int(rank) * pair::HM + wq * 32;
         if (row_base < p.M) store_box_bf16(&p.map_c, cbox, 1, lane, v, col0, row_base);
-        if (row_ok) {
-          if (p.C_f32) {
-            float* frow = p.C_f32 + size_t(row) * p.N + col0;
+        if (row_ok && p.C_f32) {
+          float* frow = p.C_f32 + size_t(row) * p.N + col0;
 #pragma unroll
-            for (int g = 0; g < 8; ++g) {
-              if (col0 + g * 4 < p.N) {
-                const float* f = reinterpret_cast<const float*>(v + g * 4);
-                st_global_cg_v4f(frow + g * 4, f[0], f[1], f[2], f[3]);
-              }
+          for (int g = 0; g < 8; ++g) {
+            if (col0 + g * 4 < p.N) {
+              const float* f = reinterpret_cast<const float*>(v + g * 4);
+              st_global_cg_v4f(frow + g * 4, f[0], f[1], f[2], f[3]);
             }
           }
+        }
+      };
+      if (p.S > 1) {
+        splitk::epilogue(p.sk, t, split, rank, wq, lane, tacc, nchunks, &bars->splitk_ok, p.status, write_c);
+      } else {
+        for (int c = 0; c < nchunks; ++c) {
+          uint32_t v[32];
+          tmem_ld_32cols(tacc + uint32_t(c * 32), v);
+          tmem_ld_wait();
+          write_c(c, v);
         }
       }
       tc_fence_before();
@@ -188,6 +204,18 @@ extern "C" int tl_ag_gemm_num_flags(int R, int M_shard, int K, int rows_per_barr
   int rpb = rows_per_barrier > 0 ? std::min(rows_per_barrier, M_shard) : tl::default_rpb(K, M_shard);
   if (effective_rpb) *effective_rpb = rpb;
   return R * tl::cdiv(M_shard, rpb);
+}
+
+extern "C" size_t tl_ag_gemm_workspace_size(int R, int M_shard, int K, int N, int sm_count) {
+  if (R < 1 || M_shard < 1 || K < 1 || N < 1) return 0;
+  if (sm_count <= 0) {
+    tl::DeviceInfo di{};
+    if (tl::device_info(&di)) return 0;
+    sm_count = di.sm_count;
+  }
+  const long long tiles = ((long long)R * M_shard + tl::pair::BM - 1) / tl::pair::BM * tl::cdiv(N, tl::pair::BN);
+  const int S = tl::splitk::choose(tiles, tl::cdiv(K, tl::pair::BK), sm_count / 2);
+  return tl::splitk::workspace_bytes(tiles, S);
 }
 
 extern "C" tl_status tl_ag_gemm_tile_order(int R, int self_rank, int M_shard, int32_t* m_order, int capacity) {
@@ -228,7 +256,8 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
   if (a->epoch == 0) return fail(TL_ERR_INVALID, "tl_ag_gemm: epoch must be nonzero");
   for (int r = 0; r < a->R; ++r)
     if (!a->A_shards[r] || !aligned16(a->A_shards[r])) return fail(TL_ERR_INVALID, "tl_ag_gemm: shard %d pointer", r);
-  if (!aligned16(a->B) || !aligned16(a->gathered) || !aligned16(a->C) || (a->C_f32 && !aligned16(a->C_f32)))
+  if (!aligned16(a->B) || !aligned16(a->gathered) || !aligned16(a->C) || (a->C_f32 && !aligned16(a->C_f32)) ||
+      (a->workspace && !aligned16(a->workspace)))
     return fail(TL_ERR_INVALID, "tl_ag_gemm: pointers must be 16-byte aligned");
   const long long M = (long long)a->R * a->M_shard;
   const int Mt = int((M + pair::BM - 1) / pair::BM);
@@ -285,8 +314,25 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
     p->Nt = cdiv(a->N, pair::BN);
     p->KB = cdiv(a->K, pair::BK);
     p->num_items = a->R * p->bpr;
-    p->num_work = Mt * p->Nt;
     p->epoch = a->epoch;
+    // split-K when the tiles leave pairs idle and the caller gave a workspace
+    const long long tiles = (long long)Mt * p->Nt;
+    p->S = a->workspace ? splitk::choose(tiles, p->KB, di.sm_count / 2) : 1;
+    if (p->S > 1) {
+      const size_t need = splitk::workspace_bytes(tiles, p->S);
+      if (a->workspace_bytes < need) {
+        st = fail(TL_ERR_INVALID, "tl_ag_gemm: workspace of %zu bytes, split-K needs %zu", a->workspace_bytes, need);
+        break;
+      }
+      uint8_t* ws = static_cast<uint8_t*>(a->workspace);
+      p->sk.counters = reinterpret_cast<uint32_t*>(ws);
+      p->sk.partials = reinterpret_cast<float*>(ws + splitk::counter_bytes(tiles));
+      p->sk.tag = (a->epoch % 0xFFFFFFu + 1u) << 8;  // nonzero; repeats every 2^24 - 1 epochs
+      p->sk.timeout_ns = p->timeout_ns;
+      p->sk.S = p->S;
+    }
+    p->KBs = p->KB / p->S;
+    p->num_work = int(tiles) * p->S;
     int32_t order[AG_MAX_MTILES];
     if ((st = tl_ag_gemm_tile_order(a->R, a->self_rank, a->M_shard, order, AG_MAX_MTILES))) break;
     for (int i = 0; i < Mt; ++i) p->m_order[i] = uint16_t(a->swizzle == TL_SWIZZLE_ROWS ? i : order[i]);

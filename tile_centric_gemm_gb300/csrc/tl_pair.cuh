@@ -35,6 +35,7 @@ struct __align__(8) Bars {
   uint64_t copy[COPY_NBUF];  // copy-warp staging
   uint32_t tmem_base;
   uint32_t abort;
+  uint32_t splitk_ok;        // split-K: every split of this CTA's half-tile arrived
 };
 
 // Four UMMA_K steps of one k-block from stage s; issued by the leader only.
