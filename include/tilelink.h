@@ -204,7 +204,7 @@ typedef struct tl_ag_gemm_args {
  * must not run concurrently.  The S units of a tile wait for one another, so a
  * split call needs its whole grid resident at once: with other kernels holding
  * SMs at the same time it can fail with TL_ERR_TIMEOUT (the AG-GEMM's flag
- * waits already need the same). 
+ * waits already need the same).
  * Workspace bytes for a shape: 0 when no split would be used.  sm_count 0 =
  * the current device's SM count (the launch uses the device's own count). */
 size_t tl_ag_gemm_workspace_size(int R, int M_shard, int K, int N, int sm_count);
