@@ -2,8 +2,9 @@
 // idle.
 //
 // A tile's k-blocks are cut into S equal ranges that run as separate work units
-// (unit = tile * S + split) on separate pairs, all in one wave of the
-// cooperative launch (tiles * S <= pairs, one unit per pair).  Each CTA of a
+// (unit = tile * S + split) on separate pairs, all in one wave of a launch
+// whose grid the device holds at once (tiles * S <= pairs, one unit per
+// pair).  Each CTA of a
 // unit writes its fp32 128 x 256 half of the partial tile into its own
 // workspace slot and counts itself in on that half-tile's counter; once all S
 // have counted in (a bounded wait), split s sums the S partials of its share of
@@ -20,8 +21,9 @@
 // GEMM uses one fixed tag, so after a call that reported a device error its
 // counters must be zeroed before the workspace is reused.
 //
-// Workspace: counters [tiles][2 halves][arrive, depart] uint32 (padded to 1 KB), then partial halves
-// [tiles][S][2] of 128 x 256 fp32 each, stored per epilogue warp (32 rows) as
+// Workspace: counters [tiles][2 halves][arrive, depart] uint32 (padded to a
+// multiple of 1 KB), then partial halves [tiles][S][2] of 128 x 256 fp32 each,
+// stored per epilogue warp (32 rows) as
 // [32-column chunk][group of 4 columns][row][4]: one warp-wide 16-byte access
 // covers 512 contiguous bytes.
 #pragma once
