@@ -3,15 +3,14 @@
 //
 // A tile's k-blocks are cut into S equal ranges that run as separate work units
 // (unit = tile * S + split) on separate pairs, all in one wave of a launch
-// whose grid the device holds at once (tiles * S <= pairs, one unit per
-// pair).  Each CTA of a
-// unit writes its fp32 128 x 256 half of the partial tile into its own
-// workspace slot and counts itself in on that half-tile's counter; once all S
-// have counted in (a bounded wait), split s sums the S partials of its share of
-// the columns, in split order 0, 1, ..., S-1 (its own from TMEM, the others
-// through L2), and writes that share of C.  The fixed order makes the result
-// independent of the schedule; spreading the sums over the S CTAs keeps each
-// one's reads at (S-1)/S of a half-tile.
+// whose grid the device holds at once (tiles * S <= pairs, one unit per pair).
+// Each CTA of a unit writes its fp32 128 x 256 half of the partial tile into
+// its own workspace slot and counts itself in on that half-tile's counter; once
+// all S have counted in (a bounded wait), split s sums the S partials of its
+// share of the columns, in split order 0, 1, ..., S-1 (its own from TMEM, the
+// others through L2), and writes that share of C.  The fixed order makes the
+// result independent of the schedule; spreading the sums over the S CTAs keeps
+// each one's reads at (S-1)/S of a half-tile.
 //
 // Each half-tile has an arrival and a departure counter holding
 // (tag << 8) | count; the split that departs last zeroes both, so a completed
@@ -23,9 +22,8 @@
 //
 // Workspace: counters [tiles][2 halves][arrive, depart] uint32 (padded to a
 // multiple of 1 KB), then partial halves [tiles][S][2] of 128 x 256 fp32 each,
-// stored per epilogue warp (32 rows) as
-// [32-column chunk][group of 4 columns][row][4]: one warp-wide 16-byte access
-// covers 512 contiguous bytes.
+// stored per epilogue warp (32 rows) as [32-column chunk][group of 4 columns]
+// [row][4]: one warp-wide 16-byte access covers 512 contiguous bytes.
 #pragma once
 
 #include "tl_epilogue.cuh"
