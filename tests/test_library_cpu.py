@@ -126,3 +126,18 @@ def test_gemm_rs_rejects_unknown_options_without_launch(B):
                           signals=64, epoch=1, options=8, timeout_ns=0, trace=None)
     assert B.lib.tl_gemm_rs(ctypes.byref(a), None) == B.TL_ERR_INVALID
     assert "options" in B.tl_last_error()
+
+
+def test_splitk_workspace_alignment_checked_without_launch(B):
+    # a split-K workspace must be 16-byte aligned; the check runs before any device query
+    ptrs = (ctypes.c_void_p * 2)(16, 32)
+    a = B.tl_ag_gemm_args(R=2, self_rank=0, M_shard=128, K=8192, N=256, mode=B.TL_MODE_PUSH, rows_per_barrier=0,
+                          swizzle=0, A_shards=ctypes.cast(ptrs, ctypes.POINTER(ctypes.c_void_p)), B=48,
+                          gathered=64, C=80, C_f32=None, signals=96, src_ready=None, epoch=1, reserved1=0,
+                          timeout_ns=0, trace=None, workspace=104, workspace_bytes=1 << 30)
+    assert B.lib.tl_ag_gemm(ctypes.byref(a), None) == B.TL_ERR_INVALID
+    assert "aligned" in B.tl_last_error()
+    g = B.tl_gemm_args(M=256, N=256, K=8192, reserved0=0, A=16, B=32, C=48, C_f32=None, signals=64, timeout_ns=0,
+                       workspace=72, workspace_bytes=1 << 30)
+    assert B.lib.tl_gemm(ctypes.byref(g), None) == B.TL_ERR_INVALID
+    assert "aligned" in B.tl_last_error()
