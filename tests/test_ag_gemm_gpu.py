@@ -259,6 +259,17 @@ def test_ag_splitk_deterministic_and_stale_counters(B):
     check_all(B, A, Bm, r3)
 
 
+@pytest.mark.parametrize("mode,host_ranks", [("pull", ()), ("push", (0, 2)), ("pull", (0, 2))])
+def test_ag_splitk_pull_mode_and_host_shards(B, mode, host_ranks):
+    # split units of one tile each wait for the tile's rows, whichever path brings them
+    R, Ms, K, N = 3, 100, 2048, 264
+    A, Bm = inputs.ag_gemm_inputs(R, Ms, K, N, "normal", seed=71 + len(host_ranks))
+    m = B.TL_MODE_PULL if mode == "pull" else B.TL_MODE_PUSH
+    r = run_ag(B, A, Bm, self_rank=1, mode=m, f32=True, trace=True, host_ranks=host_ranks,
+               ws=splitk_ws(B, R, Ms, K, N))
+    check_all(B, A, Bm, r, self_rank=1)
+
+
 def test_ag_splitk_rejects_small_workspace(B):
     import torch
     R, Ms, K, N = 2, 300, 2048, 520
