@@ -44,6 +44,8 @@ def test_gemm_parity(B, M, N, K):
     (1024, 1024, 8192, 4),   # 16 tiles, 128 k-blocks
     (300, 264, 2048, 4),     # 2 x 2 ragged tiles, 32 k-blocks
     (104, 104, 1000, 2),     # one tile, 16 k-blocks with a K tail
+    (512, 512, 8192, 16),    # the most splits: 4 tiles x 16, half the splits sum no chunk
+    (512, 264, 8192, 16),    # N tail: the second tile column has one chunk for 16 splits
 ])
 def test_gemm_splitk_parity(B, M, N, K, splits):
     import torch
