@@ -77,3 +77,29 @@ def test_gemm_llm_shape_sampled(B):
     rng = np.random.default_rng(0)
     rows, cols = rng.integers(0, 8192, 3000), rng.integers(0, 1792, 3000)
     check_bf16(to_f64(C)[rows, cols], oracle.ag_gemm.ag_gemm_at(A, Bm, rows, cols), "C sampled")
+
+
+def test_gemm_splitk_graph_replays(B):
+    # a captured call runs again with the same arguments: the last split to depart
+    # zeroes the counters, so every replay counts from zero and gives the same bits
+    import torch
+    M, N, K = 512, 512, 8192
+    A, Bm = inputs.ag_gemm_inputs(1, M, K, N, "normal", seed=91)
+    dA, dB = dev_bf16(A[0]), dev_bf16(Bm)
+    ws = torch.zeros(B.tl_gemm_workspace_size(M, N, K), dtype=torch.uint8, device="cuda")
+    C = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sig = B.Signals(1)
+    B.tl_gemm(dA, dB, C, sig, workspace=ws)  # sets the kernel's launch attributes before the capture
+    torch.cuda.synchronize()
+    want = to_bits(C).copy()
+    check_bf16(to_f64(C), oracle.ag_gemm.ag_gemm(A, Bm), "C")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        B.tl_gemm(dA, dB, C, sig, workspace=ws)
+    for _ in range(3):
+        C.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert B.tl_query_status(sig) == (0, -1)
+        np.testing.assert_array_equal(to_bits(C), want)
+        assert int(ws[:1024].count_nonzero()) == 0
