@@ -231,6 +231,7 @@ def splitk_ws(B, R, Ms, K, N):
     (1, 256, 1024, 256, 0, 2),     # one tile, 16 k-blocks in two ranges
     (3, 100, 1000, 264, 2, 2),     # K tail inside the last range (16 k-blocks, the last partial)
     (3, 100, 136, 264, 1, 1),      # too few k-blocks to split: the workspace is left unused
+    (64, 4, 8192, 256, 37, 16),    # the most ranks and the most splits: one tile over 64 shards, 16 ranges
 ])
 def test_ag_splitk_parity(B, R, Ms, K, N, self_rank, splits):
     n = B.tl_ag_gemm_workspace_size(R, Ms, K, N)
