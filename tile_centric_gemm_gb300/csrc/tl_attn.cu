@@ -14,13 +14,16 @@
 // tile.
 //   warp 0      TMA producer: the unit's Q tiles, then per key/value tile its
 //               arrival flags (peers' shards only), K (128 keys x 128 dims)
-//               and V (128 keys x 128 dims) into two-stage rings.
+//               and V (128 keys x 128 dims) into two- and three-stage rings.
 //   warp 1      MMA issuer: S_X = Q_X K^T and O_X += P_X V with
 //               tcgen05.mma.cta_group::1 (M = 128, N = 128), in the order
 //               QK_A(0) QK_B(0) | PV_A(j) QK_A(j+1) PV_B(j) QK_B(j+1) | ...,
 //               so that one tile's softmax runs while the tensor cores work on
 //               the other tile.  P V takes its A operand (P) from TMEM.
-//   warp 2      copy warp (AllGather producer), as in the AllGather-GEMM.
+//   warp 2      copy warp (AllGather producer): the AllGather-GEMM's item
+//               order and flags, but plain 16-byte loads and stores instead of
+//               bulk copies through shared memory, whose room holds the third
+//               V stage (7.10 against 7.28 ms with two V stages and staging).
 //   warp 3      idle.
 //   warps 4-7   softmax of tile A, warps 8-11 of tile B, one query row per
 //               thread: S from TMEM, running max m and sum l (base 2), P as
@@ -49,8 +52,7 @@ constexpr int KV_TILE = 128;     // keys per tile (the flag granularity too)
 constexpr int Q_ROWS = 128;      // query rows per tile
 constexpr int UNIT_ROWS = 256;   // two 128-row tiles per unit
 constexpr int KST = 2;           // K ring stages
-constexpr int VST = 2;           // V ring stages
-constexpr int ATT_COPY_NBUF = 3;
+constexpr int VST = 3;           // V ring stages
 constexpr int ATT_THREADS = 12 * 32;
 constexpr int kWarpCopyA = 2;
 constexpr int kWarpSoftmax0 = 4;
@@ -63,8 +65,7 @@ constexpr uint32_t V_STAGE = 2 * BOX;          // 32 KB: 128 keys x 128 dims (di
 constexpr uint32_t SMEM_Q = 0;
 constexpr uint32_t SMEM_K = SMEM_Q + 2 * Q_TILE;
 constexpr uint32_t SMEM_V = SMEM_K + KST * K_STAGE;
-constexpr uint32_t SMEM_COPY = SMEM_V + VST * V_STAGE;
-constexpr uint32_t SMEM_BARS = SMEM_COPY + ATT_COPY_NBUF * COPY_CHUNK;
+constexpr uint32_t SMEM_BARS = SMEM_V + VST * V_STAGE;
 
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(Q_ROWS, KV_TILE, false);  // B = K rows, K-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(Q_ROWS, HD, true);        // B = V [keys, dims], dims contiguous
@@ -75,7 +76,6 @@ struct __align__(8) AttnBars {
   uint64_t v_full[VST], v_empty[VST];
   uint64_t s_full[2], p_full[2];
   uint64_t o_full[2], o_empty[2];
-  uint64_t copy[ATT_COPY_NBUF];
   uint32_t tmem_base;
   uint32_t abort;
 };
@@ -104,7 +104,6 @@ struct AttnParams {
   int32_t num_units, num_items;
   float scale_log2;
   uint32_t epoch;
-  uint64_t host_mask_k, host_mask_v;
 };
 
 __device__ __forceinline__ void unit_of(const AttnParams& p, int u, int& h, int& qb) {
@@ -221,7 +220,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int b = 0; b < ATT_COPY_NBUF; ++b) mbar_init(&bars->copy[b], 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -365,18 +363,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) ag_attn_kernel(const __grid_co
     __syncwarp();
   } else if (warp == kWarpCopyA) {
     // ---------------------------------------------------------------- AllGather producer (K and V chunks)
+    // every shard, in device or pinned host memory, is copied with plain loads
     AgCopyJob jk{p.k_shard, p.kg, p.flags, nullptr, p.status, p.timeout_ns, p.pipe_timeout_ns,
-                 p.R, p.self, p.S, p.Hkv * HD, KV_TILE, p.T, p.num_items, p.epoch, p.host_mask_k};
+                 p.R, p.self, p.S, p.Hkv * HD, KV_TILE, p.T, p.num_items, p.epoch, 0};
     AgCopyJob jv{p.v_shard, p.vg, p.flags + p.R * p.T, nullptr, p.status, p.timeout_ns, p.pipe_timeout_ns,
-                 p.R, p.self, p.S, p.Hkv * HD, KV_TILE, p.T, p.num_items, p.epoch, p.host_mask_v};
-    uint32_t seq = 0;
-    uint8_t* stage = smem + SMEM_COPY;
+                 p.R, p.self, p.S, p.Hkv * HD, KV_TILE, p.T, p.num_items, p.epoch, 0};
     for (int it = cta; it < p.num_items; it += nctas) {
-      if (ag_copy_one<ATT_COPY_NBUF>(jk, it, stage, bars->copy, abort, seq)) break;
-      if (ag_copy_one<ATT_COPY_NBUF>(jv, it, stage, bars->copy, abort, seq)) break;
+      ag_copy_one_plain(jk, it);
+      ag_copy_one_plain(jv, it);
+      if (__shfl_sync(0xffffffffu, *abort, 0)) break;
     }
-    if (lane == 0) bulk_wait<0>();
-    __syncwarp();
   } else if (warp >= kWarpSoftmax0) {
     // ---------------------------------------------------------------- softmax warps (one row per thread)
     const int X = (warp - kWarpSoftmax0) >> 2;
@@ -592,8 +588,6 @@ extern "C" tl_status tl_ag_attn(const tl_ag_attn_args* a, void* stream) {
       p->k_shard[r] = kdev[r];
       p->v_shard[r] = vdev[r];
     }
-    p->host_mask_k = kmask;
-    p->host_mask_v = vmask;
     p->kg = static_cast<uint8_t*>(a->K_gathered);
     p->vg = static_cast<uint8_t*>(a->V_gathered);
     p->O = static_cast<uint16_t*>(a->O);

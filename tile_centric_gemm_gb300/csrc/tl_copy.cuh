@@ -29,8 +29,8 @@ struct AgCopyJob {
   uint64_t host_mask;  // bit r: shard r is host (or managed) memory, copied with plain loads
 };
 
-// Copy `bytes` (a multiple of 16) from host-resident src to dst with every lane
-// of the warp: kVec 16-byte loads in flight per lane.
+// Copy `bytes` (a multiple of 16) from src (host or device memory) to dst with
+// every lane of the warp: kVec 16-byte loads in flight per lane.
 __device__ __forceinline__ void copy_rows_plain(const uint8_t* src, uint8_t* dst, uint32_t bytes, int lane) {
   constexpr int kVec = 8;
   const uint4* s = reinterpret_cast<const uint4*>(src);
@@ -51,9 +51,52 @@ __device__ __forceinline__ void copy_rows_plain(const uint8_t* src, uint8_t* dst
   }
 }
 
-// Copy item `it` of the job (shard (self + 1 + it / bpr) mod R, row chunk
-// it % bpr) into the gathered buffer and release its flag.  Called by all 32
-// lanes of one warp.  `stage` holds NBUF buffers of COPY_CHUNK bytes; `bars`
+// Item `it` of the job: shard (self + 1 + it / bpr) mod R, row chunk it % bpr.
+struct AgItem {
+  const uint8_t* src;
+  uint8_t* dst;
+  uint32_t bytes;
+  int flag_id;
+  int r;
+};
+__device__ __forceinline__ AgItem ag_item(const AgCopyJob& j, int it) {
+  const int jj = it / j.bpr, b = it % j.bpr;
+  const int r = (j.self + 1 + jj) % j.R;
+  const int lo = b * j.rpb;
+  const int rows = min(j.rpb, j.M_shard - lo);
+  return AgItem{j.shard[r] + size_t(lo) * j.K * 2, j.gathered + (size_t(r) * j.M_shard + lo) * size_t(j.K) * 2,
+                uint32_t(rows) * uint32_t(j.K) * 2u, r * j.bpr + b, r};
+}
+// Pull mode: the source publishes readiness first (first barrier of the pull
+// protocol); a chunk whose source never became ready is neither copied nor
+// announced.  Returns whether to copy (on every lane).
+__device__ __forceinline__ bool ag_item_ready(const AgCopyJob& j, const AgItem& x, int lane) {
+  bool ready = true;
+  if (j.ready && lane == 0)
+    ready = wait_flag(j.ready + x.flag_id, j.epoch, j.status, j.timeout_ns, uint32_t(x.flag_id), TL_ERR_TIMEOUT);
+  return __shfl_sync(0xffffffffu, ready, 0);
+}
+// Plain 16-byte loads and stores by every lane, then the release of the chunk's flag.
+__device__ __forceinline__ void ag_item_copy_plain(const AgCopyJob& j, const AgItem& x, int lane) {
+  copy_rows_plain(x.src, x.dst, x.bytes, lane);
+  // produce_tile_notify: every lane's stores are ordered before lane 0's release
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) st_release(j.flags + x.flag_id, j.epoch);
+}
+
+// Copy item `it` with plain loads and stores only (no shared-memory staging):
+// for a kernel whose shared memory holds other stages.  Called by all 32 lanes
+// of one warp; consumers fence the async proxy before their TMA loads of it.
+__device__ __forceinline__ void ag_copy_one_plain(const AgCopyJob& j, int it) {
+  const int lane = int(lane_id());
+  const AgItem x = ag_item(j, it);
+  if (ag_item_ready(j, x, lane)) ag_item_copy_plain(j, x, lane);
+}
+
+// Copy item `it` into the gathered buffer and release its flag: bulk copies
+// through shared memory, or plain loads for a shard in host memory.  Called by
+// all 32 lanes of one warp.  `stage` holds NBUF buffers of COPY_CHUNK bytes; `bars`
 // NBUF mbarriers initialised with count 1; `seq` (lane 0's count of chunks
 // staged so far: buffer seq % NBUF, parity (seq / NBUF) & 1) carries the
 // staging ring's state from one call to the next.  Returns true (on every
@@ -63,26 +106,14 @@ __device__ __forceinline__ bool ag_copy_one(const AgCopyJob& j, int it, uint8_t*
                                             volatile uint32_t* abort, uint32_t& seq) {
   static_assert(NBUF >= 1 && NBUF <= COPY_NBUF, "staging buffers");
   const int lane = int(lane_id());
-  const int jj = it / j.bpr, b = it % j.bpr;
-  const int r = (j.self + 1 + jj) % j.R;
-  const int lo = b * j.rpb;
-  const int rows = min(j.rpb, j.M_shard - lo);
-  const uint8_t* src = j.shard[r] + size_t(lo) * j.K * 2;
-  uint8_t* dst = j.gathered + (size_t(r) * j.M_shard + lo) * size_t(j.K) * 2;
-  const uint32_t bytes = uint32_t(rows) * uint32_t(j.K) * 2u;
-  const int flag_id = r * j.bpr + b;
-  // pull mode: the source publishes readiness first (first barrier of the pull protocol);
-  // a chunk whose source never became ready is neither copied nor announced
-  bool ready = true;
-  if (j.ready && lane == 0)
-    ready = wait_flag(j.ready + flag_id, j.epoch, j.status, j.timeout_ns, uint32_t(flag_id), TL_ERR_TIMEOUT);
-  if (!__shfl_sync(0xffffffffu, ready, 0)) return false;
-  if ((j.host_mask >> r) & 1ull) {
-    copy_rows_plain(src, dst, bytes, lane);
-    // produce_tile_notify: every lane's stores are ordered before lane 0's release
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) st_release(j.flags + flag_id, j.epoch);
+  const AgItem x = ag_item(j, it);
+  const uint8_t* src = x.src;
+  uint8_t* dst = x.dst;
+  const uint32_t bytes = x.bytes;
+  const int flag_id = x.flag_id;
+  if (!ag_item_ready(j, x, lane)) return false;
+  if ((j.host_mask >> x.r) & 1ull) {
+    ag_item_copy_plain(j, x, lane);
     return false;
   }
   bool dead = false;
