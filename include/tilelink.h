@@ -460,9 +460,10 @@ tl_status tl_moe_down(const tl_moe_down_args* args, void* stream);
  *   O[t, h] = bf16( sum_j exp(s_j - lse) Vg[j, hk] ),  lse[h, t] = log sum_j exp(s_j)
  * One launch of single CTAs, one per SM (tcgen05.mma.cta_group::1):
  *  - producer: a copy warp per CTA moves the peers' key and value shards, 128
- *    tokens at a time, into K_gathered / V_gathered (bulk TMA copies; plain
- *    loads for pinned-host shards) and releases one flag per chunk of each
- *    (produce_tile_notify), shards self+1, ..., self+R-1, then self;
+ *    tokens at a time, into K_gathered / V_gathered (plain 16-byte loads and
+ *    stores, from device or pinned host memory) and releases one flag per
+ *    chunk of each (produce_tile_notify), shards self+1, ..., self+R-1, then
+ *    self;
  *  - consumer: work units of one head and 256 query rows (two 128-row tiles
  *    that share every key/value tile); each unit streams its own shard's keys
  *    and values first (in place, no wait), then the peers' in copy order,
