@@ -329,9 +329,31 @@ def check_gemm_rs_variant(variant, gemm_rs):
     np.testing.assert_array_equal([o[0, 0] for o in variant(A, B, "f32", "rank")], [0.0, 0.0, 0.0, 0.0])
 
 
-def check_moe_down(moe_down, route):
+def check_partial_abs_sum(partial_abs_sum):
+    """sum_r |P_r| by hand.  One element, three ranks with one-term partials 1, -2,
+    3: the magnitudes add to 6 (the signed sum is 2).  Then a partial that cancels
+    inside its own dot product: P_0 = 1*2 + (-1)*3 = -1 and P_1 = 2*1 + 0*5 = 2
+    give 3 -- not 7, the sum of |a_k| |b_k| over the terms, nor 1, the magnitude
+    of the summed partials.  Finally a 2 x 2 case by hand, rows and columns
+    distinct so a transposed operand shows."""
+    one = _bits(np.array([[1.0]]))
+    T = partial_abs_sum([_bits(np.array([[v]])) for v in (1.0, -2.0, 3.0)], [one] * 3)
+    np.testing.assert_array_equal(T, [[6.0]])
+    A = [_bits(np.array([[1.0, -1.0]])), _bits(np.array([[2.0, 0.0]]))]
+    B = [_bits(np.array([[2.0], [3.0]])), _bits(np.array([[1.0], [5.0]]))]
+    np.testing.assert_array_equal(partial_abs_sum(A, B), [[3.0]])
+    # P_0 = [[1, 2], [3, 4]] @ [[1, 0], [-1, 1]] = [[-1, 2], [-1, 4]]; P_1 = -I
+    A = [_bits(np.array([[1.0, 2.0], [3.0, 4.0]])), _bits(np.array([[-1.0, 0.0], [0.0, -1.0]]))]
+    B = [_bits(np.array([[1.0, 0.0], [-1.0, 1.0]])), _bits(np.eye(2))]
+    np.testing.assert_array_equal(partial_abs_sum(A, B), [[2.0, 2.0], [1.0, 5.0]])
+
+
+def check_moe_down(moe_down, route, moe_down_at):
     """Pins of the MoE down-projection side: brute force on a tiny case, the
-    plain-GEMM special case, and linearity in the ranks and in the gates."""
+    plain-GEMM special case, and linearity in the ranks and in the gates.  The
+    element-at-a-time sampler moe_down_at is held to the same brute force at
+    every (token, column) of the tiny case, with both gates and with slot 1's
+    gate zeroed."""
     rng = np.random.default_rng(23)
     # brute force: R = 2 ranks, T = 6 tokens of T_r = 3, top-2 of E = 3, I_r = 2, Hd = 3
     R, T_r, E, k, I_r, Hd = 2, 3, 3, 2, 2, 3
@@ -347,6 +369,7 @@ def check_moe_down(moe_down, route):
     dec = lambda b: np.asarray(b, dtype=np.uint32).astype(np.uint32) << 16
     Hf = [dec(h).view(np.float32).astype(np.float64) for h in H]
     Wf = [dec(w).view(np.float32).astype(np.float64) for w in W2]
+    brute = np.zeros((T, Hd))
     for t in range(T):
         for c in range(Hd):
             want = 0.0
@@ -359,6 +382,7 @@ def check_moe_down(moe_down, route):
                         y += Hf[r][i, j] * Wf[r][e * I_r + j, c]
                 want += float(gates[t, s]) * y
             assert abs(out[t // T_r][t % T_r, c] - want) <= 1e-12 * max(1.0, abs(want)), (t, c)
+            brute[t, c] = want
     # E = 1, k = 1, R = 1, gate 1: sorted rows are the tokens in order, out = H . W2
     H1 = [_rand_bits(rng, (4, 3))]
     W1 = [_rand_bits(rng, (3, 5))]
@@ -378,6 +402,14 @@ def check_moe_down(moe_down, route):
         e = ids[t, 0]
         y = sum(Hf[r][i] @ Wf[r][e * I_r:(e + 1) * I_r] for r in range(R))
         np.testing.assert_allclose(o0[t], float(gates[t, 0]) * y, rtol=1e-12, atol=1e-12)
+    # the sampler, every element, in a scrambled visiting order (so a mix-up of the
+    # token and column lists cannot pass), against the brute force and the zeroed gate
+    tt, cc = np.meshgrid(np.arange(T), np.arange(Hd), indexing="ij")
+    order = np.random.default_rng(29).permutation(T * Hd)
+    toks, cols = tt.ravel()[order], cc.ravel()[order]
+    np.testing.assert_allclose(moe_down_at(H, W2, ids, gates, E, toks, cols), brute[toks, cols],
+                               rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(moe_down_at(H, W2, ids, g0, E, toks, cols), o0[toks, cols], rtol=1e-12, atol=1e-12)
 
 
 # ------------------------------------------------------------------ AllGather-KV attention

@@ -181,7 +181,7 @@ def test_pins_catch_unrounded_bf16_partials():
 def test_pins_catch_swapped_gates():
     def bad(H, W2, ids, gates, E, T_r):
         return M.moe_down(H, W2, ids, np.ascontiguousarray(gates[:, ::-1]), E, T_r)
-    _fails(C.check_moe_down, bad, M.route)
+    _fails(C.check_moe_down, bad, M.route, M.moe_down_at)
 
 
 def test_pins_catch_wrong_expert_slice():
@@ -189,7 +189,7 @@ def test_pins_catch_wrong_expert_slice():
         I_r = H[0].shape[1]
         rolled = [np.roll(w, I_r, axis=0) for w in W2]
         return M.moe_down(H, rolled, ids, gates, E, T_r)
-    _fails(C.check_moe_down, bad, M.route)
+    _fails(C.check_moe_down, bad, M.route, M.moe_down_at)
 
 
 def test_pins_catch_sorted_row_for_pair_index():
@@ -203,7 +203,7 @@ def test_pins_catch_sorted_row_for_pair_index():
             return M.moe_down(H, W2, ids, gates, E, T_r)
         finally:
             M.route = old_route
-    _fails(C.check_moe_down, bad, M.route)
+    _fails(C.check_moe_down, bad, M.route, M.moe_down_at)
 
 
 def _mutated_attention(old, new):
@@ -238,3 +238,43 @@ def test_pins_catch_attention_mistakes(old, new):
     m = _mutated_attention(old, new)
     with np.errstate(all="ignore"):
         _fails(C.check_ag_attention, m.ag_kv_attention, m.gather)
+
+
+def _mutated_module(module, name, old, new):
+    """A copy of an oracle module with one source substitution, loaded as a fresh
+    module (the oracle itself is untouched)."""
+    import inspect
+    import types
+    src = inspect.getsource(module)
+    assert src.count(old) == 1, old
+    mod = types.ModuleType(name)
+    mod.__dict__["__package__"] = "oracle"
+    exec(compile(src.replace(old, new), name, "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("old,new", [
+    # slot s's expert output weighted by the other slot's gate
+    ("acc += float(gates[int(t), s]) * y", "acc += float(gates[int(t), k - 1 - s]) * y"),
+    # the first slot's expert slice used for every slot
+    ("e = int(ids[int(t), s])", "e = int(ids[int(t), 0])"),
+    # the pair's index read as its sorted row
+    ("i = int(pos[int(t) * k + s])", "i = int(t) * k + s"),
+    # the expert slice one expert off
+    ("W2_r[e * I_r:(e + 1) * I_r, int(c)]", "W2_r[(e + 1) % E * I_r:((e + 1) % E + 1) * I_r, int(c)]"),
+    # only the first rank's partial
+    ("for H_r, W2_r in zip(H_list, W2_list):\n                y +=", "for H_r, W2_r in zip(H_list[:1], W2_list[:1]):\n                y +="),
+])
+def test_pins_catch_moe_down_sampler_mistakes(old, new):
+    m = _mutated_module(M, "moe_mutant", old, new)
+    _fails(C.check_moe_down, M.moe_down, M.route, m.moe_down_at)
+
+
+@pytest.mark.parametrize("old,new", [
+    ("P = np.abs(partial(A_r, B_r))", "P = len(A_list) * np.abs(partial(A_r, B_r))"),        # scaled by R
+    ("P = np.abs(partial(A_r, B_r))", "P = partial(A_r, B_r)"),                              # signed partials
+    ("P = np.abs(partial(A_r, B_r))", "P = np.abs(bf16.decode(A_r)) @ np.abs(bf16.decode(B_r))"),  # |A||B|
+])
+def test_pins_catch_partial_abs_sum_mistakes(old, new):
+    m = _mutated_module(G, "gemm_rs_mutant", old, new)
+    _fails(C.check_partial_abs_sum, m.partial_abs_sum)

@@ -138,6 +138,10 @@ def test_gemm_rs_variant_pins():
     C.check_gemm_rs_variant(oracle.gemm_rs.gemm_rs_variant, oracle.gemm_rs.gemm_rs)
 
 
+def test_gemm_rs_partial_abs_sum_pins():
+    C.check_partial_abs_sum(oracle.gemm_rs.partial_abs_sum)
+
+
 def test_gemm_rs_partial_abs_sum_bounds_the_sum():
     from tile_centric_gemm_gb300 import inputs
     A = [inputs.normal_bf16((8, 16), 300 + r) for r in range(3)]
@@ -148,7 +152,7 @@ def test_gemm_rs_partial_abs_sum_bounds_the_sum():
 
 
 def test_moe_down_pins():
-    C.check_moe_down(oracle.moe.moe_down, oracle.moe.route)
+    C.check_moe_down(oracle.moe.moe_down, oracle.moe.route, oracle.moe.moe_down_at)
 
 
 def test_ag_attention_pins():
