@@ -289,7 +289,10 @@ tl_status tl_gemm_rs(const tl_gemm_rs_args* args, void* stream);
  *    NULL, device-side timeouts go unreported.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process: after a cudaDeviceReset of that device the module is loaded
+ *    anew and the kept address is stale, so the entry point must not be
+ *    called on a device that was reset after its first call.
  *  - Every call shares the array and it keeps the last call's contents: each
  *    call clears the flags (a stream-ordered memset) before its launch.  Calls
  *    that overlap on the GPU (different streams without ordering) race.

@@ -451,6 +451,8 @@ static __device__ __align__(256) uint8_t g_rs_noalloc_scratch[kNoAllocScratchByt
 
 // Device address of the scratch array, looked up once per device with that
 // device current.  In host code the array's name is only a host-side stand-in.
+// The address is kept until the process exits; a cudaDeviceReset reloads the
+// module and makes it stale, which the header rules out.
 tl_status noalloc_scratch(int dev, uint8_t** out) {
   static std::mutex mu;
   static uint8_t* addr[64] = {};
