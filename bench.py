@@ -426,12 +426,20 @@ def time_variants(torch, fn, flush, reps=7):
     return {"cold": statistics.median(cold), "cold_min": min(cold), "warm": statistics.median(warm)}
 
 
-def decomposed_graph(torch, B, shards, Bm, G, C, sig, ws=None):
+def decomposed_graph(torch, B, shards, Bm, G, C, sig, ws=None, library=False):
     """The prior-art decomposed schedule as a CUDA graph: the copy engine gathers
     shard after shard (rank 0 last) on a side stream while the main stream runs
-    one GEMM per shard, the local shard 0 first, each after its copy's event."""
+    one GEMM per shard, the local shard 0 first, each after its copy's event.
+    The per-shard GEMM is tl_gemm (split-K with a workspace), or torch.matmul
+    with library=True."""
     R, Ms = len(shards), shards[0].shape[0]
     s1 = torch.cuda.Stream()
+
+    def gemm(a, c):
+        if library:
+            torch.matmul(a, Bm, out=c)
+        else:
+            B.tl_gemm(a, Bm, c, sig, workspace=ws)
 
     def launches():
         main = torch.cuda.current_stream()
@@ -446,10 +454,10 @@ def decomposed_graph(torch, B, shards, Bm, G, C, sig, ws=None):
                 e.record(s1)
                 evs.append(e)
             G[0:Ms].copy_(shards[0], non_blocking=True)
-        B.tl_gemm(shards[0], Bm, C[0:Ms], sig, workspace=ws)
+        gemm(shards[0], C[0:Ms])
         for j, e in zip(range(1, R), evs):
             main.wait_event(e)
-            B.tl_gemm(G[j * Ms:(j + 1) * Ms], Bm, C[j * Ms:(j + 1) * Ms], sig, workspace=ws)
+            gemm(G[j * Ms:(j + 1) * Ms], C[j * Ms:(j + 1) * Ms])
         main.wait_stream(s1)
 
     launches()  # sets every kernel's launch attributes before the capture
@@ -484,14 +492,24 @@ def overlap_metrics(torch, B, wl):
         copy_only()
         gemm_only()
 
-    graph = decomposed_graph(torch, B, A, Bm, wl.G, wl.C, sig1)
+    # the decomposed schedule with each per-shard GEMM as fast as this library or the
+    # library GEMM makes it: tl_gemm with split-K (a shard's 28 tiles fill 28 of 76 pairs
+    # unsplit), and torch.matmul; t_decomposed is the faster of the two
+    ws_shard = torch.zeros(max(16, B.tl_gemm_workspace_size(Ms, AG["N"], K) // 4), dtype=torch.float32,
+                           device="cuda")
+    graph = decomposed_graph(torch, B, A, Bm, wl.G, wl.C, sig1, ws_shard)
+    graph_lib = decomposed_graph(torch, B, A, Bm, wl.G, wl.C, sig1, library=True)
     ag_t = {"copy": time_variants(torch, copy_only, flush), "gemm": time_variants(torch, gemm_only, flush),
             "seq": time_variants(torch, seq, flush), "decomposed": time_variants(torch, graph.replay, flush),
+            "decomposed_torch_matmul": time_variants(torch, graph_lib.replay, flush),
             "fused": time_variants(torch, wl.ag, flush),
             "torch_matmul": time_variants(torch, lambda: torch.matmul(wl.G, Bm, out=C_lib), flush)}
     t_copy, t_gemm, t_seq = ag_t["copy"]["cold"], ag_t["gemm"]["cold"], ag_t["seq"]["cold"]
-    t_dec, t_fused = ag_t["decomposed"]["cold"], ag_t["fused"]["cold"]
+    t_dec = min(ag_t["decomposed"]["cold"], ag_t["decomposed_torch_matmul"]["cold"])
+    t_fused = ag_t["fused"]["cold"]
     ag = {"t_copy_us": t_copy, "t_gemm_us": t_gemm, "t_seq_us": t_seq, "t_decomposed_us": t_dec,
+          "t_decomposed_tl_gemm_splitk_us": ag_t["decomposed"]["cold"],
+          "t_decomposed_torch_matmul_us": ag_t["decomposed_torch_matmul"]["cold"],
           "t_fused_us": t_fused, "t_torch_matmul_us": ag_t["torch_matmul"]["cold"],
           "speedup_vs_seq": t_seq / t_fused,
           "speedup_vs_decomposed": t_dec / t_fused,
@@ -510,6 +528,24 @@ def overlap_metrics(torch, B, wl):
                 B.tl_ag_gemm(A, Bm, wl.G, wl.C, sig1, ep[0], self_rank=self_rank, swizzle=sw)
             abl[f"self{self_rank}_{name}_us"] = flushed_time_us(torch, fused_sw, flush)
     ag["swizzle_ablation"] = abl
+    # push against pull (talk summary, Technical Deep Dive: push needs one barrier, pull a
+    # readiness barrier before the copy and a completion barrier after it), each with both
+    # consumer orders, for a middle calling rank; the readiness flags are set before the
+    # call, as a resident peer's would be
+    ready = B.Signals(max(1, wl.sig_ag.num_flags))
+    B.tl_tile_notify(ready, 0, wl.sig_ag.num_flags, 0x7FFF0000)
+    pp = {}
+    for mname, mode in (("push", B.TL_MODE_PUSH), ("pull", B.TL_MODE_PULL)):
+        for name, sw in (("arrival", B.TL_SWIZZLE_ARRIVAL), ("rows", B.TL_SWIZZLE_ROWS)):
+            def fused_mode(mode=mode, sw=sw):
+                ep[0] += 1
+                B.tl_ag_gemm(A, Bm, wl.G, wl.C, sig1, ep[0], self_rank=R // 2, swizzle=sw, mode=mode,
+                             src_ready=ready if mode == B.TL_MODE_PULL else None)
+            pp[f"{mname}_{name}_us"] = flushed_time_us(torch, fused_mode, flush)
+    ag["push_pull_ablation"] = pp
+    code, where = B.tl_query_status(ready)
+    if code:
+        raise RuntimeError(f"device error {code} at {where} on the readiness flags")
     # GEMM-RS: per-rank GEMMs with fp32 partials, then the rank-ordered ReduceScatter
     Rr, M, N = RS["R"], RS["M"], RS["N"]
     parts = [torch.empty(M, N, dtype=torch.float32, device="cuda") for _ in range(Rr)]
@@ -555,12 +591,30 @@ def overlap_metrics(torch, B, wl):
             B.tl_gemm_rs(wl.d_rs[:Rr], wl.d_rs[Rr:], wl.out, wl.ws, sig_rs2, ep[0], options=opt)
         abl[f"{name}_us"] = flushed_time_us(torch, rs_opt, flush, reps=5)
     rs["options_ablation"] = abl
+    # MoE AllGather + grouped GEMM (routing included) in its two data modes: pull (the
+    # consumer side gathers sorted rows in the order the tiles run) and push (source
+    # shards scatter their tokens, tiles run by the latest arrival among their barriers)
+    R_m, E_m = MOE["R"], MOE["E"]
+    m = wl.d_moe
+    moe_pp = {}
+    for mname, mode in (("pull", B.TL_MODE_PULL), ("push", B.TL_MODE_PUSH)):
+        sig_m = B.Signals(B.tl_moe_num_flags(R_m, MOE["T_r"], MOE["H"], MOE["topk"], mode=mode)[0])
+
+        def moe_mode(mode=mode, sig_m=sig_m):
+            ep[0] += 1
+            B.tl_moe_ag_gemm(m[:R_m], m[R_m + E_m], m[R_m:R_m + E_m], wl.S, wl.Y, wl.perm, wl.offs, wl.ws_moe,
+                             sig_m, ep[0], mode=mode, self_rank=R_m // 2)
+        moe_pp[f"{mname}_us"] = flushed_time_us(torch, moe_mode, flush)
+        code, where = B.tl_query_status(sig_m)
+        if code:
+            raise RuntimeError(f"device error {code} at {where} in the MoE {mname} measurement")
+    moe_pp["note"] = "cold L2, median of 7, caller rank 4, routing kernel included"
     for s in (sig1, sig_rs2, wl.sig_ag, wl.sig_rs):
         code, where = B.tl_query_status(s)
         if code:
             raise RuntimeError(f"device error {code} at {where} in the overlap measurements")
     del parts, flush
-    return {"ag_gemm": ag, "gemm_rs": rs}
+    return {"ag_gemm": ag, "gemm_rs": rs, "moe_push_pull": moe_pp}
 
 
 SWEEP = dict(R=(2, 4, 8), M=(1024, 2048, 4096, 8192, 16384), K=8192, N=1024)
