@@ -804,6 +804,69 @@ class AgAttn:
                 raise RuntimeError(f"device error {code} at {where} in the AllGather-KV attention")
 
 
+# AllGather through the slow link (pinned host memory) at small messages: R=8 ranks, K=4096
+# bf16 columns, 1..128 rows per shard (8 KB..1 MB)
+LL_SIZES = dict(R=8, K=4096, M_shard=(1, 4, 16, 64, 128))
+
+
+def ll_extras(torch, B, reps=7, batch=16):
+    """Latency of one AllGather whose peer shards cross the slow link (pinned host memory):
+    the flag-in-data protocol (tl_allgather_ll, 8-byte words of 4 data bytes + epoch) against
+    the separate-flag protocol on the same link (data, system fence, flag), and against
+    tl_allgather reading peer shards that sit in host memory with their readiness flags set
+    (pull mode: one readiness wait per chunk).  Device time per call: batches of calls
+    enqueued behind a GPU sleep, timed with CUDA events; the median over batches."""
+    from tile_centric_gemm_gb300 import inputs
+    R, K = LL_SIZES["R"], LL_SIZES["K"]
+    rows = []
+    for Ms in LL_SIZES["M_shard"]:
+        A = [inputs.to_torch_bf16(inputs.normal_bf16((Ms, K), 1200 + r)).cuda() for r in range(R)]
+        A_host = [A[0]] + [a.cpu().pin_memory() for a in A[1:]]
+        link = torch.zeros(B.tl_allgather_ll_link_bytes(R, Ms, K), dtype=torch.uint8).pin_memory()
+        G = torch.empty(R * Ms, K, dtype=torch.bfloat16, device="cuda")
+        nfl = R * B.tl_ag_gemm_num_flags(R, Ms, K)[0]
+        sig = B.Signals(max(nfl, R * Ms))
+        ready = B.Signals(max(nfl, R * Ms))
+        B.tl_tile_notify(ready, 0, ready.num_flags, 0x7FFF0000)
+        ep = [0]
+
+        def ll(protocol):
+            ep[0] += 1
+            B.tl_allgather_ll(A, link, G, sig, ep[0], protocol=protocol)
+
+        def ag_host():
+            ep[0] += 1
+            B.tl_allgather(A_host, G, sig, ep[0], mode=B.TL_MODE_PULL, src_ready=ready)
+
+        res = {"shard_bytes": Ms * K * 2}
+        for name, fn in (("flag_in_data", lambda: ll(B.TL_LL_FLAG_IN_DATA)),
+                         ("separate_flag", lambda: ll(B.TL_LL_SEPARATE_FLAG)), ("tl_allgather_host_pull", ag_host)):
+            fn()
+            ts = []
+            for _ in range(reps):
+                # the GPU first sleeps while the host enqueues a batch of calls, so the events
+                # time the calls back to back on the device, not the host's launch rate
+                torch.cuda._sleep(3_000_000)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for _ in range(batch):
+                    fn()
+                b.record()
+                b.synchronize()
+                ts.append(a.elapsed_time(b) * 1e3 / batch)
+            res[name + "_us"] = statistics.median(ts)
+        for s in (sig, ready):
+            code, where = B.tl_query_status(s)
+            if code:
+                raise RuntimeError(f"device error {code} at {where} in the slow-link AllGather")
+        res["speedup_flag_in_data_vs_separate_flag"] = res["separate_flag_us"] / res["flag_in_data_us"]
+        rows.append(res)
+        del A, A_host, link, G
+    return {"config": LL_SIZES, "link": "pinned host memory", "rows": rows,
+            "what": "one AllGather of R shards through the slow link; device time per call, batches of "
+                    "back-to-back calls enqueued behind a GPU sleep"}
+
+
 def attn_extras(torch, B, peaks, peak_src):
     a = AgAttn(B, torch)
     c = AG_ATTN
@@ -983,6 +1046,7 @@ def main():
                                                "TopK-reduce -> scatter, one call (two launches)"}}
         del down, flush
         line["extras"]["ag_attn"] = attn_extras(torch, B, peaks, peak_src)
+        line["extras"]["allgather_ll"] = ll_extras(torch, B)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, sample = time_oracle()
         line["cpu_baseline"] = {"value": tf, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",

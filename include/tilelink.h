@@ -333,6 +333,55 @@ typedef struct tl_reduce_scatter_args {
 tl_status tl_allgather(const tl_allgather_args* args, void* stream);
 tl_status tl_reduce_scatter(const tl_reduce_scatter_args* args, void* stream);
 
+/* ---------------------------------------------------------------- AllGather through a slow link, low latency
+ * The talk summary (Experimental Setup & Results, further results) reports an
+ * AllGather over PCIe with a low-latency protocol about three times faster
+ * than NCCL's; it gives no format.  This call reads it as the flag-in-data
+ * protocol: every 8-byte link word holds 4 bytes of data and 4 bytes of the
+ * call's epoch and is written and read as one 64-bit access, so a receiver that
+ * sees the epoch also sees the data -- the sender needs no fence between data
+ * and flag and the receiver polls no separate flag -- at twice the bytes on
+ * the link.  One launch emulates both sides of a push AllGather on one GPU:
+ *  - send: the shard of every rank r != self_rank with bit r of send_mask is
+ *    written into rank r's region of `link` (TL_LL_FLAG_IN_DATA: packed words;
+ *    TL_LL_SEPARATE_FLAG: the raw data, a system-scope fence, then a release
+ *    of the chunk's flag in the link buffer -- the protocol it is compared with);
+ *  - receive: rank self_rank's receiver polls each peer chunk in the link
+ *    (bounded by timeout_ns; TL_ERR_TIMEOUT in the status word with the flag
+ *    id) and writes it into rows r*M_shard ... of `gathered`, then releases the
+ *    chunk's flag in `signals` (the flag ids of tl_allgather: r * chunks + c);
+ *  - the self shard is copied into `gathered` directly.
+ * Ranks without their send_mask bit are not sent by this launch: their link
+ * regions must be filled, with the same epoch and layout, by another agent
+ * (the host, or an earlier launch).  Link layout: TL_LL_FLAG_IN_DATA -- data
+ * word w of the gathered matrix (4 bytes, row-major [R*M_shard, K] bf16) at
+ * link byte 8*w as {data (low 32 bits), epoch (high 32 bits)};
+ * TL_LL_SEPARATE_FLAG -- the gathered matrix's bytes at the same offsets, then
+ * chunk flag f (uint32) at byte R*M_shard*K*2 + 128*f.  Words of an earlier
+ * epoch are never mistaken for this call's.  All CTAs of the launch must be
+ * co-resident (receivers wait for senders of the same launch).
+ */
+typedef enum { TL_LL_FLAG_IN_DATA = 0, TL_LL_SEPARATE_FLAG = 1 } tl_ll_protocol;
+
+typedef struct tl_allgather_ll_args {
+  int32_t R, self_rank, M_shard, K;  /* as tl_allgather_args; K multiple of 8 */
+  int32_t protocol;                  /* tl_ll_protocol */
+  int32_t rows_per_barrier;          /* rows per chunk / flag; 0 = about 8 KB of a shard */
+  const void* const* A_shards;       /* host array of R pointers (device or pinned host), bf16 [M_shard, K] */
+  void* link;                        /* pinned host (the slow link) or device memory, 16-byte aligned */
+  size_t link_bytes;                 /* >= tl_allgather_ll_link_bytes(R, M_shard, K, rows_per_barrier) */
+  void* gathered;                    /* device bf16 [R*M_shard, K], written */
+  tl_signals* signals;               /* >= R * chunks flags, released per chunk */
+  uint64_t send_mask;                /* bit r: this launch sends rank r's shard (self_rank's bit is ignored) */
+  uint32_t epoch;                    /* nonzero, larger than the link buffer's last epoch */
+  uint32_t reserved0;
+  uint64_t timeout_ns;               /* 0 = 1 s */
+} tl_allgather_ll_args;
+
+/* Link bytes for a shape (the larger of the two protocols' layouts). */
+size_t tl_allgather_ll_link_bytes(int R, int M_shard, int K, int rows_per_barrier);
+tl_status tl_allgather_ll(const tl_allgather_ll_args* args, void* stream);
+
 /* ---------------------------------------------------------------- AllGather + grouped MoE GEMM
  * The AllGather + GroupGEMM part of an MoE layer (talk summary, Key Findings
  * and Experimental Setup & Results: MoE layers; Technical Deep Dive: lookup

@@ -141,3 +141,31 @@ def test_splitk_workspace_alignment_checked_without_launch(B):
                        workspace=72, workspace_bytes=1 << 30)
     assert B.lib.tl_gemm(ctypes.byref(g), None) == B.TL_ERR_INVALID
     assert "aligned" in B.tl_last_error()
+
+
+def test_allgather_ll_link_bytes(B):
+    # the larger of the two layouts: packed words (8 bytes per 4 data bytes), or the raw
+    # data followed by one 128-byte flag slot per chunk
+    assert B.tl_allgather_ll_link_bytes(8, 1024, 4096) == 2 * 8 * 1024 * 4096 * 2
+    assert B.tl_allgather_ll_link_bytes(2, 1, 8) == max(2 * 2 * 16, 2 * 16 + 2 * 128)
+    assert B.tl_allgather_ll_link_bytes(3, 37, 136, 5) == max(2 * 3 * 37 * 136 * 2, 3 * 37 * 136 * 2 + 3 * 8 * 128)
+    assert B.tl_allgather_ll_link_bytes(0, 1, 8) == 0
+
+
+def test_allgather_ll_rejects_bad_arguments_without_a_device(B):
+    # argument errors come back before any device query or launch
+    shard = (ctypes.c_void_p * 2)(16, 32)
+    pp = ctypes.cast(shard, ctypes.POINTER(ctypes.c_void_p))
+
+    def args(**kw):
+        a = dict(R=2, self_rank=0, M_shard=4, K=64, protocol=0, rows_per_barrier=0, A_shards=pp, link=64,
+                 link_bytes=1 << 20, gathered=128, signals=256, send_mask=3, epoch=1, reserved0=0, timeout_ns=0)
+        a.update(kw)
+        return B.tl_allgather_ll_args(**a)
+    for kw, code in [(dict(K=60), B.TL_ERR_UNSUPPORTED), (dict(protocol=2), B.TL_ERR_INVALID),
+                     (dict(epoch=0), B.TL_ERR_INVALID), (dict(link=None), B.TL_ERR_INVALID),
+                     (dict(link_bytes=100), B.TL_ERR_INVALID), (dict(link=72), B.TL_ERR_INVALID),
+                     (dict(self_rank=2), B.TL_ERR_INVALID), (dict(R=65), B.TL_ERR_INVALID)]:
+        a = args(**kw)
+        assert B.lib.tl_allgather_ll(ctypes.byref(a), None) == code, kw
+    assert B.lib.tl_allgather_ll(None, None) == B.TL_ERR_INVALID

@@ -22,6 +22,7 @@ TL_OK, TL_ERR_INVALID, TL_ERR_CUDA, TL_ERR_TIMEOUT, TL_ERR_UNSUPPORTED, TL_ERR_I
 TL_MODE_PULL, TL_MODE_PUSH = 0, 1
 TL_SWIZZLE_ARRIVAL, TL_SWIZZLE_ROWS = 0, 1
 TL_RS_BF16_PARTIALS, TL_RS_RING_ORDER = 1, 2
+TL_LL_FLAG_IN_DATA, TL_LL_SEPARATE_FLAG = 0, 1
 STATUS_NAMES = {0: "TL_OK", 1: "TL_ERR_INVALID", 2: "TL_ERR_CUDA", 3: "TL_ERR_TIMEOUT",
                 4: "TL_ERR_UNSUPPORTED", 5: "TL_ERR_INTERNAL"}
 
@@ -34,7 +35,7 @@ EXPORTED = [
     "tl_gemm_rs_workspace_size", "tl_gemm_rs_num_flags", "tl_gemm_rs", "tl_gemm_rs_noalloc",
     "tl_moe_workspace_size", "tl_moe_num_flags", "tl_moe_ag_gemm", "tl_allgather", "tl_reduce_scatter",
     "tl_moe_down_workspace_size", "tl_moe_down_num_flags", "tl_moe_down",
-    "tl_ag_attn_num_flags", "tl_ag_attn",
+    "tl_ag_attn_num_flags", "tl_ag_attn", "tl_allgather_ll_link_bytes", "tl_allgather_ll",
 ]
 
 
@@ -119,6 +120,16 @@ class tl_allgather_args(ctypes.Structure):
     ]
 
 
+class tl_allgather_ll_args(ctypes.Structure):
+    _fields_ = [
+        ("R", ctypes.c_int32), ("self_rank", ctypes.c_int32), ("M_shard", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("protocol", ctypes.c_int32), ("rows_per_barrier", ctypes.c_int32), ("A_shards", ctypes.POINTER(_vp)),
+        ("link", _vp), ("link_bytes", ctypes.c_size_t), ("gathered", _vp), ("signals", _vp),
+        ("send_mask", ctypes.c_uint64), ("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32),
+        ("timeout_ns", ctypes.c_uint64),
+    ]
+
+
 class tl_reduce_scatter_args(ctypes.Structure):
     _fields_ = [
         ("R", ctypes.c_int32), ("M", ctypes.c_int32), ("N", ctypes.c_int32), ("reserved0", ctypes.c_int32),
@@ -161,6 +172,8 @@ _decl("tl_moe_num_flags", _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_i))
 _decl("tl_moe_ag_gemm", _i, ctypes.POINTER(tl_moe_args), _vp)
 _decl("tl_allgather", _i, ctypes.POINTER(tl_allgather_args), _vp)
 _decl("tl_reduce_scatter", _i, ctypes.POINTER(tl_reduce_scatter_args), _vp)
+_decl("tl_allgather_ll_link_bytes", _sz, _i, _i, _i, _i)
+_decl("tl_allgather_ll", _i, ctypes.POINTER(tl_allgather_ll_args), _vp)
 _decl("tl_ag_attn_num_flags", _i, _i, _i)
 _decl("tl_ag_attn", _i, ctypes.POINTER(tl_ag_attn_args), _vp)
 
@@ -397,6 +410,27 @@ def tl_allgather(A_shards, gathered, signals: Signals, epoch: int, *, self_rank=
                           src_ready=src_ready.handle if src_ready is not None else None,
                           epoch=int(epoch) & 0xFFFFFFFF, reserved0=0, timeout_ns=int(timeout_ns))
     _check(lib.tl_allgather(ctypes.byref(a), _stream(stream)))
+
+
+def tl_allgather_ll_link_bytes(R, M_shard, K, rows_per_barrier=0):
+    return int(lib.tl_allgather_ll_link_bytes(R, M_shard, K, rows_per_barrier))
+
+
+def tl_allgather_ll(A_shards, link, gathered, signals: Signals, epoch: int, *, self_rank=0,
+                    protocol=TL_LL_FLAG_IN_DATA, send_mask=None, rows_per_barrier=0, timeout_ns=0, stream=None):
+    """AllGather through the link buffer `link` (pinned host or device tensor) with the
+    flag-in-data protocol or the separate-flag one (see tilelink.h).  send_mask None =
+    every rank sends in this launch."""
+    R = len(A_shards)
+    M_shard, K = A_shards[0].shape
+    ptrs = _ptr_array(A_shards)
+    mask = (1 << R) - 1 if send_mask is None else int(send_mask)
+    a = tl_allgather_ll_args(R=R, self_rank=self_rank, M_shard=M_shard, K=K, protocol=int(protocol),
+                             rows_per_barrier=rows_per_barrier, A_shards=ctypes.cast(ptrs, ctypes.POINTER(_vp)),
+                             link=_ptr(link), link_bytes=_nbytes(link), gathered=_ptr(gathered),
+                             signals=signals.handle, send_mask=mask, epoch=int(epoch) & 0xFFFFFFFF, reserved0=0,
+                             timeout_ns=int(timeout_ns))
+    _check(lib.tl_allgather_ll(ctypes.byref(a), _stream(stream)))
 
 
 def tl_reduce_scatter(partials, out, *, stream=None):
