@@ -119,6 +119,20 @@ tl_status tl_tile_wait(tl_signals* s, int first, int count, uint32_t value,
  * that failed (-1 if none).  Either out pointer may be NULL. */
 tl_status tl_query_status(tl_signals* s, void* stream, int* code, int* where);
 
+/* ---------------------------------------------------------------- test facility: forced arrival order
+ * Not part of the method: a way for tests to make chunks arrive in an order
+ * other than the one the consumers take them in, so that a missing or wrong
+ * wait shows up as a wrong result instead of passing by luck.  On the calling
+ * thread, every later tl_ag_gemm, tl_allgather and tl_moe_ag_gemm call has its
+ * copy warps move the chunks whose flag ids lie in [first_flag, first_flag +
+ * count) after all their other chunks, and not before hold_ns have passed since
+ * the copy warp started (a bounded spin on the global timer).  count 0 turns it
+ * off.  A call whose timeout_ns is not above twice hold_ns is rejected
+ * (TL_ERR_INVALID), so that the consumers' bounded waits outlast the hold.
+ * hold_ns at most 100 ms.  The results of the calls do not change.
+ */
+tl_status tl_test_hold_chunks(int first_flag, int count, uint64_t hold_ns);
+
 /* ---------------------------------------------------------------- GEMM
  * C = A . B, bf16 in, fp32 accumulate, bf16 (and optionally fp32) out, with no
  * communication and no waits: the compute half of AllGather-GEMM alone, used to

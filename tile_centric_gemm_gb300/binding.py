@@ -36,6 +36,7 @@ EXPORTED = [
     "tl_moe_workspace_size", "tl_moe_num_flags", "tl_moe_ag_gemm", "tl_allgather", "tl_reduce_scatter",
     "tl_moe_down_workspace_size", "tl_moe_down_num_flags", "tl_moe_down",
     "tl_ag_attn_num_flags", "tl_ag_attn", "tl_allgather_ll_link_bytes", "tl_allgather_ll",
+    "tl_test_hold_chunks",
 ]
 
 
@@ -174,6 +175,7 @@ _decl("tl_allgather", _i, ctypes.POINTER(tl_allgather_args), _vp)
 _decl("tl_reduce_scatter", _i, ctypes.POINTER(tl_reduce_scatter_args), _vp)
 _decl("tl_allgather_ll_link_bytes", _sz, _i, _i, _i, _i)
 _decl("tl_allgather_ll", _i, ctypes.POINTER(tl_allgather_ll_args), _vp)
+_decl("tl_test_hold_chunks", _i, _i, _i, _u64)
 _decl("tl_ag_attn_num_flags", _i, _i, _i)
 _decl("tl_ag_attn", _i, ctypes.POINTER(tl_ag_attn_args), _vp)
 
@@ -431,6 +433,12 @@ def tl_allgather_ll(A_shards, link, gathered, signals: Signals, epoch: int, *, s
                              signals=signals.handle, send_mask=mask, epoch=int(epoch) & 0xFFFFFFFF, reserved0=0,
                              timeout_ns=int(timeout_ns))
     _check(lib.tl_allgather_ll(ctypes.byref(a), _stream(stream)))
+
+
+def tl_test_hold_chunks(first_flag, count, hold_ns):
+    """Test facility: on this thread, later copy-warp calls move the chunks with flag ids in
+    [first_flag, first_flag + count) last, after hold_ns (see tilelink.h).  count 0 = off."""
+    _check(lib.tl_test_hold_chunks(int(first_flag), int(count), int(hold_ns)))
 
 
 def tl_reduce_scatter(partials, out, *, stream=None):

@@ -67,6 +67,8 @@ struct AgParams {
   splitk::Work sk;
   uint32_t epoch;
   uint64_t host_mask;  // shards in host memory (copied with plain loads)
+  int32_t hold_first, hold_count;  // chunks the copy warps move last (tl_test_hold_chunks)
+  uint64_t hold_ns;
   uint16_t m_order[AG_MAX_MTILES];
 };
 
@@ -185,7 +187,8 @@ __global__ void __launch_bounds__(AG_THREADS, 1) ag_gemm_kernel(const __grid_con
   } else if (warp == kWarpCopy) {
     // ---------------------------------------------------------------- AllGather producer
     AgCopyJob job{p.shard, p.gathered, p.flags, p.ready, p.status, p.timeout_ns, p.pipe_timeout_ns,
-                  p.R, p.self, p.M_shard, p.K, p.rpb, p.bpr, p.num_items, p.epoch, p.host_mask};
+                  p.R, p.self, p.M_shard, p.K, p.rpb, p.bpr, p.num_items, p.epoch, p.host_mask,
+                  p.hold_first, p.hold_count, p.hold_ns};
     ag_copy_items<AG_COPY_NBUF>(job, smem + AG_SMEM_COPY, bars->copy, abort, int(blockIdx.x), int(gridDim.x));
   }
   pair::teardown(bars, warp, tmem_base);
@@ -315,6 +318,7 @@ extern "C" tl_status tl_ag_gemm(const tl_ag_gemm_args* a, void* stream) {
     p->KB = cdiv(a->K, pair::BK);
     p->num_items = a->R * p->bpr;
     p->epoch = a->epoch;
+    if ((st = test_hold("tl_ag_gemm", p->timeout_ns, &p->hold_first, &p->hold_count, &p->hold_ns))) break;
     // split-K when the tiles leave pairs idle and the caller gave a workspace
     const long long tiles = (long long)Mt * p->Nt;
     p->S = a->workspace ? splitk::choose(tiles, p->KB, di.sm_count / 2) : 1;

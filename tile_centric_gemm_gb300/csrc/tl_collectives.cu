@@ -109,6 +109,8 @@ extern "C" tl_status tl_allgather(const tl_allgather_args* a, void* stream) {
   p.job.bpr = cdiv(a->M_shard, rpb);
   p.job.num_items = a->R * p.job.bpr;
   p.job.epoch = a->epoch;
+  if (tl_status s = test_hold("tl_allgather", p.job.timeout_ns, &p.job.hold_first, &p.job.hold_count, &p.job.hold_ns))
+    return s;
   const int grid = std::max(1, std::min(di.sm_count, p.job.num_items));
   void* args[] = {&p};
   return launch_coop(reinterpret_cast<const void*>(&allgather_kernel), grid, 32, AGC_SMEM_BYTES,

@@ -27,7 +27,29 @@ struct AgCopyJob {
   int R, self, M_shard, K, rpb, bpr, num_items;
   uint32_t epoch;
   uint64_t host_mask;  // bit r: shard r is host (or managed) memory, copied with plain loads
+  // held chunks (a test facility that forces an arrival order): chunks whose flag id lies in
+  // [hold_first, hold_first + hold_count) are copied after every other chunk of the copy
+  // warp, and not before hold_ns have passed since the warp started
+  int hold_first, hold_count;
+  uint64_t hold_ns;
 };
+
+__device__ __forceinline__ bool ag_item_held(const AgCopyJob& j, int it) {
+  if (j.hold_count <= 0) return false;
+  const int r = (j.self + 1 + it / j.bpr) % j.R;
+  const int f = r * j.bpr + it % j.bpr;
+  return f >= j.hold_first && f < j.hold_first + j.hold_count;
+}
+
+// Lane 0 spins until hold_ns have passed since t0 (a bounded wait: hold_ns is
+// checked on the host against the call's timeout), or the launch has aborted.
+__device__ __forceinline__ void hold_until(uint64_t t0, uint64_t hold_ns, volatile uint32_t* abort,
+                                           const uint32_t* status) {
+  while (now_ns() - t0 < hold_ns) {
+    if (*abort || ld_volatile(status) != 0u) break;
+    __nanosleep(1000);
+  }
+}
 
 // Copy `bytes` (a multiple of 16) from src (host or device memory) to dst with
 // every lane of the warp: kVec 16-byte loads in flight per lane.
@@ -158,12 +180,26 @@ __device__ __forceinline__ bool ag_copy_one(const AgCopyJob& j, int it, uint8_t*
 
 // Items first, first + stride, ... in copy order: shards self+1, ..., self+R-1,
 // then self; chunks ascending.  Called by all 32 lanes of one warp.
+// Held chunks (see AgCopyJob) come after all the others.
 template <int NBUF = COPY_NBUF>
 __device__ __forceinline__ void ag_copy_items(const AgCopyJob& j, uint8_t* stage, uint64_t* bars,
                                               volatile uint32_t* abort, int first, int stride) {
+  const uint64_t t0 = now_ns();
   uint32_t seq = 0;
-  for (int it = first; it < j.num_items; it += stride)
-    if (ag_copy_one<NBUF>(j, it, stage, bars, abort, seq)) break;
+  bool dead = false, any_held = false;
+  for (int it = first; it < j.num_items && !dead; it += stride) {
+    if (ag_item_held(j, it)) {
+      any_held = true;
+      continue;
+    }
+    dead = ag_copy_one<NBUF>(j, it, stage, bars, abort, seq);
+  }
+  if (any_held && !dead) {
+    if (lane_id() == 0) hold_until(t0, j.hold_ns, abort, j.status);
+    __syncwarp();
+    for (int it = first; it < j.num_items && !dead; it += stride)
+      if (ag_item_held(j, it)) dead = ag_copy_one<NBUF>(j, it, stage, bars, abort, seq);
+  }
   if (lane_id() == 0) bulk_wait<0>();
   __syncwarp();
 }

@@ -20,6 +20,12 @@
 
 namespace {
 thread_local char g_last_error[512] = "";
+// tl_test_hold_chunks: chunks [first, first + count) are copied last, after hold_ns
+struct Hold {
+  int first, count;
+  uint64_t ns;
+};
+thread_local Hold g_hold = {0, 0, 0};
 }
 
 namespace tl {
@@ -30,6 +36,16 @@ tl_status fail(tl_status code, const char* fmt, ...) {
   vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
   va_end(ap);
   return code;
+}
+
+tl_status test_hold(const char* who, uint64_t timeout_ns, int32_t* first, int32_t* count, uint64_t* hold_ns) {
+  *first = g_hold.first;
+  *count = g_hold.count;
+  *hold_ns = g_hold.ns;
+  if (g_hold.count > 0 && 2 * g_hold.ns >= timeout_ns)
+    return fail(TL_ERR_INVALID, "%s: held chunks wait %llu ns, which is not below half the timeout (%llu ns)", who,
+                (unsigned long long)g_hold.ns, (unsigned long long)timeout_ns);
+  return TL_OK;
 }
 
 tl_status cuda_ok(cudaError_t e, const char* what) {
@@ -389,3 +405,10 @@ tl_status tl_query_status(tl_signals* s, void* stream, int* code, int* where) {
 }
 
 }  // extern "C"
+
+extern "C" tl_status tl_test_hold_chunks(int first_flag, int count, uint64_t hold_ns) {
+  if (count < 0 || first_flag < 0) return tl::fail(TL_ERR_INVALID, "tl_test_hold_chunks: negative range");
+  if (hold_ns > 100000000ull) return tl::fail(TL_ERR_INVALID, "tl_test_hold_chunks: hold above 100 ms");
+  g_hold = Hold{first_flag, count, hold_ns};
+  return TL_OK;
+}

@@ -63,6 +63,11 @@ tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cuda
 tl_status classify_shards(const char* who, const void* const* shards, int R, int device, const uint8_t** dev,
                           uint64_t* host_mask);
 
+// The calling thread's held-chunk setting (tl_test_hold_chunks) for a copy-warp launch
+// whose flag waits are bounded by timeout_ns: count 0 when none.  Rejects a hold that
+// would not end well inside the waits' bound.
+tl_status test_hold(const char* who, uint64_t timeout_ns, int32_t* first, int32_t* count, uint64_t* hold_ns);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 

@@ -289,6 +289,8 @@ struct MoeParams {
   int32_t R, self, T_r, H, N, E, k, rpb, bpr, Nt, KB, num_items, max_tiles, pull, P;
   uint32_t epoch;
   const int32_t* perm;
+  int32_t hold_first, hold_count;  // chunks the copy warps move last (tl_test_hold_chunks)
+  uint64_t hold_ns;
 };
 
 __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_constant__ MoeParams p) {
@@ -393,60 +395,77 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
       const int pieces = int((row_bytes + COPY_CHUNK - 1) / COPY_CHUNK);
       uint32_t seq = 0;  // pieces loaded by this CTA: buffer seq % NBUF, parity (seq / NBUF) & 1
       bool dead = false;
-      for (int it = blockIdx.x; it < p.num_items && !dead; it += gridDim.x) {
-        // push: item = (shard r, chunk c of its tokens), each token scattered to its k sorted rows;
-        // pull: item = chunk of rpb sorted rows, each gathered from its token's shard
-        const int jj = it / p.bpr, c = it % p.bpr;
-        const int r = (p.self + jj) % p.R;  // push: shards self, self+1, ...
-        const int t0 = p.pull ? it * p.rpb : c * p.rpb;
-        const int t1 = p.pull ? min(p.P, t0 + p.rpb) : min(p.T_r, t0 + p.rpb);
-        const int nunits = (t1 - t0) * pieces;
-        int issued = 0, stored = 0;
-        while (stored < nunits) {
-          while (issued < nunits && issued - stored < MOE_COPY_NBUF) {
-            const uint32_t q = seq + uint32_t(issued);
+      const uint64_t t0 = now_ns();
+      // the flag an item releases; held items (a test facility) go after the others
+      auto flag_of = [&](int it) { return p.pull ? it : ((p.self + it / p.bpr) % p.R) * p.bpr + it % p.bpr; };
+      auto held = [&](int it) {
+        return p.hold_count > 0 && flag_of(it) >= p.hold_first && flag_of(it) < p.hold_first + p.hold_count;
+      };
+      bool any_held = false;
+      for (int pass = 0; pass < 2 && !dead; ++pass) {
+        if (pass == 1) {
+          if (!any_held) break;
+          while (now_ns() - t0 < p.hold_ns && !*abort && ld_volatile(p.status) == 0u) __nanosleep(1000);
+        }
+        for (int it = blockIdx.x; it < p.num_items && !dead; it += gridDim.x) {
+          if (held(it) != (pass == 1)) {
+            any_held = any_held || held(it);
+            continue;
+          }
+          // push: item = (shard r, chunk c of its tokens), each token scattered to its k sorted rows;
+          // pull: item = chunk of rpb sorted rows, each gathered from its token's shard
+          const int jj = it / p.bpr, c = it % p.bpr;
+          const int r = (p.self + jj) % p.R;  // push: shards self, self+1, ...
+          const int t0 = p.pull ? it * p.rpb : c * p.rpb;
+          const int t1 = p.pull ? min(p.P, t0 + p.rpb) : min(p.T_r, t0 + p.rpb);
+          const int nunits = (t1 - t0) * pieces;
+          int issued = 0, stored = 0;
+          while (stored < nunits) {
+            while (issued < nunits && issued - stored < MOE_COPY_NBUF) {
+              const uint32_t q = seq + uint32_t(issued);
+              const int buf = int(q % MOE_COPY_NBUF);
+              bulk_wait_read_dyn(stored - issued + MOE_COPY_NBUF - 1);
+              const int tl = t0 + issued / pieces, pc = issued % pieces;
+              const uint32_t off = uint32_t(pc) * COPY_CHUNK;
+              const uint32_t sz = min(COPY_CHUNK, row_bytes - off);
+              const uint8_t* src;
+              if (p.pull) {
+                const int tok = p.perm[tl] / p.k;
+                src = p.x[tok / p.T_r] + size_t(tok % p.T_r) * row_bytes + off;
+              } else {
+                src = p.x[r] + size_t(tl) * row_bytes + off;
+              }
+              mbar_arrive_expect_tx(&bars->copy[buf], sz);
+              bulk_g2s(stage + buf * COPY_CHUNK, src, sz, &bars->copy[buf]);
+              ++issued;
+            }
+            const uint32_t q = seq + uint32_t(stored);
             const int buf = int(q % MOE_COPY_NBUF);
-            bulk_wait_read_dyn(stored - issued + MOE_COPY_NBUF - 1);
-            const int tl = t0 + issued / pieces, pc = issued % pieces;
+            if (!mbar_wait(&bars->copy[buf], (q / MOE_COPY_NBUF) & 1u, abort, p.status, p.pipe_timeout_ns, 5)) {
+              dead = true;
+              break;
+            }
+            const int tl = t0 + stored / pieces, pc = stored % pieces;
             const uint32_t off = uint32_t(pc) * COPY_CHUNK;
             const uint32_t sz = min(COPY_CHUNK, row_bytes - off);
-            const uint8_t* src;
             if (p.pull) {
-              const int tok = p.perm[tl] / p.k;
-              src = p.x[tok / p.T_r] + size_t(tok % p.T_r) * row_bytes + off;
+              bulk_s2g(p.sorted + size_t(tl) * row_bytes + off, stage + buf * COPY_CHUNK, sz);
             } else {
-              src = p.x[r] + size_t(tl) * row_bytes + off;
+              const int tok = r * p.T_r + tl;
+              for (int sl = 0; sl < p.k; ++sl) {
+                const int pos = inv[tok * p.k + sl];
+                bulk_s2g(p.sorted + size_t(pos) * row_bytes + off, stage + buf * COPY_CHUNK, sz);
+              }
             }
-            mbar_arrive_expect_tx(&bars->copy[buf], sz);
-            bulk_g2s(stage + buf * COPY_CHUNK, src, sz, &bars->copy[buf]);
-            ++issued;
+            bulk_commit();
+            ++stored;
           }
-          const uint32_t q = seq + uint32_t(stored);
-          const int buf = int(q % MOE_COPY_NBUF);
-          if (!mbar_wait(&bars->copy[buf], (q / MOE_COPY_NBUF) & 1u, abort, p.status, p.pipe_timeout_ns, 5)) {
-            dead = true;
-            break;
-          }
-          const int tl = t0 + stored / pieces, pc = stored % pieces;
-          const uint32_t off = uint32_t(pc) * COPY_CHUNK;
-          const uint32_t sz = min(COPY_CHUNK, row_bytes - off);
-          if (p.pull) {
-            bulk_s2g(p.sorted + size_t(tl) * row_bytes + off, stage + buf * COPY_CHUNK, sz);
-          } else {
-            const int tok = r * p.T_r + tl;
-            for (int sl = 0; sl < p.k; ++sl) {
-              const int pos = inv[tok * p.k + sl];
-              bulk_s2g(p.sorted + size_t(pos) * row_bytes + off, stage + buf * COPY_CHUNK, sz);
-            }
-          }
-          bulk_commit();
-          ++stored;
+          seq += uint32_t(nunits);
+          bulk_wait<0>();
+          if (dead) break;
+          fence_proxy_async_global();
+          st_release(p.flags + (p.pull ? it : r * p.bpr + c), p.epoch);
         }
-        seq += uint32_t(nunits);
-        bulk_wait<0>();
-        if (dead) break;
-        fence_proxy_async_global();
-        st_release(p.flags + (p.pull ? it : r * p.bpr + c), p.epoch);
       }
       bulk_wait<0>();
     }
@@ -602,6 +621,7 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
     p->P = int(P);
     p->perm = a->perm;
     p->epoch = a->epoch;
+    if ((res = test_hold("tl_moe_ag_gemm", p->timeout_ns, &p->hold_first, &p->hold_count, &p->hold_ns))) break;
     const int pairs = std::max(1, std::min(di.sm_count / 2, std::max(max_tiles * p->Nt, (p->num_items + 1) / 2)));
     void* args[] = {p};
     res = launch_coop(reinterpret_cast<const void*>(&moe_gemm_kernel), 2 * pairs, MOE_THREADS, MOE_SMEM_BYTES, st,
