@@ -728,10 +728,10 @@ class MoeDown:
         self.sig = B.Signals(B.tl_moe_down_num_flags(c["R"], c["T_r"], c["topk"], c["E"], c["Hd"]))
         self.epoch = 0
 
-    def run(self):
+    def run(self, options=0):
         self.epoch += 1
         self.B.tl_moe_down(self.H, self.W2, self.gates, self.wl.ws_moe, self.out, self.work, self.sig, self.epoch,
-                           topk=MOE_DOWN["topk"], E=MOE_DOWN["E"])
+                           topk=MOE_DOWN["topk"], E=MOE_DOWN["E"], options=options)
 
     def check_status(self):
         code, where = self.B.tl_query_status(self.sig)
@@ -1040,10 +1040,14 @@ def main():
         down = MoeDown(B, torch, wl)
         flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
         t = flushed_time_us(torch, down.run, flush, reps=5)
+        t_bf16 = flushed_time_us(torch, lambda: down.run(options=B.TL_RS_BF16_PARTIALS), flush, reps=5)
         down.check_status()
         line["extras"] = {"moe_down": {"us": t, "tflops": MOE_DOWN_FLOPS / (t * 1e-6) / 1e12, "config": MOE_DOWN,
+                                       "bf16_partials_us": t_bf16,
+                                       "bf16_partials_tflops": MOE_DOWN_FLOPS / (t_bf16 * 1e-6) / 1e12,
                                        "what": "grouped GEMM -> ReduceScatter over ranks -> gate-weighted "
-                                               "TopK-reduce -> scatter, one call (two launches)"}}
+                                               "TopK-reduce -> scatter, one call (two launches); fp32 partials, "
+                                               "and bf16 partials (TL_RS_BF16_PARTIALS)"}}
         del down, flush
         line["extras"]["ag_attn"] = attn_extras(torch, B, peaks, peak_src)
         line["extras"]["allgather_ll"] = ll_extras(torch, B)

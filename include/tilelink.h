@@ -503,7 +503,8 @@ typedef struct tl_moe_down_args {
   size_t workspace_bytes;
   tl_signals* signals;         /* >= tl_moe_down_num_flags(...) flags */
   uint32_t epoch;              /* nonzero */
-  uint32_t reserved0;
+  uint32_t options;            /* 0, or TL_RS_BF16_PARTIALS: each rank's partial is rounded to bf16 (RNE)
+                                  before it is pushed (half the partial bytes), summed in fp32 as before */
   uint64_t timeout_ns;         /* 0 = 1 s */
 } tl_moe_down_args;
 

@@ -145,7 +145,17 @@ def moe_at(X_shards, topk_ids, W, rows, cols, route_result=None):
     return out
 
 
-def moe_down(H_list, W2_list, topk_ids, gates, E, T_r):
+def _rank_partial(p, partials):
+    """A rank's partial as it is summed: as is ("f32": exact here), or rounded to
+    bf16 first ("bf16": a rank that sends its partial in the output type)."""
+    if partials == "bf16":
+        return bf16.decode(bf16.encode_rne(p))
+    if partials != "f32":
+        raise ValueError(partials)
+    return p
+
+
+def moe_down(H_list, W2_list, topk_ids, gates, E, T_r, partials="f32"):
     """The down-projection side of the MoE layer, float64.
 
     Every expert's weights are split over the R ranks along the intermediate
@@ -155,7 +165,9 @@ def moe_down(H_list, W2_list, topk_ids, gates, E, T_r):
       Y[i]   = sum over ranks r = 0..R-1, in order, of H_r[i] . W2_r[e slice]
       out[t] = sum over slots s = 0..k-1, in order, of gates[t, s] * Y[pos(t, s)]
     where pos(t, s) is the sorted row of pair t*k + s; row shard d of out
-    (tokens d*T_r .. (d+1)*T_r - 1) is returned as out[d]."""
+    (tokens d*T_r .. (d+1)*T_r - 1) is returned as out[d].  With partials="bf16"
+    each rank's term H_r[i] . W2_r[e slice] is rounded to bf16 (nearest even)
+    before it enters the rank-ordered sum."""
     R = len(H_list)
     ids = np.asarray(topk_ids)
     T, k = ids.shape
@@ -169,7 +181,7 @@ def moe_down(H_list, W2_list, topk_ids, gates, E, T_r):
         for e in range(E):
             lo, hi = int(offsets[e]), int(offsets[e + 1])
             if hi > lo:
-                Y[lo:hi] = Y[lo:hi] + Hr[lo:hi] @ Wr[e * I_r:(e + 1) * I_r]
+                Y[lo:hi] = Y[lo:hi] + _rank_partial(Hr[lo:hi] @ Wr[e * I_r:(e + 1) * I_r], partials)
     pos = np.empty(P, dtype=np.int64)
     pos[np.asarray(perm, dtype=np.int64)] = np.arange(P)
     g = np.asarray(gates, dtype=np.float64)
@@ -179,7 +191,7 @@ def moe_down(H_list, W2_list, topk_ids, gates, E, T_r):
     return [out[d * T_r:(d + 1) * T_r] for d in range(T // T_r)]
 
 
-def moe_down_at(H_list, W2_list, topk_ids, gates, E, toks, cols, route_result=None):
+def moe_down_at(H_list, W2_list, topk_ids, gates, E, toks, cols, route_result=None, partials="f32"):
     """out[toks[i], cols[i]] (global token index) one element at a time."""
     ids = np.asarray(topk_ids)
     T, k = ids.shape
@@ -196,7 +208,8 @@ def moe_down_at(H_list, W2_list, topk_ids, gates, E, toks, cols, route_result=No
             e = int(ids[int(t), s])
             y = 0.0
             for H_r, W2_r in zip(H_list, W2_list):
-                y += float(np.dot(bf16.decode(H_r[i, :]), bf16.decode(W2_r[e * I_r:(e + 1) * I_r, int(c)])))
+                y += float(_rank_partial(np.dot(bf16.decode(H_r[i, :]), bf16.decode(W2_r[e * I_r:(e + 1) * I_r, int(c)])),
+                                         partials))
             acc += float(gates[int(t), s]) * y
         out[n] = acc
     return out

@@ -412,6 +412,27 @@ def check_moe_down(moe_down, route, moe_down_at):
     np.testing.assert_allclose(moe_down_at(H, W2, ids, g0, E, toks, cols), o0[toks, cols], rtol=1e-12, atol=1e-12)
 
 
+def check_moe_down_bf16(moe_down, moe_down_at):
+    """Pins of the bf16-partials variant of the MoE down side, by hand.  Two
+    tokens of two ranks route to the one expert (k = 1, I_r = 2, Hd = 1); rank 1
+    adds 3*2^-8 to both.  Rank 0's term is 1 + 2^-8 for token 0 (a tie between 1
+    and 1 + 2^-7, to even: 1) and 1 + 3*2^-9 for token 1 (three quarters of a
+    step: 1 + 2^-7).  So with bf16 partials token 0 gives 1 + 3*2^-8 and token 1,
+    gated by 1/2, (1 + 2^-7 + 3*2^-8) / 2; with fp32 partials 1 + 2^-6 and
+    (1 + 9*2^-9) / 2.  Rounding the sum instead of each partial gives 1 + 2^-6
+    for token 0; truncating instead of rounding gives (1 + 3*2^-8) / 2 for token 1."""
+    H = [_bits(np.array([[1.0, 2.0 ** -8], [1.0, 3 * 2.0 ** -9]])), _bits(np.array([[0.0, 3 * 2.0 ** -8]] * 2))]
+    W2 = [_bits(np.array([[1.0], [1.0]]))] * 2
+    ids = np.zeros((2, 1), dtype=np.int32)
+    gates = np.array([[1.0], [0.5]], dtype=np.float32)
+    want_bf16 = [1 + 3 * 2.0 ** -8, (1 + 2.0 ** -7 + 3 * 2.0 ** -8) / 2]
+    want_f32 = [1 + 2.0 ** -6, (1 + 9 * 2.0 ** -9) / 2]
+    for partials, want in (("bf16", want_bf16), ("f32", want_f32)):
+        out = moe_down(H, W2, ids, gates, 1, 1, partials=partials)
+        np.testing.assert_array_equal([out[0][0, 0], out[1][0, 0]], want)
+        np.testing.assert_array_equal(moe_down_at(H, W2, ids, gates, 1, [0, 1], [0, 0], partials=partials), want)
+
+
 # ------------------------------------------------------------------ AllGather-KV attention
 
 def check_ag_attention(attn, gather):

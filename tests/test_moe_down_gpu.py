@@ -44,7 +44,7 @@ def routing_workspace(B, R, T_r, E, k, ids, seed):
     return ws
 
 
-def run_down(B, R, T_r, E, k, I_r, Hd, seed):
+def run_down(B, R, T_r, E, k, I_r, Hd, seed, options=0):
     import torch
     ids = inputs.zipf_topk(R * T_r, E, k, 1.2, seed + 3000)
     H, W2, gates = inputs.moe_down_inputs(R, T_r, k, E, I_r, Hd, seed)
@@ -55,7 +55,7 @@ def run_down(B, R, T_r, E, k, I_r, Hd, seed):
     sig = B.Signals(B.tl_moe_down_num_flags(R, T_r, k, E, Hd))
     _epoch[0] += 1
     B.tl_moe_down([dev_bf16(h) for h in H], [dev_bf16(w) for w in W2], torch.from_numpy(gates).cuda(), ws_route,
-                  out, work, sig, _epoch[0], topk=k, E=E)
+                  out, work, sig, _epoch[0], topk=k, E=E, options=options)
     return dict(out=out, status=B.tl_query_status(sig), ids=ids, H=H, W2=W2, gates=gates)
 
 
@@ -102,3 +102,24 @@ def test_moe_down_full_size_sampled(B):
     check_bf16(got, want, "out sampled")
     for d in range(R):
         assert np.isfinite(to_f64(r["out"][d])).all()
+
+
+@pytest.mark.parametrize("R,T_r,E,k,I_r,Hd", [(2, 64, 5, 2, 72, 264), (4, 256, 8, 2, 256, 512),
+                                              (3, 100, 6, 3, 136, 136), (8, 128, 32, 2, 128, 512)])
+def test_moe_down_bf16_partials_parity(B, R, T_r, E, k, I_r, Hd):
+    # each rank's partial rounded to bf16 before it is pushed: against the oracle's bf16-partials
+    # variant.  The GPU rounds its fp32 accumulation of a partial, which may land one bf16 step
+    # from the exact partial rounded (a step is at most 2^-7 |P_r|); the final rounding adds
+    # 2^-9 |o|.  The magnitudes sum_s g_s sum_r |P_r| are bounded by the same oracle on |H|,
+    # |W2| and |g| (bf16 magnitudes: the sign bit cleared).
+    r = run_down(B, R, T_r, E, k, I_r, Hd, seed=120 + R + E, options=B.TL_RS_BF16_PARTIALS)
+    assert r["status"] == (0, -1), r["status"]
+    want = oracle.moe.moe_down(r["H"], r["W2"], r["ids"], r["gates"], E, T_r, partials="bf16")
+    mag = oracle.moe.moe_down([(h & 0x7FFF).astype(np.uint16) for h in r["H"]],
+                              [(w & 0x7FFF).astype(np.uint16) for w in r["W2"]], r["ids"], np.abs(r["gates"]), E, T_r)
+    for d in range(R):
+        got, o = to_f64(r["out"][d]), want[d]
+        assert np.isfinite(got).all()
+        bound = 2.0 ** -7 * mag[d] + 2.0 ** -8 * np.abs(o) + 1e-3 * np.abs(o).max()
+        assert np.all(np.abs(got - o) <= bound), f"out[{d}]: max excess {np.max(np.abs(got - o) - bound):.3e}"
+        assert np.abs(got - o).max() / np.abs(o).max() <= 2e-2

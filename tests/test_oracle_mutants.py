@@ -278,3 +278,40 @@ def test_pins_catch_moe_down_sampler_mistakes(old, new):
 def test_pins_catch_partial_abs_sum_mistakes(old, new):
     m = _mutated_module(G, "gemm_rs_mutant", old, new)
     _fails(C.check_partial_abs_sum, m.partial_abs_sum)
+
+
+@pytest.mark.parametrize("old,new", [
+    # the partials summed unrounded
+    ('    if partials == "bf16":\n        return bf16.decode(bf16.encode_rne(p))',
+     '    if partials == "bf16":\n        return p'),
+    # rounded toward zero instead of to nearest even
+    ('    if partials == "bf16":\n        return bf16.decode(bf16.encode_rne(p))',
+     '    if partials == "bf16":\n        return np.trunc(np.asarray(p) * 128.0) / 128.0'),
+])
+def test_pins_catch_moe_down_bf16_partial_mistakes(old, new):
+    m = _mutated_module(M, "moe_bf16_mutant", old, new)
+    _fails(C.check_moe_down_bf16, m.moe_down, m.moe_down_at)
+
+
+def test_pins_catch_moe_down_sum_rounded_instead_of_partials():
+    def bad(H, W2, ids, gates, E, T_r, partials="f32"):
+        if partials != "bf16":
+            return M.moe_down(H, W2, ids, gates, E, T_r)
+        R = len(H)
+        T, k = np.asarray(ids).shape
+        counts, offsets, perm = M.route(ids, E)
+        I_r = H[0].shape[1]
+        Y = np.zeros((T * k, W2[0].shape[1]))
+        for h, w in zip(H, W2):
+            hd, wd = bf16.decode(h), bf16.decode(w)
+            for e in range(E):
+                lo, hi = int(offsets[e]), int(offsets[e + 1])
+                Y[lo:hi] += hd[lo:hi] @ wd[e * I_r:(e + 1) * I_r]
+        Y = bf16.decode(bf16.encode_rne(Y))
+        pos = np.empty(T * k, dtype=np.int64)
+        pos[np.asarray(perm)] = np.arange(T * k)
+        out = np.zeros((T, Y.shape[1]))
+        for s in range(k):
+            out = out + np.asarray(gates, np.float64)[:, s:s + 1] * Y[pos[np.arange(T) * k + s]]
+        return [out[d * T_r:(d + 1) * T_r] for d in range(T // T_r)]
+    _fails(C.check_moe_down_bf16, bad, M.moe_down_at)

@@ -155,6 +155,10 @@ def test_moe_down_pins():
     C.check_moe_down(oracle.moe.moe_down, oracle.moe.route, oracle.moe.moe_down_at)
 
 
+def test_moe_down_bf16_partials_pins():
+    C.check_moe_down_bf16(oracle.moe.moe_down, oracle.moe.moe_down_at)
+
+
 def test_ag_attention_pins():
     C.check_ag_attention(oracle.attention.ag_kv_attention, oracle.attention.gather)
 

@@ -108,7 +108,7 @@ class tl_moe_down_args(ctypes.Structure):
         ("I_r", ctypes.c_int32), ("Hd", ctypes.c_int32),
         ("H", ctypes.POINTER(_vp)), ("W2", ctypes.POINTER(_vp)), ("gates", _vp), ("routing", _vp),
         ("out", ctypes.POINTER(_vp)), ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t), ("signals", _vp),
-        ("epoch", ctypes.c_uint32), ("reserved0", ctypes.c_uint32), ("timeout_ns", ctypes.c_uint64),
+        ("epoch", ctypes.c_uint32), ("options", ctypes.c_uint32), ("timeout_ns", ctypes.c_uint64),
     ]
 
 
@@ -460,7 +460,7 @@ def tl_moe_down_num_flags(R, T_r, topk, E, Hd):
 
 
 def tl_moe_down(H, W2, gates, routing, out, workspace, signals: Signals, epoch: int, *, topk, E, timeout_ns=0,
-                stream=None):
+                options=0, stream=None):
     """out[d] = the gate-weighted combine of each token's expert outputs, Y summed over ranks
     (see tilelink.h); routing is the workspace of the matching tl_moe_ag_gemm call."""
     R = len(H)
@@ -472,7 +472,7 @@ def tl_moe_down(H, W2, gates, routing, out, workspace, signals: Signals, epoch: 
                          W2=ctypes.cast(pw, ctypes.POINTER(_vp)), gates=_ptr(gates), routing=_ptr(routing),
                          out=ctypes.cast(po, ctypes.POINTER(_vp)), workspace=_ptr(workspace),
                          workspace_bytes=workspace.numel() * workspace.element_size(), signals=signals.handle,
-                         epoch=int(epoch) & 0xFFFFFFFF, reserved0=0, timeout_ns=int(timeout_ns))
+                         epoch=int(epoch) & 0xFFFFFFFF, options=int(options), timeout_ns=int(timeout_ns))
     _check(lib.tl_moe_down(ctypes.byref(a), _stream(stream)))
 
 

@@ -24,6 +24,8 @@
 // "reduced" flag that frees the slot).  The K loop runs over I_r; columns of
 // H_r past I_r read as zero, so a k-block that reaches into the next expert's
 // slice of W2_r adds nothing.
+// Option TL_RS_BF16_PARTIALS: every partial is rounded to bf16 (RNE) before it
+// is pushed and widened back to fp32 by the reducers (half the partial bytes).
 // Launch 2, moe_combine_kernel: out[d][u] = bf16(sum over slots, in order, of
 // gate * Y[sorted row of the pair]), t = d*T_r + u.
 #include <algorithm>
@@ -86,6 +88,8 @@ __device__ __forceinline__ MdItem md_item(const MdParams& p, int i, int ntiles) 
   return it;
 }
 
+// kBf16: partials travel as bf16 (TL_RS_BF16_PARTIALS); one instantiation per partial type.
+template <bool kBf16>
 __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_constant__ MdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -149,17 +153,30 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
       const bool ok = mbar_wait(&bars->tmem_full[acc], acc_ph, abort, p.status, p.pipe_timeout_ns, 4);
       if (!named_bar_and(1, kNumEpiThreads, ok)) break;
       tc_fence_after();
-      float* slot = p.slots + (size_t(i % p.ring_items) * 2 + h) * p.half_floats + my_base;
+      // element offset of this thread's first value in its half-slot (4-byte floats, or
+      // 2-byte bf16 values in half the bytes)
+      const size_t slot_el = (size_t(i % p.ring_items) * 2 + h) * p.half_floats + my_base;
       const uint64_t stream = l2_policy_evict_first();  // partial lines: written once, read once
       for (int c = 0; c < pair::BN / 32; ++c) {
         if (it.n * pair::BN + c * 32 >= p.Hd) break;
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
+        if (kBf16) {
+          uint16_t* slot16 = reinterpret_cast<uint16_t*>(p.slots) + slot_el;
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          const float* f = reinterpret_cast<const float*>(v + g * 4);
-          st_global_cg_v4f_hint(slot + size_t(c * 8 + g) * p.slice_rows * 4, f[0], f[1], f[2], f[3], stream);
+          for (int g = 0; g < 8; ++g) {
+            const float* f = reinterpret_cast<const float*>(v + g * 4);
+            st_global_cg_v2u_hint(slot16 + size_t(c * 8 + g) * p.slice_rows * 4, pack_bf16x2(f[0], f[1]),
+                                  pack_bf16x2(f[2], f[3]), stream);
+          }
+        } else {
+          float* slot = p.slots + slot_el;
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            const float* f = reinterpret_cast<const float*>(v + g * 4);
+            st_global_cg_v4f_hint(slot + size_t(c * 8 + g) * p.slice_rows * 4, f[0], f[1], f[2], f[3], stream);
+          }
         }
       }
       tc_fence_before();
@@ -214,11 +231,30 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
               j -= j >= p.R ? p.R : 0;
               int slot = ring_base + j;
               slot -= slot >= p.ring_items ? p.ring_items : 0;
-              const float* src = p.slots + (size_t(slot) * 2 + h) * p.half_floats;
+              const size_t base_el = (size_t(slot) * 2 + h) * p.half_floats;
+              if (kBf16) {
+                // raw words now, widened below, so every load of the batch is in flight together
+                const uint16_t* src16 = reinterpret_cast<const uint16_t*>(p.slots) + base_el;
+#pragma unroll
+                for (int u = 0; u < QU; ++u)
+                  if (off[u] >= 0) {
+                    const uint2 w = ld_global_cg_v2u_hint(src16 + off[u], drop);
+                    v[rr][u] = make_float4(__uint_as_float(w.x), __uint_as_float(w.y), 0.f, 0.f);
+                  }
+              } else {
+                const float* src = p.slots + base_el;
+#pragma unroll
+                for (int u = 0; u < QU; ++u)
+                  if (off[u] >= 0) v[rr][u] = ld_global_cg_v4f_hint(src + off[u], drop);
+              }
+            }
+          }
+          if (kBf16) {
+#pragma unroll
+            for (int rr = 0; rr < RB; ++rr)
 #pragma unroll
               for (int u = 0; u < QU; ++u)
-                if (off[u] >= 0) v[rr][u] = ld_global_cg_v4f_hint(src + off[u], drop);
-            }
+                v[rr][u] = unpack_bf16x4(make_uint2(__float_as_uint(v[rr][u].x), __float_as_uint(v[rr][u].y)));
           }
           // fixed rank order: ((P_0 + P_1) + P_2) + ...
 #pragma unroll
@@ -331,6 +367,7 @@ extern "C" tl_status tl_moe_down(const tl_moe_down_args* a, void* stream) {
   if (!a->H || !a->W2 || !a->gates || !a->routing || !a->out || !a->workspace || !a->signals)
     return fail(TL_ERR_INVALID, "tl_moe_down: NULL pointer argument");
   if (a->epoch == 0) return fail(TL_ERR_INVALID, "tl_moe_down: epoch must be nonzero");
+  if (a->options & ~TL_RS_BF16_PARTIALS) return fail(TL_ERR_INVALID, "tl_moe_down: unknown options 0x%x", a->options);
   for (int r = 0; r < a->R; ++r)
     if (!a->H[r] || !a->W2[r] || !a->out[r] || !aligned16(a->H[r]) || !aligned16(a->W2[r]) || !aligned16(a->out[r]))
       return fail(TL_ERR_INVALID, "tl_moe_down: rank %d pointer NULL or not 16-byte aligned", r);
@@ -384,8 +421,9 @@ extern "C" tl_status tl_moe_down(const tl_moe_down_args* a, void* stream) {
     p->half_floats = md_half_floats(a->R);
     p->epoch = a->epoch;
     void* args[] = {p};
-    st = launch_coop(reinterpret_cast<const void*>(&moe_down_kernel), 2 * pairs, MD_THREADS, MD_SMEM_BYTES,
-                     (cudaStream_t)stream, args, 2);
+    const void* kernel = (a->options & TL_RS_BF16_PARTIALS) ? reinterpret_cast<const void*>(&moe_down_kernel<true>)
+                                                             : reinterpret_cast<const void*>(&moe_down_kernel<false>);
+    st = launch_coop(kernel, 2 * pairs, MD_THREADS, MD_SMEM_BYTES, (cudaStream_t)stream, args, 2);
     if (st) break;
     CombineParams c{};
     c.Y = p->Y;
