@@ -80,7 +80,7 @@ def parse():
                     help="AG-GEMM sweep (R in {2,4,8}, M in {1024..16384}, K=8192, N=1024; shards in HBM and "
                          "peer shards in pinned host memory): copy, GEMM, sequential and fused times, one JSON line")
     ap.add_argument("--no-extras", action="store_true", help="skip the measurements outside the step")
-    ap.add_argument("--only", choices=["ag", "rs", "moe", "moe_down", "ag_attn"],
+    ap.add_argument("--only", choices=["ag", "rs", "moe", "moe_down", "ag_attn", "gemm_vs_library"],
                     help="run one fused call of the step (W untimed, then K timed back to back) and print its "
                          "device time; for profiling a single kernel on the bench's workload")
     return ap.parse_args()
@@ -939,6 +939,18 @@ def main():
         elif args.only == "ag_attn":
             attn = AgAttn(B, torch)
             fn, flops = attn.run, attn_flops(AG_ATTN, False, 0)
+        elif args.only == "gemm_vs_library":
+            # the compute half of the AG-GEMM alone (tl_gemm on the gathered matrix), then the
+            # library GEMM on the same operands: one launch of each per call, for profiling them
+            # side by side; the time printed covers both
+            wl.ag()
+            C_lib = torch.empty_like(wl.C)
+            sig_g = B.Signals(1)
+
+            def fn():
+                B.tl_gemm(wl.G, wl.d_ag[AG["R"]], wl.C, sig_g)
+                torch.matmul(wl.G, wl.d_ag[AG["R"]], out=C_lib)
+            flops = 2 * AG_FLOPS
         else:
             fn = {"ag": wl.ag, "rs": wl.rs, "moe": wl.moe}[args.only]
             flops = {"ag": AG_FLOPS, "rs": RS_FLOPS, "moe": MOE_FLOPS}[args.only]

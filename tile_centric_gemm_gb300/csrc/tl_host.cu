@@ -227,7 +227,7 @@ tl_status ensure_smem_limit(int device, const void* kernel, size_t smem) {
 }  // namespace
 
 tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cudaStream_t st, void** args,
-                      int cluster) {
+                      int cluster, bool early_start) {
   DeviceInfo di{};
   if (tl_status s = device_info(&di)) return s;
   if (cluster < 1 || grid % cluster) return fail(TL_ERR_INTERNAL, "grid %d is not a multiple of cluster %d", grid, cluster);
@@ -272,7 +272,7 @@ tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cuda
   cfg.blockDim = dim3(block);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   if (cluster > 1) {
     // Clusters: the grid is sized to the number of clusters the device holds at
     // once, so every CTA is resident together (the cooperative attribute is not
@@ -284,6 +284,11 @@ tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cuda
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (early_start) {
+      attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[1].val.programmaticStreamSerializationAllowed = 1;
+      cfg.numAttrs = 2;
+    }
     return cuda_ok(cudaLaunchKernelExC(&cfg, kernel, args), "cluster launch");
   }
   attr[0].id = cudaLaunchAttributeCooperative;

@@ -53,8 +53,11 @@ tl_status make_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t planes, 
 // for single CTAs, a cluster launch sized within the device's resident-cluster
 // capacity for clusters of `cluster` CTAs.  Fails instead of launching when the
 // grid cannot be resident at once.
+// early_start (clusters only): programmatic dependent launch -- the grid may start
+// before the previous kernel on the stream has finished, and must wait for it
+// (griddepcontrol.wait) before it reads what that kernel wrote.
 tl_status launch_coop(const void* kernel, int grid, int block, size_t smem, cudaStream_t st, void** args,
-                      int cluster = 1);
+                      int cluster = 1, bool early_start = false);
 
 // Where each of R shard pointers lives: device memory of `device` (bulk TMA
 // copies), or pinned host / managed memory (plain loads; bit r of *host_mask).

@@ -9,8 +9,10 @@
 //    dependencies come from lookup tables built from the routing and passed
 //    to the kernel.
 //
-// Two stream-ordered launches:
-//  1. moe_route_kernel (one CTA): histogram of topk_ids over experts,
+// Two stream-ordered launches, the second started early (programmatic dependent
+// launch: its prologue overlaps the first, and it waits for the first before it
+// reads the tables):
+//  1. moe_route_kernel (a cluster of 8 CTAs): histogram of topk_ids over experts,
 //     exclusive scan, stable counting sort of the (token, slot) pairs by expert
 //     (perm and its inverse), then the tile table -- per 256-row tile its
 //     expert, first sorted row, rows, lowest and highest producer barrier and
@@ -81,11 +83,13 @@ __device__ __forceinline__ unsigned same_expert_lanes(unsigned am, int e) {
 // of the P = T*k (token, slot) pairs, and its warps own consecutive sub-ranges.
 //  1. per-warp expert counts over the warp's pairs;
 //  2. (cluster barrier) every CTA reads every CTA's per-expert totals from
-//     distributed shared memory: expert offsets (exclusive scan) and, for a
-//     stable sort, the base of each of its warps per expert = offset + the counts
-//     of every lower CTA and every lower warp of this CTA; stable scatter of the
-//     pairs (perm and its inverse, in global memory);
+//     distributed shared memory: expert offsets (exclusive scan), tile offsets
+//     and, for a stable sort, the base of each of its warps per expert = offset +
+//     the counts of every lower CTA and every lower warp of this CTA; stable
+//     scatter of the pairs (perm and its inverse, in global memory), each pair
+//     also marking its tile's source rank and token barrier in shared memory;
 //  3. (cluster barrier) the tile table, one tile per warp across the cluster,
+//     the masks and barrier ranges combined from every CTA's shared memory,
 //     the tile keys gathered in CTA 0's shared memory;
 //  4. (cluster barrier) CTA 0 ranks the tiles by (key, index): the consumer order.
 __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const RouteParams p) {
@@ -96,8 +100,14 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   int32_t* s_off = ctot + E;               // [E+1] expert offsets
   int32_t* s_toff = s_off + (E + 1);       // [E+1] first tile of each expert
   int32_t* s_key = s_toff + (E + 1);       // [max_tiles] tile keys (CTA 0)
+  // per tile, over this CTA's pairs: source-rank mask, lowest and highest token barrier
+  int32_t* s_mask = s_key + p.max_tiles;
+  int32_t* s_blo = s_mask + p.max_tiles;
+  int32_t* s_bhi = s_blo + p.max_tiles;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = cluster_ctarank();
+  // the grouped GEMM may start its prologue now; it waits for this kernel before reading the tables
+  pdl_launch_dependents();
   const int P = p.T * p.k;
   const int per_cta = ((P + ROUTE_CTAS - 1) / ROUTE_CTAS + 31) / 32 * 32;
   const int c0 = min(P, int(crank) * per_cta), c1 = min(P, c0 + per_cta);
@@ -108,6 +118,11 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   int32_t* inv = p.ws + ws_inv(p.max_tiles);
 
   for (int i = tid; i < ROUTE_WARPS * E; i += ROUTE_THREADS) cnt[i] = 0;
+  for (int t = tid; t < p.max_tiles; t += ROUTE_THREADS) {
+    s_mask[t] = 0;
+    s_blo[t] = 0x7fffffff;
+    s_bhi[t] = -1;
+  }
   __syncthreads();
   // 1. per-warp histograms over contiguous ranges of pairs
   for (int base = q0; base < q1; base += 32) {
@@ -169,23 +184,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
       run += c;
     }
   }
-  __syncthreads();
-  // stable scatter: pairs keep their (token, slot) order inside an expert
-  for (int base = q0; base < q1; base += 32) {
-    const int q = base + lane;
-    const bool act = q < q1;
-    const int e = act ? min(max(p.topk[q], 0), E - 1) : 0;
-    const unsigned am = __ballot_sync(0xffffffffu, act);
-    if (act) {
-      const unsigned peers = same_expert_lanes(am, e);
-      const int pos = cnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
-      p.perm[pos] = q;
-      inv[q] = pos;
-      __syncwarp(am);
-      if (lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
-    }
-    __syncwarp();
-  }
+  __syncthreads();  // the parked counts are read; s_toff now takes the tile offsets
   // tiles per expert and their offsets (every CTA, from the same totals)
   if (tid == 0) {
     int acc = 0;
@@ -200,9 +199,36 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
         record_error(p.status, TL_ERR_INTERNAL, 0xFFFE0000u, uint32_t(acc), uint32_t(p.max_tiles));
     }
   }
+  __syncthreads();
+  // stable scatter: pairs keep their (token, slot) order inside an expert; each pair also
+  // marks its tile's source rank and token barrier range (this CTA's share of the table)
+  for (int base = q0; base < q1; base += 32) {
+    const int q = base + lane;
+    const bool act = q < q1;
+    const int e = act ? min(max(p.topk[q], 0), E - 1) : 0;
+    const unsigned am = __ballot_sync(0xffffffffu, act);
+    if (act) {
+      const unsigned peers = same_expert_lanes(am, e);
+      const int pos = cnt[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
+      p.perm[pos] = q;
+      inv[q] = pos;
+      const int tok = p.k_shift >= 0 ? (q >> p.k_shift) : q / p.k;
+      const int r = tok / p.T_r;
+      const int b = r * p.bpr + (tok - r * p.T_r) / p.rpb;
+      const int t = s_toff[e] + (pos - s_off[e]) / TM;
+      if (t < p.max_tiles) {
+        atomicOr(reinterpret_cast<unsigned*>(&s_mask[t]), 1u << r);
+        atomicMin(&s_blo[t], b);
+        atomicMax(&s_bhi[t], b);
+      }
+      __syncwarp(am);
+      if (lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
+    }
+    __syncwarp();
+  }
   if (crank == 0)
     for (int e = tid; e <= E; e += ROUTE_THREADS) p.offsets[e] = s_off[e];
-  // every CTA's perm and inverse are in global memory before any tile reads them
+  // every CTA's share of the per-tile masks and barrier ranges is complete
   cluster_sync();
   // 3. the tile table, one warp per tile across the cluster: rows of a tile are one
   //    expert's, tokens ascending
@@ -216,16 +242,14 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     const int e = lo_e;
     const int row0 = s_off[e] + (t - s_toff[e]) * TM;
     const int rows = min(TM, s_off[e + 1] - row0);
+    // the tile's source ranks and barrier range: every CTA's share, through distributed
+    // shared memory (lane c reads CTA c's)
     uint32_t mask = 0;
     int blo = 0x7fffffff, bhi = -1;
-    for (int i = lane; i < rows; i += 32) {
-      const int q = p.perm[row0 + i];
-      const int tok = p.k_shift >= 0 ? (q >> p.k_shift) : q / p.k;
-      const int r = tok / p.T_r;
-      const int b = r * p.bpr + (tok - r * p.T_r) / p.rpb;
-      mask |= 1u << r;
-      blo = min(blo, b);
-      bhi = max(bhi, b);
+    if (lane < int(ROUTE_CTAS)) {
+      mask = ld_shared_cluster_u32(map_to_rank(&s_mask[t], uint32_t(lane)));
+      blo = int(ld_shared_cluster_u32(map_to_rank(&s_blo[t], uint32_t(lane))));
+      bhi = int(ld_shared_cluster_u32(map_to_rank(&s_bhi[t], uint32_t(lane))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -305,8 +329,11 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
   const int32_t* tiles = p.ws + ws_tiles(p.max_tiles);
   const int32_t* order = p.ws + ws_order(p.max_tiles);
   const int32_t* inv = p.ws + ws_inv(p.max_tiles);
-  const int num_work = p.ws[0] * p.Nt;
   const uint32_t tmem_base = pair::setup(bars, warp);
+  // launched early (programmatic dependent launch): the routing kernel's tables are complete
+  // and visible only after this
+  pdl_wait_previous();
+  const int num_work = p.ws[0] * p.Nt;
   volatile uint32_t* abort = &bars->abort;
   const int my_work = pair_id < num_work ? (num_work - 1 - pair_id) / npairs + 1 : 0;
 
@@ -574,7 +601,7 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
   rp.max_tiles = max_tiles;
   rp.pull = pull ? 1 : 0;
   rp.k_shift = (a->topk & (a->topk - 1)) == 0 ? __builtin_ctz(unsigned(a->topk)) : -1;
-  const size_t route_smem = (size_t(ROUTE_WARPS) * a->E + a->E + 2 * (a->E + 1) + max_tiles) * sizeof(int32_t);
+  const size_t route_smem = (size_t(ROUTE_WARPS) * a->E + a->E + 2 * (a->E + 1) + 4 * size_t(max_tiles)) * sizeof(int32_t);
   if (route_smem > size_t(di.max_smem_optin))
     return fail(TL_ERR_UNSUPPORTED, "tl_moe_ag_gemm: routing needs %zu bytes of shared memory", route_smem);
   {
@@ -625,7 +652,7 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
     const int pairs = std::max(1, std::min(di.sm_count / 2, std::max(max_tiles * p->Nt, (p->num_items + 1) / 2)));
     void* args[] = {p};
     res = launch_coop(reinterpret_cast<const void*>(&moe_gemm_kernel), 2 * pairs, MOE_THREADS, MOE_SMEM_BYTES, st,
-                      args, 2);
+                      args, 2, /*early_start=*/true);
   } while (false);
   delete p;
   return res;
