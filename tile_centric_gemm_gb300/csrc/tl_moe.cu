@@ -52,7 +52,10 @@ constexpr int MOE_COPY_NBUF = 3;
 constexpr uint32_t MOE_SMEM_COPY = pair::SMEM_END;
 constexpr uint32_t MOE_SMEM_CSTAGE = MOE_SMEM_COPY + MOE_COPY_NBUF * COPY_CHUNK;
 constexpr uint32_t MOE_SMEM_BARS = MOE_SMEM_CSTAGE + kNumEpiWarps * C_BOX_BYTES;
-constexpr uint32_t MOE_SMEM_BYTES = MOE_SMEM_BARS + sizeof(pair::Bars) + 1024;
+// the copy warp's tables: the shard pointers, and the tokens of the next MOE_TOKB sorted rows
+constexpr int MOE_TOKB = 16;
+constexpr uint32_t MOE_SMEM_XS = (MOE_SMEM_BARS + uint32_t(sizeof(pair::Bars)) + 15u) / 16u * 16u;
+constexpr uint32_t MOE_SMEM_BYTES = MOE_SMEM_XS + MOE_MAX_R * 8 + MOE_TOKB * 4 + 1024;
 
 static_assert(TM == MOE_TILE_ROWS, "expert tiles are CTA-pair tiles");
 
@@ -416,8 +419,14 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
     __syncwarp();
   } else if (warp == kWarpCopy) {
     // ---------------------------------------------------------------- AllGather + local scatter
+    // shard pointers in shared memory (a parameter array read with a varying index is slow)
+    const uint8_t** xs = reinterpret_cast<const uint8_t**>(smem + MOE_SMEM_XS);
+    int32_t* stok = reinterpret_cast<int32_t*>(smem + MOE_SMEM_XS + MOE_MAX_R * 8);
+    if (lane < p.R) xs[lane] = p.x[lane];
+    __syncwarp();
     if (lane == 0) {
       uint8_t* stage = smem + MOE_SMEM_COPY;
+      int tb_base = 0, tb_end = 0;  // pull: sorted rows whose tokens are in stok
       const uint32_t row_bytes = uint32_t(p.H) * 2u;
       const int pieces = int((row_bytes + COPY_CHUNK - 1) / COPY_CHUNK);
       uint32_t seq = 0;  // pieces loaded by this CTA: buffer seq % NBUF, parity (seq / NBUF) & 1
@@ -457,10 +466,20 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
               const uint32_t sz = min(COPY_CHUNK, row_bytes - off);
               const uint8_t* src;
               if (p.pull) {
-                const int tok = p.perm[tl] / p.k;
-                src = p.x[tok / p.T_r] + size_t(tok % p.T_r) * row_bytes + off;
+                if (tl >= tb_end || tl < tb_base) {
+                  // the tokens of the next MOE_TOKB rows of the item, their loads in flight together
+                  tb_base = tl;
+                  tb_end = min(t1, tl + MOE_TOKB);
+                  int v[MOE_TOKB];
+#pragma unroll
+                  for (int i = 0; i < MOE_TOKB; ++i) v[i] = tb_base + i < tb_end ? p.perm[tb_base + i] : 0;
+#pragma unroll
+                  for (int i = 0; i < MOE_TOKB; ++i) stok[i] = v[i] / p.k;
+                }
+                const int tok = stok[tl - tb_base];
+                src = xs[tok / p.T_r] + size_t(tok % p.T_r) * row_bytes + off;
               } else {
-                src = p.x[r] + size_t(tl) * row_bytes + off;
+                src = xs[r] + size_t(tl) * row_bytes + off;
               }
               mbar_arrive_expect_tx(&bars->copy[buf], sz);
               bulk_g2s(stage + buf * COPY_CHUNK, src, sz, &bars->copy[buf]);
