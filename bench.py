@@ -80,7 +80,7 @@ def parse():
                     help="AG-GEMM sweep (R in {2,4,8}, M in {1024..16384}, K=8192, N=1024; shards in HBM and "
                          "peer shards in pinned host memory): copy, GEMM, sequential and fused times, one JSON line")
     ap.add_argument("--no-extras", action="store_true", help="skip the measurements outside the step")
-    ap.add_argument("--only", choices=["ag", "rs", "moe", "moe_down", "ag_attn", "gemm_vs_library"],
+    ap.add_argument("--only", choices=["ag", "rs", "moe", "moe_down", "ag_attn", "gemm_vs_library", "allgather_ll"],
                     help="run one fused call of the step (W untimed, then K timed back to back) and print its "
                          "device time; for profiling a single kernel on the bench's workload")
     return ap.parse_args()
@@ -939,6 +939,21 @@ def main():
         elif args.only == "ag_attn":
             attn = AgAttn(B, torch)
             fn, flops = attn.run, attn_flops(AG_ATTN, False, 0)
+        elif args.only == "allgather_ll":
+            # one slow-link AllGather (flag in data) of 8 ranks x 16 rows x 4096 columns (128 KB per
+            # shard), the link in pinned host memory; "flops" stands for the bytes gathered
+            from tile_centric_gemm_gb300 import inputs as _in
+            Ms_ll = 16
+            A_ll = [_in.to_torch_bf16(_in.normal_bf16((Ms_ll, 4096), 1200 + r)).cuda() for r in range(8)]
+            link = torch.zeros(B.tl_allgather_ll_link_bytes(8, Ms_ll, 4096), dtype=torch.uint8).pin_memory()
+            G_ll = torch.empty(8 * Ms_ll, 4096, dtype=torch.bfloat16, device="cuda")
+            sig_ll = B.Signals(8 * Ms_ll)
+            ep_ll = [0]
+
+            def fn():
+                ep_ll[0] += 1
+                B.tl_allgather_ll(A_ll, link, G_ll, sig_ll, ep_ll[0])
+            flops = 8 * Ms_ll * 4096 * 2
         elif args.only == "gemm_vs_library":
             # the compute half of the AG-GEMM alone (tl_gemm on the gathered matrix), then the
             # library GEMM on the same operands: one launch of each per call, for profiling them
