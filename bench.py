@@ -52,9 +52,9 @@ WORKLOAD = ("AG-GEMM R=8 [8192x4096]x[4096x1792] + GEMM-RS R=8 8x[8192x1792]x[17
 # DRAM traffic of one gemm_rs_kernel launch on this workload, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid only while the kernel's
 # sources hash to what was captured.
-RS_TRAFFIC_BYTES = 2_501_390_336 + 1_066_054_400
+RS_TRAFFIC_BYTES = 2_633_970_688 + 1_068_726_528
 RS_TRAFFIC_SOURCES = ("tl_gemm_rs.cu", "tl_pair.cuh", "tl_common.cuh", "tl_ptx.cuh")
-RS_TRAFFIC_SHA256 = "3ac7837d8a8014f01dc0f41abda39df49068e75757f4a8bd5588fc0b7d56fed1"
+RS_TRAFFIC_SHA256 = "4127d74e6589b88ab86f006fda99f85dbb163cced507c08cbf4c328b136a4d93"
 
 
 def rs_traffic():
@@ -1050,7 +1050,17 @@ def main():
                      "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),
                      "traffic": rs_traffic(), "traffic_unit": "bytes per launch (ncu DRAM read + write)",
                      "algorithmic_bytes": RS_BYTES,
-                     "algorithmic_bytes_with_partials": RS_BYTES + RS_PARTIAL_BYTES},
+                     "algorithmic_bytes_with_partials": RS_BYTES + RS_PARTIAL_BYTES,
+                     # every call of the step against the same peak (CUDA events around each call)
+                     "per_call": {
+                         name: {"kernels": kern, "achieved": fl / (us * 1e-3) / 1e12,
+                                "frac": fl / (us * 1e-3) / 1e12 / peak,
+                                "frac_of_sustained": fl / (us * 1e-3) / 1e12 / peaks.get("bf16_tflops_sustained", peak)}
+                         for name, kern, fl, us in (
+                             ("ag_gemm", "ag_gemm_kernel", AG_FLOPS, ag_avg),
+                             ("gemm_rs", "gemm_rs_kernel", RS_FLOPS, rs_avg),
+                             ("moe_ag_gemm", "moe_route_kernel + moe_gemm_kernel (useful flops, no padding)",
+                              MOE_FLOPS, moe_avg))}},
         "clocks": clocks,
         "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes(),

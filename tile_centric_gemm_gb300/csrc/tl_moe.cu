@@ -430,6 +430,7 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
       const uint32_t row_bytes = uint32_t(p.H) * 2u;
       const int pieces = int((row_bytes + COPY_CHUNK - 1) / COPY_CHUNK);
       uint32_t seq = 0;  // pieces loaded by this CTA: buffer seq % NBUF, parity (seq / NBUF) & 1
+      const uint64_t pol_keep = l2_policy_evict_last();
       bool dead = false;
       const uint64_t t0 = now_ns();
       // the flag an item releases; held items (a test facility) go after the others
@@ -495,7 +496,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
             const uint32_t off = uint32_t(pc) * COPY_CHUNK;
             const uint32_t sz = min(COPY_CHUNK, row_bytes - off);
             if (p.pull) {
-              bulk_s2g(p.sorted + size_t(tl) * row_bytes + off, stage + buf * COPY_CHUNK, sz);
+              // evict-last: the grouped GEMM reads these rows soon, once per column tile
+              bulk_s2g_hint(p.sorted + size_t(tl) * row_bytes + off, stage + buf * COPY_CHUNK, sz, pol_keep);
             } else {
               const int tok = r * p.T_r + tl;
               for (int sl = 0; sl < p.k; ++sl) {
