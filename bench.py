@@ -311,10 +311,23 @@ class Workload:
         self.B.tl_moe_ag_gemm(m[:R], m[R + E], m[R:R + E], self.S, d["Y"], self.perm, self.offs, self.ws_moe,
                               self.sig_moe, self.epoch)
 
-    def h2d(self, b=0):
+    def _weight(self, i):
+        """Whether input i (in h_ag + h_rs + h_moe order) is a weight: B, the B_r, the W_e."""
+        R, Rr, E = AG["R"], RS["R"], MOE["E"]
+        n_ag, n_rs = len(self.h_ag), len(self.h_rs)
+        if i < n_ag:
+            return i == R
+        if i < n_ag + n_rs:
+            return i - n_ag >= Rr
+        return MOE["R"] <= i - n_ag - n_rs < MOE["R"] + E
+
+    def h2d(self, b=0, weights=True):
+        """Copy set b's inputs in from pinned host memory: every operand, or (weights=False)
+        the activations and the routing only, the weights staying resident."""
         d = self.sets[b]
-        for h, t in zip(self.h_ag + self.h_rs + self.h_moe, d["ag"] + d["rs"] + d["moe"]):
-            t.copy_(h, non_blocking=True)
+        for i, (h, t) in enumerate(zip(self.h_ag + self.h_rs + self.h_moe, d["ag"] + d["rs"] + d["moe"])):
+            if weights or not self._weight(i):
+                t.copy_(h, non_blocking=True)
 
     def d2h(self, b=0):
         d = self.sets[b]
@@ -323,8 +336,9 @@ class Workload:
             h.copy_(t, non_blocking=True)
         self.h_Y.copy_(d["Y"], non_blocking=True)
 
-    def h2d_bytes(self):
-        return sum(t.numel() * t.element_size() for t in self.h_ag + self.h_rs + self.h_moe)
+    def h2d_bytes(self, weights=True):
+        return sum(t.numel() * t.element_size() for i, t in enumerate(self.h_ag + self.h_rs + self.h_moe)
+                   if weights or not self._weight(i))
 
     def d2h_bytes(self):
         return self.h_C.numel() * 2 + sum(t.numel() * 2 for t in self.h_out) + self.h_Y.numel() * 2
@@ -336,28 +350,33 @@ class Workload:
                 raise RuntimeError(f"device error {code} at {where}")
 
 
-def e2e_serial(torch, wl, E, stream, barrier):
-    """ms per step with the copies and the calls in one stream: H2D inputs, the three
+def e2e_serial(torch, wl, E, stream, barrier, weights=True):
+    """ms per step with the copies and the calls in one stream: H2D inputs (every
+    operand, or the activations and routing with the weights resident), the three
     calls, D2H outputs, one step after the other."""
+    wl.h2d()
     for _ in range(2):
-        wl.h2d(); wl.ag(); wl.rs(); wl.moe(); wl.d2h()
+        wl.h2d(weights=weights); wl.ag(); wl.rs(); wl.moe(); wl.d2h()
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(E):
-        wl.h2d(); wl.ag(); wl.rs(); wl.moe(); wl.d2h()
+        wl.h2d(weights=weights); wl.ag(); wl.rs(); wl.moe(); wl.d2h()
     e1.record(stream)
     barrier()
     return e0.elapsed_time(e1) / E
 
 
-def e2e_pipelined(torch, wl, E, stream, barrier):
-    """ms per step over E steps, each copying all of its inputs in and all of its
-    outputs back, with two device sets: step i computes on set i % 2 while step
-    i+1's inputs copy into the other set (copy-in stream) and step i-1's outputs
-    copy out (copy-out stream).  The timed region runs from before the first
-    copy-in to after the last copy-out."""
+def e2e_pipelined(torch, wl, E, stream, barrier, weights=True):
+    """ms per step over E steps, each copying its inputs in (every operand, or with
+    weights=False the activations and routing, the weights loaded into both sets
+    once before timing) and all of its outputs back, with two device sets: step i
+    computes on set i % 2 while step i+1's inputs copy into the other set (copy-in
+    stream) and step i-1's outputs copy out (copy-out stream).  The timed region
+    runs from before the first copy-in to after the last copy-out."""
+    wl.h2d(0)
+    wl.h2d(1)
     cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
     ev = lambda: [torch.cuda.Event(), torch.cuda.Event()]
 
@@ -372,7 +391,7 @@ def e2e_pipelined(torch, wl, E, stream, barrier):
             with torch.cuda.stream(cin):
                 if i >= 2:
                     cin.wait_event(inputs_free[b])
-                wl.h2d(b)
+                wl.h2d(b, weights=weights)
                 inputs_ready[b].record(cin)
             stream.wait_event(inputs_ready[b])
             if i >= 2:
@@ -665,13 +684,17 @@ def run_sweep(torch, B, peaks):
 
                 C_lib = torch.empty_like(C)
                 graph = decomposed_graph(torch, B, shards, Bm, G, C, sig, ws_shard)
+                graph_lib = decomposed_graph(torch, B, shards, Bm, G, C_lib, sig, library=True)
                 t_copy = flushed_time_us(torch, copy_only, flush, reps=5)
                 t_gemm = flushed_time_us(torch, gemm_only, flush, reps=5)
                 t_seq = flushed_time_us(torch, seq, flush, reps=5)
-                t_dec = flushed_time_us(torch, graph.replay, flush, reps=5)
+                # the decomposed schedule with either per-shard GEMM; the faster one is reported
+                t_dec_tl = flushed_time_us(torch, graph.replay, flush, reps=5)
+                t_dec_lib = flushed_time_us(torch, graph_lib.replay, flush, reps=5)
+                t_dec = min(t_dec_tl, t_dec_lib)
                 t_fused = flushed_time_us(torch, fused, flush, reps=5)
                 t_lib = flushed_time_us(torch, lambda: torch.matmul(G, Bm, out=C_lib), flush, reps=5)
-                del graph
+                del graph, graph_lib
                 code, where = B.tl_query_status(sig)
                 if code:
                     raise RuntimeError(f"device error {code} at {where} in the sweep (R={R}, M={M}, {placement})")
@@ -681,7 +704,9 @@ def run_sweep(torch, B, peaks):
                     if ws_ag is not None else 1
                 rows.append({"placement": placement, "R": R, "M": M, "splits": int(splits),
                              "t_copy_us": t_copy, "t_gemm_us": t_gemm,
-                             "t_seq_us": t_seq, "t_decomposed_us": t_dec, "t_fused_us": t_fused,
+                             "t_seq_us": t_seq, "t_decomposed_us": t_dec,
+                             "t_decomposed_tl_gemm_splitk_us": t_dec_tl, "t_decomposed_torch_matmul_us": t_dec_lib,
+                             "t_fused_us": t_fused,
                              "t_torch_matmul_us": t_lib, "speedup_vs_decomposed": t_dec / t_fused,
                              "tflops": flops / (t_fused * 1e-6) / 1e12,
                              "frac_of_peak": flops / (t_fused * 1e-6) / 1e12 / peaks["bf16_tflops"],
@@ -1025,8 +1050,9 @@ def main():
     # end to end through the public API with host buffers: every step copies its inputs in
     # from pinned host memory, runs the three calls and reads its outputs back
     E = max(3, args.e2e_steps)
-    e2e_serial_ms = max_over_ranks(pg, e2e_serial(torch, wl, E, stream, barrier))
-    e2e_ms = max_over_ranks(pg, e2e_pipelined(torch, wl, E, stream, barrier))
+    e2e_serial_ms = max_over_ranks(pg, e2e_serial(torch, wl, E, stream, barrier, weights=False))
+    e2e_ms = max_over_ranks(pg, e2e_pipelined(torch, wl, E, stream, barrier, weights=False))
+    e2e_all_ms = max_over_ranks(pg, e2e_pipelined(torch, wl, E, stream, barrier, weights=True))
     wl.check_status()
 
     rs_avg = statistics.mean(rs_ms)
@@ -1063,11 +1089,17 @@ def main():
                               MOE_FLOPS, moe_avg))}},
         "clocks": clocks,
         "e2e": {"value": world * step_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes(),
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": wl.h2d_bytes(weights=False),
+                "d2h_bytes_per_step": wl.d2h_bytes(),
+                "inputs": "activations (A shards, A_r, token shards) and top-k ids copied in every step; the "
+                          "weights (B, B_r, W_e) are model state, loaded once before the timed region",
                 "how": "double-buffered: step i+1's inputs copy in on a copy stream while step i computes, "
                        "step i's outputs copy out on a third stream",
                 "serial_ms_per_step": e2e_serial_ms,
-                "serial_value": world * step_flops / (e2e_serial_ms * 1e-3) / 1e12},
+                "serial_value": world * step_flops / (e2e_serial_ms * 1e-3) / 1e12,
+                "all_operands": {"value": world * step_flops / (e2e_all_ms * 1e-3) / 1e12,
+                                 "ms_per_step": e2e_all_ms, "h2d_bytes_per_step": wl.h2d_bytes(),
+                                 "what": "the same, with every weight copied in every step as well"}},
         "gpu_launches": K * wl.launches_per_step,
     }
     if not args.no_overlap:
