@@ -372,7 +372,9 @@ tl_status tl_reduce_scatter(const tl_reduce_scatter_args* args, void* stream);
  * link byte 8*w as {data (low 32 bits), epoch (high 32 bits)};
  * TL_LL_SEPARATE_FLAG -- the gathered matrix's bytes at the same offsets, then
  * chunk flag f (uint32) at byte R*M_shard*K*2 + 128*f.  Words of an earlier
- * epoch are never mistaken for this call's.  All CTAs of the launch must be
+ * epoch are never mistaken for this call's; the caller zero-fills the link
+ * buffer before its first use (its last epoch is then 0), since leftover bytes
+ * could read as a later epoch.  All CTAs of the launch must be
  * co-resident (receivers wait for senders of the same launch).
  */
 typedef enum { TL_LL_FLAG_IN_DATA = 0, TL_LL_SEPARATE_FLAG = 1 } tl_ll_protocol;
