@@ -83,7 +83,9 @@ __device__ __forceinline__ unsigned same_expert_lanes(unsigned am, int e) {
 }
 
 // Routing on a cluster of ROUTE_CTAS CTAs: CTA c owns the c-th contiguous range
-// of the P = T*k (token, slot) pairs, and its warps own consecutive sub-ranges.
+// of the P = T*k (token, slot) pairs, and its warps own consecutive sub-ranges
+// (the experts of a warp's first ROUTE_CACHE rounds of 32 pairs stay in registers
+// between the two passes over them).
 //  1. per-warp expert counts over the warp's pairs;
 //  2. (cluster barrier) every CTA reads every CTA's per-expert totals from
 //     distributed shared memory: expert offsets (exclusive scan), tile offsets
@@ -95,6 +97,17 @@ __device__ __forceinline__ unsigned same_expert_lanes(unsigned am, int e) {
 //     the masks and barrier ranges combined from every CTA's shared memory,
 //     the tile keys gathered in CTA 0's shared memory;
 //  4. (cluster barrier) CTA 0 ranks the tiles by (key, index): the consumer order.
+constexpr int ROUTE_CACHE = 4;
+
+__device__ __forceinline__ int warp_incl_scan(int v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  return v;
+}
+
 __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const RouteParams p) {
   extern __shared__ int32_t sm[];
   const int E = p.E;
@@ -102,7 +115,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   int32_t* ctot = cnt + ROUTE_WARPS * E;   // [E] this CTA's per-expert totals (read by the cluster)
   int32_t* s_off = ctot + E;               // [E+1] expert offsets
   int32_t* s_toff = s_off + (E + 1);       // [E+1] first tile of each expert
-  int32_t* s_key = s_toff + (E + 1);       // [max_tiles] tile keys (CTA 0)
+  int32_t* s_below = s_toff + (E + 1);     // [E] pairs of each expert in the lower CTAs of the cluster
+  int32_t* s_key = s_below + E;            // [max_tiles] tile keys (CTA 0)
   // per tile, over this CTA's pairs: source-rank mask, lowest and highest token barrier
   int32_t* s_mask = s_key + p.max_tiles;
   int32_t* s_blo = s_mask + p.max_tiles;
@@ -120,6 +134,13 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   int32_t* order = p.ws + ws_order(p.max_tiles);
   int32_t* inv = p.ws + ws_inv(p.max_tiles);
 
+  // the experts of the warp's first rounds, every load in flight together
+  int ecache[ROUTE_CACHE];
+#pragma unroll
+  for (int i = 0; i < ROUTE_CACHE; ++i) {
+    const int q = q0 + i * 32 + lane;
+    ecache[i] = q < q1 ? p.topk[q] : 0;
+  }
   for (int i = tid; i < ROUTE_WARPS * E; i += ROUTE_THREADS) cnt[i] = 0;
   for (int t = tid; t < p.max_tiles; t += ROUTE_THREADS) {
     s_mask[t] = 0;
@@ -128,10 +149,9 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   }
   __syncthreads();
   // 1. per-warp histograms over contiguous ranges of pairs
-  for (int base = q0; base < q1; base += 32) {
+  auto count = [&](int e, int base) {
     const int q = base + lane;
     const bool act = q < q1;
-    int e = act ? p.topk[q] : -1;
     if (act && (e < 0 || e >= E)) {
       record_error(p.status, TL_ERR_INVALID, uint32_t(q), uint32_t(e), uint32_t(E));
       e = min(max(e, 0), E - 1);
@@ -142,7 +162,12 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
       if (lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
     }
     __syncwarp();
-  }
+  };
+#pragma unroll
+  for (int i = 0; i < ROUTE_CACHE; ++i)
+    if (q0 + i * 32 < q1) count(ecache[i], q0 + i * 32);
+  for (int base = q0 + ROUTE_CACHE * 32; base < q1; base += 32)
+    count(base + lane < q1 ? p.topk[base + lane] : 0, base);
   __syncthreads();
   for (int e = tid; e < E; e += ROUTE_THREADS) {
     int c = 0;
@@ -150,8 +175,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
     ctot[e] = c;
   }
   cluster_sync();
-  // 2. expert totals and offsets from every CTA's totals, this CTA's bases
-  if (tid < 32) {
+  // 2. expert totals and offsets from every CTA's totals, then the tile offsets
+  if (warp == 0) {
     // one lane per expert (E <= 64 in two rounds): totals, then a warp scan for the offsets
     int carry = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
@@ -164,30 +189,26 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
           below += c < crank ? v : 0;
         }
       }
-      int incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
+      const int incl = warp_incl_scan(tot, lane);
       if (e < E) {
         s_off[e] = carry + incl - tot;
-        s_toff[e] = below;  // parked: the counts of lower CTAs
+        s_below[e] = below;
       }
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) s_off[E] = carry;
   }
   __syncthreads();
+  // the base of each warp per expert: the expert's offset, then the counts of the lower
+  // CTAs, then those of the lower warps of this CTA
   for (int e = tid; e < E; e += ROUTE_THREADS) {
-    int run = s_off[e] + s_toff[e];
+    int run = s_off[e] + s_below[e];
     for (int w = 0; w < ROUTE_WARPS; ++w) {
       const int c = cnt[w * E + e];
       cnt[w * E + e] = run;
       run += c;
     }
   }
-  __syncthreads();  // the parked counts are read; s_toff now takes the tile offsets
   // tiles per expert and their offsets (every CTA, from the same totals)
   if (tid == 0) {
     int acc = 0;
@@ -205,10 +226,10 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   __syncthreads();
   // stable scatter: pairs keep their (token, slot) order inside an expert; each pair also
   // marks its tile's source rank and token barrier range (this CTA's share of the table)
-  for (int base = q0; base < q1; base += 32) {
+  auto scatter = [&](int e_raw, int base) {
     const int q = base + lane;
     const bool act = q < q1;
-    const int e = act ? min(max(p.topk[q], 0), E - 1) : 0;
+    const int e = act ? min(max(e_raw, 0), E - 1) : 0;
     const unsigned am = __ballot_sync(0xffffffffu, act);
     if (act) {
       const unsigned peers = same_expert_lanes(am, e);
@@ -228,7 +249,12 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
       if (lane == __ffs(peers) - 1) cnt[warp * E + e] += __popc(peers);
     }
     __syncwarp();
-  }
+  };
+#pragma unroll
+  for (int i = 0; i < ROUTE_CACHE; ++i)
+    if (q0 + i * 32 < q1) scatter(ecache[i], q0 + i * 32);
+  for (int base = q0 + ROUTE_CACHE * 32; base < q1; base += 32)
+    scatter(base + lane < q1 ? p.topk[base + lane] : 0, base);
   if (crank == 0)
     for (int e = tid; e <= E; e += ROUTE_THREADS) p.offsets[e] = s_off[e];
   // every CTA's share of the per-tile masks and barrier ranges is complete
@@ -622,7 +648,7 @@ extern "C" tl_status tl_moe_ag_gemm(const tl_moe_args* a, void* stream) {
   rp.max_tiles = max_tiles;
   rp.pull = pull ? 1 : 0;
   rp.k_shift = (a->topk & (a->topk - 1)) == 0 ? __builtin_ctz(unsigned(a->topk)) : -1;
-  const size_t route_smem = (size_t(ROUTE_WARPS) * a->E + a->E + 2 * (a->E + 1) + 4 * size_t(max_tiles)) * sizeof(int32_t);
+  const size_t route_smem = (size_t(ROUTE_WARPS) * a->E + 2 * a->E + 2 * (a->E + 1) + 4 * size_t(max_tiles)) * sizeof(int32_t);
   if (route_smem > size_t(di.max_smem_optin))
     return fail(TL_ERR_UNSUPPORTED, "tl_moe_ag_gemm: routing needs %zu bytes of shared memory", route_smem);
   {
