@@ -18,10 +18,11 @@
 // its R partials P_r = H_r[rows of t] . W2_r[expert slice, cols of n] are items
 // tau*R + j, rank r = (tau + j) mod R, taken round-robin by the CTA pairs.
 // Per CTA: warp 0 TMA producer, warp 1 MMA issuer (leader), warps 2-5 pushers
-// (fp32 partial half-tile into a ring slot, then the arrival flag), warps 6-13
-// reducers (acquire the R arrival flags of their half, sum their row slice in
-// rank order into Y -- only rows of the tile's expert -- and release the
-// "reduced" flag that frees the slot).  The K loop runs over I_r; columns of
+// (the fp32 partial half-tile into a ring slot, then the arrival flag), warps
+// 6-13 reducers (acquire the R arrival flags of their half, sum their row slice
+// in rank order into Y, and release the "reduced" flag that frees the slot).
+// Both move only the rows of the tile's expert: the padding rows of an expert's
+// last tile are computed by the MMAs but neither pushed nor read.  The K loop runs over I_r; columns of
 // H_r past I_r read as zero, so a k-block that reaches into the next expert's
 // slice of W2_r adds nothing.
 // Option TL_RS_BF16_PARTIALS: every partial is rounded to bf16 (RNE) before it
@@ -157,11 +158,14 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
       // 2-byte bf16 values in half the bytes)
       const size_t slot_el = (size_t(i % p.ring_items) * 2 + h) * p.half_floats + my_base;
       const uint64_t stream = l2_policy_evict_first();  // partial lines: written once, read once
+      // a row past the tile's expert (the padding of its last tile) is neither pushed nor read
+      const bool row_used = h * pair::HM + row_in_half < it.rows;
       for (int c = 0; c < pair::BN / 32; ++c) {
         if (it.n * pair::BN + c * 32 >= p.Hd) break;
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
+        if (!row_used) continue;
         if (kBf16) {
           uint16_t* slot16 = reinterpret_cast<uint16_t*>(p.slots) + slot_el;
 #pragma unroll
@@ -200,7 +204,8 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
       }
       __syncwarp();
       const int s0 = it.j * p.slice_rows;
-      const int s_rows = max(0, min(p.slice_rows, pair::HM - s0));
+      // rows of the slice that belong to the tile's expert (the pushers skip the others)
+      const int s_rows = max(0, min(min(p.slice_rows, pair::HM - s0), it.rows - (h * pair::HM + s0)));
       const int n_cols = min(pair::BN, p.Hd - it.n * pair::BN);
       const int total = s_rows * (n_cols / 4);
       // rank r's partial was pushed by item tau*R + j(r), j(r) = (r - tau) mod R
@@ -274,10 +279,9 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
             }
           }
         }
-        // only rows of this tile's expert: the rows after them belong to the next tile
 #pragma unroll
         for (int u = 0; u < QU; ++u)
-          if (off[u] >= 0 && lrow[u] < it.rows)
+          if (off[u] >= 0)
             *reinterpret_cast<float4*>(p.Y + size_t(it.row0 + lrow[u]) * p.Hd + ocol[u]) = acc4[u];
       }
       // slice j of this half of tile tau is read: release its "reduced" flag (slot-free barrier)
