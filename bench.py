@@ -822,6 +822,22 @@ class AgAttn:
         v = self.torch.cat(self.V).permute(1, 0, 2).unsqueeze(0)
         return F.scaled_dot_product_attention(q, k, v, enable_gqa=True)
 
+    def torch_cudnn(self):
+        """torch: gather by concatenation, then the cuDNN fused attention (key/value heads
+        expanded to the query heads when the backend takes no grouped heads)."""
+        from torch.nn.attention import SDPBackend, sdpa_kernel
+        F = self.torch.nn.functional
+        q = self.Q.permute(1, 0, 2).unsqueeze(0)
+        k = self.torch.cat(self.K).permute(1, 0, 2).unsqueeze(0)
+        v = self.torch.cat(self.V).permute(1, 0, 2).unsqueeze(0)
+        with sdpa_kernel([SDPBackend.CUDNN_ATTENTION]):
+            try:
+                return F.scaled_dot_product_attention(q, k, v, enable_gqa=True)
+            except RuntimeError:
+                g = q.shape[1] // k.shape[1]
+                return F.scaled_dot_product_attention(q, k.repeat_interleave(g, dim=1),
+                                                      v.repeat_interleave(g, dim=1))
+
     def check_status(self):
         for s in (self.sig, self.sig_ag):
             code, where = self.B.tl_query_status(s)
@@ -918,6 +934,13 @@ def attn_extras(torch, B, peaks, peak_src):
                                  "speedup_of_fused": t_torch / out["full"]["us"]}
     except Exception as ex:  # a torch build without a fused attention for this device
         out["torch_cat_sdpa"] = {"unavailable": str(ex).splitlines()[0][:200]}
+    try:
+        t_cudnn = flushed_time_us(torch, a.torch_cudnn, flush, reps=3)
+        fl = attn_flops(c, False, 0)
+        out["torch_cat_cudnn_sdpa"] = {"us": t_cudnn, "tflops": fl / (t_cudnn * 1e-6) / 1e12,
+                                       "speedup_of_fused": t_cudnn / out["full"]["us"]}
+    except Exception as ex:  # no cuDNN attention for this device or build
+        out["torch_cat_cudnn_sdpa"] = {"unavailable": str(ex).splitlines()[0][:200]}
     # the copy runs inside the fused launch; alone it would add this much to a copy-then-attend schedule
     out["copy_frac_of_fused"] = t_copy / out["full"]["us"]
     del a, flush
