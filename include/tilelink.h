@@ -410,8 +410,8 @@ tl_status tl_allgather_ll(const tl_allgather_ll_args* args, void* stream);
  *   Y[i, :]            = sorted_tokens[i] . W_{expert of row i}   (fp32 accumulate, bf16)
  * Two stream-ordered launches: a routing kernel on a cluster of 8 CTAs
  * (histogram, scan, stable counting sort, tile table, tile order) and one
- * persistent kernel, launched early so that its prologue overlaps the routing
- * (programmatic dependent launch; it waits for the routing's tables), in
+ * persistent kernel launched with programmatic dependent launch (its launch is
+ * set up while the routing runs; it waits for the routing's tables), in
  * which copy warps move token rows into `sorted_tokens` while tcgen05 GEMM
  * tiles of 256 rows of one expert wait on the flags their lookup-table entry
  * names and multiply their sorted rows by their expert's weight.  The two data

@@ -9,21 +9,23 @@
 //    dependencies come from lookup tables built from the routing and passed
 //    to the kernel.
 //
-// Two stream-ordered launches, the second started early (programmatic dependent
-// launch: its prologue overlaps the first, and it waits for the first before it
-// reads the tables):
+// Two stream-ordered launches, the second with programmatic dependent launch (its
+// launch is set up while the first runs, and it waits for the first to finish
+// before it reads the tables):
 //  1. moe_route_kernel (a cluster of 8 CTAs): histogram of topk_ids over experts,
 //     exclusive scan, stable counting sort of the (token, slot) pairs by expert
 //     (perm and its inverse), then the tile table -- per 256-row tile its
 //     expert, first sorted row, rows, lowest and highest producer barrier and
 //     source-rank mask -- and the consumer tile order.
-//  2. moe_gemm_kernel (persistent CTA pairs, one CTA per SM): copy warps
-//     gather every token row of every shard and scatter it to its k sorted
-//     positions in `sorted_tokens` (bulk TMA, one flag per chunk of
-//     rows_per_barrier tokens, shards in the order self, self+1, ...); the TMA
-//     warps of each 256-row expert tile acquire the flags of its barrier range,
-//     then a tcgen05.mma.cta_group::2 grouped GEMM multiplies the tile's sorted
-//     rows by its expert's weight.
+//  2. moe_gemm_kernel (persistent CTA pairs, one CTA per SM): copy warps move
+//     the token rows into `sorted_tokens` with bulk TMA copies -- pull mode
+//     (default): chunks of rows_per_barrier sorted rows in sorted order, each row
+//     fetched from its token's shard, one flag per chunk; push mode: each
+//     shard's tokens, in the order self, self+1, ..., scattered to their k sorted
+//     positions, one flag per chunk of a shard's tokens.  The TMA warps of each
+//     256-row expert tile acquire the flags of its barrier range, then a
+//     tcgen05.mma.cta_group::2 grouped GEMM multiplies the tile's sorted rows by
+//     its expert's weight.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -123,7 +125,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS, 1) moe_route_kernel(const Route
   int32_t* s_bhi = s_blo + p.max_tiles;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t crank = cluster_ctarank();
-  // the grouped GEMM may start its prologue now; it waits for this kernel before reading the tables
+  // the grouped GEMM's launch may proceed now; it waits for this kernel before reading the tables
   pdl_launch_dependents();
   const int P = p.T * p.k;
   const int per_cta = ((P + ROUTE_CTAS - 1) / ROUTE_CTAS + 31) / 32 * 32;
@@ -359,8 +361,8 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
   const int32_t* order = p.ws + ws_order(p.max_tiles);
   const int32_t* inv = p.ws + ws_inv(p.max_tiles);
   const uint32_t tmem_base = pair::setup(bars, warp);
-  // launched early (programmatic dependent launch): the routing kernel's tables are complete
-  // and visible only after this
+  // programmatic dependent launch: the routing kernel's tables are complete and visible
+  // only after this
   pdl_wait_previous();
   const int num_work = p.ws[0] * p.Nt;
   volatile uint32_t* abort = &bars->abort;
