@@ -237,16 +237,26 @@ tl_status tl_ag_gemm(const tl_ag_gemm_args* args, void* stream);
  * GEMM that notifies each finished partial tile, and a reduce stage that waits
  * on its own and its peers' tiles).  One launch on pairs of CTAs
  * (cta_group::2, 256 x 256 tiles; CTA h of a pair owns rows h*128..h*128+127
- * of every tile): every fp32 partial half-tile is pushed into a receive slot of
- * `workspace` (a ring of three waves of slots, reused as the launch proceeds)
- * and its arrival flag released; output tiles run in destination order, m
- * tiles innermost, and the R partials of one output tile are produced back to
- * back, rank (d + 1 + tau + j) mod R at position j of output tile tau.
- * Reducer warps of the CTAs that computed them each reduce one row slice of
- * their half after acquiring its R arrival flags, adding the partials in rank
- * order 0..R-1 in fp32, write bf16 rows into out[d], and release a "reduced"
- * flag; a pusher reuses a ring slot only after the reduced flags of the tile
- * that used it before.
+ * of every tile); output tiles tau run in destination order, n tile by n tile
+ * with the m tiles innermost.  Two schedules, with the same result bits:
+ *  - chain (options 0): the partials are summed on the way, like the partial
+ *    sums of a ring reduce passing from rank to rank.  Partials are produced
+ *    rank by rank (all tiles' rank-0 partials, then all rank-1 partials, ...);
+ *    the pushers of rank r wait for rank r-1's arrival flag of the tile, add
+ *    their fp32 partial to the tile's running sum in `workspace` (one fp32
+ *    tile per output tile), and release their arrival and reduced flags; rank
+ *    R-1 writes bf16 of the sum into out[d].  Each rank's operands are then
+ *    read from memory about once.
+ *  - push and reduce (any other options): every partial half-tile is pushed
+ *    into a receive slot of `workspace` (a ring of three waves of slots,
+ *    reused as the launch proceeds) and its arrival flag released; the R
+ *    partials of one output tile are produced back to back, rank
+ *    (d + 1 + tau + j) mod R at position j of output tile tau.  Reducer warps
+ *    of the CTAs that computed them each reduce one row slice of their half
+ *    after acquiring its R arrival flags, adding the partials in rank order
+ *    (or ring order) in fp32, write bf16 rows into out[d], and release a
+ *    "reduced" flag; a pusher reuses a ring slot only after the reduced flags
+ *    of the tile that used it before.
  */
 /* GEMM-RS options (bits of tl_gemm_rs_args.options), closer to a real
  * ReduceScatter's traffic; the default (0) is fp32 partials summed in rank order. */
@@ -269,14 +279,17 @@ typedef struct tl_gemm_rs_args {
   uint64_t timeout_ns;         /* 0 = 1 s */
   int32_t* trace;              /* optional device int32 [tl_gemm_rs_num_flags(R, M, N) / 4]:
                                   trace[item] = ((d * m_tiles + m) * n_tiles + n) * R + r,
-                                  the output tile and rank of each produced partial,
-                                  m_tiles = ceil(M/R/256), n_tiles = ceil(N/256) */
+                                  the output tile and rank of each produced partial in
+                                  production order (the schedule's), m_tiles =
+                                  ceil(M/R/256), n_tiles = ceil(N/256) */
 } tl_gemm_rs_args;
 
-/* Workspace bytes for the current device: min(items, 3 * pairs) items of two
- * half-slots of R * ceil(128/R) * 256 floats, pairs = half the SM count.
- * A half-slot is laid out [slice][column/4][row in slice][4], one contiguous
- * block per reducer slice. */
+/* Workspace bytes for the current device: the larger of the chain schedule's
+ * running sums (tiles fp32 tiles, tiles = R * ceil(M/R/256) * ceil(N/256)) and
+ * the push schedule's ring, min(items, 3 * pairs) items of two half-slots of
+ * R * ceil(128/R) * 256 floats, pairs = half the SM count.  Both are laid out
+ * in half-tiles [slice][column/4][row in slice][4], one contiguous block per
+ * row slice. */
 size_t tl_gemm_rs_workspace_size(int R, int M, int N);
 /* Flags a GEMM-RS call needs: 4 * R * tiles (arrival and reduced flags for
  * both halves), tiles = R * ceil(M/R/256) * ceil(N/256). */
@@ -288,15 +301,16 @@ tl_status tl_gemm_rs(const tl_gemm_rs_args* args, void* stream);
  * callers that cannot allocate device memory -- a runtime whose allocator owns
  * the device and forbids cudaMalloc on its hot path, code that runs before any
  * allocator exists, or an embedding that may only pass the buffers it already
- * holds.  Same operation, arguments and kernel as tl_gemm_rs, except:
+ * holds.  Same operation and arguments as tl_gemm_rs, always with the push and
+ * reduce schedule (the same result bits as the chain schedule), except:
  *  - args->workspace, args->workspace_bytes and args->signals must be NULL/0.
  *    The flags, a status word and the fp32 receive slots live in one static
  *    device array of TL_GEMM_RS_NOALLOC_MAX_BYTES (64 MiB), which every GPU
  *    that loads the library holds until the process exits.
  *  - A problem that needs more scratch than that fails with
  *    TL_ERR_UNSUPPORTED and launches nothing.  It needs roundup256(256 + 4*F)
- *    bytes of flags plus tl_gemm_rs_workspace_size(R, M, N) bytes of slots,
- *    F = tl_gemm_rs_num_flags(R, M, N).
+ *    bytes of flags plus the ring of receive slots described under
+ *    tl_gemm_rs_workspace_size, F = tl_gemm_rs_num_flags(R, M, N).
  *  - dev_status: optional caller-owned device pointer to 4 uint32 words
  *    (16-byte aligned) where the kernel records its first device-side error
  *    (code, where, value seen, value expected); the caller zeroes it.  With

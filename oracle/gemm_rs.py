@@ -123,6 +123,18 @@ def output_tiles(R, M, N, BM, BN):
     return [(d, m, n) for d in range(R) for n in range(Nt) for m in range(Mt)]
 
 
+def chain_order(R, M, N, BM, BN):
+    """Production order of the chain accumulation: (tau, d, m, n, r).
+
+    The rank-ordered sum accumulated on the way, like the partial sums of a ring
+    reduce passing from rank to rank: every output tile's rank-0 partial, then
+    every tile's rank-1 partial, and so on, the tiles of each rank in the order
+    of output_tiles; the rank-r partial of a tile is added to the running sum
+    left by rank r-1."""
+    tiles = output_tiles(R, M, N, BM, BN)
+    return [(tau, d, m, n, r) for r in range(R) for tau, (d, m, n) in enumerate(tiles)]
+
+
 def item_order(R, M, N, BM, BN):
     """Production order of partial tiles: (tau, d, m, n, r).
 

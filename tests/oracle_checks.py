@@ -181,6 +181,23 @@ def check_rs_item_order(item_order):
     assert len({p % R for p in pos}) == R
 
 
+def check_rs_chain_order(chain_order):
+    fx = golden_json("rs_chain_order_small.json")
+    for c in fx["cases"]:
+        got = chain_order(c["R"], c["M"], c["N"], c["BM"], c["BN"])
+        assert [list(t) for t in got] == c["items"]
+    # properties: every (tile, rank) once; ranks never decrease; within a rank the tiles
+    # run in index order, and tile indices follow destination, then n, then m
+    R, M, N, BM, BN = 4, 2048, 512, 256, 256
+    items = chain_order(R, M, N, BM, BN)
+    ntiles = len(items) // R
+    assert sorted((t, r) for (t, _, _, _, r) in items) == [(t, r) for t in range(ntiles) for r in range(R)]
+    assert [r for (*_, r) in items] == sorted(r for (*_, r) in items)
+    assert [t for (t, *_) in items] == [t for _ in range(R) for t in range(ntiles)]
+    Mt, Nt = -(-(M // R) // BM), -(-N // BN)
+    assert all(t == (d * Nt + n) * Mt + m for (t, d, m, n, _) in items)
+
+
 # ------------------------------------------------------------------ MoE
 
 def check_moe_tile_order(tile_order, tile_sources):

@@ -42,9 +42,12 @@ def run_rs(B, A, Bl, *, timeout_ns=0, options=0):
     return dict(out=out, sig=sig, status=status, epoch=_epoch[0], nflags=nflags, items=nflags // 4, trace=trace)
 
 
-def expected_trace(R, M, N):
+def expected_trace(R, M, N, options=0):
+    """Production order: the chain accumulation for the default options (fp32 partials in
+    rank order), the push-and-reduce order for the others."""
     Mt, Nt = -(-(M // R) // 256), -(-N // 256)
-    return [((d * Mt + m) * Nt + n) * R + r for (_, d, m, n, r) in oracle.gemm_rs.item_order(R, M, N, 256, 256)]
+    order = oracle.gemm_rs.chain_order if options == 0 else oracle.gemm_rs.item_order
+    return [((d * Mt + m) * Nt + n) * R + r for (_, d, m, n, r) in order(R, M, N, 256, 256)]
 
 
 def check_flags(r):

@@ -315,3 +315,19 @@ def test_pins_catch_moe_down_sum_rounded_instead_of_partials():
             out = out + np.asarray(gates, np.float64)[:, s:s + 1] * Y[pos[np.arange(T) * k + s]]
         return [out[d * T_r:(d + 1) * T_r] for d in range(T // T_r)]
     _fails(C.check_moe_down_bf16, bad, M.moe_down_at)
+
+
+def test_pins_catch_tile_major_chain_order():
+    # the push schedule's order (a tile's ranks together) in place of rank by rank
+    def bad(R, Mm, N, BM, BN):
+        return [(t, d, m, n, r) for t, (d, m, n) in enumerate(G.output_tiles(R, Mm, N, BM, BN)) for r in range(R)]
+    _fails(C.check_rs_chain_order, bad)
+
+
+def test_pins_catch_chain_order_with_n_innermost_tiles():
+    def bad(R, Mm, N, BM, BN):
+        Md = Mm // R
+        Mt, Nt = -(-Md // BM), -(-N // BN)
+        tiles = [(d, m, n) for d in range(R) for m in range(Mt) for n in range(Nt)]
+        return [(t, d, m, n, r) for r in range(R) for t, (d, m, n) in enumerate(tiles)]
+    _fails(C.check_rs_chain_order, bad)

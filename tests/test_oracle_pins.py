@@ -103,6 +103,10 @@ def test_rs_item_order_pins():
     C.check_rs_item_order(oracle.gemm_rs.item_order)
 
 
+def test_rs_chain_order_pins():
+    C.check_rs_chain_order(oracle.gemm_rs.chain_order)
+
+
 def test_moe_routing_pins():
     M = oracle.moe
     C.check_moe_routing(M.route, M.tile_table, M.tile_sources)

@@ -40,6 +40,21 @@
 // tensor pipe is not stalled by the reduction.  Flags: [0, 2*items) arrival
 // flags indexed 2*(tau*R + r) + h; [2*items, 4*items) reduced flags indexed
 // 2*(tau*R + j) + h.
+//
+// Chain schedule (the default: fp32 partials summed in rank order).  The same
+// sum, accumulated on the way instead of at the destination, like the partial
+// sums of a ring reduce travelling from rank to rank: items run rank by rank
+// (item i = r * tiles + tau: every tile's rank-0 partial, then every tile's
+// rank-1 partial, ...), and the pushers of (tau, r) wait for rank r-1's arrival
+// flag of the tile (peer_tile_wait), add their partial to the tile's fp32
+// running sum S_tau = ((P_0 + P_1) + ...) + P_r in the workspace and release
+// their own flag; rank R-1 writes bf16(S_tau) to out[d] instead.  Each rank's
+// A_r and B_r are then read from DRAM about once (the push-and-reduce schedule
+// re-reads B for every destination) and no partial is read back from a ring
+// slot; S_tau costs one fp32 read and write per rank.  The results are the
+// same bits as the push-and-reduce schedule's.  Deadlock freedom: (tau, r)
+// waits only on (tau, r-1), an item with a lower index, and every pair takes
+// its items in increasing index order.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -81,21 +96,30 @@ struct Item {
   int tau, d, mt, nt, r, j;
 };
 
+template <bool kChain>
 __device__ __forceinline__ Item item_of(const RsParams& p, int i) {
   Item it;
-  it.tau = i / p.R;
-  it.j = i % p.R;
+  if (kChain) {
+    // rank by rank; j = r names the item's flags
+    it.r = i / p.num_tiles;
+    it.tau = i - it.r * p.num_tiles;
+    it.j = it.r;
+  } else {
+    it.tau = i / p.R;
+    it.j = i % p.R;
+  }
   const int per_d = p.Mt_d * p.Nt;
   it.d = it.tau / per_d;
   const int rem = it.tau % per_d;
   it.mt = rem % p.Mt_d;
   it.nt = rem / p.Mt_d;
-  it.r = (it.d + 1 + it.tau + it.j) % p.R;
+  if (!kChain) it.r = (it.d + 1 + it.tau + it.j) % p.R;
   return it;
 }
 
-// kBf16: partials travel as bf16 (TL_RS_BF16_PARTIALS); one instantiation per partial type.
-template <bool kBf16>
+// kBf16: partials travel as bf16 (TL_RS_BF16_PARTIALS); kChain: the chain schedule
+// (fp32, rank order only).
+template <bool kBf16, bool kChain>
 __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_constant__ RsParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -119,7 +143,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       // destination's n tiles and B columns across its m tiles
       const uint64_t keep = l2_policy_evict_last();
       for (int i = pair_id; i < p.num_items && !*abort; i += npairs) {
-        const Item it = item_of(p, i);
+        const Item it = item_of<kChain>(p, i);
         if (p.trace && rank == 0) p.trace[i] = ((it.d * p.Mt_d + it.mt) * p.Nt + it.nt) * p.R + it.r;
         const int row0 = it.d * p.Md + it.mt * pair::BM + h * pair::HM;
         for (int kb = 0; kb < p.KB; ++kb)
@@ -135,7 +159,80 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
     if (lane == 0 && rank == 0)
       pair::mma_loop(smem, bars, tmem_base, my_items, p.KB, abort, p.status, p.pipe_timeout_ns);
     __syncwarp();
-  } else if (warp < kWarpRed0) {
+  } else if (kChain && warp < kWarpRed0) {
+    // ---------------------------------------------------------------- pushers: chain accumulation
+    const int wq = warp & 3;
+    const int et = (warp - kWarpEpi0) * 32 + lane;  // 0..127 among pusher threads
+    const int row_in_half = wq * 32 + lane;
+    // S_tau in the half-slot layout [slice][col/4][row in slice][4] of the push schedule
+    const int my_slice = row_in_half / p.slice_rows, my_row = row_in_half % p.slice_rows;
+    const size_t my_base = (size_t(my_slice) * 64 * p.slice_rows + my_row) * 4;
+    int jj = 0;
+    for (int i = pair_id; i < p.num_items; i += npairs, ++jj) {
+      const Item it = item_of<true>(p, i);
+      const int acc = jj & 1;
+      const uint32_t acc_ph = uint32_t(jj >> 1) & 1u;
+      // peer_tile_wait: rank r-1's partial is in S_tau (it ran a whole pass of tiles earlier)
+      if (it.r > 0 && lane == 0) {
+        const int f = 2 * (it.tau * p.R + it.r - 1) + h;
+        wait_flag(arrived + f, p.epoch, p.status, p.timeout_ns, uint32_t(f), TL_ERR_TIMEOUT);
+      }
+      __syncwarp();
+      const bool ok = mbar_wait(&bars->tmem_full[acc], acc_ph, abort, p.status, p.pipe_timeout_ns, 4);
+      if (!named_bar_and(1, kNumEpiThreads, ok)) break;
+      tc_fence_after();
+      float* S = p.slots + (size_t(it.tau) * 2 + h) * p.half_floats + my_base;
+      const bool first = it.r == 0, last = it.r == p.R - 1;
+      const int orow = it.mt * pair::BM + h * pair::HM + row_in_half;  // row of out[d]
+      uint16_t* orowp = p.out[it.d] + size_t(orow) * p.N;
+      const uint64_t keep = l2_policy_evict_last();  // S_tau is read again by the next rank
+      for (int c = 0; c < pair::BN / 32; ++c) {
+        const int col0 = it.nt * pair::BN + c * 32;
+        if (col0 >= p.N) break;
+        uint32_t v[32];
+        tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
+        tmem_ld_wait();
+        float* f = reinterpret_cast<float*>(v);
+        float* sc = S + size_t(c * 8) * p.slice_rows * 4;
+        if (!first) {
+          // ((P_0 + P_1) + ...) + P_r in fp32, one rounding per rank
+          float4 sv[8];
+#pragma unroll
+          for (int g = 0; g < 8; ++g) sv[g] = ld_global_cg_v4f_hint(sc + size_t(g) * p.slice_rows * 4, keep);
+#pragma unroll
+          for (int g = 0; g < 8; ++g) {
+            f[g * 4 + 0] = __fadd_rn(sv[g].x, f[g * 4 + 0]);
+            f[g * 4 + 1] = __fadd_rn(sv[g].y, f[g * 4 + 1]);
+            f[g * 4 + 2] = __fadd_rn(sv[g].z, f[g * 4 + 2]);
+            f[g * 4 + 3] = __fadd_rn(sv[g].w, f[g * 4 + 3]);
+          }
+        }
+        if (!last) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            st_global_cg_v4f_hint(sc + size_t(g) * p.slice_rows * 4, f[g * 4], f[g * 4 + 1], f[g * 4 + 2],
+                                  f[g * 4 + 3], keep);
+        } else if (orow < p.Md) {
+          // the destination's row shard: bf16 of the complete sum
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+            if (col0 + g * 8 < p.N)
+              st_global_v4(orowp + col0 + g * 8, pack_bf16x2(f[g * 8], f[g * 8 + 1]),
+                           pack_bf16x2(f[g * 8 + 2], f[g * 8 + 3]), pack_bf16x2(f[g * 8 + 4], f[g * 8 + 5]),
+                           pack_bf16x2(f[g * 8 + 6], f[g * 8 + 7]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) pair::release_accumulator(bars, acc, rank);
+      // produce_tile_notify: every pusher thread's writes are ordered before thread 0's release
+      named_bar_sync(1, kNumEpiThreads);
+      if (et == 0) {
+        st_release(arrived + 2 * (it.tau * p.R + it.r) + h, p.epoch);
+        st_release(reduced + 2 * (it.tau * p.R + it.r) + h, p.epoch);
+      }
+    }
+  } else if (!kChain && warp < kWarpRed0) {
     // ---------------------------------------------------------------- pushers
     const int wq = warp & 3;                         // TMEM lane quarter of this warp
     const int et = (warp - kWarpEpi0) * 32 + lane;  // 0..127 among pusher threads
@@ -146,7 +243,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
     const size_t my_base = (size_t(my_slice) * 64 * p.slice_rows + my_row) * 4;
     int jj = 0;
     for (int i = pair_id; i < p.num_items; i += npairs, ++jj) {
-      const Item it = item_of(p, i);
+      const Item it = item_of<false>(p, i);
       const int acc = jj & 1;
       const uint32_t acc_ph = uint32_t(jj >> 1) & 1u;
       // slot free: the R reducers of this half of the tile that last used the slot are done with it
@@ -196,11 +293,11 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       named_bar_sync(1, kNumEpiThreads);
       if (et == 0) st_release(arrived + 2 * (it.tau * p.R + it.r) + h, p.epoch);
     }
-  } else {
+  } else if (!kChain) {
     // ---------------------------------------------------------------- reducers (this CTA's half)
     const int et = (warp - kWarpRed0) * 32 + lane;  // 0..127 among reducer threads
     for (int i = pair_id; i < p.num_items; i += npairs) {
-      const Item it = item_of(p, i);
+      const Item it = item_of<false>(p, i);
       // consume_tile_wait / peer_tile_wait: all R partials of this half have arrived
       if (lane == 0) {
         for (int r = 0; r < p.R; ++r) {
@@ -355,9 +452,13 @@ tl_status rs_check(const tl_gemm_rs_args* a, const char* who) {
   return TL_OK;
 }
 
-// Fill the kernel parameters and launch.
+// bytes of the chain schedule's running sums: one fp32 tile per output tile
+size_t rs_chain_bytes(int R, int M, int N) { return size_t(rs_num_tiles(R, M, N)) * 2 * rs_half_floats(R) * sizeof(float); }
+
+// Fill the kernel parameters and launch.  chain: the chain schedule is allowed (the
+// workspace holds rs_chain_bytes); it runs for the default options.
 tl_status rs_launch(RsParams* p, const tl_gemm_rs_args* a, float* slots, uint32_t* flags, uint32_t* status,
-                    int sm_count, cudaStream_t st) {
+                    int sm_count, cudaStream_t st, bool chain) {
   for (int r = 0; r < a->R; ++r) {
     if (tl_status s = make_map_bf16(&p->map_a[r], a->A[r], a->M, a->K_r, size_t(a->K_r) * 2, pair::HM, pair::BK))
       return s;
@@ -387,8 +488,9 @@ tl_status rs_launch(RsParams* p, const tl_gemm_rs_args* a, float* slots, uint32_
   const int pairs = rs_pairs(p->num_items, sm_count);
   p->ring_items = rs_ring_items(p->num_items, pairs);
   void* args[] = {p};
-  const void* kernel = (a->options & TL_RS_BF16_PARTIALS) ? reinterpret_cast<const void*>(&gemm_rs_kernel<true>)
-                                                           : reinterpret_cast<const void*>(&gemm_rs_kernel<false>);
+  const void* kernel = (a->options & TL_RS_BF16_PARTIALS) ? reinterpret_cast<const void*>(&gemm_rs_kernel<true, false>)
+                       : (chain && a->options == 0)       ? reinterpret_cast<const void*>(&gemm_rs_kernel<false, true>)
+                                                          : reinterpret_cast<const void*>(&gemm_rs_kernel<false, false>);
   return launch_coop(kernel, 2 * pairs, RS_THREADS, RS_SMEM_BYTES, st, args, 2);
 }
 
@@ -401,7 +503,7 @@ extern "C" size_t tl_gemm_rs_workspace_size(int R, int M, int N) {
   const int sms = tl::current_sm_count();
   // without a usable device, size for every item (always enough)
   const int ring = sms >= 2 ? tl::rs_ring_items(items, tl::rs_pairs(items, sms)) : items;
-  return tl::rs_slots_bytes(ring, R);
+  return std::max(tl::rs_slots_bytes(ring, R), tl::rs_chain_bytes(R, M, N));
 }
 
 extern "C" int tl_gemm_rs_num_flags(int R, int M, int N) {
@@ -427,7 +529,7 @@ extern "C" tl_status tl_gemm_rs(const tl_gemm_rs_args* a, void* stream) {
   if (!p) return fail(TL_ERR_INTERNAL, "out of host memory");
   std::memset(p, 0, sizeof(RsParams));
   const tl_status st = rs_launch(p, a, static_cast<float*>(a->workspace), a->signals->flags, a->signals->status,
-                                 di.sm_count, (cudaStream_t)stream);
+                                 di.sm_count, (cudaStream_t)stream, true);
   delete p;
   return st;
 }
@@ -504,7 +606,8 @@ extern "C" tl_status tl_gemm_rs_noalloc(const tl_gemm_rs_args* a, uint32_t* dev_
     return s;
   RsParams p;  // on the stack: no heap allocation on this path
   std::memset(&p, 0, sizeof(RsParams));
-  return rs_launch(&p, a, slots, flags, dev_status ? dev_status : status, di.sm_count, st);
+  // the fixed scratch holds a ring of receive slots: the push-and-reduce schedule (the same bits)
+  return rs_launch(&p, a, slots, flags, dev_status ? dev_status : status, di.sm_count, st, false);
 }
 
 namespace {
