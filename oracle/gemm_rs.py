@@ -123,16 +123,25 @@ def output_tiles(R, M, N, BM, BN):
     return [(d, m, n) for d in range(R) for n in range(Nt) for m in range(Mt)]
 
 
-def chain_order(R, M, N, BM, BN):
+CHAIN_GROUP = 2  # destinations whose tiles form one group of the chain order
+
+
+def chain_order(R, M, N, BM, BN, group=CHAIN_GROUP):
     """Production order of the chain accumulation: (tau, d, m, n, r).
 
     The rank-ordered sum accumulated on the way, like the partial sums of a ring
-    reduce passing from rank to rank: every output tile's rank-0 partial, then
-    every tile's rank-1 partial, and so on, the tiles of each rank in the order
-    of output_tiles; the rank-r partial of a tile is added to the running sum
-    left by rank r-1."""
+    reduce passing from rank to rank.  The destinations are taken in groups of
+    `group` (the last group may be smaller); within a group, every tile's
+    rank-0 partial, then every tile's rank-1 partial, and so on, the tiles in
+    the order of output_tiles.  The rank-r partial of a tile is added to the
+    running sum left by rank r-1."""
     tiles = output_tiles(R, M, N, BM, BN)
-    return [(tau, d, m, n, r) for r in range(R) for tau, (d, m, n) in enumerate(tiles)]
+    items = []
+    for g0 in range(0, R, group):
+        members = [(tau, t) for tau, t in enumerate(tiles) if g0 <= t[0] < g0 + group]
+        for r in range(R):
+            items += [(tau, d, m, n, r) for tau, (d, m, n) in members]
+    return items
 
 
 def item_order(R, M, N, BM, BN):

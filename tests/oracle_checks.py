@@ -186,14 +186,19 @@ def check_rs_chain_order(chain_order):
     for c in fx["cases"]:
         got = chain_order(c["R"], c["M"], c["N"], c["BM"], c["BN"])
         assert [list(t) for t in got] == c["items"]
-    # properties: every (tile, rank) once; ranks never decrease; within a rank the tiles
-    # run in index order, and tile indices follow destination, then n, then m
-    R, M, N, BM, BN = 4, 2048, 512, 256, 256
+    # properties: every (tile, rank) once; destination groups of two in order, within a
+    # group ranks never decrease and the group's tiles run in index order at every
+    # rank; tile indices follow destination, then n, then m
+    R, M, N, BM, BN = 5, 2560, 512, 256, 256
     items = chain_order(R, M, N, BM, BN)
     ntiles = len(items) // R
     assert sorted((t, r) for (t, _, _, _, r) in items) == [(t, r) for t in range(ntiles) for r in range(R)]
-    assert [r for (*_, r) in items] == sorted(r for (*_, r) in items)
-    assert [t for (t, *_) in items] == [t for _ in range(R) for t in range(ntiles)]
+    groups = [d // 2 for (_, d, _, _, _) in items]
+    assert groups == sorted(groups)
+    for g in set(groups):
+        sub = [(t, r) for (t, d, _, _, r) in items if d // 2 == g]
+        tiles = sorted({t for t, _ in sub})
+        assert sub == [(t, r) for r in range(R) for t in tiles]
     Mt, Nt = -(-(M // R) // BM), -(-N // BN)
     assert all(t == (d * Nt + n) * Mt + m for (t, d, m, n, _) in items)
 

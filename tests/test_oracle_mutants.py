@@ -331,3 +331,9 @@ def test_pins_catch_chain_order_with_n_innermost_tiles():
         tiles = [(d, m, n) for d in range(R) for m in range(Mt) for n in range(Nt)]
         return [(t, d, m, n, r) for r in range(R) for t, (d, m, n) in enumerate(tiles)]
     _fails(C.check_rs_chain_order, bad)
+
+
+def test_pins_catch_chain_order_without_destination_groups():
+    def bad(R, Mm, N, BM, BN):
+        return G.chain_order(R, Mm, N, BM, BN, group=R)
+    _fails(C.check_rs_chain_order, bad)

@@ -43,18 +43,20 @@
 //
 // Chain schedule (the default: fp32 partials summed in rank order).  The same
 // sum, accumulated on the way instead of at the destination, like the partial
-// sums of a ring reduce travelling from rank to rank: items run rank by rank
-// (item i = r * tiles + tau: every tile's rank-0 partial, then every tile's
-// rank-1 partial, ...), and the pushers of (tau, r) wait for rank r-1's arrival
-// flag of the tile (peer_tile_wait), add their partial to the tile's fp32
-// running sum S_tau = ((P_0 + P_1) + ...) + P_r in the workspace and release
-// their own flag; rank R-1 writes bf16(S_tau) to out[d] instead.  Each rank's
-// A_r and B_r are then read from DRAM about once (the push-and-reduce schedule
-// re-reads B for every destination) and no partial is read back from a ring
-// slot; S_tau costs one fp32 read and write per rank.  The results are the
-// same bits as the push-and-reduce schedule's.  Deadlock freedom: (tau, r)
-// waits only on (tau, r-1), an item with a lower index, and every pair takes
-// its items in increasing index order.
+// sums of a ring reduce travelling from rank to rank: the destinations are
+// taken in groups of kChainGroup, and within a group items run rank by rank
+// (every tile's rank-0 partial, then every tile's rank-1 partial, ...).  The
+// pushers of (tau, r) wait for rank r-1's arrival flag of the tile
+// (peer_tile_wait), add their partial to the tile's fp32 running sum
+// S_tau = ((P_0 + P_1) + ...) + P_r in the workspace (the next chunk's sums
+// loaded while the current one is added) and release their own flags; rank
+// R-1 writes bf16(S_tau) to out[d] instead.  A group's running sums (17 MB per
+// destination at 1024 x 4096) stay in L2 from rank to rank, each rank's B_r is
+// read once per group and A_r about once, and no partial is read back from a
+// ring slot.  The results are the same bits as the push-and-reduce
+// schedule's.  Deadlock freedom: (tau, r) waits only on (tau, r-1), an item
+// with a lower index, and every pair takes its items in increasing index
+// order.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
@@ -75,6 +77,8 @@ constexpr uint32_t RS_SMEM_BARS = pair::SMEM_END;
 constexpr uint32_t RS_SMEM_BYTES = RS_SMEM_BARS + sizeof(pair::Bars) + 1024;
 constexpr int RB = 8;                             // ranks loaded per batch in the reduce
 constexpr int QU = 2;                             // float4 elements per thread per round in the reduce
+// chain schedule: destinations whose running sums stay in L2 while their R ranks pass
+constexpr int kChainGroup = 2;
 
 struct RsParams {
   CUtensorMap map_a[RS_MAX_RANKS];  // A_r [M, K_r], box 128 rows
@@ -100,9 +104,13 @@ template <bool kChain>
 __device__ __forceinline__ Item item_of(const RsParams& p, int i) {
   Item it;
   if (kChain) {
-    // rank by rank; j = r names the item's flags
-    it.r = i / p.num_tiles;
-    it.tau = i - it.r * p.num_tiles;
+    // groups of kChainGroup destinations; within a group rank by rank, the group's
+    // tiles in order; j = r names the item's flags
+    const int tpg = min(p.num_tiles, kChainGroup * p.Mt_d * p.Nt);
+    const int g = i / (p.R * tpg), rem = i - g * (p.R * tpg);
+    const int gt = min(tpg, p.num_tiles - g * tpg);  // tiles of this (perhaps last, smaller) group
+    it.r = rem / gt;
+    it.tau = g * tpg + (rem - it.r * gt);
     it.j = it.r;
   } else {
     it.tau = i / p.R;
@@ -186,9 +194,22 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       const int orow = it.mt * pair::BM + h * pair::HM + row_in_half;  // row of out[d]
       uint16_t* orowp = p.out[it.d] + size_t(orow) * p.N;
       const uint64_t keep = l2_policy_evict_last();  // S_tau is read again by the next rank
-      for (int c = 0; c < pair::BN / 32; ++c) {
+      const int nch = min(pair::BN / 32, (p.N - it.nt * pair::BN + 31) / 32);
+      float4 sn[8];  // the next chunk's running sums, loaded one chunk ahead
+      if (!first) {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) sn[g] = ld_global_cg_v4f_hint(S + size_t(g) * p.slice_rows * 4, keep);
+      }
+      for (int c = 0; c < nch; ++c) {
         const int col0 = it.nt * pair::BN + c * 32;
-        if (col0 >= p.N) break;
+        float4 sv[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) sv[g] = sn[g];
+        if (!first && c + 1 < nch) {
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            sn[g] = ld_global_cg_v4f_hint(S + size_t((c + 1) * 8 + g) * p.slice_rows * 4, keep);
+        }
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
@@ -196,9 +217,6 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
         float* sc = S + size_t(c * 8) * p.slice_rows * 4;
         if (!first) {
           // ((P_0 + P_1) + ...) + P_r in fp32, one rounding per rank
-          float4 sv[8];
-#pragma unroll
-          for (int g = 0; g < 8; ++g) sv[g] = ld_global_cg_v4f_hint(sc + size_t(g) * p.slice_rows * 4, keep);
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
             f[g * 4 + 0] = __fadd_rn(sv[g].x, f[g * 4 + 0]);
