@@ -239,15 +239,18 @@ tl_status tl_ag_gemm(const tl_ag_gemm_args* args, void* stream);
  * (cta_group::2, 256 x 256 tiles; CTA h of a pair owns rows h*128..h*128+127
  * of every tile); output tiles tau run in destination order, n tile by n tile
  * with the m tiles innermost.  Two schedules, with the same result bits:
- *  - chain (options 0): the partials are summed on the way, like the partial
- *    sums of a ring reduce passing from rank to rank.  Partials are produced
- *    rank by rank (all tiles' rank-0 partials, then all rank-1 partials, ...);
- *    the pushers of rank r wait for rank r-1's arrival flag of the tile, add
- *    their fp32 partial to the tile's running sum in `workspace` (one fp32
- *    tile per output tile), and release their arrival and reduced flags; rank
- *    R-1 writes bf16 of the sum into out[d].  Each rank's operands are then
- *    read from memory about once.
- *  - push and reduce (any other options): every partial half-tile is pushed
+ *  - chain (tl_gemm_rs): the partials are summed on the way, like the partial
+ *    sums of a ring reduce passing from rank to rank.  Destinations are taken
+ *    in groups of two; within a group, pass j produces every tile's partial of
+ *    the j-th rank of the summation order (rank j, or rank d+1+j mod R with
+ *    TL_RS_RING_ORDER); the pushers of pass j wait for pass j-1's arrival flag
+ *    of the tile, add their fp32 partial (rounded to bf16 first with
+ *    TL_RS_BF16_PARTIALS) to the tile's running sum in `workspace` (one fp32
+ *    tile per output tile), and release the arrival and reduced flags of
+ *    (tile, j); pass R-1 writes bf16 of the sum into out[d].  A group's sums
+ *    stay in L2 from pass to pass and each rank's operands are read from
+ *    memory about once per group.
+ *  - push and reduce (tl_gemm_rs_noalloc): every partial half-tile is pushed
  *    into a receive slot of `workspace` (a ring of three waves of slots,
  *    reused as the launch proceeds) and its arrival flag released; the R
  *    partials of one output tile are produced back to back, rank

@@ -126,21 +126,22 @@ def output_tiles(R, M, N, BM, BN):
 CHAIN_GROUP = 2  # destinations whose tiles form one group of the chain order
 
 
-def chain_order(R, M, N, BM, BN, group=CHAIN_GROUP):
+def chain_order(R, M, N, BM, BN, group=CHAIN_GROUP, order="rank"):
     """Production order of the chain accumulation: (tau, d, m, n, r).
 
-    The rank-ordered sum accumulated on the way, like the partial sums of a ring
+    The ordered sum accumulated on the way, like the partial sums of a ring
     reduce passing from rank to rank.  The destinations are taken in groups of
-    `group` (the last group may be smaller); within a group, every tile's
-    rank-0 partial, then every tile's rank-1 partial, and so on, the tiles in
-    the order of output_tiles.  The rank-r partial of a tile is added to the
-    running sum left by rank r-1."""
+    `group` (the last group may be smaller); within a group, pass j adds every
+    tile's partial of the j-th rank of its summation order (rank j, or rank
+    d+1+j mod R in ring order; see summation_order), the tiles in the order of
+    output_tiles, so that a tile's pass-j partial joins the running sum left by
+    pass j-1."""
     tiles = output_tiles(R, M, N, BM, BN)
     items = []
     for g0 in range(0, R, group):
         members = [(tau, t) for tau, t in enumerate(tiles) if g0 <= t[0] < g0 + group]
-        for r in range(R):
-            items += [(tau, d, m, n, r) for tau, (d, m, n) in members]
+        for j in range(R):
+            items += [(tau, d, m, n, summation_order(R, d, order)[j]) for tau, (d, m, n) in members]
     return items
 
 

@@ -186,6 +186,9 @@ def check_rs_chain_order(chain_order):
     for c in fx["cases"]:
         got = chain_order(c["R"], c["M"], c["N"], c["BM"], c["BN"])
         assert [list(t) for t in got] == c["items"]
+    for c in fx["ring_cases"]:
+        got = chain_order(c["R"], c["M"], c["N"], c["BM"], c["BN"], order="ring")
+        assert [list(t) for t in got] == c["items"]
     # properties: every (tile, rank) once; destination groups of two in order, within a
     # group ranks never decrease and the group's tiles run in index order at every
     # rank; tile indices follow destination, then n, then m

@@ -43,11 +43,11 @@ def run_rs(B, A, Bl, *, timeout_ns=0, options=0):
 
 
 def expected_trace(R, M, N, options=0):
-    """Production order: the chain accumulation for the default options (fp32 partials in
-    rank order), the push-and-reduce order for the others."""
+    """Production order of tl_gemm_rs: the chain accumulation, in rank or ring order."""
     Mt, Nt = -(-(M // R) // 256), -(-N // 256)
-    order = oracle.gemm_rs.chain_order if options == 0 else oracle.gemm_rs.item_order
-    return [((d * Mt + m) * Nt + n) * R + r for (_, d, m, n, r) in order(R, M, N, 256, 256)]
+    order = "ring" if options & 2 else "rank"
+    items = oracle.gemm_rs.chain_order(R, M, N, 256, 256, order=order)
+    return [((d * Mt + m) * Nt + n) * R + r for (_, d, m, n, r) in items]
 
 
 def check_flags(r):

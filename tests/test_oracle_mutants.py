@@ -337,3 +337,13 @@ def test_pins_catch_chain_order_without_destination_groups():
     def bad(R, Mm, N, BM, BN):
         return G.chain_order(R, Mm, N, BM, BN, group=R)
     _fails(C.check_rs_chain_order, bad)
+
+
+def test_pins_catch_chain_ring_order_from_rank_zero():
+    # ring order started at rank d instead of d + 1
+    def bad(R, Mm, N, BM, BN, group=G.CHAIN_GROUP, order="rank"):
+        items = G.chain_order(R, Mm, N, BM, BN, group=group)
+        if order == "ring":
+            items = [(t, d, m, n, (d + r) % R) for (t, d, m, n, r) in items]
+        return items
+    _fails(C.check_rs_chain_order, bad)

@@ -41,16 +41,18 @@
 // flags indexed 2*(tau*R + r) + h; [2*items, 4*items) reduced flags indexed
 // 2*(tau*R + j) + h.
 //
-// Chain schedule (the default: fp32 partials summed in rank order).  The same
-// sum, accumulated on the way instead of at the destination, like the partial
-// sums of a ring reduce travelling from rank to rank: the destinations are
-// taken in groups of kChainGroup, and within a group items run rank by rank
-// (every tile's rank-0 partial, then every tile's rank-1 partial, ...).  The
-// pushers of (tau, r) wait for rank r-1's arrival flag of the tile
-// (peer_tile_wait), add their partial to the tile's fp32 running sum
-// S_tau = ((P_0 + P_1) + ...) + P_r in the workspace (the next chunk's sums
-// loaded while the current one is added) and release their own flags; rank
-// R-1 writes bf16(S_tau) to out[d] instead.  A group's running sums (17 MB per
+// Chain schedule (tl_gemm_rs, every option).  The same sum, accumulated on the
+// way instead of at the destination, like the partial sums of a ring reduce
+// travelling from rank to rank: the destinations are taken in groups of
+// kChainGroup, and within a group items run pass by pass (pass j: every tile's
+// partial of the j-th rank of the summation order -- rank j, or rank d+1+j mod
+// R in ring order).  The pushers of (tau, j) wait for pass j-1's arrival flag
+// of the tile (peer_tile_wait), add their partial (rounded to bf16 first with
+// bf16 partials) to the tile's fp32 running sum S_tau in the workspace (the
+// next chunk's sums loaded while the current one is added) and release the
+// flags of (tau, j); pass R-1 writes bf16(S_tau) to out[d] instead.  The
+// push-and-reduce schedule above runs for the no-allocation entry point, whose
+// fixed scratch holds a ring of slots but not a running sum per tile.  A group's running sums (17 MB per
 // destination at 1024 x 4096) stay in L2 from rank to rank, each rank's B_r is
 // read once per group and A_r about once, and no partial is read back from a
 // ring slot.  The results are the same bits as the push-and-reduce
@@ -109,9 +111,8 @@ __device__ __forceinline__ Item item_of(const RsParams& p, int i) {
     const int tpg = min(p.num_tiles, kChainGroup * p.Mt_d * p.Nt);
     const int g = i / (p.R * tpg), rem = i - g * (p.R * tpg);
     const int gt = min(tpg, p.num_tiles - g * tpg);  // tiles of this (perhaps last, smaller) group
-    it.r = rem / gt;
-    it.tau = g * tpg + (rem - it.r * gt);
-    it.j = it.r;
+    it.j = rem / gt;                                 // the pass: position in the summation order
+    it.tau = g * tpg + (rem - it.j * gt);
   } else {
     it.tau = i / p.R;
     it.j = i % p.R;
@@ -122,11 +123,13 @@ __device__ __forceinline__ Item item_of(const RsParams& p, int i) {
   it.mt = rem % p.Mt_d;
   it.nt = rem / p.Mt_d;
   if (!kChain) it.r = (it.d + 1 + it.tau + it.j) % p.R;
+  // chain: pass j adds rank j, or rank d+1+j (mod R) in ring order
+  else it.r = p.ring_order ? (it.d + 1 + it.j) % p.R : it.j;
   return it;
 }
 
-// kBf16: partials travel as bf16 (TL_RS_BF16_PARTIALS); kChain: the chain schedule
-// (fp32, rank order only).
+// kBf16: partials rounded to bf16 (TL_RS_BF16_PARTIALS); kChain: the chain schedule
+// (every option), else push and reduce (the no-allocation entry point).
 template <bool kBf16, bool kChain>
 __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_constant__ RsParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -180,9 +183,10 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       const Item it = item_of<true>(p, i);
       const int acc = jj & 1;
       const uint32_t acc_ph = uint32_t(jj >> 1) & 1u;
-      // peer_tile_wait: rank r-1's partial is in S_tau (it ran a whole pass of tiles earlier)
-      if (it.r > 0 && lane == 0) {
-        const int f = 2 * (it.tau * p.R + it.r - 1) + h;
+      // peer_tile_wait: the previous pass's partial is in S_tau (it ran a whole pass of the
+      // group's tiles earlier)
+      if (it.j > 0 && lane == 0) {
+        const int f = 2 * (it.tau * p.R + it.j - 1) + h;
         wait_flag(arrived + f, p.epoch, p.status, p.timeout_ns, uint32_t(f), TL_ERR_TIMEOUT);
       }
       __syncwarp();
@@ -190,7 +194,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       if (!named_bar_and(1, kNumEpiThreads, ok)) break;
       tc_fence_after();
       float* S = p.slots + (size_t(it.tau) * 2 + h) * p.half_floats + my_base;
-      const bool first = it.r == 0, last = it.r == p.R - 1;
+      const bool first = it.j == 0, last = it.j == p.R - 1;
       const int orow = it.mt * pair::BM + h * pair::HM + row_in_half;  // row of out[d]
       uint16_t* orowp = p.out[it.d] + size_t(orow) * p.N;
       const uint64_t keep = l2_policy_evict_last();  // S_tau is read again by the next rank
@@ -214,9 +218,18 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
         float* f = reinterpret_cast<float*>(v);
+        if (kBf16) {
+          // the partial rounded to bf16 (RNE) before it joins the sum
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const uint32_t w = pack_bf16x2(f[2 * q], f[2 * q + 1]);  // low half: f[2q]
+            f[2 * q] = __uint_as_float(w << 16);
+            f[2 * q + 1] = __uint_as_float(w & 0xFFFF0000u);
+          }
+        }
         float* sc = S + size_t(c * 8) * p.slice_rows * 4;
         if (!first) {
-          // ((P_0 + P_1) + ...) + P_r in fp32, one rounding per rank
+          // ((P_a + P_b) + ...) + P_r in fp32, one rounding per pass
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
             f[g * 4 + 0] = __fadd_rn(sv[g].x, f[g * 4 + 0]);
@@ -246,8 +259,8 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       // produce_tile_notify: every pusher thread's writes are ordered before thread 0's release
       named_bar_sync(1, kNumEpiThreads);
       if (et == 0) {
-        st_release(arrived + 2 * (it.tau * p.R + it.r) + h, p.epoch);
-        st_release(reduced + 2 * (it.tau * p.R + it.r) + h, p.epoch);
+        st_release(arrived + 2 * (it.tau * p.R + it.j) + h, p.epoch);
+        st_release(reduced + 2 * (it.tau * p.R + it.j) + h, p.epoch);
       }
     }
   } else if (!kChain && warp < kWarpRed0) {
@@ -473,8 +486,8 @@ tl_status rs_check(const tl_gemm_rs_args* a, const char* who) {
 // bytes of the chain schedule's running sums: one fp32 tile per output tile
 size_t rs_chain_bytes(int R, int M, int N) { return size_t(rs_num_tiles(R, M, N)) * 2 * rs_half_floats(R) * sizeof(float); }
 
-// Fill the kernel parameters and launch.  chain: the chain schedule is allowed (the
-// workspace holds rs_chain_bytes); it runs for the default options.
+// Fill the kernel parameters and launch.  chain: the chain schedule (the workspace
+// holds rs_chain_bytes), else push and reduce through a ring of receive slots.
 tl_status rs_launch(RsParams* p, const tl_gemm_rs_args* a, float* slots, uint32_t* flags, uint32_t* status,
                     int sm_count, cudaStream_t st, bool chain) {
   for (int r = 0; r < a->R; ++r) {
@@ -506,9 +519,11 @@ tl_status rs_launch(RsParams* p, const tl_gemm_rs_args* a, float* slots, uint32_
   const int pairs = rs_pairs(p->num_items, sm_count);
   p->ring_items = rs_ring_items(p->num_items, pairs);
   void* args[] = {p};
-  const void* kernel = (a->options & TL_RS_BF16_PARTIALS) ? reinterpret_cast<const void*>(&gemm_rs_kernel<true, false>)
-                       : (chain && a->options == 0)       ? reinterpret_cast<const void*>(&gemm_rs_kernel<false, true>)
-                                                          : reinterpret_cast<const void*>(&gemm_rs_kernel<false, false>);
+  const bool bf16 = (a->options & TL_RS_BF16_PARTIALS) != 0;
+  const void* kernel = chain ? (bf16 ? reinterpret_cast<const void*>(&gemm_rs_kernel<true, true>)
+                                     : reinterpret_cast<const void*>(&gemm_rs_kernel<false, true>))
+                             : (bf16 ? reinterpret_cast<const void*>(&gemm_rs_kernel<true, false>)
+                                     : reinterpret_cast<const void*>(&gemm_rs_kernel<false, false>));
   return launch_coop(kernel, 2 * pairs, RS_THREADS, RS_SMEM_BYTES, st, args, 2);
 }
 
