@@ -501,9 +501,11 @@ tl_status tl_moe_ag_gemm(const tl_moe_args* args, void* stream);
  *   out[d][u] = bf16( sum over slots s = 0..topk-1, in order, of
  *                     gates[t, s] * Y[pos(t, s)] ),   t = d*T_r + u          (fp32)
  * Two stream-ordered launches: a grouped GEMM-ReduceScatter on pairs of CTAs
- * (items = (expert tile, 256-column tile, rank), the R partials of a tile pushed
- * into receive slots, reducers summing them in rank order into Y, as in
- * tl_gemm_rs), then the TopK-reduce that combines and scatters.  The routing
+ * (items = (expert tile, 256-column tile, rank); each tile's partials are added
+ * into its fp32 running sum rank after rank, rank r's pass waiting on rank
+ * r-1's arrival flag, and rank R-1's pass writes the sum into Y: the chain
+ * schedule of tl_gemm_rs, output tiles in groups of 96), then the TopK-reduce
+ * that combines and scatters.  The routing
  * (sorted rows, tile table, inverse permutation) is the workspace a
  * tl_moe_ag_gemm call on the same topk_ids, R, T_r, E and topk left behind.
  * Limits: R <= 32, E <= 64, I_r and Hd multiples of 8.
@@ -525,13 +527,15 @@ typedef struct tl_moe_down_args {
   tl_signals* signals;         /* >= tl_moe_down_num_flags(...) flags */
   uint32_t epoch;              /* nonzero */
   uint32_t options;            /* 0, or TL_RS_BF16_PARTIALS: each rank's partial is rounded to bf16 (RNE)
-                                  before it is pushed (half the partial bytes), summed in fp32 as before */
+                                  before it joins the fp32 running sum */
   uint64_t timeout_ns;         /* 0 = 1 s */
 } tl_moe_down_args;
 
-/* Workspace bytes: the fp32 receive ring (as for GEMM-RS) and Y [P, Hd] fp32. */
+/* Workspace bytes: the fp32 running sums of every output tile (max_tiles * ceil(Hd/256)
+ * tiles of 256 x 256) and Y [P, Hd] fp32.  0 for invalid sizes. */
 size_t tl_moe_down_workspace_size(int R, int T_r, int topk, int E, int Hd);
-/* Flags: 4 * R * max_tiles * ceil(Hd/256), max_tiles = ceil(P/256) + E. */
+/* Flags: 2 * R * max_tiles * ceil(Hd/256) (one per pass and CTA half of every output
+ * tile), max_tiles = ceil(P/256) + E; -1 for invalid sizes. */
 int tl_moe_down_num_flags(int R, int T_r, int topk, int E, int Hd);
 tl_status tl_moe_down(const tl_moe_down_args* args, void* stream);
 

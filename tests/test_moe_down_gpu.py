@@ -123,3 +123,34 @@ def test_moe_down_bf16_partials_parity(B, R, T_r, E, k, I_r, Hd):
         bound = 2.0 ** -7 * mag[d] + 2.0 ** -8 * np.abs(o) + 1e-3 * np.abs(o).max()
         assert np.all(np.abs(got - o) <= bound), f"out[{d}]: max excess {np.max(np.abs(got - o) - bound):.3e}"
         assert np.abs(got - o).max() / np.abs(o).max() <= 2e-2
+
+
+@pytest.mark.parametrize("options", [0, 1])
+def test_moe_down_sums_ranks_in_order(B, options):
+    # every routed row's partials are 2^24, 1 and -2^24 from ranks 0, 1 and 2 (one-hot H_r rows,
+    # W2_r rows of those values).  Their fp32 sum in rank order is exactly 0, since 2^24 + 1
+    # rounds to 2^24; adding 1 last, or -2^24 before 2^24, gives 1.  All three values are bf16,
+    # so the bf16-partials option gives the same.
+    import torch
+    R, T_r, E, k, I_r, Hd = 3, 64, 4, 2, 64, 264
+    ids = inputs.zipf_topk(R * T_r, E, k, 1.2, 7)
+    P = R * T_r * k
+    ws_route = routing_workspace(B, R, T_r, E, k, ids, 7)
+    H = np.zeros((P, I_r), dtype=np.uint16)
+    H[:, 0] = 0x3F80  # 1.0
+    W2 = []
+    for v in (0x4B80, 0x3F80, 0xCB80):  # 2^24, 1, -2^24
+        w = np.zeros((E * I_r, Hd), dtype=np.uint16)
+        w[np.arange(E) * I_r, :] = v
+        W2.append(w)
+    gates = np.random.default_rng(7).uniform(0.5, 1.0, (R * T_r, k)).astype(np.float32)
+    out = [torch.full((T_r, Hd), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+    work = torch.full((B.tl_moe_down_workspace_size(R, T_r, k, E, Hd) // 4,), float("nan"), dtype=torch.float32,
+                      device="cuda")
+    sig = B.Signals(B.tl_moe_down_num_flags(R, T_r, k, E, Hd))
+    _epoch[0] += 1
+    B.tl_moe_down([dev_bf16(H)] * R, [dev_bf16(w) for w in W2], torch.from_numpy(gates).cuda(), ws_route,
+                  out, work, sig, _epoch[0], topk=k, E=E, options=options)
+    assert B.tl_query_status(sig) == (0, -1)
+    for d in range(R):
+        assert (to_f64(out[d]) == 0).all(), f"out[{d}] not exactly 0: ranks summed out of order"

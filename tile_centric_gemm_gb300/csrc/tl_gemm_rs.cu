@@ -46,8 +46,10 @@
 // travelling from rank to rank: the destinations are taken in groups of
 // kChainGroup, and within a group items run pass by pass (pass j: every tile's
 // partial of the j-th rank of the summation order -- rank j, or rank d+1+j mod
-// R in ring order).  The pushers of (tau, j) wait for pass j-1's arrival flag
-// of the tile (peer_tile_wait), add their partial (rounded to bf16 first with
+// R in ring order).  Eight warps drain each accumulator (the pushers and
+// reducer warps 6-9, one per TMEM lane quarter and column half); those of
+// (tau, j) wait for pass j-1's arrival flag of the tile (peer_tile_wait), add
+// their partial (rounded to bf16 first with
 // bf16 partials) to the tile's fp32 running sum S_tau in the workspace (the
 // next chunk's sums loaded while the current one is added) and release the
 // flags of (tau, j); pass R-1 writes bf16(S_tau) to out[d] instead.  The
@@ -81,6 +83,11 @@ constexpr int RB = 8;                             // ranks loaded per batch in t
 constexpr int QU = 2;                             // float4 elements per thread per round in the reduce
 // chain schedule: destinations whose running sums stay in L2 while their R ranks pass
 constexpr int kChainGroup = 2;
+// The chain schedule's epilogue: two groups of four warps, each adding half of the columns.
+constexpr int kChainParts = 2;
+constexpr int kChainEpiWarps = kNumEpiWarps * kChainParts;
+constexpr int kChainEpiThreads = kChainEpiWarps * 32;
+constexpr int kChainChunks = pair::BN / 32 / kChainParts;
 
 struct RsParams {
   CUtensorMap map_a[RS_MAX_RANKS];  // A_r [M, K_r], box 128 rows
@@ -170,10 +177,14 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
     if (lane == 0 && rank == 0)
       pair::mma_loop(smem, bars, tmem_base, my_items, p.KB, abort, p.status, p.pipe_timeout_ns);
     __syncwarp();
-  } else if (kChain && warp < kWarpRed0) {
+  } else if (kChain && warp < kWarpEpi0 + kChainEpiWarps) {
     // ---------------------------------------------------------------- pushers: chain accumulation
+    // Two groups of four warps (the pushers and the first four reducer warps, which the
+    // chain does not need), one warp per TMEM lane quarter in each; group q adds columns
+    // [q, q+1) * 128 of every accumulator.
     const int wq = warp & 3;
-    const int et = (warp - kWarpEpi0) * 32 + lane;  // 0..127 among pusher threads
+    const int part = (warp - kWarpEpi0) / kNumEpiWarps;
+    const int et = (warp - kWarpEpi0) * 32 + lane;  // 0..255 among chain epilogue threads
     const int row_in_half = wq * 32 + lane;
     // S_tau in the half-slot layout [slice][col/4][row in slice][4] of the push schedule
     const int my_slice = row_in_half / p.slice_rows, my_row = row_in_half % p.slice_rows;
@@ -191,7 +202,7 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       }
       __syncwarp();
       const bool ok = mbar_wait(&bars->tmem_full[acc], acc_ph, abort, p.status, p.pipe_timeout_ns, 4);
-      if (!named_bar_and(1, kNumEpiThreads, ok)) break;
+      if (!named_bar_and(1, kChainEpiThreads, ok)) break;
       tc_fence_after();
       float* S = p.slots + (size_t(it.tau) * 2 + h) * p.half_floats + my_base;
       const bool first = it.j == 0, last = it.j == p.R - 1;
@@ -199,17 +210,19 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
       uint16_t* orowp = p.out[it.d] + size_t(orow) * p.N;
       const uint64_t keep = l2_policy_evict_last();  // S_tau is read again by the next rank
       const int nch = min(pair::BN / 32, (p.N - it.nt * pair::BN + 31) / 32);
-      float4 sn[8];  // the next chunk's running sums, loaded one chunk ahead
-      if (!first) {
+      // this warp's share of the columns; the next chunk's running sums loaded one chunk ahead
+      const int c_lo = part * kChainChunks, c_hi = min(nch, c_lo + kChainChunks);
+      float4 sn[8];
+      if (!first && c_lo < c_hi) {
 #pragma unroll
-        for (int g = 0; g < 8; ++g) sn[g] = ld_global_cg_v4f_hint(S + size_t(g) * p.slice_rows * 4, keep);
+        for (int g = 0; g < 8; ++g) sn[g] = ld_global_cg_v4f_hint(S + size_t(c_lo * 8 + g) * p.slice_rows * 4, keep);
       }
-      for (int c = 0; c < nch; ++c) {
+      for (int c = c_lo; c < c_hi; ++c) {
         const int col0 = it.nt * pair::BN + c * 32;
         float4 sv[8];
 #pragma unroll
         for (int g = 0; g < 8; ++g) sv[g] = sn[g];
-        if (!first && c + 1 < nch) {
+        if (!first && c + 1 < c_hi) {
 #pragma unroll
           for (int g = 0; g < 8; ++g)
             sn[g] = ld_global_cg_v4f_hint(S + size_t((c + 1) * 8 + g) * p.slice_rows * 4, keep);
@@ -254,10 +267,11 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
         }
       }
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) pair::release_accumulator(bars, acc, rank);
-      // produce_tile_notify: every pusher thread's writes are ordered before thread 0's release
-      named_bar_sync(1, kNumEpiThreads);
+      // every chain warp has read its columns of the accumulator and stored its share: the
+      // first group's warps hand the accumulator back, and thread 0 releases the pass
+      // (produce_tile_notify; the barrier orders every thread's writes before it)
+      named_bar_sync(1, kChainEpiThreads);
+      if (part == 0 && lane == 0) pair::release_accumulator(bars, acc, rank);
       if (et == 0) {
         st_release(arrived + 2 * (it.tau * p.R + it.j) + h, p.epoch);
         st_release(reduced + 2 * (it.tau * p.R + it.j) + h, p.epoch);

@@ -147,22 +147,28 @@ struct Producer {
     }
     return true;
   }
-  // The same with an L2 eviction-priority policy on the operand lines.
+  // The same with L2 eviction-priority policies on the operand lines (pol_a for A, pol_b for B).
   __device__ __forceinline__ bool load_hint(uint8_t* smem, Bars* bars, uint32_t rank, const CUtensorMap* ma, int a_x,
-                                            int a_y, const CUtensorMap* mb, int b_x, int b_y, uint64_t pol,
-                                            volatile uint32_t* abort, uint32_t* status, uint64_t pipe_timeout) {
+                                            int a_y, const CUtensorMap* mb, int b_x, int b_y, uint64_t pol_a,
+                                            uint64_t pol_b, volatile uint32_t* abort, uint32_t* status,
+                                            uint64_t pipe_timeout) {
     if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort, status, pipe_timeout, 1)) return false;
     if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], PAIR_STAGE_TX);
     const uint32_t full = map_to_rank(&bars->full[s], 0);
-    tma_load_2d_pair_hint(smem + SMEM_A + s * A_STAGE, ma, full, a_x, a_y, pol);
+    tma_load_2d_pair_hint(smem + SMEM_A + s * A_STAGE, ma, full, a_x, a_y, pol_a);
     uint8_t* b_dst = smem + SMEM_B + s * B_STAGE;
-    tma_load_2d_pair_hint(b_dst, mb, full, b_x, b_y, pol);
-    tma_load_2d_pair_hint(b_dst + B_BOX_BYTES, mb, full, b_x + 64, b_y, pol);
+    tma_load_2d_pair_hint(b_dst, mb, full, b_x, b_y, pol_b);
+    tma_load_2d_pair_hint(b_dst + B_BOX_BYTES, mb, full, b_x + 64, b_y, pol_b);
     if (++s == STAGES) {
       s = 0;
       ph ^= 1u;
     }
     return true;
+  }
+  __device__ __forceinline__ bool load_hint(uint8_t* smem, Bars* bars, uint32_t rank, const CUtensorMap* ma, int a_x,
+                                            int a_y, const CUtensorMap* mb, int b_x, int b_y, uint64_t pol,
+                                            volatile uint32_t* abort, uint32_t* status, uint64_t pipe_timeout) {
+    return load_hint(smem, bars, rank, ma, a_x, a_y, mb, b_x, b_y, pol, pol, abort, status, pipe_timeout);
   }
 };
 
