@@ -348,6 +348,23 @@ struct MoeParams {
   uint64_t hold_ns;
 };
 
+// Work item q of the grouped GEMM: unit q in consumer order (expert tile order[q / Nt],
+// 256-column tile q % Nt).  A last column tile of at most 128 columns runs as an N = 128
+// product (narrow).
+struct MoeWork {
+  int t, n, col0;
+  bool narrow;
+};
+
+__device__ __forceinline__ MoeWork moe_work(const MoeParams& p, const int32_t* order, int q) {
+  MoeWork w;
+  w.t = order[q / p.Nt];
+  w.n = q % p.Nt;
+  w.col0 = w.n * pair::BN;
+  w.narrow = p.N - w.col0 <= pair::HN;
+  return w;
+}
+
 __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_constant__ MoeParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -372,9 +389,9 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
     // ---------------------------------------------------------------- TMA producer (this CTA's 128 rows)
     pair::Producer prod;
     int last_t = -1;
-    for (int w = pair_id; w < num_work; w += npairs) {
-      const int t = order[w / p.Nt];
-      const int n = w % p.Nt;
+    for (int q = pair_id; q < num_work; q += npairs) {
+      const MoeWork w = moe_work(p, order, q);
+      const int t = w.t;
       const int32_t* tr = tiles + 6 * t;
       const int e = tr[0], row0 = tr[1];
       if (t != last_t) {
@@ -385,30 +402,33 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
       last_t = t;
       __syncwarp();
       if (lane == 0) {
-        if (p.trace && rank == 0) p.trace[w] = t * p.Nt + n;
+        if (p.trace && rank == 0) p.trace[q] = t * p.Nt + w.n;
         fence_proxy_async_global();
+        const int b_x = w.col0 + h * (w.narrow ? pair::HN / 2 : pair::HN);
         for (int kb = 0; kb < p.KB; ++kb)
-          if (!prod.load(smem, bars, rank, &p.map_a, kb * pair::BK, row0 + h * pair::HM, &p.map_w[e],
-                         n * pair::BN + h * pair::HN, kb * pair::BK, abort, p.status, p.pipe_timeout_ns))
+          if (!prod.load(smem, bars, rank, &p.map_a, kb * pair::BK, row0 + h * pair::HM, &p.map_w[e], b_x,
+                         kb * pair::BK, abort, p.status, p.pipe_timeout_ns, w.narrow))
             break;
       }
       if (__shfl_sync(0xffffffffu, *abort, 0)) break;
     }
   } else if (warp == kWarpMma) {
     // ---------------------------------------------------------------- MMA issuer (leader)
-    if (lane == 0 && rank == 0)
-      pair::mma_loop(smem, bars, tmem_base, my_work, p.KB, abort, p.status, p.pipe_timeout_ns);
+    if (lane == 0 && rank == 0) {
+      pair::mma_loop(smem, bars, tmem_base, my_work, p.KB, abort, p.status, p.pipe_timeout_ns,
+                     [&](int j) { return moe_work(p, order, pair_id + j * npairs).narrow; });
+    }
     __syncwarp();
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kNumEpiWarps) {
     // ---------------------------------------------------------------- epilogue: rows of this expert only
     const int wq = warp & 3;
     uint8_t* cbox = smem + MOE_SMEM_CSTAGE + uint32_t(wq) * C_BOX_BYTES;
     int j = 0;
-    for (int w = pair_id; w < num_work; w += npairs, ++j) {
+    for (int q = pair_id; q < num_work; q += npairs, ++j) {
       const int acc = j & 1;
       const uint32_t acc_ph = uint32_t(j >> 1) & 1u;
-      const int32_t* tr = tiles + 6 * order[w / p.Nt];
-      const int n = w % p.Nt;
+      const MoeWork w = moe_work(p, order, q);
+      const int32_t* tr = tiles + 6 * w.t;
       const int row0 = tr[1], rows = tr[2];
       const bool ok = mbar_wait(&bars->tmem_full[acc], acc_ph, abort, p.status, p.pipe_timeout_ns, 4);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -419,8 +439,9 @@ __global__ void __launch_bounds__(MOE_THREADS, 1) moe_gemm_kernel(const __grid_c
       // (plain stores: the rows after them belong to the next tile), or none
       const int box_r0 = h * pair::HM + wq * 32;
       const bool whole = box_r0 + 32 <= rows;
-      for (int c = 0; c < pair::BN / 32; ++c) {
-        const int col0 = n * pair::BN + c * 32;
+      const int nchunks = (w.narrow ? pair::HN : pair::BN) / 32;
+      for (int c = 0; c < nchunks; ++c) {
+        const int col0 = w.col0 + c * 32;
         if (col0 >= p.N) break;
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);

@@ -22,10 +22,13 @@ constexpr uint32_t A_STAGE = HM * BK * 2;            // 16 KB
 constexpr uint32_t B_STAGE = BK * HN * 2;            // 16 KB = 2 boxes of 64 x 64
 constexpr uint32_t CTA_STAGE_TX = A_STAGE + B_STAGE;  // bytes one CTA loads per stage
 constexpr uint32_t PAIR_STAGE_TX = 2 * CTA_STAGE_TX;  // bytes the leader's full barrier expects
+// A narrow tile (at most HN columns left, N = 128): each CTA stages one 64-column box of B.
+constexpr uint32_t PAIR_STAGE_TX_NARROW = 2 * (A_STAGE + B_BOX_BYTES);
 constexpr uint32_t SMEM_A = 0;
 constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE;
 constexpr uint32_t SMEM_END = SMEM_B + STAGES * B_STAGE;  // 192 KB
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, true);
+constexpr uint32_t IDESC_NARROW = idesc_bf16_f32(BM, BN / 2, true);
 
 struct __align__(8) Bars {
   uint64_t full[STAGES];     // leader: both CTAs' TMA bytes of a stage
@@ -38,15 +41,17 @@ struct __align__(8) Bars {
   uint32_t splitk_ok;        // split-K: every split of this CTA's half-tile arrived
 };
 
-// Four UMMA_K steps of one k-block from stage s; issued by the leader only.
-__device__ __forceinline__ void mma_kblock(uint8_t* smem, int s, uint32_t d_tmem, bool first) {
+// Four UMMA_K steps of one k-block from stage s; issued by the leader only.  A narrow tile
+// (IDESC_NARROW) reads only the first B box of each CTA.
+__device__ __forceinline__ void mma_kblock(uint8_t* smem, int s, uint32_t d_tmem, bool first,
+                                           uint32_t idesc = IDESC) {
   const uint32_t a0 = smem_u32(smem + SMEM_A + s * A_STAGE);
   const uint32_t b0 = smem_u32(smem + SMEM_B + s * B_STAGE);
 #pragma unroll
   for (int kk = 0; kk < BK / UMMA_K; ++kk) {
     const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
     const uint64_t bd = sdesc_sw128(b0 + kk * 2048, B_BOX_BYTES, 1024);
-    tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (first && kk == 0) ? 0u : 1u);
+    tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
   }
 }
 
@@ -101,9 +106,16 @@ __device__ __forceinline__ void release_accumulator(Bars* bars, int acc, uint32_
   else mbar_arrive_cluster(map_to_rank(&bars->tmem_empty[acc], 0));
 }
 
-// MMA issuer loop of the leader: `ntiles` tiles of `kb` k-blocks each, ring state in (s, ph).
+struct NeverNarrow {
+  __device__ __forceinline__ bool operator()(int) const { return false; }
+};
+
+// MMA issuer loop of the leader: `ntiles` tiles of `kb` k-blocks each, ring state in (s, ph);
+// narrow(j) says whether this pair's j-th tile is a narrow one (N = 128).
+template <class Narrow = NeverNarrow>
 __device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, uint32_t tmem_base, int ntiles, int KB,
-                                         volatile uint32_t* abort, uint32_t* status, uint64_t pipe_timeout) {
+                                         volatile uint32_t* abort, uint32_t* status, uint64_t pipe_timeout,
+                                         Narrow narrow = Narrow()) {
   int s = 0;
   uint32_t ph = 0;
   for (int j = 0; j < ntiles && !*abort; ++j) {
@@ -112,10 +124,11 @@ __device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, uint32_t tme
     if (!mbar_wait(&bars->tmem_empty[acc], acc_ph ^ 1u, abort, status, pipe_timeout, 2)) return;
     tc_fence_after();
     const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+    const uint32_t idesc = narrow(j) ? IDESC_NARROW : IDESC;
     for (int kb = 0; kb < KB; ++kb) {
       if (!mbar_wait(&bars->full[s], ph, abort, status, pipe_timeout, 3)) return;
       tc_fence_after();
-      mma_kblock(smem, s, d_tmem, kb == 0);
+      mma_kblock(smem, s, d_tmem, kb == 0, idesc);
       tc_commit_pair(&bars->empty[s], 0x3);
       if (++s == STAGES) {
         s = 0;
@@ -131,16 +144,17 @@ __device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, uint32_t tme
 struct Producer {
   int s = 0;
   uint32_t ph = 0;
+  // narrow: a narrow tile, one 64-column box of B from b_x (the CTA's half of 128 columns).
   __device__ __forceinline__ bool load(uint8_t* smem, Bars* bars, uint32_t rank, const CUtensorMap* ma, int a_x,
                                        int a_y, const CUtensorMap* mb, int b_x, int b_y, volatile uint32_t* abort,
-                                       uint32_t* status, uint64_t pipe_timeout) {
+                                       uint32_t* status, uint64_t pipe_timeout, bool narrow = false) {
     if (!mbar_wait(&bars->empty[s], ph ^ 1u, abort, status, pipe_timeout, 1)) return false;
-    if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], PAIR_STAGE_TX);
+    if (rank == 0) mbar_arrive_expect_tx(&bars->full[s], narrow ? PAIR_STAGE_TX_NARROW : PAIR_STAGE_TX);
     const uint32_t full = map_to_rank(&bars->full[s], 0);
     tma_load_2d_pair(smem + SMEM_A + s * A_STAGE, ma, full, a_x, a_y);
     uint8_t* b_dst = smem + SMEM_B + s * B_STAGE;
     tma_load_2d_pair(b_dst, mb, full, b_x, b_y);
-    tma_load_2d_pair(b_dst + B_BOX_BYTES, mb, full, b_x + 64, b_y);
+    if (!narrow) tma_load_2d_pair(b_dst + B_BOX_BYTES, mb, full, b_x + 64, b_y);
     if (++s == STAGES) {
       s = 0;
       ph ^= 1u;
