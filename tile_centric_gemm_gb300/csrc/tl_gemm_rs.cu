@@ -46,10 +46,11 @@
 // travelling from rank to rank: the destinations are taken in groups of
 // kChainGroup, and within a group items run pass by pass (pass j: every tile's
 // partial of the j-th rank of the summation order -- rank j, or rank d+1+j mod
-// R in ring order).  Eight warps drain each accumulator (the pushers and
-// reducer warps 6-9, one per TMEM lane quarter and column half); those of
-// (tau, j) wait for pass j-1's arrival flag of the tile (peer_tile_wait), add
-// their partial (rounded to bf16 first with
+// R in ring order).  The chain launches 11 warps: eight drain each accumulator
+// (warps 2-9, one per TMEM lane quarter and column half, each freeing the
+// accumulator after its last read of it; warp 10 releases a pass's flags once
+// all eight have stored their share); those of (tau, j) wait for pass j-1's
+// arrival flag of the tile (peer_tile_wait), add their partial (rounded to bf16 first with
 // bf16 partials) to the tile's fp32 running sum S_tau in the workspace (the
 // next chunk's sums loaded while the current one is added) and release the
 // flags of (tau, j); pass R-1 writes bf16(S_tau) to out[d] instead.  The
@@ -78,7 +79,14 @@ constexpr int kNumRedWarps = 8;
 constexpr int kNumRedThreads = kNumRedWarps * 32;
 constexpr int RS_THREADS = (kWarpRed0 + kNumRedWarps) * 32;
 constexpr uint32_t RS_SMEM_BARS = pair::SMEM_END;
-constexpr uint32_t RS_SMEM_BYTES = RS_SMEM_BARS + sizeof(pair::Bars) + 1024;
+// chain schedule, per accumulator: the epilogue threads' stores are done (stored[a], one
+// arrival per chain epilogue thread) and the notifier has released the pass (notified[a])
+struct ChainBars {
+  uint64_t stored[2];
+  uint64_t notified[2];
+};
+constexpr uint32_t RS_SMEM_CHAIN = RS_SMEM_BARS + (uint32_t(sizeof(pair::Bars)) + 7u) / 8u * 8u;
+constexpr uint32_t RS_SMEM_BYTES = RS_SMEM_CHAIN + sizeof(ChainBars) + 1024;
 constexpr int RB = 8;                             // ranks loaded per batch in the reduce
 constexpr int QU = 2;                             // float4 elements per thread per round in the reduce
 // chain schedule: destinations whose running sums stay in L2 while their R ranks pass
@@ -87,6 +95,8 @@ constexpr int kChainGroup = 2;
 constexpr int kChainParts = 2;
 constexpr int kChainEpiWarps = kNumEpiWarps * kChainParts;
 constexpr int kChainEpiThreads = kChainEpiWarps * 32;
+constexpr int kWarpChainNotify = kWarpEpi0 + kChainEpiWarps;  // releases each pass's flags
+constexpr int RS_CHAIN_THREADS = (kWarpChainNotify + 1) * 32;  // the chain launches no reducer warps
 constexpr int kChainChunks = pair::BN / 32 / kChainParts;
 
 struct RsParams {
@@ -138,16 +148,25 @@ __device__ __forceinline__ Item item_of(const RsParams& p, int i) {
 // kBf16: partials rounded to bf16 (TL_RS_BF16_PARTIALS); kChain: the chain schedule
 // (every option), else push and reduce (the no-allocation entry point).
 template <bool kBf16, bool kChain>
-__global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_constant__ RsParams p) {
+__global__ void __launch_bounds__(kChain ? RS_CHAIN_THREADS : RS_THREADS, 1)
+    gemm_rs_kernel(const __grid_constant__ RsParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   pair::Bars* bars = reinterpret_cast<pair::Bars*>(smem + RS_SMEM_BARS);
+  ChainBars* cb = reinterpret_cast<ChainBars*>(smem + RS_SMEM_CHAIN);
   const int warp = int(warp_id());
   const int lane = int(lane_id());
   const uint32_t rank = cluster_ctarank();
   const int h = int(rank);
   const int pair_id = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
-  const uint32_t tmem_base = pair::setup(bars, warp);
+  if (kChain && threadIdx.x == 0) {
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&cb->stored[a], kChainEpiThreads);
+      mbar_init(&cb->notified[a], 1);
+    }
+  }
+  // chain: every chain epilogue warp of both CTAs frees the accumulator after its last read
+  const uint32_t tmem_base = pair::setup(bars, warp, kChain ? 2 * kChainEpiWarps : 2 * kNumEpiWarps);
   volatile uint32_t* abort = &bars->abort;
   const int my_items = pair_id < p.num_items ? (p.num_items - 1 - pair_id) / npairs + 1 : 0;
   uint32_t* arrived = p.flags;                         // 2*(tau*R + r) + h
@@ -177,6 +196,23 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
     if (lane == 0 && rank == 0)
       pair::mma_loop(smem, bars, tmem_base, my_items, p.KB, abort, p.status, p.pipe_timeout_ns);
     __syncwarp();
+  } else if (kChain && warp == kWarpChainNotify) {
+    // ---------------------------------------------------------------- chain notifier
+    // produce_tile_notify for each pass, off the epilogue's path: once every epilogue thread
+    // has stored its share of the item (their arrivals order their writes before this
+    // thread's release), release the pass's arrival and "reduced" flags
+    if (lane == 0) {
+      int jj = 0;
+      for (int i = pair_id; i < p.num_items; i += npairs, ++jj) {
+        const Item it = item_of<true>(p, i);
+        const int acc = jj & 1;
+        if (!mbar_wait(&cb->stored[acc], uint32_t(jj >> 1) & 1u, abort, p.status, p.pipe_timeout_ns, 6)) break;
+        st_release(arrived + 2 * (it.tau * p.R + it.j) + h, p.epoch);
+        st_release(reduced + 2 * (it.tau * p.R + it.j) + h, p.epoch);
+        mbar_arrive(&cb->notified[acc]);
+      }
+    }
+    __syncwarp();
   } else if (kChain && warp < kWarpEpi0 + kChainEpiWarps) {
     // ---------------------------------------------------------------- pushers: chain accumulation
     // Two groups of four warps (the pushers and the first four reducer warps, which the
@@ -184,7 +220,6 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
     // [q, q+1) * 128 of every accumulator.
     const int wq = warp & 3;
     const int part = (warp - kWarpEpi0) / kNumEpiWarps;
-    const int et = (warp - kWarpEpi0) * 32 + lane;  // 0..255 among chain epilogue threads
     const int row_in_half = wq * 32 + lane;
     // S_tau in the half-slot layout [slice][col/4][row in slice][4] of the push schedule
     const int my_slice = row_in_half / p.slice_rows, my_row = row_in_half % p.slice_rows;
@@ -230,6 +265,12 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
+        if (c == c_hi - 1) {
+          // this warp's last read of the accumulator: hand it back before the adds and stores
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) pair::release_accumulator(bars, acc, rank);
+        }
         float* f = reinterpret_cast<float*>(v);
         if (kBf16) {
           // the partial rounded to bf16 (RNE) before it joins the sum
@@ -266,16 +307,18 @@ __global__ void __launch_bounds__(RS_THREADS, 1) gemm_rs_kernel(const __grid_con
                            pack_bf16x2(f[g * 8 + 6], f[g * 8 + 7]));
         }
       }
-      tc_fence_before();
-      // every chain warp has read its columns of the accumulator and stored its share: the
-      // first group's warps hand the accumulator back, and thread 0 releases the pass
-      // (produce_tile_notify; the barrier orders every thread's writes before it)
-      named_bar_sync(1, kChainEpiThreads);
-      if (part == 0 && lane == 0) pair::release_accumulator(bars, acc, rank);
-      if (et == 0) {
-        st_release(arrived + 2 * (it.tau * p.R + it.j) + h, p.epoch);
-        st_release(reduced + 2 * (it.tau * p.R + it.j) + h, p.epoch);
+      if (c_lo >= c_hi) {
+        // no columns for this warp (a narrow last column tile): nothing to read
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) pair::release_accumulator(bars, acc, rank);
       }
+      // this thread's writes of the item are done: the notifier releases the pass once all
+      // have arrived (it has handled the item two back, which used the same barrier)
+      if (jj >= 2 && !mbar_wait(&cb->notified[acc], (uint32_t(jj >> 1) & 1u) ^ 1u, abort, p.status,
+                                p.pipe_timeout_ns, 7))
+        break;
+      mbar_arrive(&cb->stored[acc]);
     }
   } else if (!kChain && warp < kWarpRed0) {
     // ---------------------------------------------------------------- pushers
@@ -538,7 +581,7 @@ tl_status rs_launch(RsParams* p, const tl_gemm_rs_args* a, float* slots, uint32_
                                      : reinterpret_cast<const void*>(&gemm_rs_kernel<false, true>))
                              : (bf16 ? reinterpret_cast<const void*>(&gemm_rs_kernel<true, false>)
                                      : reinterpret_cast<const void*>(&gemm_rs_kernel<false, false>));
-  return launch_coop(kernel, 2 * pairs, RS_THREADS, RS_SMEM_BYTES, st, args, 2);
+  return launch_coop(kernel, 2 * pairs, chain ? RS_CHAIN_THREADS : RS_THREADS, RS_SMEM_BYTES, st, args, 2);
 }
 
 }  // namespace

@@ -23,7 +23,9 @@
 // so a group's running sums stay in L2 from one pass to the next.  Items are
 // taken round-robin by the CTA pairs.  Per CTA: warp 0 TMA producer, warp 1
 // MMA issuer (leader), warps 2-9 epilogue (one row of the half-tile and half of
-// its columns per thread).
+// its columns per thread; each warp frees the accumulator after its last read of
+// it), warp 10 notifier (releases a pass's flag once every epilogue thread has
+// stored its share).
 // Only the rows of the tile's expert are summed and written: the padding rows
 // of an expert's last tile are computed by the MMAs but belong to the next
 // expert's rows of Y.  The K loop runs over I_r; columns of H_r past I_r read
@@ -51,9 +53,17 @@ constexpr int MD_MAX_E = 64;
 constexpr int kEpiParts = 2;
 constexpr int kChunksPerPart = pair::BN / 32 / kEpiParts;
 constexpr int kNumMdEpiThreads = kNumEpiThreads * kEpiParts;
-constexpr int MD_THREADS = kWarpEpi0 * 32 + kNumMdEpiThreads;
+constexpr int kWarpNotify = kWarpEpi0 + kNumMdEpiThreads / 32;  // releases each pass's flag
+constexpr int MD_THREADS = (kWarpNotify + 1) * 32;
 constexpr uint32_t MD_SMEM_BARS = pair::SMEM_END;
-constexpr uint32_t MD_SMEM_BYTES = MD_SMEM_BARS + sizeof(pair::Bars) + 1024;
+// per accumulator: the epilogue threads' sums and Y rows are stored (stored[a], one arrival
+// per epilogue thread), and the notifier has released the item's flag (notified[a])
+struct MdBars {
+  uint64_t stored[2];
+  uint64_t notified[2];
+};
+constexpr uint32_t MD_SMEM_MDBARS = MD_SMEM_BARS + (uint32_t(sizeof(pair::Bars)) + 7u) / 8u * 8u;
+constexpr uint32_t MD_SMEM_BYTES = MD_SMEM_MDBARS + sizeof(MdBars) + 1024;
 constexpr int kChainTiles = 96;                     // output tiles whose sums are in flight together
 constexpr int kHalfFloats = pair::HM * pair::BN;     // one CTA's half of a tile's running sum
 
@@ -102,12 +112,20 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   pair::Bars* bars = reinterpret_cast<pair::Bars*>(smem + MD_SMEM_BARS);
+  MdBars* mdb = reinterpret_cast<MdBars*>(smem + MD_SMEM_MDBARS);
   const int warp = int(warp_id());
   const int lane = int(lane_id());
   const uint32_t rank = cluster_ctarank();
   const int h = int(rank);
   const int pair_id = int(blockIdx.x >> 1), npairs = int(gridDim.x >> 1);
-  const uint32_t tmem_base = pair::setup(bars, warp);
+  if (threadIdx.x == 0) {
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&mdb->stored[a], kNumMdEpiThreads);
+      mbar_init(&mdb->notified[a], 1);
+    }
+  }
+  // every epilogue warp of both CTAs frees the accumulator once it has read its columns
+  const uint32_t tmem_base = pair::setup(bars, warp, 2 * (kNumMdEpiThreads / 32));
   volatile uint32_t* abort = &bars->abort;
   const int ntiles = min(p.ws[0], p.max_tiles);
   const int num_items = ntiles * p.Nt * p.R;
@@ -135,11 +153,26 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
     if (lane == 0 && rank == 0)
       pair::mma_loop(smem, bars, tmem_base, my_items, p.KB, abort, p.status, p.pipe_timeout_ns);
     __syncwarp();
+  } else if (warp == kWarpNotify) {
+    // ---------------------------------------------------------------- notifier
+    // produce_tile_notify for each pass, off the epilogue's path: once every epilogue
+    // thread has stored its share of the item (their arrivals order their writes before
+    // this thread's release), release the pass's arrival flag
+    if (lane == 0) {
+      int jj = 0;
+      for (int i = pair_id; i < num_items; i += npairs, ++jj) {
+        const MdItem it = md_item(p, i, ntiles);
+        const int acc = jj & 1;
+        if (!mbar_wait(&mdb->stored[acc], uint32_t(jj >> 1) & 1u, abort, p.status, p.pipe_timeout_ns, 6)) break;
+        st_release(arrived + 2 * (it.tau * p.R + it.j) + h, p.epoch);
+        mbar_arrive(&mdb->notified[acc]);
+      }
+    }
+    __syncwarp();
   } else {
     // ---------------------------------------------------------------- epilogue: chain accumulation
     const int wq = warp & 3;                               // TMEM lane quarter of this warp
     const int part = (warp - kWarpEpi0) / kNumEpiWarps;    // its share of the columns
-    const int et = (warp - kWarpEpi0) * 32 + lane;
     const int row_in_half = wq * 32 + lane;
     int jj = 0;
     for (int i = pair_id; i < num_items; i += npairs, ++jj) {
@@ -185,6 +218,12 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
         uint32_t v[32];
         tmem_ld_32cols(tmem_base + (uint32_t(wq * 32) << 16) + uint32_t(acc * pair::BN + c * 32), v);
         tmem_ld_wait();
+        if (c == c_hi - 1) {
+          // this warp's last read of the accumulator: hand it back before the adds and stores
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) pair::release_accumulator(bars, acc, rank);
+        }
         if (!row_used) continue;
         float* f = reinterpret_cast<float*>(v);
         if (kBf16) {
@@ -221,14 +260,18 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
                   make_float4(f[g * 4], f[g * 4 + 1], f[g * 4 + 2], f[g * 4 + 3]);
         }
       }
-      tc_fence_before();
-      // every epilogue warp has read its columns of the accumulator and stored its share:
-      // the first group's warps hand the accumulator back to the MMA issuer, and thread 0
-      // releases the pass (produce_tile_notify; the barrier orders every thread's writes
-      // before it)
-      named_bar_sync(1, kNumMdEpiThreads);
-      if (part == 0 && lane == 0) pair::release_accumulator(bars, acc, rank);
-      if (et == 0) st_release(arrived + 2 * (it.tau * p.R + it.j) + h, p.epoch);
+      if (c_lo >= c_hi) {
+        // no columns for this warp (a narrow last column tile): nothing to read
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) pair::release_accumulator(bars, acc, rank);
+      }
+      // this thread's writes of the item are done: the notifier releases the pass once all
+      // have arrived (it has handled the item two back, which used the same barrier)
+      if (jj >= 2 && !mbar_wait(&mdb->notified[acc], (uint32_t(jj >> 1) & 1u) ^ 1u, abort, p.status,
+                                p.pipe_timeout_ns, 7))
+        break;
+      mbar_arrive(&mdb->stored[acc]);
     }
   }
   pair::teardown(bars, warp, tmem_base);

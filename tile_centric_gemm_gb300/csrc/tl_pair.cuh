@@ -34,7 +34,7 @@ struct __align__(8) Bars {
   uint64_t full[STAGES];     // leader: both CTAs' TMA bytes of a stage
   uint64_t empty[STAGES];    // both CTAs: stage consumed (multicast commit)
   uint64_t tmem_full[2];     // both CTAs: accumulator ready (multicast commit)
-  uint64_t tmem_empty[2];    // leader: 8 epilogue warps of the pair drained it
+  uint64_t tmem_empty[2];    // leader: the epilogue warps of the pair drained it
   uint64_t copy[COPY_NBUF];  // copy-warp staging
   uint32_t tmem_base;
   uint32_t abort;
@@ -58,7 +58,9 @@ __device__ __forceinline__ void mma_kblock(uint8_t* smem, int s, uint32_t d_tmem
 // Initialise the pair's barriers (thread 0 of each CTA) and allocate TMEM
 // (warp kWarpMma of each CTA), then synchronise the cluster so that no CTA
 // signals a barrier of its peer before the peer has initialised it.
-__device__ __forceinline__ uint32_t setup(Bars* bars, int warp) {
+// epi_arrivals: arrivals that free an accumulator (by default one per epilogue warp of
+// both CTAs).
+__device__ __forceinline__ uint32_t setup(Bars* bars, int warp, uint32_t epi_arrivals = 2 * kNumEpiWarps) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bars->full[s], 1);
@@ -66,7 +68,7 @@ __device__ __forceinline__ uint32_t setup(Bars* bars, int warp) {
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&bars->tmem_full[a], 1);
-      mbar_init(&bars->tmem_empty[a], 2 * kNumEpiWarps);
+      mbar_init(&bars->tmem_empty[a], epi_arrivals);
     }
     for (int b = 0; b < COPY_NBUF; ++b) mbar_init(&bars->copy[b], 1);
     bars->abort = 0;
