@@ -67,6 +67,12 @@ constexpr uint32_t MD_SMEM_BYTES = MD_SMEM_MDBARS + sizeof(MdBars) + 1024;
 constexpr int kChainTiles = 96;                     // output tiles whose sums are in flight together
 constexpr int kHalfFloats = pair::HM * pair::BN;     // one CTA's half of a tile's running sum
 
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 struct MdParams {
   CUtensorMap map_h[MD_MAX_RANKS];  // H_r [P, I_r], box 128 rows x 64
   CUtensorMap map_w[MD_MAX_RANKS];  // W2_r [E*I_r, Hd], box 64 x 64
@@ -136,13 +142,16 @@ __global__ void __launch_bounds__(MD_THREADS, 1) moe_down_kernel(const __grid_co
     // ---------------------------------------------------------------- TMA producer (this CTA's halves)
     if (lane == 0) {
       pair::Producer prod;
-      // operands stay in L2 ahead of the running sums' write-backs
+      // the rows of H stay in L2 for the tile's column tiles (evict-last, like the running
+      // sums); the weight panels, which small experts read once, do not push them out
+      // (evict-normal)
       const uint64_t keep = l2_policy_evict_last();
+      const uint64_t norm = l2_policy_evict_normal();
       for (int i = pair_id; i < num_items && !*abort; i += npairs) {
         const MdItem it = md_item(p, i, ntiles);
         for (int kb = 0; kb < p.KB; ++kb)
           if (!prod.load_hint(smem, bars, rank, &p.map_h[it.j], kb * pair::BK, it.row0 + h * pair::HM,
-                              &p.map_w[it.j], it.n * pair::BN + h * pair::HN, it.e * p.I_r + kb * pair::BK, keep,
+                              &p.map_w[it.j], it.n * pair::BN + h * pair::HN, it.e * p.I_r + kb * pair::BK, keep, norm,
                               abort, p.status, p.pipe_timeout_ns))
             break;
       }
