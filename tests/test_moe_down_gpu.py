@@ -61,7 +61,8 @@ def run_down(B, R, T_r, E, k, I_r, Hd, seed, options=0):
 
 @pytest.mark.parametrize("R,T_r,E,k,I_r,Hd", [(2, 64, 5, 2, 72, 264), (4, 256, 8, 2, 256, 512),
                                               (32, 4, 64, 2, 8, 8),  # the most ranks and experts, smallest sizes
-                                              (3, 100, 6, 3, 136, 136), (1, 300, 4, 1, 64, 256)])
+                                              (3, 100, 6, 3, 136, 136), (1, 300, 4, 1, 64, 256),
+                                              (2, 16, 12, 9, 64, 136)])  # topk above 8: the generic combine
 def test_moe_down_parity(B, R, T_r, E, k, I_r, Hd):
     r = run_down(B, R, T_r, E, k, I_r, Hd, seed=80 + R + E)
     assert r["status"] == (0, -1), r["status"]
