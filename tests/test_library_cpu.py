@@ -169,3 +169,19 @@ def test_allgather_ll_rejects_bad_arguments_without_a_device(B):
         a = args(**kw)
         assert B.lib.tl_allgather_ll(ctypes.byref(a), None) == code, kw
     assert B.lib.tl_allgather_ll(None, None) == B.TL_ERR_INVALID
+
+
+def test_moe_down_sizes(B):
+    # the chain schedule's workspace: an fp32 running sum per output tile (max_tiles x
+    # ceil(Hd/256) tiles of 256 x 256, 256-byte aligned), then Y [P, Hd] fp32; one flag per
+    # pass and 128-row half of every output tile
+    def max_tiles(P, E):
+        return -(-P // 256) + E
+    for (R, T_r, k, E, Hd) in [(8, 1024, 2, 32, 4096), (3, 100, 3, 6, 136), (1, 1, 1, 1, 8), (32, 4, 2, 64, 8)]:
+        P = R * T_r * k
+        tiles = max_tiles(P, E) * -(-Hd // 256)
+        sums = tiles * 2 * 128 * 256 * 4
+        assert B.tl_moe_down_workspace_size(R, T_r, k, E, Hd) == -(-sums // 256) * 256 + P * Hd * 4
+        assert B.tl_moe_down_num_flags(R, T_r, k, E, Hd) == 2 * R * tiles
+    assert B.tl_moe_down_workspace_size(0, 1, 1, 1, 8) == 0
+    assert B.tl_moe_down_num_flags(1, 0, 1, 1, 8) == -1
